@@ -1,0 +1,450 @@
+"""Benchmark of the owner-local Muon optimizer step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch of synthetic input resident in HBM:
+W-way gradient deposit + Nesterov momentum + Frobenius norm, Newton–Schulz (5 quintic
+iterations) of every owned matrix, the scaled update with decoupled weight decay, and AdamW on
+the packed tail.  The default workload is the GPT-2-small owner set (48 matrices of hidden 768,
+W = 8 bf16 contributions).  The same contribution batch is reused every step; momentum, weights
+and AdamW state evolve.  Inputs (about 2 GB) exceed the 129 MB L2, so no flush is inserted.
+
+Prints ONE JSON line (rank 0).  ``value`` is owner-step milliseconds (lower is better); the
+Newton–Schulz TFLOP/s count 4 m^2 n + 2 m^3 FLOPs per iteration (m <= n).  ``--impl reference``
+times the CPU float64 oracle on the machine's host cores instead, on a bounded per-step sample,
+extrapolated to the whole owned set.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import get_config, synth  # noqa: E402
+
+METRIC = "owner Muon step ms; Newton–Schulz TFLOP/s and % of GB300 bf16 dense peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- workload
+class Workload:
+    """Owned set of one rank, its buffers, and seeded inputs drawn on the device."""
+
+    def __init__(self, cfg: int, owner_rank_shift: int, device):
+        from matrix_optimizer_owner_gb300 import owner_step
+        self.wl = wl = get_config(cfg)
+        self.rank = (wl.rank + owner_rank_shift) % wl.world_size
+        params = [(p.rows, p.cols, p.block, p.is_matrix) for p in wl.params]
+        self.lay = lay = owner_step.owned_layout(params, wl.world_size, self.rank)
+        self.shapes = [(wl.params[i].rows, wl.params[i].cols) for i in lay.matrices]
+        self.runner = owner_step.OwnerStep(self.shapes, lay.matrix_offsets, lay.n_tail,
+                                           device=device)
+        self.dev = device
+        r = self.runner
+        dt = synth.torch_dtype(wl.contrib_dtype)
+        for pi, off, (rr, cc) in zip(lay.matrices, lay.matrix_offsets, self.shapes):
+            r.weights[off:off + rr * cc] = synth.weight(wl, pi, device)
+        for pi, off in zip(lay.tails, lay.tail_offsets):
+            n = wl.params[pi].numel
+            r.tail_p[off:off + n] = synth.weight(wl, pi, device)
+        self.contrib = []
+        for w in range(wl.W):
+            buf = torch.empty(r.n, dtype=dt, device=device)
+            for pi, off, (rr, cc) in zip(lay.matrices, lay.matrix_offsets, self.shapes):
+                buf[off:off + rr * cc] = synth.contribution(wl, 0, pi, w, device)
+            self.contrib.append(buf)
+        self.tail_contrib = []
+        for w in range(wl.W if lay.n_tail else 0):
+            buf = torch.empty(lay.n_tail, dtype=dt, device=device)
+            for pi, off in zip(lay.tails, lay.tail_offsets):
+                n = wl.params[pi].numel
+                buf[off:off + n] = synth.contribution(wl, 0, pi, w, device)
+            self.tail_contrib.append(buf)
+        self.elem_bytes = 2 if dt == torch.bfloat16 else 4
+
+    # algorithmic work per step ------------------------------------------------------------
+    def ns_flops(self):
+        s = self.wl.hyper.ns_steps
+        nominal = executed = 0
+        for rr, cc in self.shapes:
+            m, n = min(rr, cc), max(rr, cc)
+            nominal += s * (4 * m * m * n + 2 * m ** 3)
+            executed += s * (m * (m + 1) * n + m * m * (m + 1) + 2 * m * m * n)
+        return nominal, executed
+
+    def stream_bytes(self):
+        N = sum(r * c for r, c in self.shapes)
+        W, e = self.wl.W, self.elem_bytes
+        return {"reduce_momentum_norm": N * (W * e + 10), "apply_update": N * 10,
+                "adamw_tail": self.lay.n_tail * (W * e + 24)}
+
+    def launches_per_step(self):
+        r = self.runner
+        n_split = r.oset.split_count()
+        groups = (1 if n_split else 0) + (1 if n_split < len(self.shapes) else 0)
+        unaligned = sum(1 for (rr, cc), o in zip(self.shapes, self.lay.matrix_offsets)
+                        if o % 8 or cc % 8)
+        return 2 + 3 * self.wl.hyper.ns_steps * groups + 2 * unaligned + 1 + \
+            (1 if self.lay.n_tail else 0)
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for _, _, flags in rows for k, f in enumerate(flags)
+                          if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "samples": len(rows),
+                "reasons": reasons}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(wb: "Workload", budget_s: float, max_mats=None):
+    """Time the oracle's owner step on a bounded sample of the owned set (host cores).
+
+    Returns (seconds spent, nominal NS FLOPs covered, elements covered, sample text)."""
+    from oracle import step as ostep
+    wl, lay, r = wb.wl, wb.lay, wb.runner
+    hp = wl.hyper
+    spent = flops = elems = 0.0
+    taken = 0
+    order = list(range(len(wb.shapes)))
+    for k in order:
+        if spent >= budget_s or (max_mats is not None and taken >= max_mats):
+            break
+        rr, cc = wb.shapes[k]
+        off = lay.matrix_offsets[k]
+        W0 = r.weights[off:off + rr * cc].double().cpu().numpy().reshape(rr, cc)
+        cs = [c[off:off + rr * cc].double().cpu().numpy().reshape(rr, cc) for c in wb.contrib]
+        t0 = time.perf_counter()
+        ostep.muon_matrix_step(W0, np.zeros_like(W0), cs, momentum=hp.momentum,
+                               nesterov=hp.nesterov, grad_scale=hp.grad_scale,
+                               ns_steps=hp.ns_steps, a=hp.ns_a, b=hp.ns_b, c=hp.ns_c,
+                               eps=hp.ns_eps, lr=hp.lr, weight_decay=hp.weight_decay,
+                               lr_adjust=hp.lr_adjust)
+        spent += time.perf_counter() - t0
+        m, n = min(rr, cc), max(rr, cc)
+        flops += hp.ns_steps * (4 * m * m * n + 2 * m ** 3)
+        elems += rr * cc
+        taken += 1
+    return spent, flops, elems, f"{taken} of {len(wb.shapes)} owned matrices, one step"
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def extrapolated_ms(wb, spent, flops):
+    nominal, _ = wb.ns_flops()
+    return 1e3 * spent * nominal / flops if flops else None
+
+
+# ----------------------------------------------------------------------------- runs
+def time_steps(wb, steps, warmup, stream, clock_window_s=0.0):
+    """Warm up, keep stepping (untimed) for ``clock_window_s`` so the clock sampler, already
+    running, sees the GPU under this load, then time exactly ``steps`` steps."""
+    hp = wb.wl.hyper
+    r = wb.runner
+    for _ in range(warmup):
+        r.step(wb.contrib, wb.tail_contrib, hp)
+    torch.cuda.synchronize()
+    t_end = time.perf_counter() + clock_window_s
+    while time.perf_counter() < t_end:
+        for _ in range(4):
+            r.step(wb.contrib, wb.tail_contrib, hp)
+        torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(steps):
+        e = ev[k]
+        r.t += 1
+        e[0].record(stream)
+        r.reduce_momentum(wb.contrib, hp)
+        e[1].record(stream)
+        r.newton_schulz(hp)
+        e[2].record(stream)
+        r.apply_update(hp)
+        e[3].record(stream)
+        r.adamw_tail(wb.tail_contrib, hp, r.t)
+        e[4].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    total = start.elapsed_time(end)
+    phases = {name: sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(steps))
+              for i, name in enumerate(["reduce_momentum_norm", "newton_schulz", "apply_update",
+                                        "adamw_tail"])}
+    return total, phases
+
+
+def time_e2e(wb, steps, stream):
+    """Same step through the C ABI with host buffers: H2D of the step's contributions from
+    pinned memory, the step, D2H of the per-matrix update norms."""
+    hp = wb.wl.hyper
+    r = wb.runner
+    host_c = [c.cpu().pin_memory() for c in wb.contrib]
+    host_t = [c.cpu().pin_memory() for c in wb.tail_contrib]
+    norm_h = torch.empty(r.norm.numel(), dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        for d, h in zip(wb.contrib, host_c):
+            d.copy_(h, non_blocking=True)
+        for d, h in zip(wb.tail_contrib, host_t):
+            d.copy_(h, non_blocking=True)
+        r.step(wb.contrib, wb.tail_contrib, hp)
+        norm_h.copy_(r.norm, non_blocking=True)
+    e.record(stream)
+    torch.cuda.synchronize()
+    h2d = sum(c.numel() * c.element_size() for c in host_c + host_t)
+    return s.elapsed_time(e) / steps, h2d, norm_h.numel() * 4
+
+
+def config_block(wb, cfg):
+    wl = wb.wl
+    return {"workload": wl.name, "config_index": cfg, "owner_rank": wb.rank,
+            "matrices": len(wb.shapes), "owned_elements": int(sum(r * c for r, c in wb.shapes)),
+            "tail_elements": wb.lay.n_tail, "W": wl.W, "contrib_dtype": wl.contrib_dtype,
+            "ns_steps": wl.hyper.ns_steps, "l2": "inputs > 129 MB L2, no flush",
+            "parallelism": "owner replicas, no collective"}
+
+
+def run_ours(args, rank, world, local_rank):
+    from matrix_optimizer_owner_gb300 import mfsdp
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wb = Workload(args.config, rank, dev)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        total_ms, phases = time_steps(wb, args.steps, max(args.warmup, 3), stream,
+                                      args.clock_window_s)
+    clocks = clk.summary()
+    if clocks is not None:
+        clocks["window"] = f"{args.clock_window_s:.1f} s of untimed steps + the timed region"
+    status = mfsdp.mfsdp_query_status()
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+
+    e2e_ms, h2d, d2h = time_e2e(wb, max(3, min(args.steps, 10)), stream) if not args.no_e2e \
+        else (float("nan"), 0, 0)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    nominal, executed = wb.ns_flops()
+    ns_ms = phases["newton_schulz"] / args.steps
+    ns_tf_nominal = nominal / (ns_ms * 1e-3) / 1e12
+    ns_tf_exec = executed / (ns_ms * 1e-3) / 1e12
+    peak_tf = float(peaks["bf16_tflops"])
+    sb = wb.stream_bytes()
+    gbs = {k: (sb[k] / (phases[k] / args.steps * 1e-3) / 1e9 if phases[k] > 0 else None)
+           for k in sb}
+    line = {
+        "metric": METRIC, "value": round(ms, 4), "unit": "ms", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded, device-drawn)", "config": config_block(wb, args.config),
+        "ns_tflops": round(ns_tf_nominal, 1), "ns_tflops_executed": round(ns_tf_exec, 1),
+        "ns_frac_of_peak": round(ns_tf_exec / peak_tf, 4),
+        "phases_ms_per_step": {k: round(v / args.steps, 4) for k, v in phases.items()},
+        "streaming_gbs": {k: (round(v, 1) if v else None) for k, v in gbs.items()},
+        "roofline": {"kernel": "ns_gemm_kernel (all Newton–Schulz launches of a step)",
+                     "bound": "tensor", "achieved": round(ns_tf_exec, 1),
+                     "peak": peak_tf, "unit": "TFLOP/s", "frac": round(ns_tf_exec / peak_tf, 4),
+                     "traffic": None, "peak_source": f"{peak_src} bf16 burst",
+                     "flops_counted": "symmetric-executed m(m+1)n + m^2(m+1) + 2m^2n per iteration"},
+        "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": wb.launches_per_step() * args.steps,
+        "clocks": clocks, "device_status": status,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        spent, flops, elems, sample = oracle_sample(wb, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(extrapolated_ms(wb, spent, flops), 1), "unit": "ms",
+                                "cores": blas_threads(), "kind": "oracle",
+                                "sample": sample + f" ({spent:.1f} s), extrapolated by "
+                                          "nominal Newton–Schulz FLOP share"}
+    return line
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: ownership from the oracle's planner, inputs drawn on
+    the host, and each step times the oracle's Muon step on ``--ref-mats`` owned matrices
+    (cycling through the set) plus the AdamW tail, extrapolated to the whole owned set by
+    nominal Newton–Schulz FLOP share.  No library code and no GPU work on this path."""
+    if rank != 0:
+        return None
+    from oracle import plan as oplan
+    from oracle import step as ostep
+    wl = get_config(args.config)
+    hp = wl.hyper
+    ps = [oplan.Param(p.rows, p.cols, p.block, p.is_matrix) for p in wl.params]
+    mats, tails = oplan.owned(ps, oplan.plan(ps, wl.world_size), wl.rank)
+    flops_of = lambda i: hp.ns_steps * (4 * min(ps[i].rows, ps[i].cols) ** 2 *
+                                        max(ps[i].rows, ps[i].cols) +
+                                        2 * min(ps[i].rows, ps[i].cols) ** 3)
+    total_flops = sum(flops_of(i) for i in mats)
+    per_step, cursor = [], 0
+    for k in range(max(args.warmup, 0) + args.steps):
+        spent = flops = 0.0
+        for _ in range(min(args.ref_mats, len(mats))):
+            i = mats[cursor % len(mats)]
+            cursor += 1
+            p = wl.params[i]
+            W0 = synth.weight(wl, i).double().numpy().reshape(p.rows, p.cols)
+            cs = [synth.contribution(wl, 0, i, w).double().numpy().reshape(p.rows, p.cols)
+                  for w in range(wl.W)]
+            t0 = time.perf_counter()
+            ostep.muon_matrix_step(W0, np.zeros_like(W0), cs, momentum=hp.momentum,
+                                   nesterov=hp.nesterov, grad_scale=hp.grad_scale,
+                                   ns_steps=hp.ns_steps, a=hp.ns_a, b=hp.ns_b, c=hp.ns_c,
+                                   eps=hp.ns_eps, lr=hp.lr, weight_decay=hp.weight_decay,
+                                   lr_adjust=hp.lr_adjust)
+            spent += time.perf_counter() - t0
+            flops += flops_of(i)
+        if k >= args.warmup:
+            per_step.append(1e3 * spent * total_flops / flops)
+    v = statistics.mean(per_step)
+    config = {"workload": wl.name, "config_index": args.config, "owner_rank": wl.rank,
+              "matrices": len(mats),
+              "owned_elements": int(sum(ps[i].numel for i in mats)),
+              "tail_elements": int(sum(ps[i].numel for i in tails)), "W": wl.W,
+              "contrib_dtype": wl.contrib_dtype, "ns_steps": hp.ns_steps,
+              "l2": "host oracle", "parallelism": "rank 0 only"}
+    return {
+        "metric": METRIC, "value": round(v, 1), "unit": "ms", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v, 1),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, host-drawn)", "config": config, "impl": "reference",
+        "cpu_baseline": {"value": round(v, 1), "unit": "ms", "cores": blas_threads(),
+                         "kind": "oracle",
+                         "sample": f"{args.ref_mats} owned matrices per step (cycling), "
+                                   "extrapolated by nominal Newton–Schulz FLOP share"},
+        "e2e": {"value": round(v, 1), "unit": "ms", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-mats", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--clock-window-s", type=float, default=1.0)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("nccl")
+    try:
+        line = run_ours(args, rank, world, local_rank)
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,246 @@
+/*
+ * mfsdp.h — C ABI of the owner-local Muon optimizer step on one GB300 (sm_103a).
+ *
+ * Source: "MatrixFSDP: communication-free matrix optimizers under ZeRO-3 parameter sharding"
+ * (academ.us/article/2607.05895).  Under owner-shaped ZeRO-3 placement (§3) every 2D weight is
+ * whole on one owner rank, so after the backward gradient reduction has deposited the full
+ * gradient there, the owner's Muon step needs no communication (§3, §4.4).  This library is
+ * that owner-local step:
+ *
+ *   mfsdp_plan_owner_set          owner assignment + segment table (host only)   §4.1
+ *   mfsdp_owner_reduce_momentum   W-way gradient deposit + Nesterov momentum + norm  §3, §4.2
+ *   mfsdp_newton_schulz           quintic Newton–Schulz of every owned matrix      §2
+ *   mfsdp_apply_update            scaled update with decoupled weight decay        §5.1
+ *   mfsdp_adamw_tail              AdamW on the packed non-2D tail                  §3, §5.1
+ *
+ * Conventions shared by every call:
+ *   - Pointers named *_dev / buffers are DEVICE pointers (cudaMalloc'd or torch tensors on the
+ *     current device); descriptor arrays (mfsdp_param_desc, mfsdp_matrix, contribution pointer
+ *     lists) are HOST arrays read during the call and not retained.
+ *   - The caller owns all memory, including the workspace.  The library never allocates or
+ *     frees device memory.  Its only device-side global state is one status word per device.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device work is enqueued on
+ *     it and the call returns without synchronising.
+ *   - Every argument is validated before anything is launched; a negative mfsdp_status is
+ *     returned and nothing is enqueued.  MFSDP_ECUDA reports a CUDA runtime failure.
+ *     Conditions found on the device (a bounded wait that ran out, a non-finite norm) are
+ *     recorded in the device status word and returned by mfsdp_query_status.
+ *   - bf16 buffers hold IEEE bfloat16 values (uint16_t storage).  fp32 buffers are float.
+ *     All device buffers must be 16-byte aligned.
+ *   - Matrices are row-major rows x cols.  m = min(rows, cols), n = max(rows, cols).
+ */
+#ifndef MFSDP_H
+#define MFSDP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MFSDP_OK = 0,
+  MFSDP_EINVAL = -1,      /* null pointer, bad enum, bad count, unbound set, mismatched buffer */
+  MFSDP_ESHAPE = -2,      /* negative or oversized dimension, overlapping matrices */
+  MFSDP_EALIGN = -3,      /* a device pointer is not 16-byte aligned, workspace not 256-aligned */
+  MFSDP_ENOTCONTIG = -4,  /* a plan would give a parameter more than one local segment */
+  MFSDP_EWORKSPACE = -5,  /* workspace smaller than mfsdp_owner_set_workspace_bytes() */
+  MFSDP_ECUDA = -6,       /* a CUDA runtime / driver call failed */
+  MFSDP_ETIMEOUT = -7,    /* device status: a bounded device-side wait ran out */
+  MFSDP_ENONFINITE = -8,  /* device status: a matrix norm was NaN or Inf */
+  MFSDP_ENODEVICE = -9    /* no usable sm_103 device for a device call */
+} mfsdp_status;
+
+/* ------------------------------------------------------------------------------------------
+ * Owner planning (§3, §4.1, §4.2).  Host only; needs no GPU.
+ * ------------------------------------------------------------------------------------------ */
+
+typedef struct {
+  int64_t rows;       /* >= 0 */
+  int64_t cols;       /* >= 0; vectors use cols = 1 */
+  int32_t block;      /* FSDP unit id; blocks are visited in order of first appearance */
+  int32_t is_matrix;  /* 1 = 2D weight (Muon role of its own), 0 = joins the block's tail role */
+} mfsdp_param_desc;
+
+typedef struct {
+  int32_t owner;         /* owner rank in [0, world_size) */
+  int32_t role;          /* role id: blocks in order, roles by first declaration index */
+  int64_t local_offset;  /* element offset in the owner's block-local shard */
+  int64_t rank_offset;   /* element offset in the owner's flat matrix buffer (matrices) or
+                            flat tail buffer (vectors); both in (block, declaration) order */
+  int64_t numel;
+} mfsdp_segment;
+
+typedef enum {
+  MFSDP_POLICY_ROLE_GREEDY = 0,  /* per block, largest role first, to the least-loaded rank */
+  MFSDP_POLICY_SCOPE_GREEDY = 1  /* the same rule over the roles of all blocks pooled */
+} mfsdp_policy;
+
+/*
+ * Assign every role (one per 2D matrix, one packed non-2D tail per block; §3) to an owner
+ * rank and lay out the owned segments (§4.1).  The load is owner-resident numel; ties go to
+ * the lowest rank.  Within each (block, rank) the owned roles are laid out by first
+ * declaration index, a role's parameters in declaration order, unpadded, so every parameter
+ * has one contiguous local segment and a tail is one whole segment.
+ *
+ *   params          [n_params] host array, declaration order.
+ *   seg_out         [n_params] host array, written.
+ *   block_rank_numel_out  nullable host array of capacity n_params * world_size; on return
+ *                   entry [k * world_size + r] = O_{B_k, r} (§4.2), numel of the k-th block
+ *                   (first-appearance order) resident on rank r.
+ *   n_blocks_out    nullable; receives the number of distinct blocks.
+ * Errors: MFSDP_EINVAL (null params/seg_out with n_params > 0, world_size <= 0, bad policy),
+ *         MFSDP_ESHAPE (negative dimension or numel overflow).
+ * Deterministic and thread-safe.
+ */
+int mfsdp_plan_owner_set(const mfsdp_param_desc* params, int64_t n_params, int32_t world_size,
+                         int32_t policy, mfsdp_segment* seg_out, int64_t* block_rank_numel_out,
+                         int64_t* n_blocks_out);
+
+/* ------------------------------------------------------------------------------------------
+ * The owned-matrix set.  Built once from the owner's matrix table; its launch tables, tensor
+ * maps and Newton–Schulz scratch live in a caller-provided device workspace.
+ * ------------------------------------------------------------------------------------------ */
+
+typedef struct {
+  int64_t rows, cols;  /* >= 0; an empty matrix is skipped by every call */
+  int64_t offset;      /* element offset of the matrix in the flat owner buffers */
+} mfsdp_matrix;
+
+typedef struct mfsdp_owner_set_s mfsdp_owner_set;
+
+/*
+ * Describe the owner's matrices.  `mats` [n_mats] host array: each matrix occupies
+ * [offset, offset + rows*cols) of every flat per-element buffer (weights, momentum, NS input,
+ * NS output); ranges must not overlap.  Matrices with rows*cols <= split_max_numel run
+ * Newton–Schulz with split bf16 operands (value = hi + lo, three products per multiply,
+ * about 16 significant bits); the others use plain bf16 operands with fp32 accumulation.
+ * No device work; *out is a host object owned by the caller (mfsdp_owner_set_destroy).
+ * Errors: MFSDP_EINVAL, MFSDP_ESHAPE (negative size, overlap, dimension >= 2^31).
+ */
+int mfsdp_owner_set_create(const mfsdp_matrix* mats, int32_t n_mats, int64_t split_max_numel,
+                           mfsdp_owner_set** out);
+int mfsdp_owner_set_destroy(mfsdp_owner_set* set);
+
+/* Device workspace bytes the set needs (launch tables, norm partials, tensor maps, the
+ * Newton–Schulz ping buffer and the m x m Gram / polynomial buffers of every matrix). */
+int mfsdp_owner_set_workspace_bytes(const mfsdp_owner_set* set, size_t* bytes_out);
+
+/* Number of matrices that run in split (hi + lo) precision. */
+int mfsdp_owner_set_split_count(const mfsdp_owner_set* set, int32_t* count_out);
+
+/*
+ * Bind the set to its device buffers on the current device and write its launch tables and
+ * TMA tensor maps into `workspace` (enqueued on `stream`).  The workspace must stay untouched
+ * by the caller while the set is bound.  ns_input / ortho_out are the flat bf16 buffers of
+ * mfsdp_owner_reduce_momentum's output and mfsdp_newton_schulz's output; ns_input_lo /
+ * ortho_lo are their low halves, required iff the set has split matrices (else may be NULL).
+ * ns_input must not alias ortho_out.  Re-binding replaces the previous binding.
+ * Errors: MFSDP_EINVAL, MFSDP_EALIGN, MFSDP_EWORKSPACE, MFSDP_ECUDA, MFSDP_ENODEVICE.
+ */
+int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace_bytes,
+                         const void* ns_input, const void* ns_input_lo, void* ortho_out,
+                         void* ortho_lo, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * The owner-local step.  All calls need a bound set; buffers are flat over the set.
+ * ------------------------------------------------------------------------------------------ */
+
+typedef enum { MFSDP_DTYPE_F32 = 0, MFSDP_DTYPE_BF16 = 1 } mfsdp_dtype;
+
+/*
+ * Owner gradient deposit fused with Nesterov momentum and the Frobenius norm (§3, §4.2: the
+ * reduced full gradient lands in the owner segment; §2: Muon's input is the momentum-
+ * buffered gradient).  Per element e of every matrix:
+ *     G = grad_scale * sum_{w<W} contrib[w][e]          (fp32, w in order)
+ *     B = momentum * B + (1 - momentum) * G             (momentum_buf, updated in place)
+ *     U = nesterov ? (1 - momentum) * G + momentum * B : B
+ *     ns_input[e] = bf16_rne(U);  ns_input_lo[e] = bf16_rne(U - ns_input[e])  (split matrices)
+ *     reduced_grad_out[e] = G                            (nullable)
+ * and per matrix i: norm_out[i] = ||U_i||_F of the fp32 U, reduced in a fixed order (per-CTA
+ * fp32 partial sums, then an fp64 sum in index order): bitwise reproducible run to run.
+ *   contrib  host array of W device pointers to flat contribution buffers (dtype contrib_dtype).
+ *   W in [1, 64].  momentum_buf fp32 [flat]; ns_input bf16 [flat] (must be the bound buffer).
+ *   norm_out fp32 [n_mats] device.
+ * A non-finite norm sets MFSDP_ENONFINITE in the device status word.
+ */
+int mfsdp_owner_reduce_momentum(const mfsdp_owner_set* set, const void* const* contrib, int32_t W,
+                                int32_t contrib_dtype, float grad_scale, float momentum,
+                                int32_t nesterov, float* momentum_buf, void* ns_input,
+                                void* ns_input_lo, float* reduced_grad_out, float* norm_out,
+                                void* stream);
+
+/*
+ * Quintic Newton–Schulz orthogonalisation of every owned matrix (§2: steps built from
+ * products such as X X^T that couple all rows).  Per matrix, with s = 1/(norm[i] + eps):
+ *     X = s * U  (U = ns_input, + ns_input_lo for split matrices), transposed if rows > cols;
+ *     repeat `steps` times:  A = X X^T;  B = b*A + c*A A;  X = a*X + B X
+ *     ortho_out = X (transposed back), ortho_lo = low half for split matrices.
+ * Runs as three grouped, persistent tcgen05 GEMM launches per iteration over all matrices;
+ * only the upper-triangle tiles of the symmetric A and A A are computed.  Operands are bf16
+ * (or split bf16), accumulation fp32 in tensor memory; each phase's output is rounded to
+ * bf16 once.  ns_input / ortho_out must be the bound buffers.  steps in [1, 64].
+ * A device wait that runs out sets MFSDP_ETIMEOUT in the status word.
+ */
+int mfsdp_newton_schulz(const mfsdp_owner_set* set, const void* ns_input, const void* ns_input_lo,
+                        const float* norm, int32_t steps, float a, float b, float c, float eps,
+                        void* ortho_out, void* ortho_lo, void* stream);
+
+typedef enum {
+  MFSDP_LR_ORIGINAL = 0,        /* scale s = sqrt(max(1, rows/cols)) */
+  MFSDP_LR_MATCH_RMS_ADAMW = 1  /* scale s = 0.2 * sqrt(max(rows, cols)) */
+} mfsdp_lr_adjust;
+
+/*
+ * Scaled update with decoupled weight decay (§5.1: torch.optim.Muon semantics):
+ *     W = W * (1 - lr*weight_decay) - lr * s(rows, cols) * (ortho + ortho_lo)
+ * weights fp32 [flat] in place; ortho bf16 [flat]; ortho_lo bf16 [flat] or NULL (used only on
+ * split matrices).
+ */
+int mfsdp_apply_update(const mfsdp_owner_set* set, float* weights, const void* ortho,
+                       const void* ortho_lo, float lr, float weight_decay, int32_t lr_adjust,
+                       void* stream);
+
+/*
+ * AdamW on a packed non-2D tail of n elements (§3: the tail is one whole segment on its
+ * owner and stays on AdamW; §5.1 hyperparameters).  g = grad_scale * sum_w contrib[w];
+ *     p = p*(1 - lr*wd);  m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*g^2;
+ *     p = p - lr * (m / (1 - b1^step)) / (sqrt(v / (1 - b2^step)) + eps)
+ * param, exp_avg, exp_avg_sq fp32 [n] device, updated in place; step >= 1 (shared by the
+ * whole tail).  Stateless: needs no owner set.  n == 0 returns MFSDP_OK without a launch.
+ */
+int mfsdp_adamw_tail(const void* const* contrib, int32_t W, int32_t contrib_dtype,
+                     float grad_scale, int64_t n, float* param, float* exp_avg,
+                     float* exp_avg_sq, int64_t step, float lr, float beta1, float beta2,
+                     float eps, float weight_decay, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Status and diagnostics.
+ * ------------------------------------------------------------------------------------------ */
+
+/* Synchronise `stream`, read and clear the current device's status word.  *device_status_out
+ * is MFSDP_OK, MFSDP_ETIMEOUT or MFSDP_ENONFINITE (timeout wins).  Returns MFSDP_ECUDA if the
+ * synchronisation itself failed. */
+int mfsdp_query_status(void* stream, int32_t* device_status_out);
+
+/* Static description of a status code. */
+const char* mfsdp_status_string(int status);
+
+/* Limit, in nanoseconds, of every bounded device-side wait launched afterwards by this process
+ * (default 2e9).  0 restores the default. */
+int mfsdp_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Failure-detection check: launch one CTA that waits on an mbarrier nothing will arrive at,
+ * bounded by limit_ns.  The wait runs out, the kernel records MFSDP_ETIMEOUT in the status
+ * word and returns; the context stays usable. */
+int mfsdp_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
+/* Library ABI version (major * 100 + minor). */
+int mfsdp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MFSDP_H */

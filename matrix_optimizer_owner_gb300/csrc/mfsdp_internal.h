@@ -1,0 +1,146 @@
+// Internal declarations shared by the host API and the kernels of libmfsdp.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace mfsdp {
+
+// ---- device status word bits (kept in one __device__ int per device) ----------------------
+constexpr int kStatusTimeout = 1;
+constexpr int kStatusNonFinite = 2;
+
+// ---- streaming kernels (gradient deposit + momentum + norm, update) -----------------------
+constexpr int kMaxContrib = 64;
+constexpr int kStreamThreads = 256;
+constexpr int kVec = 8;                                   // elements per thread per access
+constexpr int kVecsPerThread = 8;                         // vectors per thread per CTA
+constexpr int kChunk = kStreamThreads * kVec * kVecsPerThread;  // 16384 elements per CTA
+
+struct DevMat {            // one owned matrix, as the streaming kernels see it
+  int64_t offset;          // element offset in the flat owner buffers
+  int64_t numel;
+  int64_t rows, cols;
+  int32_t cta_begin;       // first CTA of this matrix in the per-matrix CTA partition
+  int32_t split;           // 1: NS input / output carry a low bf16 half
+  float scale_original;    // sqrt(max(1, rows/cols))
+  float scale_rms;         // 0.2 * sqrt(max(rows, cols))
+};
+
+struct ContribPtrs {
+  const void* p[kMaxContrib];
+};
+
+struct ReduceParams {
+  ContribPtrs contrib;
+  int32_t W;
+  int32_t n_mats;
+  int32_t total_ctas;
+  int32_t nesterov;
+  const DevMat* mats;
+  float grad_scale, mu, one_minus_mu;
+  float* momentum;
+  uint16_t* uhat;
+  uint16_t* uhat_lo;       // nullable
+  float* grad;             // nullable
+  float* partials;         // [total_ctas]
+};
+
+struct NormParams {
+  const DevMat* mats;
+  int32_t n_mats;
+  const float* partials;
+  float* norm;             // [n_mats]
+  int* status;
+};
+
+struct UpdateParams {
+  const DevMat* mats;
+  int32_t n_mats;
+  int32_t total_ctas;
+  int32_t lr_adjust;
+  float decay;             // 1 - lr * weight_decay
+  float lr;
+  float* weights;
+  const uint16_t* ortho;
+  const uint16_t* ortho_lo;  // nullable
+};
+
+struct AdamParams {
+  ContribPtrs contrib;
+  int32_t W;
+  int64_t n;
+  float grad_scale;
+  float decay;             // 1 - lr * weight_decay
+  float b1, one_minus_b1, b2, one_minus_b2;
+  float step_size;         // lr / (1 - b1^t)
+  float inv_sqrt_bc2;      // 1 / sqrt(1 - b2^t)
+  float eps;
+  float* p;
+  float* m;
+  float* v;
+};
+
+struct CopyParams {        // strided 2D bf16 copy (pack / unpack of unaligned matrices)
+  const uint16_t* src;
+  uint16_t* dst;
+  int64_t rows, cols, ld_src, ld_dst;
+};
+
+cudaError_t launch_reduce_momentum(const ReduceParams& p, int contrib_dtype, cudaStream_t s);
+cudaError_t launch_norm_finalize(const NormParams& p, cudaStream_t s);
+cudaError_t launch_apply_update(const UpdateParams& p, cudaStream_t s);
+cudaError_t launch_adamw(const AdamParams& p, int contrib_dtype, cudaStream_t s);
+cudaError_t launch_copy2d(const CopyParams& p, cudaStream_t s);
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int* status, cudaStream_t s);
+int* status_word_address();  // device address of this device's status word (nullptr on error)
+
+// ---- Newton–Schulz grouped GEMM (tcgen05 / TMEM / TMA) ------------------------------------
+constexpr int kBM = 128;   // tile rows    = UMMA M (one CTA, TMEM lanes 0..127)
+constexpr int kBN = 256;   // tile columns = UMMA N
+constexpr int kBK = 64;    // k per pipeline stage = one 128-byte swizzle atom of bf16
+constexpr int kNsThreads = 192;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+
+enum NsKind : int32_t { kGram = 0, kPoly = 1, kApply = 2 };
+
+struct NsProblem {         // one output matrix of one Newton–Schulz phase
+  int32_t M, N, K;         // output M x N, contraction length K
+  int32_t a_mn, b_mn;      // operand storage: 0 = K-major rows, 1 = MN-major rows
+  int32_t sym;             // symmetric output: only tiles touching the upper triangle run
+  int32_t kind;            // NsKind: epilogue out = alpha*acc + beta*D
+  int32_t first;           // first iteration: fold s = 1/(norm + eps) into alpha / beta
+  int32_t mat;             // matrix index (norm)
+  int32_t map_a, map_b;    // tensor-map indices of the hi operands; lo = index + 1
+  int32_t pad_;
+  const uint16_t* d_hi;    // epilogue addend D (kPoly: A, kApply: X), row pitch ldd
+  const uint16_t* d_lo;
+  int64_t ldd;
+  uint16_t* o_hi;          // output, row pitch ldo
+  uint16_t* o_lo;
+  int64_t ldo;
+};
+
+struct NsTile {
+  int32_t prob, tm, tn, pad_;
+};
+
+struct NsLaunchParams {
+  const NsProblem* probs;
+  const NsTile* tiles;
+  int32_t ntiles;
+  int32_t pad_;
+  const CUtensorMap* maps;
+  const float* norm;
+  float eps, a, b, c;
+  uint64_t wait_limit_ns;
+  int* status;
+};
+
+size_t ns_smem_bytes(bool split);
+cudaError_t ns_prepare_kernels();  // set the dynamic shared memory attribute once per device
+cudaError_t launch_ns_phase(const NsLaunchParams& p, bool split, int grid, cudaStream_t s);
+
+}  // namespace mfsdp

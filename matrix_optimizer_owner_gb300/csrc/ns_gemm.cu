@@ -1,0 +1,464 @@
+// Newton–Schulz phases as one persistent, grouped tcgen05 GEMM launch per phase.
+//
+// "MatrixFSDP: communication-free matrix optimizers under ZeRO-3 parameter sharding", §2: Muon
+// orthogonalises each whole 2D matrix with Newton–Schulz steps built from products such as
+// X X^T.  One quintic iteration, X of shape m x n with m <= n, is three products:
+//     gram  A  = X X^T            (m x m, K = n, symmetric: upper-triangle tiles only)
+//     poly  B  = b*A + c*A A      (m x m, K = m, symmetric: upper-triangle tiles only)
+//     apply X' = a*X + B X        (m x n, K = m)
+// A launch runs one phase for every owned matrix: a static list of 128 x 256 output tiles,
+// taken round-robin by a persistent grid of one CTA per SM.
+//
+// CTA roles (192 threads):
+//   warp 0 (one lane)  TMA producer: 64 x 64 bf16 boxes, 128-byte swizzle, into a ring of
+//                      pipeline stages guarded by full/empty mbarriers;
+//   warp 1 (one lane)  MMA issuer: tcgen05.mma kind::f16 (M=128, N=256, K=16) from shared-
+//                      memory descriptors into one of two TMEM accumulators (2 x 256 columns);
+//   warps 2-5          epilogue: tcgen05.ld rows of the accumulator, out = alpha*acc + beta*D,
+//                      round to bf16 (and the low half in split mode), store; symmetric tiles
+//                      store the upper triangle and its mirror.
+// Operands come from row-major bf16 buffers.  A "K-major" operand has the contraction index
+// contiguous (rows of X for X X^T); an "MN-major" operand has the output index contiguous
+// (X as the right factor of B X).  Both map to the canonical 128-byte-swizzled UMMA layouts.
+//
+// Every mbarrier wait is bounded (globaltimer): when a wait runs out the kernel records the
+// timeout in the status word, raises an abort flag every role polls, waits (bounded) for its
+// own TMA loads and MMAs in flight, frees its tensor memory and returns.
+#include <cuda_bf16.h>
+
+#include "mfsdp_internal.h"
+
+namespace mfsdp {
+namespace {
+
+constexpr uint32_t kBoxBytes = 64 * 64 * 2;               // one 64 x 64 bf16 TMA box
+constexpr uint32_t kABytes = kBM * kBK * 2;               // 16 KB
+constexpr uint32_t kBBytes = kBN * kBK * 2;               // 32 KB
+constexpr uint32_t kTmemCols = 2 * kBN;                   // two fp32 accumulators
+
+template <bool SPLIT>
+struct Cfg {
+  static constexpr int kOps = SPLIT ? 2 : 1;              // hi (+ lo) operand copies
+  static constexpr int kStages = SPLIT ? 2 : 4;
+  static constexpr uint32_t kStageBytes = kOps * (kABytes + kBBytes);
+  static constexpr uint32_t kBarOffset = kStages * kStageBytes;
+  static constexpr uint32_t kSmem = 1024 + kBarOffset + 256;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+struct Guard {                 // shared abort flag + the launch's wait limit
+  volatile int* abort;
+  uint64_t limit_ns;
+  int* status;
+};
+
+// Wait for the phase of `parity` to complete.  Returns false if the kernel is aborting or the
+// wait ran out (which starts the abort).  `honor_abort` = false is used during teardown.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Guard& g,
+                                       bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31) == 0) {
+      if (honor_abort && *g.abort) return false;
+      if (globaltimer() - t0 > g.limit_ns) {
+        atomicOr(g.status, kStatusTimeout);
+        *g.abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane; waits for the load to land.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 layout: start >> 4 at bit 0,
+// leading-dimension byte offset >> 4 at bit 16, stride-dimension byte offset >> 4 at bit 32,
+// version 1 at bit 46, swizzle mode 2 = 128B at bit 61).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// K-major operand: rows of 64 k-values (128 B), 8-row swizzle atoms 1024 B apart; the k-step
+// j of 16 elements starts 32 bytes further.  MN-major operand: 64-wide output-index chunks
+// (one box each, 8 KB apart), 8 k-rows of 128 B per atom; k-step j starts 16 rows further.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, int j) {
+  return mn_major ? smem_desc(base + (uint32_t)j * 2048u, kBoxBytes, 1024u)
+                  : smem_desc(base + (uint32_t)j * 32u, 16u, 1024u);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bit 4), bf16 A (bits 7-9) and B
+// (bits 10-12), A / B major-ness (bits 15 / 16), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+__device__ __forceinline__ uint32_t make_idesc(int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+// Load `rows` rows (a multiple of 64) of one operand tile for k-block k0 into `dst`.
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, int mn_major,
+                                             int r0, int k0, int boxes, uint32_t bar) {
+  for (int c = 0; c < boxes; ++c) {
+    if (mn_major)
+      tma_load(dst + (uint32_t)c * kBoxBytes, map, r0 + 64 * c, k0, bar);
+    else
+      tma_load(dst + (uint32_t)c * kBoxBytes, map, k0, r0 + 64 * c, bar);
+  }
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint16_t f2bf(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+__device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+// 32 consecutive bf16 of row r starting at column c0 (c0 % 8 == 0, pitch % 8 == 0) as fp32.
+__device__ __forceinline__ void load_row32(const uint16_t* p, int64_t ld, int r, int c0, int N,
+                                           float (&d)[32]) {
+  const uint16_t* row = p + (int64_t)r * ld + c0;
+  if (c0 + 32 <= N) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = *reinterpret_cast<const uint4*>(row + 8 * q);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        d[8 * q + 2 * k] = bf_lo(w[k]);
+        d[8 * q + 2 * k + 1] = bf_hi(w[k]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) d[j] = (c0 + j < N) ? bf2f(row[j]) : 0.f;
+  }
+}
+
+__device__ __forceinline__ void store_row32(uint16_t* p, int64_t ld, int r, int c0, int cmin,
+                                            int N, const uint16_t (&h)[32]) {
+  uint16_t* row = p + (int64_t)r * ld + c0;
+  if (cmin <= c0 && c0 + 32 <= N) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 v;
+      v.x = (uint32_t)h[8 * q + 0] | ((uint32_t)h[8 * q + 1] << 16);
+      v.y = (uint32_t)h[8 * q + 2] | ((uint32_t)h[8 * q + 3] << 16);
+      v.z = (uint32_t)h[8 * q + 4] | ((uint32_t)h[8 * q + 5] << 16);
+      v.w = (uint32_t)h[8 * q + 6] | ((uint32_t)h[8 * q + 7] << 16);
+      *reinterpret_cast<uint4*>(row + 8 * q) = v;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (c0 + j >= cmin && c0 + j < N) row[j] = h[j];
+  }
+}
+
+// ---------------------------------------------------------------- the kernel
+template <bool SPLIT>
+__global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_constant__ NsLaunchParams P) {
+  using C = Cfg<SPLIT>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+  // bars: full[S] | empty[S] | tfull[2] | tempty[2] | drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const int full0 = 0, empty0 = S, tfull0 = 2 * S, tempty0 = 2 * S + 2, drain = 2 * S + 4;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar(full0 + s), 1);
+      mbar_init(bar(empty0 + s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar(tfull0 + a), 1);
+      mbar_init(bar(tempty0 + a), 4);
+    }
+    mbar_init(bar(drain), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const Guard g{abort_flag, P.wait_limit_ns, P.status};
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0, last_parity = 0;  // per-stage bit masks, for the teardown wait
+    for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
+      const NsTile tile = P.tiles[t];
+      const NsProblem& pr = P.probs[tile.prob];
+      const CUtensorMap* ma = P.maps + pr.map_a;
+      const CUtensorMap* mb = P.maps + pr.map_b;
+      const int m0 = tile.tm * kBM, n0 = tile.tn * kBN, nk = (pr.K + kBK - 1) / kBK;
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait(bar(empty0 + stage), phase ^ 1u, g)) { ok = false; break; }
+        const uint32_t sb = sbase + (uint32_t)stage * C::kStageBytes;
+        const uint32_t fb = bar(full0 + stage);
+        mbar_expect_tx(fb, C::kStageBytes);
+        const int k0 = kb * kBK;
+        load_operand(sb, ma, pr.a_mn, m0, k0, kBM / 64, fb);
+        load_operand(sb + kABytes, mb, pr.b_mn, n0, k0, kBN / 64, fb);
+        if (SPLIT) {
+          load_operand(sb + kABytes + kBBytes, ma + 1, pr.a_mn, m0, k0, kBM / 64, fb);
+          load_operand(sb + 2 * kABytes + kBBytes, mb + 1, pr.b_mn, n0, k0, kBN / 64, fb);
+        }
+        armed |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+    }
+    // teardown: every load this thread issued has landed before the CTA may exit
+    for (int s = 0; s < S; ++s)
+      if (armed & (1u << s)) mbar_wait(bar(full0 + s), (last_parity >> s) & 1u, g, false);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
+      const NsTile tile = P.tiles[t];
+      const NsProblem& pr = P.probs[tile.prob];
+      const int nk = (pr.K + kBK - 1) / kBK;
+      const uint32_t idesc = make_idesc(pr.a_mn, pr.b_mn);
+      if (!mbar_wait(bar(tempty0 + acc), acc_phase ^ 1u, g)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait(bar(full0 + stage), phase, g)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = sbase + (uint32_t)stage * C::kStageBytes;
+        const uint32_t sbb = sa + kABytes;
+#pragma unroll
+        for (int j = 0; j < kBK / 16; ++j) {
+          const uint64_t ad = operand_desc(sa, pr.a_mn, j);
+          const uint64_t bd = operand_desc(sbb, pr.b_mn, j);
+          tc_mma(d_tmem, ad, bd, idesc, (kb | j) != 0);
+          if (SPLIT) {
+            const uint64_t adl = operand_desc(sa + kABytes + kBBytes, pr.a_mn, j);
+            const uint64_t bdl = operand_desc(sbb + kABytes + kBBytes, pr.b_mn, j);
+            tc_mma(d_tmem, ad, bdl, idesc, 1u);   // hi * lo
+            tc_mma(d_tmem, adl, bd, idesc, 1u);   // lo * hi
+          }
+        }
+        tc_commit(bar(empty0 + stage));  // frees the stage once these MMAs have read it
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      tc_commit(bar(tfull0 + acc));      // accumulator ready for the epilogue
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    // teardown: all MMAs issued by this thread have completed
+    tc_commit(bar(drain));
+    mbar_wait(bar(drain), 0u, g, false);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 are this warp's rows
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
+      const NsTile tile = P.tiles[t];
+      const NsProblem& pr = P.probs[tile.prob];
+      if (!mbar_wait(bar(tfull0 + acc), acc_phase, g)) break;
+      tc_fence_after();
+      float alpha = 1.f, beta = 0.f;
+      const float s = 1.f / (P.norm[pr.mat] + P.eps);
+      if (pr.kind == kGram) {
+        alpha = pr.first ? s * s : 1.f;
+      } else if (pr.kind == kPoly) {
+        alpha = P.c;
+        beta = P.b;
+      } else {
+        alpha = pr.first ? s : 1.f;
+        beta = P.a * alpha;
+      }
+      const int m0 = tile.tm * kBM, n0 = tile.tn * kBN;
+      const int rw = m0 + quarter * 32;  // first row of this warp
+      const int r = rw + lane;
+      const bool rvalid = r < pr.M;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
+      for (int cc = 0; cc < kBN / 32; ++cc) {
+        const int c0 = n0 + cc * 32;
+        if (c0 >= pr.N || rw >= pr.M) break;           // warp-uniform
+        if (pr.sym && c0 + 31 < rw) continue;          // chunk entirely below the diagonal
+        float v[32];
+        tc_ld32(taddr + (uint32_t)(cc * 32), v);
+        if (!rvalid) continue;
+        if (beta != 0.f) {
+          float d[32];
+          load_row32(pr.d_hi, pr.ldd, r, c0, pr.N, d);
+          if (SPLIT) {
+            float dl[32];
+            load_row32(pr.d_lo, pr.ldd, r, c0, pr.N, dl);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) d[j] += dl[j];
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = fmaf(alpha, v[j], beta * d[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= alpha;
+        }
+        uint16_t h[32], l[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          h[j] = f2bf(v[j]);
+          if (SPLIT) l[j] = f2bf(v[j] - bf2f(h[j]));
+        }
+        const int cmin = pr.sym ? r : 0;  // symmetric: this row stores columns >= r ...
+        store_row32(pr.o_hi, pr.ldo, r, c0, cmin, pr.N, h);
+        if (SPLIT) store_row32(pr.o_lo, pr.ldo, r, c0, cmin, pr.N, l);
+        if (pr.sym && c0 + 31 > r) {      // ... and mirrors columns > r into row c, column r
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c = c0 + j;
+            if (c > r && c < pr.N) {
+              pr.o_hi[(int64_t)c * pr.ldo + r] = h[j];
+              if (SPLIT) pr.o_lo[(int64_t)c * pr.ldo + r] = l[j];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(tempty0 + acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+size_t ns_smem_bytes(bool split) { return split ? Cfg<true>::kSmem : Cfg<false>::kSmem; }
+
+cudaError_t ns_prepare_kernels() {
+  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)Cfg<false>::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(ns_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)Cfg<true>::kSmem);
+}
+
+cudaError_t launch_ns_phase(const NsLaunchParams& p, bool split, int grid, cudaStream_t s) {
+  if (p.ntiles <= 0) return cudaSuccess;
+  if (split)
+    ns_gemm_kernel<true><<<grid, kNsThreads, Cfg<true>::kSmem, s>>>(p);
+  else
+    ns_gemm_kernel<false><<<grid, kNsThreads, Cfg<false>::kSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mfsdp

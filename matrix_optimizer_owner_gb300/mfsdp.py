@@ -1,0 +1,186 @@
+"""Python binding of ``include/mfsdp.h``: the same entry points, argument marshalling only.
+
+Tensors are torch tensors on the current CUDA device (PyTorch provides device memory and
+streams; every step of the optimizer runs in the library's kernels).  Each wrapper enqueues on
+``torch.cuda.current_stream()`` unless a stream is given, and raises ``MfsdpError`` on a
+non-zero status.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+from typing import Optional, Sequence, Tuple
+
+from . import _lib
+from ._lib import Matrix, ParamDesc, Segment
+
+POLICY_ROLE_GREEDY = 0
+POLICY_SCOPE_GREEDY = 1
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+LR_ORIGINAL = 0
+LR_MATCH_RMS_ADAMW = 1
+
+
+class MfsdpError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {_lib.STATUS_NAMES.get(status, status)}")
+
+
+def _check(fn: str, st: int) -> None:
+    if st != 0:
+        raise MfsdpError(fn, st)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _ptr_array(tensors: Sequence) -> C.Array:
+    return (C.c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise TypeError(f"contribution dtype {t.dtype} is not float32 or bfloat16")
+
+
+def mfsdp_version() -> int:
+    return _lib.load().mfsdp_version()
+
+
+def mfsdp_status_string(status: int) -> str:
+    return _lib.load().mfsdp_status_string(status).decode()
+
+
+# ------------------------------------------------------------------------------- planner
+def mfsdp_plan_owner_set(params: Sequence[Tuple[int, int, int, bool]], world_size: int,
+                         policy: int = POLICY_ROLE_GREEDY):
+    """params: (rows, cols, block, is_matrix) per parameter, declaration order.
+
+    Returns (segments, block_rank_numel, n_blocks): segments as a list of dicts with keys
+    owner, role, local_offset, rank_offset, numel; block_rank_numel[k][r] = O_{B_k, r}.
+    """
+    lib = _lib.load()
+    n = len(params)
+    pd = (ParamDesc * max(n, 1))()
+    for i, (r, c, b, m) in enumerate(params):
+        pd[i] = ParamDesc(r, c, b, 1 if m else 0)
+    seg = (Segment * max(n, 1))()
+    brn = (C.c_int64 * max(n * world_size, 1))()
+    nb = C.c_int64(0)
+    _check("mfsdp_plan_owner_set",
+           lib.mfsdp_plan_owner_set(pd, n, world_size, policy, seg, brn, C.byref(nb)))
+    segs = [{"owner": s.owner, "role": s.role, "local_offset": s.local_offset,
+             "rank_offset": s.rank_offset, "numel": s.numel} for s in seg[:n]]
+    table = [[brn[k * world_size + r] for r in range(world_size)] for k in range(nb.value)]
+    return segs, table, nb.value
+
+
+# ------------------------------------------------------------------------------- owner set
+class OwnerSet:
+    """Handle of ``mfsdp_owner_set``: create, query workspace, bind, destroy."""
+
+    def __init__(self, mats: Sequence[Tuple[int, int, int]], split_max_numel: int = 0):
+        lib = _lib.load()
+        n = len(mats)
+        arr = (Matrix * max(n, 1))()
+        for i, (r, c, off) in enumerate(mats):
+            arr[i] = Matrix(r, c, off)
+        h = C.c_void_p()
+        _check("mfsdp_owner_set_create",
+               lib.mfsdp_owner_set_create(arr, n, split_max_numel, C.byref(h)))
+        self.handle = h
+        self.n_mats = n
+        self._bound = ()
+
+    def workspace_bytes(self) -> int:
+        b = C.c_size_t(0)
+        _check("mfsdp_owner_set_workspace_bytes",
+               _lib.load().mfsdp_owner_set_workspace_bytes(self.handle, C.byref(b)))
+        return b.value
+
+    def split_count(self) -> int:
+        k = C.c_int32(0)
+        _check("mfsdp_owner_set_split_count",
+               _lib.load().mfsdp_owner_set_split_count(self.handle, C.byref(k)))
+        return k.value
+
+    def bind(self, workspace, ns_input, ns_input_lo, ortho_out, ortho_lo, stream=None) -> None:
+        _check("mfsdp_owner_set_bind", _lib.load().mfsdp_owner_set_bind(
+            self.handle, _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _ptr(ns_input), _ptr(ns_input_lo), _ptr(ortho_out), _ptr(ortho_lo), _stream(stream)))
+        self._bound = (workspace, ns_input, ns_input_lo, ortho_out, ortho_lo)  # keep alive
+
+    def close(self) -> None:
+        if self.handle:
+            _lib.load().mfsdp_owner_set_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------------------------- step calls
+def mfsdp_owner_reduce_momentum(oset: OwnerSet, contrib: Sequence, grad_scale: float,
+                                momentum: float, nesterov: bool, momentum_buf, ns_input,
+                                ns_input_lo, reduced_grad_out, norm_out, stream=None) -> None:
+    ptrs = _ptr_array(contrib)
+    _check("mfsdp_owner_reduce_momentum", _lib.load().mfsdp_owner_reduce_momentum(
+        oset.handle, ptrs, len(contrib), _dtype_code(contrib[0]), grad_scale, momentum,
+        1 if nesterov else 0, _ptr(momentum_buf), _ptr(ns_input), _ptr(ns_input_lo),
+        _ptr(reduced_grad_out), _ptr(norm_out), _stream(stream)))
+
+
+def mfsdp_newton_schulz(oset: OwnerSet, ns_input, ns_input_lo, norm, steps: int, a: float,
+                        b: float, c: float, eps: float, ortho_out, ortho_lo, stream=None) -> None:
+    _check("mfsdp_newton_schulz", _lib.load().mfsdp_newton_schulz(
+        oset.handle, _ptr(ns_input), _ptr(ns_input_lo), _ptr(norm), steps, a, b, c, eps,
+        _ptr(ortho_out), _ptr(ortho_lo), _stream(stream)))
+
+
+def mfsdp_apply_update(oset: OwnerSet, weights, ortho, ortho_lo, lr: float, weight_decay: float,
+                       lr_adjust: int = LR_ORIGINAL, stream=None) -> None:
+    _check("mfsdp_apply_update", _lib.load().mfsdp_apply_update(
+        oset.handle, _ptr(weights), _ptr(ortho), _ptr(ortho_lo), lr, weight_decay, lr_adjust,
+        _stream(stream)))
+
+
+def mfsdp_adamw_tail(contrib: Sequence, grad_scale: float, param, exp_avg, exp_avg_sq, step: int,
+                     lr: float, beta1: float, beta2: float, eps: float, weight_decay: float,
+                     stream=None) -> None:
+    ptrs = _ptr_array(contrib)
+    _check("mfsdp_adamw_tail", _lib.load().mfsdp_adamw_tail(
+        ptrs, len(contrib), _dtype_code(contrib[0]), grad_scale, param.numel(), _ptr(param),
+        _ptr(exp_avg), _ptr(exp_avg_sq), step, lr, beta1, beta2, eps, weight_decay,
+        _stream(stream)))
+
+
+def mfsdp_query_status(stream=None) -> int:
+    out = C.c_int32(0)
+    _check("mfsdp_query_status", _lib.load().mfsdp_query_status(_stream(stream), C.byref(out)))
+    return out.value
+
+
+def mfsdp_set_wait_limit_ns(limit_ns: int) -> None:
+    _check("mfsdp_set_wait_limit_ns", _lib.load().mfsdp_set_wait_limit_ns(limit_ns))
+
+
+def mfsdp_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check("mfsdp_selftest_wait_timeout",
+           _lib.load().mfsdp_selftest_wait_timeout(limit_ns, _stream(stream)))

@@ -1,0 +1,150 @@
+"""Host-side tests of libmfsdp (CPU only): exported symbols, the C++ owner planner against the
+oracle planner (bit-exact), argument validation and error codes.  Nothing here launches GPU
+work."""
+
+import ctypes as C
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from oracle import plan as oplan
+from workloads import get_config
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from matrix_optimizer_owner_gb300 import _lib
+    if not os.path.exists(_lib.LIB_PATH):
+        from matrix_optimizer_owner_gb300 import build
+        build.build()
+    return _lib.load()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "mfsdp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mfsdp_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from matrix_optimizer_owner_gb300 import _lib
+    names = header_functions()
+    assert len(names) >= 14
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)$", out, flags=re.M))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert getattr(lib, n) is not None
+    # the binding describes every declared entry point
+    assert set(names) == set(_lib.SIGNATURES)
+
+
+def test_version_and_status_strings(lib):
+    from matrix_optimizer_owner_gb300 import mfsdp
+    assert mfsdp.mfsdp_version() == 100
+    assert mfsdp.mfsdp_status_string(-7) == "device wait timed out"
+    assert mfsdp.mfsdp_status_string(12345) == "unknown status"
+
+
+def _params(wl):
+    return [(p.rows, p.cols, p.block, p.is_matrix) for p in wl.params]
+
+
+def _oracle(params, W, policy):
+    ps = [oplan.Param(r, c, b, m) for r, c, b, m in params]
+    segs = oplan.plan(ps, W, policy)
+    brn = oplan.block_rank_numel(ps, segs, W)
+    table = [[brn[(b, r)] for r in range(W)] for b in oplan.block_order(ps)]
+    return [{"owner": s.owner, "role": s.role, "local_offset": s.local_offset,
+             "rank_offset": s.rank_offset, "numel": s.numel} for s in segs], table
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("policy", [0, 1])
+def test_planner_bit_exact_on_workloads(lib, cfg, policy):
+    from matrix_optimizer_owner_gb300 import mfsdp
+    wl = get_config(cfg)
+    params = _params(wl)
+    for W in sorted({1, 2, 3, 8, wl.world_size}):
+        segs, table, nb = mfsdp.mfsdp_plan_owner_set(params, W, policy)
+        osegs, otable = _oracle(params, W, policy)
+        assert segs == osegs
+        assert table == otable and nb == len(otable)
+
+
+def test_planner_bit_exact_on_random_sets(lib):
+    from matrix_optimizer_owner_gb300 import mfsdp
+    rng = np.random.default_rng(123)
+    for trial in range(300):
+        n = int(rng.integers(0, 30))
+        params = []
+        for _ in range(n):
+            is_mat = bool(rng.random() < 0.6)
+            r = int(rng.integers(0, 9))
+            c = int(rng.integers(0, 9)) if is_mat else 1
+            params.append((r, c, int(rng.integers(0, 5)), is_mat))
+        W = int(rng.integers(1, 6))
+        for policy in (0, 1):
+            segs, table, nb = mfsdp.mfsdp_plan_owner_set(params, W, policy)
+            osegs, otable = _oracle(params, W, policy)
+            assert segs == osegs, (trial, params, W, policy)
+            assert table == otable
+
+
+def test_planner_error_codes(lib):
+    from matrix_optimizer_owner_gb300 import _lib as L
+    pd = (L.ParamDesc * 1)(L.ParamDesc(2, 2, 0, 1))
+    seg = (L.Segment * 1)()
+    assert lib.mfsdp_plan_owner_set(pd, 1, 0, 0, seg, None, None) == -1      # world size
+    assert lib.mfsdp_plan_owner_set(pd, 1, 2, 7, seg, None, None) == -1      # policy
+    assert lib.mfsdp_plan_owner_set(None, 1, 2, 0, seg, None, None) == -1    # null params
+    bad = (L.ParamDesc * 1)(L.ParamDesc(-1, 2, 0, 1))
+    assert lib.mfsdp_plan_owner_set(bad, 1, 2, 0, seg, None, None) == -2     # negative dim
+    huge = (L.ParamDesc * 1)(L.ParamDesc(1 << 40, 1 << 40, 0, 1))
+    assert lib.mfsdp_plan_owner_set(huge, 1, 2, 0, seg, None, None) == -2    # numel overflow
+    assert lib.mfsdp_plan_owner_set(None, 0, 2, 0, None, None, None) == 0    # empty model
+
+
+def test_owner_set_validation_and_workspace(lib):
+    from matrix_optimizer_owner_gb300 import mfsdp
+    s = mfsdp.OwnerSet([(64, 64, 0), (64, 256, 4096), (256, 64, 20480), (128, 128, 36864)],
+                       split_max_numel=32768)
+    assert s.split_count() == 4
+    ws = s.workspace_bytes()
+    assert ws > 0 and ws % 256 == 0
+    big = mfsdp.OwnerSet([(2304, 768, 0)], split_max_numel=0)
+    assert big.split_count() == 0
+    # m x m Gram + polynomial buffers and the ping X buffer are in the workspace
+    assert big.workspace_bytes() >= 2304 * 768 * 2 + 2 * 768 * 768 * 2
+    with pytest.raises(mfsdp.MfsdpError) as e:
+        mfsdp.OwnerSet([(4, 4, 0), (4, 4, 8)])                         # overlapping ranges
+    assert e.value.status == -2
+    with pytest.raises(mfsdp.MfsdpError) as e:
+        mfsdp.OwnerSet([(-4, 4, 0)])
+    assert e.value.status == -2
+    empty = mfsdp.OwnerSet([])
+    assert empty.workspace_bytes() > 0
+    # step calls on an unbound set are rejected before anything is launched
+    nul = C.c_void_p(0)
+    ptrs = (C.c_void_p * 1)(256)
+    assert lib.mfsdp_owner_reduce_momentum(s.handle, ptrs, 1, 1, 1.0, 0.9, 1, 256, 512, 768,
+                                           None, 1024, nul) == -1
+    assert lib.mfsdp_newton_schulz(s.handle, 256, 512, 1024, 5, 3.4, -4.7, 2.0, 1e-7, 768, 1024,
+                                   nul) == -1
+    assert lib.mfsdp_apply_update(s.handle, 256, 512, None, 0.02, 0.01, 0, nul) == -1
+    # AdamW argument checks (no launch: they fail first)
+    assert lib.mfsdp_adamw_tail(ptrs, 1, 1, 1.0, 16, 256, 512, 768, 0, 1e-3, 0.9, 0.95, 1e-8,
+                                0.01, nul) == -1                         # step 0
+    assert lib.mfsdp_adamw_tail(ptrs, 0, 1, 1.0, 16, 256, 512, 768, 1, 1e-3, 0.9, 0.95, 1e-8,
+                                0.01, nul) == -1                         # W = 0
+    assert lib.mfsdp_adamw_tail(ptrs, 1, 1, 1.0, 16, 258, 512, 768, 1, 1e-3, 0.9, 0.95, 1e-8,
+                                0.01, nul) == -3                         # misaligned
+    assert lib.mfsdp_adamw_tail(ptrs, 1, 1, 1.0, 0, 0, 0, 0, 1, 1e-3, 0.9, 0.95, 1e-8,
+                                0.01, nul) == 0                          # empty tail
