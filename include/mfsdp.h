@@ -216,6 +216,46 @@ int mfsdp_adamw_tail(const void* const* contrib, int32_t W, int32_t contrib_dtyp
                      float eps, float weight_decay, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Gradient deposit without any allocation.  The paper has no counterpart to this call; it
+ * exists for callers of this library that cannot allocate device memory: code running under
+ * another system's memory manager (a framework or serving runtime that owns all device memory
+ * and gives extensions no cudaMalloc), and processes that reserve memory once at start-up and
+ * must not allocate on the step path.  They cannot provide the workspace of
+ * mfsdp_owner_set_bind.
+ * ------------------------------------------------------------------------------------------ */
+
+#define MFSDP_NOALLOC_SCRATCH_BYTES (4u << 20) /* fixed per-device scratch, held until exit */
+#define MFSDP_NOALLOC_MAX_MATRICES 4096
+
+/*
+ * Same computation and outputs as mfsdp_owner_reduce_momentum, for the matrices of the host
+ * table `mats` [n_mats] (as in mfsdp_owner_set_create: rows, cols, element offset into the
+ * flat buffers; ranges must not overlap).  Matrices with 0 < rows*cols <= split_max_numel
+ * also get the low bf16 half in ns_input_lo (nullable: then no low half is written).  Needs no
+ * owner set and no workspace: its scratch — the matrix table and one fp32 norm partial per
+ * 16384 elements — lives in a fixed MFSDP_NOALLOC_SCRATCH_BYTES array in the library's own
+ * device memory, and the call allocates nothing (no cudaMalloc / cudaFree, no allocating
+ * library routine, no host heap).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture begins.
+ *   - All calls on a device share the one array, and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero (every call rewrites the table, and each partial
+ *     is written before it is read).  Calls whose work overlaps on the GPU — in different
+ *     streams, or from different host threads — race on the array and give wrong results;
+ *     order them on one stream.
+ * Limits: n_mats <= MFSDP_NOALLOC_MAX_MATRICES and sum_i ceil(rows_i*cols_i / 16384) <=
+ * (MFSDP_NOALLOC_SCRATCH_BYTES - MFSDP_NOALLOC_MAX_MATRICES*48) / 4 (about 16.4e9 elements);
+ * larger problems return MFSDP_EWORKSPACE before anything is enqueued.
+ * Other errors as mfsdp_owner_reduce_momentum.
+ */
+int mfsdp_owner_reduce_momentum_noalloc(const mfsdp_matrix* mats, int32_t n_mats,
+                                        int64_t split_max_numel, const void* const* contrib,
+                                        int32_t W, int32_t contrib_dtype, float grad_scale,
+                                        float momentum, int32_t nesterov, float* momentum_buf,
+                                        void* ns_input, void* ns_input_lo,
+                                        float* reduced_grad_out, float* norm_out, void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * Status and diagnostics.
  * ------------------------------------------------------------------------------------------ */
 

@@ -51,6 +51,9 @@ SIGNATURES = {
     "mfsdp_apply_update": (C.c_int, [_vp, _vp, _vp, _vp, _f32, _f32, _i32, _vp]),
     "mfsdp_adamw_tail": (C.c_int, [C.POINTER(_vp), _i32, _i32, _f32, _i64, _vp, _vp, _vp, _i64,
                                    _f32, _f32, _f32, _f32, _f32, _vp]),
+    "mfsdp_owner_reduce_momentum_noalloc": (C.c_int, [C.POINTER(Matrix), _i32, _i64,
+                                                      C.POINTER(_vp), _i32, _i32, _f32, _f32,
+                                                      _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mfsdp_query_status": (C.c_int, [_vp, C.POINTER(_i32)]),
     "mfsdp_status_string": (C.c_char_p, [C.c_int]),
     "mfsdp_set_wait_limit_ns": (C.c_int, [_u64]),
