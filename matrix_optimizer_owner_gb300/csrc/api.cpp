@@ -49,6 +49,7 @@ struct mfsdp_owner_set_s {
   int32_t total_ctas = 0;
   int32_t n_split = 0;
   bool any_unaligned = false;
+  bool offsets_aligned = true;      // every matrix offset is a multiple of 8 elements
   std::vector<NsTile> tiles[3][2];  // [phase][split]
   size_t off_devmats = 0, off_partials = 0, off_maps = 0, off_probs = 0, off_tiles = 0;
   size_t tile_off[3][2] = {};
@@ -119,9 +120,9 @@ int check_device(const mfsdp_owner_set* set) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA; }
 
-
-
 }  // namespace
+
+uint64_t mfsdp::wait_limit_ns() { return g_wait_limit_ns.load(); }
 
 extern "C" {
 
@@ -184,6 +185,7 @@ int mfsdp_owner_set_create(const mfsdp_matrix* mats, int32_t n_mats, int64_t spl
     }
     s->n_split += mi.split;
     if (mi.numel > 0 && !mi.aligned) s->any_unaligned = true;
+    if (mi.numel > 0 && q.offset % 8 != 0) s->offsets_aligned = false;
   }
   s->total_ctas = (int32_t)ctas;
   // Ranges must not overlap.
@@ -467,6 +469,9 @@ int mfsdp_owner_reduce_momentum(const mfsdp_owner_set* set, const void* const* c
   p.n_mats = (int32_t)set->mats.size();
   p.total_ctas = set->total_ctas;
   p.nesterov = nesterov ? 1 : 0;
+  p.offsets_aligned = set->offsets_aligned ? 1 : 0;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.status = set->status;
   p.mats = reinterpret_cast<const DevMat*>(set->ws + set->off_devmats);
   p.grad_scale = grad_scale;
   p.mu = momentum;

@@ -34,12 +34,28 @@ struct ContribPtrs {
   const void* p[kMaxContrib];
 };
 
+constexpr int kMaxBulkStages = 8;
+constexpr size_t kBulkStageBudget = 48 * 1024;   // bytes of one bulk-copy stage
+constexpr size_t kBulkSmemBudget = 192 * 1024;   // bytes of all stages of one CTA
+
+struct BulkCfg {           // bulk-copy pipeline shape of the deposit kernel
+  int32_t sub_elems;       // elements per stage
+  int32_t stage_bytes;
+  int32_t stages;
+  int32_t pad_;
+  uint64_t wait_limit_ns;
+};
+
 struct ReduceParams {
   ContribPtrs contrib;
   int32_t W;
   int32_t n_mats;
   int32_t total_ctas;
   int32_t nesterov;
+  int32_t offsets_aligned;  // every matrix offset is a multiple of 8 elements
+  int32_t pad_;
+  uint64_t wait_limit_ns;
+  int* status;
   const DevMat* mats;
   float grad_scale, mu, one_minus_mu;
   float* momentum;
@@ -97,12 +113,13 @@ cudaError_t launch_adamw(const AdamParams& p, int contrib_dtype, cudaStream_t s)
 cudaError_t launch_copy2d(const CopyParams& p, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int* status, cudaStream_t s);
 int* status_word_address();  // device address of this device's status word (nullptr on error)
+uint64_t wait_limit_ns();    // limit of every bounded device-side wait (mfsdp_set_wait_limit_ns)
 
 // ---- Newton–Schulz grouped GEMM (tcgen05 / TMEM / TMA) ------------------------------------
 constexpr int kBM = 128;   // tile rows    = UMMA M (one CTA, TMEM lanes 0..127)
 constexpr int kBN = 256;   // tile columns = UMMA N
 constexpr int kBK = 64;    // k per pipeline stage = one 128-byte swizzle atom of bf16
-constexpr int kNsThreads = 192;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+constexpr int kNsThreads = 320;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2-9 epilogue
 
 enum NsKind : int32_t { kGram = 0, kPoly = 1, kApply = 2 };
 

@@ -130,6 +130,11 @@ extern "C" int mfsdp_owner_reduce_momentum_noalloc(
   p.n_mats = n_mats;
   p.total_ctas = cta;
   p.nesterov = nesterov ? 1 : 0;
+  p.offsets_aligned = 1;
+  for (int32_t i = 0; i < n_mats; ++i)
+    if (mats[i].rows * mats[i].cols > 0 && mats[i].offset % 8 != 0) p.offsets_aligned = 0;
+  p.wait_limit_ns = wait_limit_ns();
+  p.status = status;
   p.mats = table;
   p.grad_scale = grad_scale;
   p.mu = momentum;

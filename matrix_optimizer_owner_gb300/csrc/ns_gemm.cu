@@ -9,12 +9,12 @@
 // A launch runs one phase for every owned matrix: a static list of 128 x 256 output tiles,
 // taken round-robin by a persistent grid of one CTA per SM.
 //
-// CTA roles (192 threads):
+// CTA roles (320 threads):
 //   warp 0 (one lane)  TMA producer: 64 x 64 bf16 boxes, 128-byte swizzle, into a ring of
 //                      pipeline stages guarded by full/empty mbarriers;
 //   warp 1 (one lane)  MMA issuer: tcgen05.mma kind::f16 (M=128, N=256, K=16) from shared-
 //                      memory descriptors into one of two TMEM accumulators (2 x 256 columns);
-//   warps 2-5          epilogue: tcgen05.ld rows of the accumulator, out = alpha*acc + beta*D,
+//   warps 2-9          epilogue: tcgen05.ld rows of the accumulator, out = alpha*acc + beta*D,
 //                      round to bf16 (and the low half in split mode), store; symmetric tiles
 //                      store the upper triangle and its mirror.
 // Operands come from row-major bf16 buffers.  A "K-major" operand has the contraction index
@@ -35,6 +35,9 @@ constexpr uint32_t kBoxBytes = 64 * 64 * 2;               // one 64 x 64 bf16 TM
 constexpr uint32_t kABytes = kBM * kBK * 2;               // 16 KB
 constexpr uint32_t kBBytes = kBN * kBK * 2;               // 32 KB
 constexpr uint32_t kTmemCols = 2 * kBN;                   // two fp32 accumulators
+constexpr int kEpiWarps = (kNsThreads / 32) - 2;          // epilogue warps: 2 per lane quarter
+constexpr int kEpiChunks = (kBN / 32) / (kEpiWarps / 4);  // 32-column chunks per epilogue warp
+static_assert(kEpiWarps == 8 && kEpiChunks == 4, "epilogue layout");
 
 template <bool SPLIT>
 struct Cfg {
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar(tfull0 + a), 1);
-      mbar_init(bar(tempty0 + a), 4);
+      mbar_init(bar(tempty0 + a), kEpiWarps);
     }
     mbar_init(bar(drain), 1);
     *abort_flag = 0;
@@ -355,45 +358,76 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
     mbar_wait(bar(drain), 0u, g, false);
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 are this warp's rows
+    // Two warps per TMEM lane quarter: warps 2-5 take columns 0-127 of the tile, warps 6-9
+    // columns 128-255.  The addend rows D of a tile are loaded into registers before the wait
+    // for its accumulator, so their latency overlaps the tile's main loop.
+    const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31 are this warp's rows
+    const int c_first = ((warp - 2) >> 2) * kEpiChunks;  // first 32-column chunk of this warp
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
       const NsTile tile = P.tiles[t];
       const NsProblem& pr = P.probs[tile.prob];
+      const int M = pr.M, N = pr.N, kind = pr.kind, sym = pr.sym;
+      const int m0 = tile.tm * kBM, n0 = tile.tn * kBN;
+      const int rw = m0 + quarter * 32;  // first row of this warp
+      const int r = rw + lane;
+      const bool rvalid = r < M;
+      const float s = 1.f / (P.norm[pr.mat] + P.eps);
+      uint4 dpre[kEpiChunks][4];
+      if (!SPLIT && kind != kGram && rvalid) {
+#pragma unroll
+        for (int q = 0; q < kEpiChunks; ++q) {
+          const int c0 = n0 + (c_first + q) * 32;
+          if (c0 + 32 <= N && !(sym && c0 + 31 < rw)) {
+            const uint4* src = reinterpret_cast<const uint4*>(pr.d_hi + (int64_t)r * pr.ldd + c0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dpre[q][k] = src[k];
+          }
+        }
+      }
       if (!mbar_wait(bar(tfull0 + acc), acc_phase, g)) break;
       tc_fence_after();
       float alpha = 1.f, beta = 0.f;
-      const float s = 1.f / (P.norm[pr.mat] + P.eps);
-      if (pr.kind == kGram) {
+      if (kind == kGram) {
         alpha = pr.first ? s * s : 1.f;
-      } else if (pr.kind == kPoly) {
+      } else if (kind == kPoly) {
         alpha = P.c;
         beta = P.b;
       } else {
         alpha = pr.first ? s : 1.f;
         beta = P.a * alpha;
       }
-      const int m0 = tile.tm * kBM, n0 = tile.tn * kBN;
-      const int rw = m0 + quarter * 32;  // first row of this warp
-      const int r = rw + lane;
-      const bool rvalid = r < pr.M;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
-      for (int cc = 0; cc < kBN / 32; ++cc) {
+#pragma unroll
+      for (int q = 0; q < kEpiChunks; ++q) {
+        const int cc = c_first + q;
         const int c0 = n0 + cc * 32;
-        if (c0 >= pr.N || rw >= pr.M) break;           // warp-uniform
-        if (pr.sym && c0 + 31 < rw) continue;          // chunk entirely below the diagonal
+        if (c0 >= N || rw >= M) break;                 // warp-uniform
+        if (sym && c0 + 31 < rw) continue;             // chunk entirely below the diagonal
         float v[32];
         tc_ld32(taddr + (uint32_t)(cc * 32), v);
         if (!rvalid) continue;
         if (beta != 0.f) {
           float d[32];
-          load_row32(pr.d_hi, pr.ldd, r, c0, pr.N, d);
-          if (SPLIT) {
-            float dl[32];
-            load_row32(pr.d_lo, pr.ldd, r, c0, pr.N, dl);
+          if (!SPLIT && c0 + 32 <= N) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) d[j] += dl[j];
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t w[4] = {dpre[q][k].x, dpre[q][k].y, dpre[q][k].z, dpre[q][k].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                d[8 * k + 2 * e] = bf_lo(w[e]);
+                d[8 * k + 2 * e + 1] = bf_hi(w[e]);
+              }
+            }
+          } else {
+            load_row32(pr.d_hi, pr.ldd, r, c0, N, d);
+            if (SPLIT) {
+              float dl[32];
+              load_row32(pr.d_lo, pr.ldd, r, c0, N, dl);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) d[j] += dl[j];
+            }
           }
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = fmaf(alpha, v[j], beta * d[j]);
@@ -407,14 +441,14 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
           h[j] = f2bf(v[j]);
           if (SPLIT) l[j] = f2bf(v[j] - bf2f(h[j]));
         }
-        const int cmin = pr.sym ? r : 0;  // symmetric: this row stores columns >= r ...
-        store_row32(pr.o_hi, pr.ldo, r, c0, cmin, pr.N, h);
-        if (SPLIT) store_row32(pr.o_lo, pr.ldo, r, c0, cmin, pr.N, l);
-        if (pr.sym && c0 + 31 > r) {      // ... and mirrors columns > r into row c, column r
+        const int cmin = sym ? r : 0;  // symmetric: this row stores columns >= r ...
+        store_row32(pr.o_hi, pr.ldo, r, c0, cmin, N, h);
+        if (SPLIT) store_row32(pr.o_lo, pr.ldo, r, c0, cmin, N, l);
+        if (sym && c0 + 31 > r) {      // ... and mirrors columns > r into row c, column r
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int c = c0 + j;
-            if (c > r && c < pr.N) {
+            if (c > r && c < N) {
               pr.o_hi[(int64_t)c * pr.ldo + r] = h[j];
               if (SPLIT) pr.o_lo[(int64_t)c * pr.ldo + r] = l[j];
             }

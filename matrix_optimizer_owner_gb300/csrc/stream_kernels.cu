@@ -33,29 +33,6 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
-// Load 8 consecutive contribution elements as fp32.
-template <typename T>
-__device__ __forceinline__ void load8(const void* base, int64_t e, float (&x)[8]);
-
-template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const void* base, int64_t e, float (&x)[8]) {
-  const uint4 v = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + e));
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = bf16_bits_to_float(w[i] & 0xFFFFu);
-    x[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
-  }
-}
-
-template <>
-__device__ __forceinline__ void load8<float>(const void* base, int64_t e, float (&x)[8]) {
-  const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + e);
-  const float4 a = __ldcs(p), b = __ldcs(p + 1);
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-
 template <typename T>
 __device__ __forceinline__ float load1(const void* base, int64_t e);
 template <>
@@ -93,12 +70,101 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return s;  // valid in thread 0
 }
 
+// Raw 16-byte-aligned load of 8 contribution elements (one or two 16-byte vectors).
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+  uint4 v;
+  __device__ __forceinline__ void load(const void* base, int64_t e) {
+    v = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + e));
+  }
+  __device__ __forceinline__ void add_to(float (&g)[8]) const {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      g[2 * i] += bf16_bits_to_float(w[i] & 0xFFFFu);
+      g[2 * i + 1] += bf16_bits_to_float(w[i] >> 16);
+    }
+  }
+};
+template <>
+struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const void* base, int64_t e) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + e);
+    a = __ldcs(p);
+    b = __ldcs(p + 1);
+  }
+  __device__ __forceinline__ void add_to(float (&g)[8]) const {
+    g[0] += a.x; g[1] += a.y; g[2] += a.z; g[3] += a.w;
+    g[4] += b.x; g[5] += b.y; g[6] += b.z; g[7] += b.w;
+  }
+};
+
+// Momentum update, Nesterov input and the bf16 outputs of 8 consecutive elements at e, given
+// their deposited gradient g (before grad_scale) and old momentum m8; adds u^2 to ss.
+__device__ __forceinline__ void finish8(const ReduceParams& P, bool lo_out, int64_t e,
+                                        float (&g)[8], const float (&m8)[8], float& ss) {
+  const float gs = P.grad_scale, mu = P.mu, omm = P.one_minus_mu;
+  float bm[8], u[8];
+  uint32_t hb[4], lb[4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float gj = g[j] * gs;
+    g[j] = gj;
+    bm[j] = fmaf(mu, m8[j], omm * gj);
+    u[j] = P.nesterov ? fmaf(omm, gj, mu * bm[j]) : bm[j];
+    ss = fmaf(u[j], u[j], ss);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint16_t h0 = float_to_bf16_bits(u[2 * j]), h1 = float_to_bf16_bits(u[2 * j + 1]);
+    hb[j] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+    const uint16_t l0 = float_to_bf16_bits(u[2 * j] - bf16_bits_to_float(h0));
+    const uint16_t l1 = float_to_bf16_bits(u[2 * j + 1] - bf16_bits_to_float(h1));
+    lb[j] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+  }
+  float4* mp = reinterpret_cast<float4*>(P.momentum + e);
+  mp[0] = make_float4(bm[0], bm[1], bm[2], bm[3]);
+  mp[1] = make_float4(bm[4], bm[5], bm[6], bm[7]);
+  *reinterpret_cast<uint4*>(P.uhat + e) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+  if (lo_out) *reinterpret_cast<uint4*>(P.uhat_lo + e) = make_uint4(lb[0], lb[1], lb[2], lb[3]);
+  if (P.grad) {
+    float4* gp = reinterpret_cast<float4*>(P.grad + e);
+    gp[0] = make_float4(g[0], g[1], g[2], g[3]);
+    gp[1] = make_float4(g[4], g[5], g[6], g[7]);
+  }
+}
+
+// The same for one element (scalar tails and unaligned matrices).
+template <typename T>
+__device__ __forceinline__ void finish1(const ReduceParams& P, bool lo_out, int64_t e, float& ss) {
+  float g = 0.f;
+  for (int w = 0; w < P.W; ++w) g += load1<T>(P.contrib.p[w], e);
+  g *= P.grad_scale;
+  const float bm = fmaf(P.mu, P.momentum[e], P.one_minus_mu * g);
+  P.momentum[e] = bm;
+  const float u = P.nesterov ? fmaf(P.one_minus_mu, g, P.mu * bm) : bm;
+  const uint16_t h = float_to_bf16_bits(u);
+  P.uhat[e] = h;
+  if (lo_out) P.uhat_lo[e] = float_to_bf16_bits(u - bf16_bits_to_float(h));
+  if (P.grad) P.grad[e] = g;
+  ss = fmaf(u, u, ss);
+}
+
 // ------------------------------------------------------------------------------------------
-// Owner gradient deposit + Nesterov momentum + norm partials.
+// Owner gradient deposit + Nesterov momentum + norm partials, register path (used when some
+// matrix starts at an element offset that is not a multiple of 8).  One CTA per chunk of
+// kChunk elements; passes of kPassVecs 8-element vectors per thread with the contribution loop
+// unrolled by kUnrollW, so kPassVecs x kUnrollW independent 16-byte loads are in flight.
+// Contributions are summed in index order w = 0, 1, ... for every element.
 // ------------------------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(kStreamThreads)
+__global__ void __launch_bounds__(kStreamThreads, 2)
 reduce_momentum_kernel(const __grid_constant__ ReduceParams P) {
+  constexpr int kPassVecs = 2;
+  constexpr int kUnrollW = sizeof(T) == 2 ? 4 : 2;
   __shared__ float red[kStreamThreads / 32];
   const int b = blockIdx.x;
   const int mi = find_matrix(P.mats, P.n_mats, b);
@@ -106,91 +172,229 @@ reduce_momentum_kernel(const __grid_constant__ ReduceParams P) {
   const int64_t start = (int64_t)(b - dm.cta_begin) * kChunk;
   const int64_t cnt = min((int64_t)kChunk, dm.numel - start);
   const int64_t base = dm.offset + start;
-  const float gs = P.grad_scale, mu = P.mu, omm = P.one_minus_mu;
   const bool lo_out = dm.split && P.uhat_lo != nullptr;
+  const int W = P.W;
   float ss = 0.f;
-
-  auto one = [&](float g, int64_t e) {
-    g *= gs;
-    const float bm = fmaf(mu, P.momentum[e], omm * g);
-    P.momentum[e] = bm;
-    const float u = P.nesterov ? fmaf(omm, g, mu * bm) : bm;
-    const uint16_t h = float_to_bf16_bits(u);
-    P.uhat[e] = h;
-    if (lo_out) P.uhat_lo[e] = float_to_bf16_bits(u - bf16_bits_to_float(h));
-    if (P.grad) P.grad[e] = g;
-    ss = fmaf(u, u, ss);
-  };
-
   int64_t done = 0;
   if ((base & 7) == 0) {
     const int64_t nvec = cnt / kVec;
-    for (int64_t v0 = 0; v0 < nvec; v0 += (int64_t)kStreamThreads * kVecsPerThread) {
-      float g[kVecsPerThread][8];
+    for (int64_t v0 = 0; v0 < nvec; v0 += (int64_t)kStreamThreads * kPassVecs) {
+      int64_t ev[kPassVecs];
+      bool ok[kPassVecs];
 #pragma unroll
-      for (int i = 0; i < kVecsPerThread; ++i)
+      for (int i = 0; i < kPassVecs; ++i) {
+        const int64_t v = v0 + (int64_t)i * kStreamThreads + threadIdx.x;
+        ok[i] = v < nvec;
+        ev[i] = base + (ok[i] ? v : 0) * kVec;
+      }
+      float g[kPassVecs][8];
+#pragma unroll
+      for (int i = 0; i < kPassVecs; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) g[i][j] = 0.f;
-      for (int w = 0; w < P.W; ++w) {
-        const void* cw = P.contrib.p[w];
+      int w = 0;
+      for (; w + kUnrollW <= W; w += kUnrollW) {
+        Raw8<T> raw[kUnrollW][kPassVecs];
 #pragma unroll
-        for (int i = 0; i < kVecsPerThread; ++i) {
-          const int64_t v = v0 + (int64_t)i * kStreamThreads + threadIdx.x;
-          if (v < nvec) {
-            float x[8];
-            load8<T>(cw, base + v * kVec, x);
+        for (int u = 0; u < kUnrollW; ++u)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) g[i][j] += x[j];
+          for (int i = 0; i < kPassVecs; ++i)
+            if (ok[i]) raw[u][i].load(P.contrib.p[w + u], ev[i]);
+#pragma unroll
+        for (int u = 0; u < kUnrollW; ++u)
+#pragma unroll
+          for (int i = 0; i < kPassVecs; ++i)
+            if (ok[i]) raw[u][i].add_to(g[i]);
+      }
+      for (; w < W; ++w) {
+#pragma unroll
+        for (int i = 0; i < kPassVecs; ++i)
+          if (ok[i]) {
+            Raw8<T> raw;
+            raw.load(P.contrib.p[w], ev[i]);
+            raw.add_to(g[i]);
           }
-        }
       }
 #pragma unroll
-      for (int i = 0; i < kVecsPerThread; ++i) {
-        const int64_t v = v0 + (int64_t)i * kStreamThreads + threadIdx.x;
-        if (v >= nvec) continue;
-        const int64_t e = base + v * kVec;
-        float4* mp = reinterpret_cast<float4*>(P.momentum + e);
+      for (int i = 0; i < kPassVecs; ++i) {
+        if (!ok[i]) continue;
+        const float4* mp = reinterpret_cast<const float4*>(P.momentum + ev[i]);
         const float4 m0 = mp[0], m1 = mp[1];
-        const float mo[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-        float bm[8], u[8];
-        uint32_t hb[4], lb[4];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float gj = g[i][j] * gs;
-          g[i][j] = gj;
-          bm[j] = fmaf(mu, mo[j], omm * gj);
-          u[j] = P.nesterov ? fmaf(omm, gj, mu * bm[j]) : bm[j];
-          ss = fmaf(u[j], u[j], ss);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint16_t h0 = float_to_bf16_bits(u[2 * j]), h1 = float_to_bf16_bits(u[2 * j + 1]);
-          hb[j] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-          const uint16_t l0 = float_to_bf16_bits(u[2 * j] - bf16_bits_to_float(h0));
-          const uint16_t l1 = float_to_bf16_bits(u[2 * j + 1] - bf16_bits_to_float(h1));
-          lb[j] = (uint32_t)l0 | ((uint32_t)l1 << 16);
-        }
-        mp[0] = make_float4(bm[0], bm[1], bm[2], bm[3]);
-        mp[1] = make_float4(bm[4], bm[5], bm[6], bm[7]);
-        *reinterpret_cast<uint4*>(P.uhat + e) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
-        if (lo_out) *reinterpret_cast<uint4*>(P.uhat_lo + e) = make_uint4(lb[0], lb[1], lb[2], lb[3]);
-        if (P.grad) {
-          float4* gp = reinterpret_cast<float4*>(P.grad + e);
-          gp[0] = make_float4(g[i][0], g[i][1], g[i][2], g[i][3]);
-          gp[1] = make_float4(g[i][4], g[i][5], g[i][6], g[i][7]);
-        }
+        const float m8[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        finish8(P, lo_out, ev[i], g[i], m8, ss);
       }
     }
     done = nvec * kVec;
   }
-  for (int64_t k = done + threadIdx.x; k < cnt; k += kStreamThreads) {  // scalar remainder
-    const int64_t e = base + k;
-    float g = 0.f;
-    for (int w = 0; w < P.W; ++w) g += load1<T>(P.contrib.p[w], e);
-    one(g, e);
-  }
+  for (int64_t k = done + threadIdx.x; k < cnt; k += kStreamThreads)  // scalar remainder
+    finish1<T>(P, lo_out, base + k, ss);
   const float tot = block_sum(ss, red);
   if (threadIdx.x == 0) P.partials[b] = tot;
+}
+
+// ------------------------------------------------------------------------------------------
+// Owner gradient deposit + Nesterov momentum + norm partials, bulk-copy path.
+// A persistent grid walks the same per-matrix chunk partition (chunk c = CTA c of the
+// partition; CTA b takes chunks b, b + grid, ...).  Each chunk is split into sub-chunks of
+// E elements; thread 0 streams every sub-chunk's W contribution slices and momentum slice
+// into a ring of shared-memory stages with cp.async.bulk (completion counted on one mbarrier
+// per stage) several stages ahead, and all 256 threads consume a stage from shared memory and
+// write the new momentum and the bf16 NS input straight to global memory.  A chunk is always
+// processed by one CTA with the same element-to-thread mapping, so its norm partial does not
+// depend on the grid size.  Waits are bounded; on expiry the kernel records a timeout, stops
+// issuing, drains its copies in flight and exits.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ bool bulk_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ bool bulk_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns, int* status,
+                          volatile int* abort_flag, bool honor_abort) {
+  if (bulk_try_wait(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t i = 1;; ++i) {
+    if (bulk_try_wait(bar, parity)) return true;
+    if ((i & 31) == 0) {
+      if (honor_abort && *abort_flag) return false;
+      if (gtimer() - t0 > limit_ns) {
+        atomicOr(status, kStatusTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+reduce_momentum_bulk_kernel(const __grid_constant__ ReduceParams P,
+                            const __grid_constant__ BulkCfg C) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  __shared__ float red[kStreamThreads / 32];
+  __shared__ int abort_flag;
+  __shared__ __align__(8) uint64_t full[kMaxBulkStages];
+  const int tid = threadIdx.x;
+  const int W = P.W, E = C.sub_elems, S = C.stages;
+  const uint32_t cbytes = (uint32_t)sizeof(T);
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(sm);
+  auto fbar = [&](int s) { return (uint32_t)__cvta_generic_to_shared(&full[s]); };
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(fbar(s)), "r"(1u));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    abort_flag = 0;
+  }
+  __syncthreads();
+
+  // Producer cursor (thread 0): the next (chunk, sub-chunk) to fetch.
+  int pc = blockIdx.x, psub = 0, issued = 0;
+  uint32_t armed = 0, last_parity = 0;
+  auto issue_next = [&]() {
+    if (pc >= P.total_ctas) return;
+    const int mi = find_matrix(P.mats, P.n_mats, pc);
+    const DevMat dm = P.mats[mi];
+    const int64_t rel0 = (int64_t)(pc - dm.cta_begin) * kChunk;
+    const int64_t ccnt = min((int64_t)kChunk, dm.numel - rel0);
+    const int64_t e0 = dm.offset + rel0 + (int64_t)psub * E;
+    const int n = (int)min((int64_t)E, ccnt - (int64_t)psub * E);
+    const int n8 = n & ~7;
+    const int st = issued % S;
+    const uint32_t bar = fbar(st);
+    const uint32_t dst = sbase + (uint32_t)st * C.stage_bytes;
+    const uint32_t bytes = (uint32_t)n8 * (cbytes * W + 4u);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+    if (n8 > 0) {
+      for (int w = 0; w < W; ++w)
+        bulk_copy(dst + (uint32_t)(w * E) * cbytes,
+                  static_cast<const uint8_t*>(P.contrib.p[w]) + e0 * cbytes,
+                  (uint32_t)n8 * cbytes, bar);
+      bulk_copy(dst + (uint32_t)(W * E) * cbytes, P.momentum + e0, (uint32_t)n8 * 4u, bar);
+    }
+    armed |= 1u << st;
+    last_parity = (last_parity & ~(1u << st)) | ((uint32_t)((issued / S) & 1) << st);
+    ++issued;
+    if ((int64_t)(++psub) * E >= ccnt) {
+      psub = 0;
+      pc += gridDim.x;
+    }
+  };
+  if (tid == 0)
+    for (int k = 0; k < S - 1; ++k) issue_next();
+
+  float ss = 0.f;
+  int q = 0;  // consumer sub-chunk counter
+  bool stop = false;
+  for (int c = blockIdx.x; c < P.total_ctas && !stop; c += gridDim.x) {
+    const int mi = find_matrix(P.mats, P.n_mats, c);
+    const DevMat dm = P.mats[mi];
+    const int64_t rel0 = (int64_t)(c - dm.cta_begin) * kChunk;
+    const int64_t ccnt = min((int64_t)kChunk, dm.numel - rel0);
+    const int64_t cbase = dm.offset + rel0;
+    const bool lo_out = dm.split && P.uhat_lo != nullptr;
+    for (int64_t sub0 = 0; sub0 < ccnt; sub0 += E, ++q) {
+      if (tid == 0) issue_next();  // stage (q + S - 1) % S was freed by the last barrier
+      const int st = q % S;
+      const bool ok = bulk_wait(fbar(st), (uint32_t)((q / S) & 1), C.wait_limit_ns, P.status,
+                                &abort_flag, true);
+      if (__syncthreads_or(!ok)) { stop = true; break; }
+      const int n = (int)min((int64_t)E, ccnt - sub0);
+      const int n8 = n & ~7;
+      const int64_t e0 = cbase + sub0;
+      const uint8_t* stage = sm + (size_t)st * C.stage_bytes;
+      const float4* mo = reinterpret_cast<const float4*>(stage + (size_t)(W * E) * cbytes);
+      for (int v = tid; v < (n8 >> 3); v += kStreamThreads) {
+        float g[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int w = 0; w < W; ++w) {
+          const uint8_t* cw = stage + (size_t)(w * E) * cbytes;
+          Raw8<T> r;
+          if (sizeof(T) == 2) {
+            reinterpret_cast<uint4*>(&r)[0] = reinterpret_cast<const uint4*>(cw)[v];
+          } else {
+            reinterpret_cast<float4*>(&r)[0] = reinterpret_cast<const float4*>(cw)[2 * v];
+            reinterpret_cast<float4*>(&r)[1] = reinterpret_cast<const float4*>(cw)[2 * v + 1];
+          }
+          r.add_to(g);
+        }
+        const float4 m0 = mo[2 * v], m1 = mo[2 * v + 1];
+        const float m8[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        finish8(P, lo_out, e0 + (int64_t)v * 8, g, m8, ss);
+      }
+      if (tid < n - n8) finish1<T>(P, lo_out, e0 + n8 + tid, ss);  // last < 8 elements
+      __syncthreads();  // every thread is done with the stage: the producer may refill it
+    }
+    if (stop) break;
+    const float tot = block_sum(ss, red);
+    if (tid == 0) P.partials[c] = tot;
+    ss = 0.f;
+    __syncthreads();
+  }
+  // every copy this CTA issued has landed before it exits
+  if (tid == 0)
+    for (int s = 0; s < S; ++s)
+      if (armed & (1u << s))
+        bulk_wait(fbar(s), (last_parity >> s) & 1u, C.wait_limit_ns, P.status, &abort_flag, false);
 }
 
 // One CTA per matrix: nu = sqrt(sum of its CTA partials), summed in fp64 in index order.
@@ -343,11 +547,42 @@ int grid_for(int64_t n, int threads, int cap) {
 
 cudaError_t launch_reduce_momentum(const ReduceParams& p, int contrib_dtype, cudaStream_t s) {
   if (p.total_ctas <= 0) return cudaSuccess;
-  if (contrib_dtype == 1)
-    reduce_momentum_kernel<__nv_bfloat16><<<p.total_ctas, kStreamThreads, 0, s>>>(p);
-  else
-    reduce_momentum_kernel<float><<<p.total_ctas, kStreamThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  if (!p.offsets_aligned) {
+    if (contrib_dtype == 1)
+      reduce_momentum_kernel<__nv_bfloat16><<<p.total_ctas, kStreamThreads, 0, s>>>(p);
+    else
+      reduce_momentum_kernel<float><<<p.total_ctas, kStreamThreads, 0, s>>>(p);
+    return cudaGetLastError();
+  }
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // Sub-chunk of E elements: the W contribution slices plus the momentum slice of one stage
+  // fit in kBulkStageBudget bytes; as many stages as fit in kBulkSmemBudget (2 to 8).
+  const int esz = contrib_dtype == 1 ? 2 : 4;
+  const int per_elem = p.W * esz + 4;
+  int E = (int)(kBulkStageBudget / per_elem) / 256 * 256;
+  E = E < 256 ? 256 : (E > 2048 ? 2048 : E);
+  BulkCfg c{};
+  c.sub_elems = E;
+  c.stage_bytes = E * per_elem;
+  const int stages = (int)(kBulkSmemBudget / c.stage_bytes);
+  c.stages = stages < 2 ? 2 : (stages > kMaxBulkStages ? kMaxBulkStages : stages);
+  c.wait_limit_ns = p.wait_limit_ns;
+  const size_t smem = (size_t)c.stages * c.stage_bytes;
+  const int grid = p.total_ctas < sms ? p.total_ctas : sms;
+  if (contrib_dtype == 1) {
+    e = cudaFuncSetAttribute(reduce_momentum_bulk_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+      reduce_momentum_bulk_kernel<__nv_bfloat16><<<grid, kStreamThreads, smem, s>>>(p, c);
+  } else {
+    e = cudaFuncSetAttribute(reduce_momentum_bulk_kernel<float>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) reduce_momentum_bulk_kernel<float><<<grid, kStreamThreads, smem, s>>>(p, c);
+  }
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 cudaError_t launch_norm_finalize(const NormParams& p, cudaStream_t s) {
