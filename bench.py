@@ -48,12 +48,24 @@ def load_peaks():
 
 
 # ----------------------------------------------------------------------------- workload
+def shapes_workload(spec: str):
+    """A custom owned set for profiling: "RxC,RxC,..." matrices, W = 8 bf16 contributions of
+    std 1e-3, no tail, the step's usual hyperparameters."""
+    from workloads.configs import ParamSpec, Workload as Wl
+    params = []
+    for i, tok in enumerate(spec.split(",")):
+        r, c = (int(v) for v in tok.lower().split("x"))
+        params.append(ParamSpec(f"m{i}", r, c, i, True))
+    return Wl(9, f"custom owned set {spec}, W=8 bf16", tuple(params), world_size=1, rank=0, W=8,
+              contrib_dtype="bf16", grad_std=1e-3)
+
+
 class Workload:
     """Owned set of one rank, its buffers, and seeded inputs drawn on the device."""
 
-    def __init__(self, cfg: int, owner_rank_shift: int, device):
+    def __init__(self, cfg: int, owner_rank_shift: int, device, shapes=None):
         from matrix_optimizer_owner_gb300 import owner_step
-        self.wl = wl = get_config(cfg)
+        self.wl = wl = get_config(cfg) if not shapes else shapes_workload(shapes)
         self.rank = (wl.rank + owner_rank_shift) % wl.world_size
         params = [(p.rows, p.cols, p.block, p.is_matrix) for p in wl.params]
         self.lay = lay = owner_step.owned_layout(params, wl.world_size, self.rank)
@@ -291,7 +303,7 @@ def run_ours(args, rank, world, local_rank):
     from matrix_optimizer_owner_gb300 import mfsdp
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    wb = Workload(args.config, rank, dev)
+    wb = Workload(args.config, rank, dev, args.shapes)
     stream = torch.cuda.current_stream()
     peaks, peak_src = load_peaks()
 
@@ -418,6 +430,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--shapes", default=None,
+                    help='custom owned set for profiling, e.g. "4096x14336,1024x4096"')
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-mats", type=int, default=2)

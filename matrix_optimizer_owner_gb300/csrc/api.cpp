@@ -18,7 +18,13 @@ using namespace mfsdp;
 namespace {
 
 constexpr int kSlotU = 0, kSlotP = 1, kSlotO = 2, kSlotA = 3, kSlotB = 4, kSlots = 5;
-constexpr int kMapsPerMatrix = 2 * kSlots;  // hi / lo per slot
+// Per slot and half (hi, lo): [2D 64x64 box, 2D 64x128 box, 3D 64x64x2 box].  64x64 boxes and
+// the 3D view serve MN-major operands (the 3D view, 64 elements x rows x 64-element chunks with a
+// 128-byte chunk stride, loads a 128-wide half-tile in one operation; it exists only when the
+// row length is a multiple of 64, so it never reaches past a row); 64x128 boxes load a 128-row
+// K-major half-tile.
+constexpr int kMapsPerHalf = 3;
+constexpr int kMapsPerMatrix = 2 * kMapsPerHalf * kSlots;
 constexpr int kGroupRows = 8;               // tile-row group of the rasterised tile order
 
 // Problem-array variants: which X buffer a phase reads and writes.
@@ -58,6 +64,7 @@ struct mfsdp_owner_set_s {
   bool bound = false;
   int device = -1;
   int num_sms = 0;
+  int pair_clusters = 0;            // co-resident CTA pairs of the pair kernel
   int* status = nullptr;
   char* ws = nullptr;
   const void* ns_input = nullptr;
@@ -82,14 +89,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D bf16 tensor map over a rows x cols row-major buffer of pitch ld elements: 64 x 64 boxes,
+// 2D bf16 tensor map over a rows x cols row-major buffer of pitch ld elements: 64 x box_rows boxes,
 // 128-byte swizzle, zero fill outside the tensor.
-bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+// 3D view of the same buffer for MN-major loads: (64 within a chunk, rows, cols / 64 chunks).
+bool encode_map3d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), 128};
+  cuuint32_t box[3] = {64, 64, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
+                uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -99,13 +121,14 @@ bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, 
 
 // Output tiles of one problem in a rasterised order: groups of kGroupRows tile-rows, each group
 // walked column by column, so the CTAs running at the same time share operand panels in L2.
-void add_tiles(std::vector<NsTile>& out, int32_t prob, int64_t M, int64_t N, bool sym) {
-  const int64_t tm_n = (M + kBM - 1) / kBM, tn_n = (N + kBN - 1) / kBN;
+void add_tiles(std::vector<NsTile>& out, int32_t prob, int64_t M, int64_t N, bool sym,
+               int64_t bm) {
+  const int64_t tm_n = (M + bm - 1) / bm, tn_n = (N + kBN - 1) / kBN;
   for (int64_t g0 = 0; g0 < tm_n; g0 += kGroupRows) {
     const int64_t g1 = std::min(tm_n, g0 + kGroupRows);
     for (int64_t tn = 0; tn < tn_n; ++tn)
       for (int64_t tm = g0; tm < g1; ++tm) {
-        if (sym && tm * kBM >= (tn + 1) * kBN) continue;  // entirely below the diagonal
+        if (sym && tm * bm >= (tn + 1) * kBN) continue;  // entirely below the diagonal
         out.push_back(NsTile{prob, (int32_t)tm, (int32_t)tn, 0});
       }
   }
@@ -212,11 +235,13 @@ int mfsdp_owner_set_create(const mfsdp_matrix* mats, int32_t n_mats, int64_t spl
     for (int32_t i : o) {
       const MatInfo& m = s->mats[i];
       if (m.numel == 0) continue;
+      // bf16 matrices run on CTA pairs (256-row tiles), split ones on single CTAs (128 rows)
       auto& dst = s->tiles[ph][m.split ? 1 : 0];
+      const int64_t bm = m.split ? kBM : kPairBM;
       if (ph < 2)
-        add_tiles(dst, i, m.m, m.m, true);
+        add_tiles(dst, i, m.m, m.m, true, bm);
       else
-        add_tiles(dst, i, m.tr ? m.n : m.m, m.tr ? m.m : m.n, false);
+        add_tiles(dst, i, m.tr ? m.n : m.m, m.tr ? m.m : m.n, false, bm);
     }
   }
 
@@ -294,6 +319,8 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
   if (prop.major != 10 || prop.minor != 3) return MFSDP_ENODEVICE;
   if (!encode_fn()) return MFSDP_ECUDA;
   if (ns_prepare_kernels() != cudaSuccess) return MFSDP_ECUDA;
+  const int pair_clusters = ns_pair_max_clusters(prop.multiProcessorCount);
+  if (pair_clusters < 1) return MFSDP_ECUDA;
   int* status = status_word_address();
   if (!status) return MFSDP_ECUDA;
 
@@ -329,6 +356,11 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
     return m.cols;
   };
 
+  // Whether a slot buffer has the 3D MN-major view (its row length is a multiple of 64).
+  auto view3d = [&](const MatInfo& m, int slot) -> bool {
+    return ((slot == kSlotA || slot == kSlotB) ? m.m : m.cols) % 64 == 0;
+  };
+
   // Tensor maps.
   std::vector<CUtensorMap> maps((size_t)kMapsPerMatrix * std::max(n, 1));
   std::memset(maps.data(), 0, maps.size() * sizeof(CUtensorMap));
@@ -338,8 +370,13 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
     for (int slot = 0; slot < kSlots; ++slot)
       for (int h = 0; h < (m.split ? 2 : 1); ++h) {
         const bool sq = slot == kSlotA || slot == kSlotB;
-        if (!encode_map(&maps[(size_t)i * kMapsPerMatrix + 2 * slot + h], slot_ptr(m, slot, h),
-                        sq ? m.m : m.rows, sq ? m.m : m.cols, slot_ld(m, slot)))
+        const int64_t rows = sq ? m.m : m.rows, cols = sq ? m.m : m.cols;
+        CUtensorMap* mp = &maps[(size_t)i * kMapsPerMatrix + 2 * kMapsPerHalf * slot + kMapsPerHalf * h];
+        if (!encode_map(mp, slot_ptr(m, slot, h), rows, cols, slot_ld(m, slot), 64u) ||
+            !encode_map(mp + 1, slot_ptr(m, slot, h), rows, cols, slot_ld(m, slot), 128u))
+          return MFSDP_ECUDA;
+        if (cols % 64 == 0 && !encode_map3d(mp + 2, slot_ptr(m, slot, h), rows, cols,
+                                            slot_ld(m, slot)))
           return MFSDP_ECUDA;
       }
   }
@@ -360,7 +397,8 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
       p.kind = kGram;
       p.first = first;
       p.mat = i;
-      p.map_a = p.map_b = mb + 2 * src;
+      p.map_a = p.map_b = mb + 2 * kMapsPerHalf * src;
+      p.mn3d = m.tr && view3d(m, src) ? 3 : 0;
       p.o_hi = slot_ptr(m, kSlotA, 0);
       p.o_lo = m.split ? slot_ptr(m, kSlotA, 1) : nullptr;
       p.ldo = m.ldm;
@@ -373,15 +411,16 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
         p.N = (int32_t)m.n;
         p.a_mn = 0;
         p.b_mn = 1;
-        p.map_a = mb + 2 * kSlotB;
-        p.map_b = mb + 2 * src;
+        p.map_a = mb + 2 * kMapsPerHalf * kSlotB;
+        p.map_b = mb + 2 * kMapsPerHalf * src;
+        p.mn3d = view3d(m, src) ? 2 : 0;
       } else {      // Y' = a Y + Y B with Y = X^T in the caller's layout: both K-major
         p.M = (int32_t)m.n;
         p.N = (int32_t)m.m;
         p.a_mn = 0;
         p.b_mn = 0;
-        p.map_a = mb + 2 * src;
-        p.map_b = mb + 2 * kSlotB;
+        p.map_a = mb + 2 * kMapsPerHalf * src;
+        p.map_b = mb + 2 * kMapsPerHalf * kSlotB;
       }
       p.K = (int32_t)m.m;
       p.kind = kApply;
@@ -400,7 +439,7 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
     poly.sym = 1;
     poly.kind = kPoly;
     poly.mat = i;
-    poly.map_a = poly.map_b = mb + 2 * kSlotA;
+    poly.map_a = poly.map_b = mb + 2 * kMapsPerHalf * kSlotA;
     poly.d_hi = slot_ptr(m, kSlotA, 0);
     poly.d_lo = m.split ? slot_ptr(m, kSlotA, 1) : nullptr;
     poly.ldd = m.ldm;
@@ -434,6 +473,7 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
   set->bound = true;
   set->device = dev;
   set->num_sms = prop.multiProcessorCount;
+  set->pair_clusters = pair_clusters;
   set->status = status;
   set->ws = ws;
   set->ns_input = ns_input;
@@ -542,7 +582,8 @@ int mfsdp_newton_schulz(const mfsdp_owner_set* set, const void* ns_input, const 
       lp.probs = probs + (size_t)variant * n;
       lp.tiles = tiles + set->tile_off[phase][p];
       lp.ntiles = (int32_t)cnt;
-      const int grid = (int)std::min<size_t>(cnt, (size_t)set->num_sms);
+      const int grid = p == 1 ? (int)std::min<size_t>(cnt, (size_t)set->num_sms)
+                              : set->pair_clusters;
       e = launch_ns_phase(lp, p == 1, grid, st);
     }
   };
@@ -643,9 +684,10 @@ int mfsdp_query_status(void* stream, int32_t* device_status_out) {
   int v = 0;
   if (cudaMemcpy(&v, addr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MFSDP_ECUDA;
   if (cudaMemset(addr, 0, sizeof(int)) != cudaSuccess) return MFSDP_ECUDA;
-  *device_status_out = (v & kStatusTimeout) ? MFSDP_ETIMEOUT
-                       : (v & kStatusNonFinite) ? MFSDP_ENONFINITE
-                                                : MFSDP_OK;
+  *device_status_out = (v & kStatusTimeout)        ? MFSDP_ETIMEOUT
+                       : (v & kStatusTmemMismatch) ? MFSDP_ECUDA
+                       : (v & kStatusNonFinite)    ? MFSDP_ENONFINITE
+                                                   : MFSDP_OK;
   return MFSDP_OK;
 }
 

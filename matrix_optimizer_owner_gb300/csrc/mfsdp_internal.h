@@ -12,6 +12,7 @@ namespace mfsdp {
 // ---- device status word bits (kept in one __device__ int per device) ----------------------
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusNonFinite = 2;
+constexpr int kStatusTmemMismatch = 4;  // a CTA pair received different tensor-memory bases
 
 // ---- streaming kernels (gradient deposit + momentum + norm, update) -----------------------
 constexpr int kMaxContrib = 64;
@@ -119,6 +120,7 @@ uint64_t wait_limit_ns();    // limit of every bounded device-side wait (mfsdp_s
 constexpr int kBM = 128;   // tile rows    = UMMA M (one CTA, TMEM lanes 0..127)
 constexpr int kBN = 256;   // tile columns = UMMA N
 constexpr int kBK = 64;    // k per pipeline stage = one 128-byte swizzle atom of bf16
+constexpr int kPairBM = 256;  // tile rows of the CTA-pair kernel (128 per CTA)
 constexpr int kNsThreads = 320;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2-9 epilogue
 
 enum NsKind : int32_t { kGram = 0, kPoly = 1, kApply = 2 };
@@ -130,8 +132,9 @@ struct NsProblem {         // one output matrix of one Newton–Schulz phase
   int32_t kind;            // NsKind: epilogue out = alpha*acc + beta*D
   int32_t first;           // first iteration: fold s = 1/(norm + eps) into alpha / beta
   int32_t mat;             // matrix index (norm)
-  int32_t map_a, map_b;    // tensor-map indices of the hi operands; lo = index + 1
-  int32_t pad_;
+  int32_t map_a, map_b;    // tensor-map indices of the hi operands (2D 64x64 box); +1: 2D
+                           // 64x128 box, +2: 3D 64x64x2 MN-major view, +3: the lo half's maps
+  int32_t mn3d;            // bit 0 / bit 1: the A / B operand is MN-major and has the 3D view
   const uint16_t* d_hi;    // epilogue addend D (kPoly: A, kApply: X), row pitch ldd
   const uint16_t* d_lo;
   int64_t ldd;
@@ -158,6 +161,8 @@ struct NsLaunchParams {
 
 size_t ns_smem_bytes(bool split);
 cudaError_t ns_prepare_kernels();  // set the dynamic shared memory attribute once per device
+int ns_pair_max_clusters(int num_sms);  // co-resident CTA pairs of the pair kernel (-1: error)
+// split: single-CTA kernel, `grid` CTAs; else the CTA-pair kernel, `grid` pairs.
 cudaError_t launch_ns_phase(const NsLaunchParams& p, bool split, int grid, cudaStream_t s);
 
 }  // namespace mfsdp

@@ -10,8 +10,8 @@
 // taken round-robin by a persistent grid of one CTA per SM.
 //
 // CTA roles (320 threads):
-//   warp 0 (one lane)  TMA producer: 64 x 64 bf16 boxes, 128-byte swizzle, into a ring of
-//                      pipeline stages guarded by full/empty mbarriers;
+//   warp 0             TMA producers, one lane per pipeline stage: 64-wide, 128-byte-swizzled
+//                      bf16 boxes into a ring of stages guarded by full/empty mbarriers;
 //   warp 1 (one lane)  MMA issuer: tcgen05.mma kind::f16 (M=128, N=256, K=16) from shared-
 //                      memory descriptors into one of two TMEM accumulators (2 x 256 columns);
 //   warps 2-9          epilogue: tcgen05.ld rows of the accumulator, out = alpha*acc + beta*D,
@@ -25,6 +25,8 @@
 // timeout in the status word, raises an abort flag every role polls, waits (bounded) for its
 // own TMA loads and MMAs in flight, frees its tensor memory and returns.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "mfsdp_internal.h"
 
@@ -89,11 +91,8 @@ struct Guard {                 // shared abort flag + the launch's wait limit
   int* status;
 };
 
-// Wait for the phase of `parity` to complete.  Returns false if the kernel is aborting or the
-// wait ran out (which starts the abort).  `honor_abort` = false is used during teardown.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Guard& g,
-                                       bool honor_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const Guard& g,
+                                            bool honor_abort) {
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -106,6 +105,14 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Guar
       }
     }
   }
+}
+
+// Wait for the phase of `parity` to complete (CTA-scope acquire): inline fast path, bounded slow
+// path.  Returns false if the kernel is aborting or the wait ran out (which starts the abort).
+// `honor_abort` = false is used during teardown.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Guard& g,
+                                          bool honor_abort = true) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, g, honor_abort);
 }
 
 __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -181,16 +188,10 @@ __device__ __forceinline__ uint32_t make_idesc(int a_mn, int b_mn) {
          ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 }
 
-// Load `rows` rows (a multiple of 64) of one operand tile for k-block k0 into `dst`.
-__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, int mn_major,
-                                             int r0, int k0, int boxes, uint32_t bar) {
-  for (int c = 0; c < boxes; ++c) {
-    if (mn_major)
-      tma_load(dst + (uint32_t)c * kBoxBytes, map, r0 + 64 * c, k0, bar);
-    else
-      tma_load(dst + (uint32_t)c * kBoxBytes, map, k0, r0 + 64 * c, bar);
-  }
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -240,6 +241,58 @@ __device__ __forceinline__ void store_row32(uint16_t* p, int64_t ld, int r, int 
   }
 }
 
+
+// ---------------------------------------------------------------- multi-lane TMA producers
+// A thread's TMA loads run one after another (a 64 x 128 box costs a thread ~600-750 cycles,
+// whatever the pipeline depth), so one issuing thread cannot feed the tensor cores.  The
+// producer warp therefore runs one issuer per pipeline stage: lane l owns stage l, and the
+// lanes step through the k-block sequence in lockstep, each round issuing a fixed sequence of
+// predicated TMA instructions (operand major-ness only changes which predicates are on).
+
+// Position in the k-block sequence of the tiles t0, t0 + step, ...
+struct KCursor {
+  int t, kb;
+  __device__ __forceinline__ void norm(const NsLaunchParams& P, int step) {
+    while (t < P.ntiles) {
+      const int nk = (P.probs[P.tiles[t].prob].K + kBK - 1) / kBK;
+      if (kb < nk) break;
+      kb -= nk;
+      t += step;
+    }
+  }
+};
+
+__device__ __forceinline__ void tma_load_p(bool p, uint32_t dst, const CUtensorMap* map, int x,
+                                           int y, uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %5, 0;\n"
+      " @p cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];\n}\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "r"((uint32_t)p)
+      : "memory");
+}
+
+__device__ __forceinline__ void expect_tx_p(bool p, uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n"
+      " @p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n}\n" ::"r"(bar),
+      "r"(bytes), "r"((uint32_t)p)
+      : "memory");
+}
+
+// `rows` rows (128 or 256) of one operand tile: MN-major as 64-wide boxes (map), K-major as
+// 128-row boxes (map + 1); the same predicated instructions run in every lane.
+template <int ROWS>
+__device__ __forceinline__ void issue_operand_p(bool p, uint32_t dst, const CUtensorMap* map,
+                                                int mn, int r0, int k0, uint32_t bar) {
+#pragma unroll
+  for (int c = 0; c < ROWS / 64; ++c) {
+    tma_load_p(p && mn, dst + (uint32_t)c * kBoxBytes, map, r0 + 64 * c, k0, bar);
+    if (c < ROWS / 128)
+      tma_load_p(p && !mn, dst + (uint32_t)c * 2 * kBoxBytes, map + 1, k0, r0 + 128 * c, bar);
+  }
+}
+
 // ---------------------------------------------------------------- the kernel
 template <bool SPLIT>
 __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_constant__ NsLaunchParams P) {
@@ -283,39 +336,58 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
   const uint32_t tmem_base = *tmem_slot;
   const Guard g{abort_flag, P.wait_limit_ns, P.status};
 
-  if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------ TMA producer
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t armed = 0, last_parity = 0;  // per-stage bit masks, for the teardown wait
-    for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
-      const NsTile tile = P.tiles[t];
-      const NsProblem& pr = P.probs[tile.prob];
-      const CUtensorMap* ma = P.maps + pr.map_a;
-      const CUtensorMap* mb = P.maps + pr.map_b;
-      const int m0 = tile.tm * kBM, n0 = tile.tn * kBN, nk = (pr.K + kBK - 1) / kBK;
-      bool ok = true;
-      for (int kb = 0; kb < nk; ++kb) {
-        if (!mbar_wait(bar(empty0 + stage), phase ^ 1u, g)) { ok = false; break; }
-        const uint32_t sb = sbase + (uint32_t)stage * C::kStageBytes;
-        const uint32_t fb = bar(full0 + stage);
-        mbar_expect_tx(fb, C::kStageBytes);
-        const int k0 = kb * kBK;
-        load_operand(sb, ma, pr.a_mn, m0, k0, kBM / 64, fb);
-        load_operand(sb + kABytes, mb, pr.b_mn, n0, k0, kBN / 64, fb);
-        if (SPLIT) {
-          load_operand(sb + kABytes + kBBytes, ma + 1, pr.a_mn, m0, k0, kBM / 64, fb);
-          load_operand(sb + 2 * kABytes + kBBytes, mb + 1, pr.b_mn, n0, k0, kBN / 64, fb);
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producers (lane = stage)
+    if (lane < S) {
+      const unsigned pmask = (1u << S) - 1u;
+      KCursor cur{(int)blockIdx.x, lane};
+      cur.norm(P, gridDim.x);
+      uint32_t q = (uint32_t)lane;  // position in the k-block sequence; stage = q % S = lane
+      bool armed = false;
+      uint32_t last_par = 0;
+      const uint32_t sb = sbase + (uint32_t)lane * C::kStageBytes;
+      const uint32_t fb = bar(full0 + lane);
+      for (;;) {
+        bool act = cur.t < P.ntiles && !*abort_flag;
+        if (!__any_sync(pmask, act)) break;
+        const uint32_t ph = (q / S) & 1u;
+        if (act && !mbar_wait(bar(empty0 + lane), ph ^ 1u, g)) act = false;
+        const CUtensorMap* ma = P.maps;
+        const CUtensorMap* mb = P.maps;
+        int a_mn = 0, b_mn = 0, m0 = 0, n0 = 0, k0 = 0;
+        if (act) {
+          const NsTile tile = P.tiles[cur.t];
+          const NsProblem& pr = P.probs[tile.prob];
+          ma = P.maps + pr.map_a;
+          mb = P.maps + pr.map_b;
+          a_mn = pr.a_mn;
+          b_mn = pr.b_mn;
+          m0 = tile.tm * kBM;
+          n0 = tile.tn * kBN;
+          k0 = cur.kb * kBK;
+          if (cur.kb == 0) {
+            prefetch_map(ma + (a_mn ? 0 : 1));
+            prefetch_map(mb + (b_mn ? 0 : 1));
+          }
         }
-        armed |= 1u << stage;
-        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == S) { stage = 0; phase ^= 1u; }
+        expect_tx_p(act, fb, C::kStageBytes);
+        issue_operand_p<kBM>(act, sb, ma, a_mn, m0, k0, fb);
+        issue_operand_p<kBN>(act, sb + kABytes, mb, b_mn, n0, k0, fb);
+        if (SPLIT) {
+          issue_operand_p<kBM>(act, sb + kABytes + kBBytes, ma + 3, a_mn, m0, k0, fb);
+          issue_operand_p<kBN>(act, sb + 2 * kABytes + kBBytes, mb + 3, b_mn, n0, k0, fb);
+        }
+        if (act) {
+          armed = true;
+          last_par = ph;
+        }
+        q += S;
+        cur.kb += S;
+        cur.norm(P, gridDim.x);
       }
-      if (!ok) break;
+      // teardown: every load this lane issued has landed before the CTA may exit
+      if (armed) mbar_wait(bar(full0 + lane), last_par, g, false);
     }
-    // teardown: every load this thread issued has landed before the CTA may exit
-    for (int s = 0; s < S; ++s)
-      if (armed & (1u << s)) mbar_wait(bar(full0 + s), (last_parity >> s) & 1u, g, false);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     int stage = 0, acc = 0;
@@ -324,7 +396,8 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
       const NsTile tile = P.tiles[t];
       const NsProblem& pr = P.probs[tile.prob];
       const int nk = (pr.K + kBK - 1) / kBK;
-      const uint32_t idesc = make_idesc(pr.a_mn, pr.b_mn);
+      const int a_mn = pr.a_mn, b_mn = pr.b_mn;
+      const uint32_t idesc = make_idesc(a_mn, b_mn);
       if (!mbar_wait(bar(tempty0 + acc), acc_phase ^ 1u, g)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
@@ -336,12 +409,12 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
         const uint32_t sbb = sa + kABytes;
 #pragma unroll
         for (int j = 0; j < kBK / 16; ++j) {
-          const uint64_t ad = operand_desc(sa, pr.a_mn, j);
-          const uint64_t bd = operand_desc(sbb, pr.b_mn, j);
+          const uint64_t ad = operand_desc(sa, a_mn, j);
+          const uint64_t bd = operand_desc(sbb, b_mn, j);
           tc_mma(d_tmem, ad, bd, idesc, (kb | j) != 0);
           if (SPLIT) {
-            const uint64_t adl = operand_desc(sa + kABytes + kBBytes, pr.a_mn, j);
-            const uint64_t bdl = operand_desc(sbb + kABytes + kBBytes, pr.b_mn, j);
+            const uint64_t adl = operand_desc(sa + kABytes + kBBytes, a_mn, j);
+            const uint64_t bdl = operand_desc(sbb + kABytes + kBBytes, b_mn, j);
             tc_mma(d_tmem, ad, bdl, idesc, 1u);   // hi * lo
             tc_mma(d_tmem, adl, bd, idesc, 1u);   // lo * hi
           }
@@ -473,12 +546,381 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
   }
 }
 
+
+// ================================================================ CTA-pair kernel
+// The same three phases on 256 x 256 output tiles computed by a pair of CTAs (a cluster of
+// two) with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): CTA rank r holds rows
+// 128r..128r+127 of the A tile and rows 128r..128r+127 of the 256-row B tile in its own
+// shared memory, and receives rows 128r..128r+127 of the accumulator in its own tensor
+// memory.  Per k-block each CTA stages 32 KB instead of 48 KB, so six stages fit, and the
+// pair reads each B panel once instead of twice.
+//   both CTAs  warp 0, four issuing lanes: TMA loads of the CTA's own halves; completion is
+//              counted on the leader's (rank 0) full barrier;
+//   leader     warp 1 lane 0: waits the full barrier, issues the pair MMAs, and commits to
+//              the empty barrier and accumulator-full barrier of both CTAs (multicast);
+//   both CTAs  warps 2-9: epilogue of the CTA's 128 rows; release the accumulator by arriving
+//              on the leader's accumulator-empty barrier (16 arrivals).
+// Tensor memory is allocated by one warp of each CTA (cta_group::2) and both CTAs check that
+// they received the same base column before any work; on a mismatch the kernel records an
+// error and does nothing.
+struct PairCfg {
+  static constexpr int kStages = 6;
+  static constexpr uint32_t kHalfA = 128 * kBK * 2;       // 16 KB: this CTA's A rows
+  static constexpr uint32_t kHalfB = 128 * kBK * 2;       // 16 KB: this CTA's B rows
+  static constexpr uint32_t kStageBytes = kHalfA + kHalfB;
+  static constexpr uint32_t kBarOffset = kStages * kStageBytes;
+  static constexpr uint32_t kSmem = 1024 + kBarOffset + 256;
+  static constexpr uint32_t kTmemCols = 512;              // two 128 x 256 fp32 accumulators
+  static constexpr int kAccs = kTmemCols / kBN;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of the variable at shared::cta address `a` in CTA `rank`.
+__device__ __forceinline__ uint32_t map_rank(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __noinline__ bool mbar_wait_cl_slow(uint32_t bar, uint32_t parity, const Guard& g,
+                                               bool honor_abort) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    if ((i & 31) == 0) {
+      if (honor_abort && *g.abort) return false;
+      if (globaltimer() - t0 > g.limit_ns) {
+        atomicOr(g.status, kStatusTimeout);
+        *g.abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// The same with cluster-scope acquire, for barriers that receive arrivals from the peer CTA's
+// threads (the accumulator-empty barrier).
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, const Guard& g,
+                                             bool honor_abort = true) {
+  return mbar_try_wait_cl(bar, parity) || mbar_wait_cl_slow(bar, parity, g, honor_abort);
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+
+__device__ __forceinline__ void tma_load3d_pair_p(bool p, uint32_t dst, const CUtensorMap* map,
+                                                  int x, int y, int z, uint32_t leader_bar) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " @p cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];\n}\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(leader_bar),
+      "r"((uint32_t)p)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_pair_p(bool p, uint32_t dst, const CUtensorMap* map,
+                                                int x, int y, uint32_t leader_bar) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %5, 0;\n"
+      " @p cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];\n}\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(leader_bar), "r"((uint32_t)p)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __grid_constant__ NsLaunchParams P) {
+  using C = PairCfg;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+  // bars: full[S] | empty[S] | tfull[2] | tempty[2] | drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const int full0 = 0, empty0 = S, tfull0 = 2 * S, tempty0 = 2 * S + 2, drain = 2 * S + 4;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar(full0 + s), 1);
+      mbar_init(bar(empty0 + s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar(tfull0 + a), 1);
+      mbar_init(bar(tempty0 + a), 2 * kEpiWarps);
+    }
+    mbar_init(bar(drain), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  uint32_t peer_base;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];"
+               : "=r"(peer_base)
+               : "r"(map_rank(smem_u32(tmem_slot), rank ^ 1u))
+               : "memory");
+  const bool usable = peer_base == tmem_base;
+  if (!usable && threadIdx.x == 0) atomicOr(P.status, kStatusTmemMismatch);
+  const Guard g{abort_flag, P.wait_limit_ns, P.status};
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (!usable) {
+    // nothing runs: fall through to the teardown
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ TMA producers (both CTAs)
+    // Four lanes in lockstep, one round per two k-blocks: lane bit 1 picks the k-block of the
+    // round (even / odd), lane bit 0 the operand (A / B half).  Each lane issues one 16 KB
+    // load per round (or two 8 KB loads for an MN-major operand without the 3D view); the
+    // leader's A lane arms the stage's full barrier for the bytes of both CTAs.
+    if (lane < 4) {
+      const int par = lane >> 1, opnd = lane & 1;
+      KCursor cur{pair, par};
+      cur.norm(P, npairs);
+      uint32_t q = (uint32_t)par;  // position in the k-block sequence
+      uint32_t armed = 0, last_par = 0;
+      for (;;) {
+        bool act = cur.t < P.ntiles && !*abort_flag;
+        if (!__any_sync(0xFu, act)) break;
+        const int stage = (int)(q % S);
+        const uint32_t ph = (q / S) & 1u;
+        if (act && !mbar_wait(bar(empty0 + stage), ph ^ 1u, g)) act = false;
+        const CUtensorMap* mp = P.maps;
+        int mn = 0, view3 = 0, r0 = 0, k0 = 0;
+        if (act) {
+          const NsTile tile = P.tiles[cur.t];
+          const NsProblem& pr = P.probs[tile.prob];
+          mp = P.maps + (opnd ? pr.map_b : pr.map_a);
+          mn = opnd ? pr.b_mn : pr.a_mn;
+          view3 = (pr.mn3d >> opnd) & 1;
+          r0 = opnd ? tile.tn * kBN + 128 * (int)rank : tile.tm * 256 + 128 * (int)rank;
+          k0 = cur.kb * kBK;
+          if (cur.kb == 0) prefetch_map(mp + (mn ? (view3 ? 2 : 0) : 1));
+        }
+        const uint32_t fb_local = bar(full0 + stage);
+        const uint32_t fb = map_rank(fb_local, 0);
+        const uint32_t dst = sbase + (uint32_t)stage * C::kStageBytes + (opnd ? C::kHalfA : 0u);
+        expect_tx_p(act && leader && opnd == 0, fb_local, 2 * C::kStageBytes);
+        tma_load3d_pair_p(act && mn && view3, dst, mp + 2, 0, k0, r0 / 64, fb);
+        tma_load_pair_p(act && mn && !view3, dst, mp, r0, k0, fb);
+        tma_load_pair_p(act && mn && !view3, dst + kBoxBytes, mp, r0 + 64, k0, fb);
+        tma_load_pair_p(act && !mn, dst, mp + 1, k0, r0, fb);
+        if (act && opnd == 0) {
+          armed |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (ph << stage);
+        }
+        q += 2;
+        cur.kb += 2;
+        cur.norm(P, npairs);
+      }
+      // teardown: the leader's full barriers count both CTAs' bytes
+      if (leader)
+        for (int st = 0; st < S; ++st)
+          if (armed & (1u << st)) mbar_wait(bar(full0 + st), (last_par >> st) & 1u, g, false);
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    for (int t = pair; t < P.ntiles; t += npairs) {
+      const NsTile tile = P.tiles[t];
+      const NsProblem& pr = P.probs[tile.prob];
+      const int nk = (pr.K + kBK - 1) / kBK;
+      const int a_mn = pr.a_mn, b_mn = pr.b_mn;
+      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) |
+                             ((uint32_t)b_mn << 16) | ((uint32_t)(kBN >> 3) << 17) |
+                             ((uint32_t)(256 >> 4) << 24);
+      if (!mbar_wait_cl(bar(tempty0 + acc), acc_phase ^ 1u, g)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait(bar(full0 + stage), phase, g)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = sbase + (uint32_t)stage * C::kStageBytes;
+        const uint32_t sbb = sa + C::kHalfA;
+#pragma unroll
+        for (int j = 0; j < kBK / 16; ++j)
+          tc_mma_pair(d_tmem, operand_desc(sa, a_mn, j), operand_desc(sbb, b_mn, j), idesc,
+                      (kb | j) != 0);
+        tc_commit_pair(bar(empty0 + stage), 0x3);
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      tc_commit_pair(bar(tfull0 + acc), 0x3);
+      if (++acc == C::kAccs) { acc = 0; acc_phase ^= 1u; }
+    }
+    tc_commit_pair(bar(drain), 0x1);
+    mbar_wait(bar(drain), 0u, g, false);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int quarter = warp & 3;
+    const int c_first = ((warp - 2) >> 2) * kEpiChunks;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = pair; t < P.ntiles; t += npairs) {
+      const NsTile tile = P.tiles[t];
+      const NsProblem& pr = P.probs[tile.prob];
+      const int M = pr.M, N = pr.N, kind = pr.kind, sym = pr.sym;
+      const int m0 = tile.tm * 256 + 128 * (int)rank, n0 = tile.tn * kBN;
+      const int rw = m0 + quarter * 32;
+      const int r = rw + lane;
+      const bool rvalid = r < M;
+      const float s = 1.f / (P.norm[pr.mat] + P.eps);
+      uint4 dpre[kEpiChunks][4];
+      if (kind != kGram && rvalid) {
+#pragma unroll
+        for (int q = 0; q < kEpiChunks; ++q) {
+          const int c0 = n0 + (c_first + q) * 32;
+          if (c0 + 32 <= N && !(sym && c0 + 31 < rw)) {
+            const uint4* src = reinterpret_cast<const uint4*>(pr.d_hi + (int64_t)r * pr.ldd + c0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dpre[q][k] = src[k];
+          }
+        }
+      }
+      if (!mbar_wait(bar(tfull0 + acc), acc_phase, g)) break;
+      tc_fence_after();
+      float alpha = 1.f, beta = 0.f;
+      if (kind == kGram) {
+        alpha = pr.first ? s * s : 1.f;
+      } else if (kind == kPoly) {
+        alpha = P.c;
+        beta = P.b;
+      } else {
+        alpha = pr.first ? s : 1.f;
+        beta = P.a * alpha;
+      }
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
+#pragma unroll
+      for (int q = 0; q < kEpiChunks; ++q) {
+        const int cc = c_first + q;
+        const int c0 = n0 + cc * 32;
+        if (c0 >= N || rw >= M) break;                 // warp-uniform
+        if (sym && c0 + 31 < rw) continue;             // chunk entirely below the diagonal
+        float v[32];
+        tc_ld32(taddr + (uint32_t)(cc * 32), v);
+        if (!rvalid) continue;
+        if (beta != 0.f) {
+          float d[32];
+          if (c0 + 32 <= N) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t w[4] = {dpre[q][k].x, dpre[q][k].y, dpre[q][k].z, dpre[q][k].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                d[8 * k + 2 * e] = bf_lo(w[e]);
+                d[8 * k + 2 * e + 1] = bf_hi(w[e]);
+              }
+            }
+          } else {
+            load_row32(pr.d_hi, pr.ldd, r, c0, N, d);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = fmaf(alpha, v[j], beta * d[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= alpha;
+        }
+        uint16_t h[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) h[j] = f2bf(v[j]);
+        const int cmin = sym ? r : 0;
+        store_row32(pr.o_hi, pr.ldo, r, c0, cmin, N, h);
+        if (sym && c0 + 31 > r) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c = c0 + j;
+            if (c > r && c < N) pr.o_hi[(int64_t)c * pr.ldo + r] = h[j];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_rank(bar(tempty0 + acc), 0));
+      if (++acc == C::kAccs) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncwarp();
+  __syncthreads();
+  cluster_sync_all();  // neither CTA leaves while its peer may still use its memory
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(C::kTmemCols)
+                 : "memory");
+  }
+}
+
 }  // namespace
 
 size_t ns_smem_bytes(bool split) { return split ? Cfg<true>::kSmem : Cfg<false>::kSmem; }
 
 cudaError_t ns_prepare_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<false>,
+  cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)PairCfg::kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ns_gemm_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Cfg<false>::kSmem);
   if (e != cudaSuccess) return e;
@@ -486,13 +928,44 @@ cudaError_t ns_prepare_kernels() {
                               (int)Cfg<true>::kSmem);
 }
 
+int ns_pair_max_clusters(int num_sms) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+  cfg.blockDim = dim3(kNsThreads, 1, 1);
+  cfg.dynamicSmemBytes = PairCfg::kSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, ns_gemm_pair_kernel, &cfg) != cudaSuccess) return -1;
+  return n;
+}
+
 cudaError_t launch_ns_phase(const NsLaunchParams& p, bool split, int grid, cudaStream_t s) {
   if (p.ntiles <= 0) return cudaSuccess;
-  if (split)
+  if (split) {
     ns_gemm_kernel<true><<<grid, kNsThreads, Cfg<true>::kSmem, s>>>(p);
-  else
-    ns_gemm_kernel<false><<<grid, kNsThreads, Cfg<false>::kSmem, s>>>(p);
-  return cudaGetLastError();
+    return cudaGetLastError();
+  }
+  // bf16 operands: CTA pairs; `grid` is the number of co-resident pairs
+  const int pairs = std::max(1, std::min(p.ntiles, grid));
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(kNsThreads, 1, 1);
+  cfg.dynamicSmemBytes = PairCfg::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel, p);
 }
 
 }  // namespace mfsdp
