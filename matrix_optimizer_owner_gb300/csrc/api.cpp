@@ -18,12 +18,12 @@ using namespace mfsdp;
 namespace {
 
 constexpr int kSlotU = 0, kSlotP = 1, kSlotO = 2, kSlotA = 3, kSlotB = 4, kSlots = 5;
-// Per slot and half (hi, lo): [2D 64x64 box, 2D 64x128 box, 3D 64x64x2 box].  64x64 boxes and
-// the 3D view serve MN-major operands (the 3D view, 64 elements x rows x 64-element chunks with a
-// 128-byte chunk stride, loads a 128-wide half-tile in one operation; it exists only when the
-// row length is a multiple of 64, so it never reaches past a row); 64x128 boxes load a 128-row
-// K-major half-tile.
-constexpr int kMapsPerHalf = 3;
+// Per slot and half (hi, lo): [2D 64x64 box, 2D 64x128 box, 3D 64x64x2 box, 2D 32x32 box].
+// 64x64 boxes and the 3D view serve MN-major operands (the 3D view, 64 elements x rows x
+// 64-element chunks with a 128-byte chunk stride, loads a 128-wide half-tile in one operation;
+// it exists only when the row length is a multiple of 64, so it never reaches past a row);
+// 64x128 boxes load a 128-row K-major half-tile; unswizzled 32x32 boxes carry the epilogue's
+// TMA stores (a warp's 32 rows x 32 columns).
 constexpr int kMapsPerMatrix = 2 * kMapsPerHalf * kSlots;
 constexpr int kGroupRows = 8;               // tile-row group of the rasterised tile order
 
@@ -106,15 +106,16 @@ bool encode_map3d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
 }
 
 bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
-                uint32_t box_rows) {
+                uint32_t box_rows, uint32_t box_cols = 64, bool swizzle = true) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -373,7 +374,9 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
         const int64_t rows = sq ? m.m : m.rows, cols = sq ? m.m : m.cols;
         CUtensorMap* mp = &maps[(size_t)i * kMapsPerMatrix + 2 * kMapsPerHalf * slot + kMapsPerHalf * h];
         if (!encode_map(mp, slot_ptr(m, slot, h), rows, cols, slot_ld(m, slot), 64u) ||
-            !encode_map(mp + 1, slot_ptr(m, slot, h), rows, cols, slot_ld(m, slot), 128u))
+            !encode_map(mp + 1, slot_ptr(m, slot, h), rows, cols, slot_ld(m, slot), 128u) ||
+            !encode_map(mp + 3, slot_ptr(m, slot, h), rows, cols, slot_ld(m, slot), 32u, 32u,
+                        false))
           return MFSDP_ECUDA;
         if (cols % 64 == 0 && !encode_map3d(mp + 2, slot_ptr(m, slot, h), rows, cols,
                                             slot_ld(m, slot)))
@@ -402,6 +405,7 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
       p.o_hi = slot_ptr(m, kSlotA, 0);
       p.o_lo = m.split ? slot_ptr(m, kSlotA, 1) : nullptr;
       p.ldo = m.ldm;
+      p.map_o = mb + 2 * kMapsPerHalf * kSlotA + 3;  // 32x32 store box
       return p;
     };
     auto apply = [&](int src, int dst, int first) {
@@ -432,6 +436,7 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
       p.o_hi = slot_ptr(m, dst, 0);
       p.o_lo = m.split ? slot_ptr(m, dst, 1) : nullptr;
       p.ldo = slot_ld(m, dst);
+      p.map_o = mb + 2 * kMapsPerHalf * dst + 3;  // 32x32 store box
       return p;
     };
     NsProblem poly{};
@@ -443,6 +448,7 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
     poly.d_hi = slot_ptr(m, kSlotA, 0);
     poly.d_lo = m.split ? slot_ptr(m, kSlotA, 1) : nullptr;
     poly.ldd = m.ldm;
+    poly.map_o = mb + 2 * kMapsPerHalf * kSlotB + 3;  // 32x32 store box
     poly.o_hi = slot_ptr(m, kSlotB, 0);
     poly.o_lo = m.split ? slot_ptr(m, kSlotB, 1) : nullptr;
     poly.ldo = m.ldm;

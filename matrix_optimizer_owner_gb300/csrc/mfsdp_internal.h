@@ -121,6 +121,7 @@ constexpr int kBM = 128;   // tile rows    = UMMA M (one CTA, TMEM lanes 0..127)
 constexpr int kBN = 256;   // tile columns = UMMA N
 constexpr int kBK = 64;    // k per pipeline stage = one 128-byte swizzle atom of bf16
 constexpr int kPairBM = 256;  // tile rows of the CTA-pair kernel (128 per CTA)
+constexpr int kMapsPerHalf = 4;  // tensor maps per buffer half (see NsProblem::map_a)
 constexpr int kNsThreads = 320;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2-9 epilogue
 
 enum NsKind : int32_t { kGram = 0, kPoly = 1, kApply = 2 };
@@ -133,8 +134,11 @@ struct NsProblem {         // one output matrix of one Newton–Schulz phase
   int32_t first;           // first iteration: fold s = 1/(norm + eps) into alpha / beta
   int32_t mat;             // matrix index (norm)
   int32_t map_a, map_b;    // tensor-map indices of the hi operands (2D 64x64 box); +1: 2D
-                           // 64x128 box, +2: 3D 64x64x2 MN-major view, +3: the lo half's maps
+                           // 64x128 box, +2: 3D 64x64x2 MN-major view, +3: 2D 32x32 unswizzled
+                           // box (stores), +kMapsPerHalf: the lo half's maps
   int32_t mn3d;            // bit 0 / bit 1: the A / B operand is MN-major and has the 3D view
+  int32_t map_o;           // tensor-map index of the output's 32x32 store box (hi)
+  int32_t pad2_;
   const uint16_t* d_hi;    // epilogue addend D (kPoly: A, kApply: X), row pitch ldd
   const uint16_t* d_lo;
   int64_t ldd;

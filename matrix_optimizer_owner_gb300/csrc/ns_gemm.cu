@@ -374,8 +374,8 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
         issue_operand_p<kBM>(act, sb, ma, a_mn, m0, k0, fb);
         issue_operand_p<kBN>(act, sb + kABytes, mb, b_mn, n0, k0, fb);
         if (SPLIT) {
-          issue_operand_p<kBM>(act, sb + kABytes + kBBytes, ma + 3, a_mn, m0, k0, fb);
-          issue_operand_p<kBN>(act, sb + 2 * kABytes + kBBytes, mb + 3, b_mn, n0, k0, fb);
+          issue_operand_p<kBM>(act, sb + kABytes + kBBytes, ma + kMapsPerHalf, a_mn, m0, k0, fb);
+          issue_operand_p<kBN>(act, sb + 2 * kABytes + kBBytes, mb + kMapsPerHalf, b_mn, n0, k0, fb);
         }
         if (act) {
           armed = true;
@@ -568,7 +568,9 @@ struct PairCfg {
   static constexpr uint32_t kHalfA = 128 * kBK * 2;       // 16 KB: this CTA's A rows
   static constexpr uint32_t kHalfB = 128 * kBK * 2;       // 16 KB: this CTA's B rows
   static constexpr uint32_t kStageBytes = kHalfA + kHalfB;
-  static constexpr uint32_t kBarOffset = kStages * kStageBytes;
+  static constexpr uint32_t kStagingOffset = kStages * kStageBytes;
+  static constexpr uint32_t kStagingPerWarp = 2 * 32 * 32 * 2;  // a 32x32 block + its transpose
+  static constexpr uint32_t kBarOffset = kStagingOffset + kEpiWarps * kStagingPerWarp;
   static constexpr uint32_t kSmem = 1024 + kBarOffset + 256;
   static constexpr uint32_t kTmemCols = 512;              // two 128 x 256 fp32 accumulators
   static constexpr int kAccs = kTmemCols / kBN;
@@ -659,6 +661,16 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uin
       " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// TMA store of a 32 x 32 bf16 block from shared memory (unswizzled, row-major) at (x, y);
+// rows / columns outside the tensor are not written.
+__device__ __forceinline__ void tma_store_block(const CUtensorMap* map, uint32_t src, int x,
+                                                int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
 }
 
 __device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t cta_mask) {
@@ -812,6 +824,9 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int quarter = warp & 3;
     const int c_first = ((warp - 2) >> 2) * kEpiChunks;
+    uint16_t* stage_blk =
+        reinterpret_cast<uint16_t*>(smem + C::kStagingOffset + (warp - 2) * C::kStagingPerWarp);
+    const uint32_t stage_addr = smem_u32(stage_blk);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = pair; t < P.ntiles; t += npairs) {
@@ -848,6 +863,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
         beta = P.a * alpha;
       }
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
+      const CUtensorMap* map_o = P.maps + pr.map_o;
 #pragma unroll
       for (int q = 0; q < kEpiChunks; ++q) {
         const int cc = c_first + q;
@@ -856,7 +872,6 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
         if (sym && c0 + 31 < rw) continue;             // chunk entirely below the diagonal
         float v[32];
         tc_ld32(taddr + (uint32_t)(cc * 32), v);
-        if (!rvalid) continue;
         if (beta != 0.f) {
           float d[32];
           if (c0 + 32 <= N) {
@@ -869,8 +884,11 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
                 d[8 * k + 2 * e + 1] = bf_hi(w[e]);
               }
             }
-          } else {
+          } else if (rvalid) {
             load_row32(pr.d_hi, pr.ldd, r, c0, N, d);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) d[j] = 0.f;
           }
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = fmaf(alpha, v[j], beta * d[j]);
@@ -881,14 +899,39 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
         uint16_t h[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) h[j] = f2bf(v[j]);
-        const int cmin = sym ? r : 0;
-        store_row32(pr.o_hi, pr.ldo, r, c0, cmin, N, h);
-        if (sym && c0 + 31 > r) {
+        if (sym && c0 == rw) {
+          // block on the diagonal: row r stores columns >= r and mirrors columns > r
+          if (rvalid) {
+            store_row32(pr.o_hi, pr.ldo, r, c0, r, N, h);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int c = c0 + j;
-            if (c > r && c < N) pr.o_hi[(int64_t)c * pr.ldo + r] = h[j];
+            for (int j = 0; j < 32; ++j) {
+              const int c = c0 + j;
+              if (c > r && c < N) pr.o_hi[(int64_t)c * pr.ldo + r] = h[j];
+            }
           }
+          continue;
+        }
+        // off-diagonal block: stage it (and its transpose for a symmetric output) in this
+        // warp's shared memory and write it with TMA stores
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
+        uint4* row = reinterpret_cast<uint4*>(stage_blk + lane * 32);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          row[k] = make_uint4((uint32_t)h[8 * k] | ((uint32_t)h[8 * k + 1] << 16),
+                              (uint32_t)h[8 * k + 2] | ((uint32_t)h[8 * k + 3] << 16),
+                              (uint32_t)h[8 * k + 4] | ((uint32_t)h[8 * k + 5] << 16),
+                              (uint32_t)h[8 * k + 6] | ((uint32_t)h[8 * k + 7] << 16));
+        if (sym) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) stage_blk[1024 + j * 32 + lane] = h[j];
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_block(map_o, stage_addr, c0, rw);
+          if (sym) tma_store_block(map_o, stage_addr + 2048u, rw, c0);
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
       }
       tc_fence_before();
@@ -896,6 +939,8 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
       if (lane == 0) mbar_arrive_cluster(map_rank(bar(tempty0 + acc), 0));
       if (++acc == C::kAccs) { acc = 0; acc_phase ^= 1u; }
     }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // stores done
+    __syncwarp();
   }
 
   tc_fence_before();
