@@ -105,8 +105,11 @@ bool encode_map3d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D bf16 tensor map over a row-major rows x cols buffer of pitch ld; boxes of box_rows x
+// box_cols with a 128-byte swizzle (operand loads) or a 64-byte swizzle (the epilogue's
+// 32 x 32 staging blocks).
 bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
-                uint32_t box_rows, uint32_t box_cols = 64, bool swizzle = true) {
+                uint32_t box_rows, uint32_t box_cols = 64, bool swizzle128 = true) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -115,7 +118,7 @@ bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, 
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -405,7 +408,7 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
       p.o_hi = slot_ptr(m, kSlotA, 0);
       p.o_lo = m.split ? slot_ptr(m, kSlotA, 1) : nullptr;
       p.ldo = m.ldm;
-      p.map_o = mb + 2 * kMapsPerHalf * kSlotA + 3;  // 32x32 store box
+      p.map_o = mb + 2 * kMapsPerHalf * kSlotA + 3;  // 32x32 store box (64-byte swizzle)
       return p;
     };
     auto apply = [&](int src, int dst, int first) {
@@ -436,7 +439,7 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
       p.o_hi = slot_ptr(m, dst, 0);
       p.o_lo = m.split ? slot_ptr(m, dst, 1) : nullptr;
       p.ldo = slot_ld(m, dst);
-      p.map_o = mb + 2 * kMapsPerHalf * dst + 3;  // 32x32 store box
+      p.map_o = mb + 2 * kMapsPerHalf * dst + 3;  // 32x32 store box (64-byte swizzle)
       return p;
     };
     NsProblem poly{};
@@ -448,7 +451,7 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
     poly.d_hi = slot_ptr(m, kSlotA, 0);
     poly.d_lo = m.split ? slot_ptr(m, kSlotA, 1) : nullptr;
     poly.ldd = m.ldm;
-    poly.map_o = mb + 2 * kMapsPerHalf * kSlotB + 3;  // 32x32 store box
+    poly.map_o = mb + 2 * kMapsPerHalf * kSlotB + 3;  // 32x32 store box (64-byte swizzle)
     poly.o_hi = slot_ptr(m, kSlotB, 0);
     poly.o_lo = m.split ? slot_ptr(m, kSlotB, 1) : nullptr;
     poly.ldo = m.ldm;

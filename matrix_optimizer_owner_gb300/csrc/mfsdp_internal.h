@@ -137,7 +137,7 @@ struct NsProblem {         // one output matrix of one Newton–Schulz phase
                            // 64x128 box, +2: 3D 64x64x2 MN-major view, +3: 2D 32x32 unswizzled
                            // box (stores), +kMapsPerHalf: the lo half's maps
   int32_t mn3d;            // bit 0 / bit 1: the A / B operand is MN-major and has the 3D view
-  int32_t map_o;           // tensor-map index of the output's 32x32 store box (hi)
+  int32_t map_o;           // tensor-map index of the output's 32x32 store box (hi, 64B swizzle)
   int32_t pad2_;
   const uint16_t* d_hi;    // epilogue addend D (kPoly: A, kApply: X), row pitch ldd
   const uint16_t* d_lo;

@@ -65,11 +65,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -113,15 +108,6 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Guard& g,
                                           bool honor_abort = true) {
   return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, g, honor_abort);
-}
-
-__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -663,8 +649,86 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
-// TMA store of a 32 x 32 bf16 block from shared memory (unswizzled, row-major) at (x, y);
-// rows / columns outside the tensor are not written.
+// ---------------------------------------------------------------- pair-kernel epilogue helpers
+// Staging block of one epilogue warp: 32 rows x 32 bf16, 64 B per row, the four 16-byte
+// chunks of row r stored in the order k ^ ((r >> 1) & 3).  With that permutation a warp
+// access of one chunk of each of 32 rows (one row per lane) and a warp access of 8 whole rows
+// (four lanes per row) both spread over all eight 16-byte bank groups: 4 wavefronts for
+// 512 B, the minimum.
+__device__ __forceinline__ uint32_t stg_off(int r, int k) {
+  return (uint32_t)(r * 64 + ((k ^ ((r >> 1) & 3)) << 4));
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void sts16(uint32_t a, uint16_t v) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(v) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+
+// Eight bf16 at (r, c) of a row-major buffer (c % 8 == 0, ld % 8 == 0), zero outside M x N.
+__device__ __forceinline__ uint4 load_granule(const uint16_t* p, int64_t ld, int r, int c, int M,
+                                              int N) {
+  if (r >= M || c >= N) return make_uint4(0u, 0u, 0u, 0u);
+  const uint16_t* src = p + (int64_t)r * ld + c;
+  if (c + 8 <= N) return *reinterpret_cast<const uint4*>(src);
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  for (int e = 0; e < 8; ++e)
+    if (c + e < N) w[e >> 1] |= (uint32_t)src[e] << (16 * (e & 1));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Store eight bf16 at (r, c); elements outside M x N are not written.
+__device__ __forceinline__ void store_granule(uint16_t* p, int64_t ld, int r, int c, int M, int N,
+                                              uint4 v) {
+  if (r >= M || c >= N) return;
+  uint16_t* dst = p + (int64_t)r * ld + c;
+  if (c + 8 <= N) {
+    *reinterpret_cast<uint4*>(dst) = v;
+    return;
+  }
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int e = 0; e < 8; ++e)
+    if (c + e < N) dst[e] = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
+}
+
+// tcgen05.ld of 32 consecutive fp32 columns of this thread's TMEM lane, split in issue and
+// wait so that other work overlaps the load; the registers are read-write operands of the
+// wait, so no use of them can move above it.
+__device__ __forceinline__ void tc_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_store_block(const CUtensorMap* map, uint32_t src, int x,
                                                 int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
@@ -822,11 +886,64 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
     mbar_wait(bar(drain), 0u, g, false);
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue (both CTAs)
+    // Warp w covers TMEM lane quarter (w & 3), i.e. 32 rows of the CTA's 128, and four
+    // 32-column chunks.  The addend D is read from global memory in coalesced form (a warp
+    // access covers 8 rows x 64 B), two chunks ahead, and turned into one row per lane
+    // through the warp's 4 KB staging area; each output block is written there (64-byte
+    // swizzled, the layout of the store map) and leaves by TMA store.  A symmetric output uses
+    // both 2 KB halves (block + transpose) and waits for the previous store group; any other
+    // output alternates between the halves, so one store may still be reading the other half.
+    // A launch runs one phase, so its outputs are all symmetric (Gram, polynomial) or all not
+    // (apply).
     const int quarter = warp & 3;
     const int c_first = ((warp - 2) >> 2) * kEpiChunks;
-    uint16_t* stage_blk =
-        reinterpret_cast<uint16_t*>(smem + C::kStagingOffset + (warp - 2) * C::kStagingPerWarp);
-    const uint32_t stage_addr = smem_u32(stage_blk);
+    const uint32_t stg0 = sbase + C::kStagingOffset + (uint32_t)(warp - 2) * C::kStagingPerWarp;
+    const uint32_t stg_t = stg0 + 2048u;  // the transposed block of a symmetric output
+    uint32_t nstore = 0;
+    const int crow = lane >> 2, cchunk = lane & 3;
+    // Where this warp's D of tile t comes from: the addend at the warp's first row and first
+    // column, its pitch, and packed in one word which of the four chunks have one (bits 0-3),
+    // the rows left from there (bits 4-9, at most 32) and the columns left (bits 10-17, at
+    // most 128).
+    struct DSrc {
+      const uint16_t* p;
+      int ld;
+      uint32_t bits;
+    };
+    auto dsrc_of = [&](int t) {
+      DSrc d{nullptr, 0, 0u};
+      if (t >= P.ntiles) return d;
+      const NsTile tl = P.tiles[t];
+      const NsProblem& pp = P.probs[tl.prob];
+      const int rw_ = tl.tm * 256 + 128 * (int)rank + quarter * 32;
+      const int cb = tl.tn * kBN + c_first * 32;
+      if (pp.kind == kGram || rw_ >= pp.M) return d;
+      d.p = pp.d_hi + (int64_t)rw_ * pp.ldd + cb;
+      d.ld = (int)pp.ldd;
+      uint32_t live = 0u;
+#pragma unroll
+      for (int q = 0; q < kEpiChunks; ++q) {
+        const int c0_ = cb + 32 * q;
+        if (c0_ < pp.N && !(pp.sym && c0_ + 31 < rw_)) live |= 1u << q;
+      }
+      const uint32_t rows = (uint32_t)min(pp.M - rw_, 32), cols = (uint32_t)min(pp.N - cb, 128);
+      d.bits = live | (rows << 4) | (cols << 10);
+      return d;
+    };
+    auto load_d = [&](const DSrc& ds, int q, uint4 (&dst)[4]) {
+      if (!((ds.bits >> q) & 1u)) return;
+      const int rows = (int)((ds.bits >> 4) & 63u), cols = (int)(ds.bits >> 10);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        dst[i] = load_granule(ds.p, ds.ld, 8 * i + crow, 32 * q + 8 * cchunk, rows, cols);
+    };
+    // D is prefetched two chunks ahead (chunk q + 2 of the tile, or chunk q - 2 of the next
+    // one), in a ring of two register slots: slot q & 1 holds chunk q.
+    uint4 dpre[2][4];
+    DSrc cur = dsrc_of(pair);
+    load_d(cur, 0, dpre[0]);
+    load_d(cur, 1, dpre[1]);
+    DSrc nxt = dsrc_of(pair + npairs);  // the tables are read a tile before they are needed
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = pair; t < P.ntiles; t += npairs) {
@@ -836,20 +953,15 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
       const int m0 = tile.tm * 256 + 128 * (int)rank, n0 = tile.tn * kBN;
       const int rw = m0 + quarter * 32;
       const int r = rw + lane;
-      const bool rvalid = r < M;
       const float s = 1.f / (P.norm[pr.mat] + P.eps);
-      uint4 dpre[kEpiChunks][4];
-      if (kind != kGram && rvalid) {
-#pragma unroll
-        for (int q = 0; q < kEpiChunks; ++q) {
-          const int c0 = n0 + (c_first + q) * 32;
-          if (c0 + 32 <= N && !(sym && c0 + 31 < rw)) {
-            const uint4* src = reinterpret_cast<const uint4*>(pr.d_hi + (int64_t)r * pr.ldd + c0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) dpre[q][k] = src[k];
-          }
-        }
-      }
+      const DSrc nxt2 = dsrc_of(t + 2 * npairs);
+      // refill slot q & 1 once chunk q has taken its D
+      auto refill = [&](int q) {
+        if (q + 2 < kEpiChunks)
+          load_d(cur, q + 2, dpre[q & 1]);
+        else
+          load_d(nxt, q + 2 - kEpiChunks, dpre[q & 1]);
+      };
       if (!mbar_wait(bar(tfull0 + acc), acc_phase, g)) break;
       tc_fence_after();
       float alpha = 1.f, beta = 0.f;
@@ -863,81 +975,97 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
         beta = P.a * alpha;
       }
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
-      const CUtensorMap* map_o = P.maps + pr.map_o;
 #pragma unroll
       for (int q = 0; q < kEpiChunks; ++q) {
         const int cc = c_first + q;
         const int c0 = n0 + cc * 32;
-        if (c0 >= N || rw >= M) break;                 // warp-uniform
-        if (sym && c0 + 31 < rw) continue;             // chunk entirely below the diagonal
-        float v[32];
-        tc_ld32(taddr + (uint32_t)(cc * 32), v);
-        if (beta != 0.f) {
-          float d[32];
-          if (c0 + 32 <= N) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint32_t w[4] = {dpre[q][k].x, dpre[q][k].y, dpre[q][k].z, dpre[q][k].w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                d[8 * k + 2 * e] = bf_lo(w[e]);
-                d[8 * k + 2 * e + 1] = bf_hi(w[e]);
-              }
-            }
-          } else if (rvalid) {
-            load_row32(pr.d_hi, pr.ldd, r, c0, N, d);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) d[j] = 0.f;
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = fmaf(alpha, v[j], beta * d[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] *= alpha;
+        // warp-uniform: the chunk has rows and columns, and is not below the diagonal
+        if (c0 >= N || rw >= M || (sym && c0 + 31 < rw)) {
+          refill(q);
+          continue;
         }
-        uint16_t h[32];
+        uint32_t a32[32];
+        tc_ld32_issue(taddr + (uint32_t)(cc * 32), a32);
+        const uint32_t half = sym ? 0u : (nstore & 1u);
+        const uint32_t stg = stg0 + half * 2048u;
+        if (lane == 0) {
+          if (sym)
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          else
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        }
+        __syncwarp();
+        uint32_t dw[16];  // D as bf16 pairs, one row per lane
+        if (beta != 0.f) {
+          // D from the coalesced layout to one row per lane
 #pragma unroll
-        for (int j = 0; j < 32; ++j) h[j] = f2bf(v[j]);
+          for (int i = 0; i < 4; ++i) sts128(stg + stg_off(8 * i + crow, cchunk), dpre[q & 1][i]);
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 w4 = lds128(stg + stg_off(lane, k));
+            dw[4 * k] = w4.x;
+            dw[4 * k + 1] = w4.y;
+            dw[4 * k + 2] = w4.z;
+            dw[4 * k + 3] = w4.w;
+          }
+          __syncwarp();
+        }
+        refill(q);
+        tc_ld_wait(a32);
+        uint32_t hw[16];  // bf16 pairs (column 2k in the low half)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float v0 = __uint_as_float(a32[2 * k]), v1 = __uint_as_float(a32[2 * k + 1]);
+          if (beta != 0.f) {
+            v0 = fmaf(alpha, v0, beta * bf_lo(dw[k]));
+            v1 = fmaf(alpha, v1, beta * bf_hi(dw[k]));
+          } else {
+            v0 *= alpha;
+            v1 *= alpha;
+          }
+          hw[k] = (uint32_t)f2bf(v0) | ((uint32_t)f2bf(v1) << 16);
+        }
         if (sym && c0 == rw) {
           // block on the diagonal: row r stores columns >= r and mirrors columns > r
-          if (rvalid) {
-            store_row32(pr.o_hi, pr.ldo, r, c0, r, N, h);
+          if (r < M) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int c = c0 + j;
-              if (c > r && c < N) pr.o_hi[(int64_t)c * pr.ldo + r] = h[j];
+              const uint16_t hj = (uint16_t)(hw[j >> 1] >> (16 * (j & 1)));
+              if (c >= r && c < N) pr.o_hi[(int64_t)r * pr.ldo + c] = hj;
+              if (c > r && c < N) pr.o_hi[(int64_t)c * pr.ldo + r] = hj;
             }
           }
           continue;
         }
-        // off-diagonal block: stage it (and its transpose for a symmetric output) in this
-        // warp's shared memory and write it with TMA stores
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-        __syncwarp();
-        uint4* row = reinterpret_cast<uint4*>(stage_blk + lane * 32);
+        // off-diagonal block (and its transpose for a symmetric output): stage, then TMA store
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          row[k] = make_uint4((uint32_t)h[8 * k] | ((uint32_t)h[8 * k + 1] << 16),
-                              (uint32_t)h[8 * k + 2] | ((uint32_t)h[8 * k + 3] << 16),
-                              (uint32_t)h[8 * k + 4] | ((uint32_t)h[8 * k + 5] << 16),
-                              (uint32_t)h[8 * k + 6] | ((uint32_t)h[8 * k + 7] << 16));
+          sts128(stg + stg_off(lane, k), make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2],
+                                                    hw[4 * k + 3]));
         if (sym) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) stage_blk[1024 + j * 32 + lane] = h[j];
+          for (int j = 0; j < 32; ++j)
+            sts16(stg_t + stg_off(j, lane >> 3) + (uint32_t)((lane & 7) * 2),
+                  (uint16_t)(hw[j >> 1] >> (16 * (j & 1))));
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          tma_store_block(map_o, stage_addr, c0, rw);
-          if (sym) tma_store_block(map_o, stage_addr + 2048u, rw, c0);
+          const CUtensorMap* map_o = P.maps + pr.map_o;
+          tma_store_block(map_o, stg, c0, rw);
+          if (sym) tma_store_block(map_o, stg_t, rw, c0);
           asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
+        ++nstore;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_rank(bar(tempty0 + acc), 0));
       if (++acc == C::kAccs) { acc = 0; acc_phase ^= 1u; }
+      cur = nxt;
+      nxt = nxt2;
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // stores done
     __syncwarp();

@@ -236,10 +236,11 @@ reduce_momentum_kernel(const __grid_constant__ ReduceParams P) {
 // Owner gradient deposit + Nesterov momentum + norm partials, bulk-copy path.
 // A persistent grid walks the same per-matrix chunk partition (chunk c = CTA c of the
 // partition; CTA b takes chunks b, b + grid, ...).  Each chunk is split into sub-chunks of
-// E elements; thread 0 streams every sub-chunk's W contribution slices and momentum slice
-// into a ring of shared-memory stages with cp.async.bulk (completion counted on one mbarrier
-// per stage) several stages ahead, and all 256 threads consume a stage from shared memory and
-// write the new momentum and the bf16 NS input straight to global memory.  A chunk is always
+// E elements; warp 0 streams every sub-chunk's W contribution slices and momentum slice
+// (one slice per lane) into a ring of shared-memory stages with cp.async.bulk (completion
+// counted on one mbarrier per stage) several stages ahead, and all 256 threads consume a
+// stage from shared memory and write the new momentum and the bf16 NS input straight to
+// global memory.  A chunk is always
 // processed by one CTA with the same element-to-thread mapping, so its norm partial does not
 // depend on the grid size.  Waits are bounded; on expiry the kernel records a timeout, stops
 // issuing, drains its copies in flight and exits.
@@ -307,7 +308,9 @@ reduce_momentum_bulk_kernel(const __grid_constant__ ReduceParams P,
   }
   __syncthreads();
 
-  // Producer cursor (thread 0): the next (chunk, sub-chunk) to fetch.
+  const int lane = tid & 31;
+  const bool producer = tid < 32;  // warp 0 walks the producer cursor, every lane alike
+  // Producer cursor (warp 0): the next (chunk, sub-chunk) to fetch.
   int pc = blockIdx.x, psub = 0, issued = 0;
   uint32_t armed = 0, last_parity = 0;
   auto issue_next = [&]() {
@@ -323,14 +326,20 @@ reduce_momentum_bulk_kernel(const __grid_constant__ ReduceParams P,
     const uint32_t bar = fbar(st);
     const uint32_t dst = sbase + (uint32_t)st * C.stage_bytes;
     const uint32_t bytes = (uint32_t)n8 * (cbytes * W + 4u);
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
+    if (lane == 0)
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                   : "memory");
     if (n8 > 0) {
-      for (int w = 0; w < W; ++w)
-        bulk_copy(dst + (uint32_t)(w * E) * cbytes,
-                  static_cast<const uint8_t*>(P.contrib.p[w]) + e0 * cbytes,
-                  (uint32_t)n8 * cbytes, bar);
-      bulk_copy(dst + (uint32_t)(W * E) * cbytes, P.momentum + e0, (uint32_t)n8 * 4u, bar);
+      // one slice per lane: a thread's bulk copies run one after another, so the W + 1 copies
+      // of a stage are spread over the lanes of warp 0 to run side by side
+      for (int w = lane; w <= W; w += 32) {
+        if (w < W)
+          bulk_copy(dst + (uint32_t)(w * E) * cbytes,
+                    static_cast<const uint8_t*>(P.contrib.p[w]) + e0 * cbytes,
+                    (uint32_t)n8 * cbytes, bar);
+        else
+          bulk_copy(dst + (uint32_t)(W * E) * cbytes, P.momentum + e0, (uint32_t)n8 * 4u, bar);
+      }
     }
     armed |= 1u << st;
     last_parity = (last_parity & ~(1u << st)) | ((uint32_t)((issued / S) & 1) << st);
@@ -340,7 +349,7 @@ reduce_momentum_bulk_kernel(const __grid_constant__ ReduceParams P,
       pc += gridDim.x;
     }
   };
-  if (tid == 0)
+  if (producer)
     for (int k = 0; k < S - 1; ++k) issue_next();
 
   float ss = 0.f;
@@ -354,12 +363,11 @@ reduce_momentum_bulk_kernel(const __grid_constant__ ReduceParams P,
     const int64_t cbase = dm.offset + rel0;
     const bool lo_out = dm.split && P.uhat_lo != nullptr;
     for (int64_t sub0 = 0; sub0 < ccnt; sub0 += E, ++q) {
-      if (tid == 0) issue_next();  // stage (q + S - 1) % S was freed by the last barrier
+      if (producer) issue_next();  // stage (q + S - 1) % S was freed by the last barrier
       const int st = q % S;
       const bool ok = bulk_wait(fbar(st), (uint32_t)((q / S) & 1), C.wait_limit_ns, P.status,
                                 &abort_flag, true);
-      if (__syncthreads_or(!ok)) { stop = true; break; }
-      const int n = (int)min((int64_t)E, ccnt - sub0);
+      const int n = ok ? (int)min((int64_t)E, ccnt - sub0) : 0;  // nothing to read on a failure
       const int n8 = n & ~7;
       const int64_t e0 = cbase + sub0;
       const uint8_t* stage = sm + (size_t)st * C.stage_bytes;
@@ -382,7 +390,9 @@ reduce_momentum_bulk_kernel(const __grid_constant__ ReduceParams P,
         finish8(P, lo_out, e0 + (int64_t)v * 8, g, m8, ss);
       }
       if (tid < n - n8) finish1<T>(P, lo_out, e0 + n8 + tid, ss);  // last < 8 elements
-      __syncthreads();  // every thread is done with the stage: the producer may refill it
+      // every thread is done with the stage (the producer may refill it), and all stop together
+      // if any wait failed
+      if (__syncthreads_or(!ok)) { stop = true; break; }
     }
     if (stop) break;
     const float tot = block_sum(ss, red);
@@ -559,11 +569,14 @@ cudaError_t launch_reduce_momentum(const ReduceParams& p, int contrib_dtype, cud
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   // Sub-chunk of E elements: the W contribution slices plus the momentum slice of one stage
-  // fit in kBulkStageBudget bytes; as many stages as fit in kBulkSmemBudget (2 to 8).
+  // fit in kBulkStageBudget bytes (fewer contributions, longer copies: each bulk copy has a
+  // fixed issue cost); as many stages as fit in kBulkSmemBudget (2 to 8).
   const int esz = contrib_dtype == 1 ? 2 : 4;
   const int per_elem = p.W * esz + 4;
-  int E = (int)(kBulkStageBudget / per_elem) / 256 * 256;
-  E = E < 256 ? 256 : (E > 2048 ? 2048 : E);
+  // E is a power of two from 256 up: it divides the chunk, and for E >= 2048 every thread of
+  // the CTA gets the same number of 8-element vectors per stage.
+  int E = 256;
+  while (2 * E <= kChunk && (size_t)(2 * E) * per_elem <= kBulkStageBudget) E *= 2;
   BulkCfg c{};
   c.sub_elems = E;
   c.stage_bytes = E * per_elem;
