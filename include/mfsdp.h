@@ -8,6 +8,8 @@
  * that owner-local step:
  *
  *   mfsdp_plan_owner_set          owner assignment + segment table (host only)   §4.1
+ *   mfsdp_score_plan              per-rank resource estimates, gamma_B (host)     §4.1, §4.2
+ *   mfsdp_plan_cost_aware         CostAware: scope plan within a workspace cap    §4.1
  *   mfsdp_owner_reduce_momentum   W-way gradient deposit + Nesterov momentum + norm  §3, §4.2
  *   mfsdp_newton_schulz           quintic Newton–Schulz of every owned matrix      §2
  *   mfsdp_apply_update            scaled update with decoupled weight decay        §5.1
@@ -97,6 +99,66 @@ typedef enum {
 int mfsdp_plan_owner_set(const mfsdp_param_desc* params, int64_t n_params, int32_t world_size,
                          int32_t policy, mfsdp_segment* seg_out, int64_t* block_rank_numel_out,
                          int64_t* n_blocks_out);
+
+/* Element sizes and step length the resource scorer prices a plan with. */
+typedef struct {
+  int32_t param_bytes;  /* bytes per parameter element (2 = bf16) */
+  int32_t grad_bytes;   /* bytes per gradient element */
+  int32_t state_bytes;  /* bytes per optimizer-state element (4 = fp32) */
+  int32_t ns_steps;     /* Newton–Schulz iterations per optimizer step */
+} mfsdp_cost_model;
+
+/* Per-rank estimates of a plan (§4.1 resource scorer).  The pages name these quantities but
+ * give no formulas; with O_{B,r} the numel of block B owned by rank r, P_B the numel of
+ * block B and W the world size:
+ *   param_bytes / grad_bytes  owned numel x element size;
+ *   state_bytes               (owned matrix numel + 2 x owned tail numel) x state size
+ *                             (Muon momentum; AdamW first and second moments);
+ *   comm_bytes                one owner-segment collective over every block (materialise or
+ *                             gradient reduce), sent + received:
+ *                             sum_B ((W - 1) O_{B,r} + P_B - O_{B,r}) x param_bytes;
+ *   workspace_bytes           receive buffers of the gradient reduce into the rank's owner
+ *                             segments: max_B (W - 1) O_{B,r} x grad_bytes;
+ *   optimizer_flops           nominal Newton–Schulz FLOPs of the owned matrices,
+ *                             ns_steps x (4 m^2 n + 2 m^3), m = min(rows, cols), n = max. */
+typedef struct {
+  int64_t param_bytes;
+  int64_t grad_bytes;
+  int64_t state_bytes;
+  int64_t comm_bytes;
+  int64_t workspace_bytes;
+  double optimizer_flops;
+} mfsdp_rank_resources;
+
+/*
+ * Score a plan made by mfsdp_plan_owner_set (or any segment table with one owner per
+ * parameter).
+ *   segs       [n_params] host array; only owner and numel are read.
+ *   model      element sizes (each >= 1) and ns_steps (>= 0).
+ *   ranks_out  [world_size] host array, written.
+ *   gamma_out  nullable host array of capacity n_params; entry k = gamma_{B_k} =
+ *              max_r O_{B_k,r} / (P_{B_k} / W) (§4.2) for the k-th block in first-appearance
+ *              order, 0 for an empty block.
+ *   n_blocks_out  nullable; receives the number of blocks.
+ * Errors: MFSDP_EINVAL (null arrays with n_params > 0, world_size <= 0, bad model, an owner
+ *         outside [0, world_size)), MFSDP_ESHAPE (negative dimension, numel != rows x cols,
+ *         byte-count overflow).
+ */
+int mfsdp_score_plan(const mfsdp_param_desc* params, int64_t n_params, int32_t world_size,
+                     const mfsdp_segment* segs, const mfsdp_cost_model* model,
+                     mfsdp_rank_resources* ranks_out, double* gamma_out, int64_t* n_blocks_out);
+
+/*
+ * CostAware (§4.1): plan with RoleGreedy and with ScopeGreedy and take the scope plan only if
+ * its largest per-rank workspace_bytes (as scored above) is at most workspace_cap_bytes; a
+ * cap <= 0 stands for the role plan's own largest workspace.  Otherwise the role plan.
+ *   seg_out     [n_params] host array, written with the plan taken.
+ *   policy_out  nullable; receives MFSDP_POLICY_SCOPE_GREEDY or MFSDP_POLICY_ROLE_GREEDY.
+ * Errors: as mfsdp_plan_owner_set and mfsdp_score_plan.
+ */
+int mfsdp_plan_cost_aware(const mfsdp_param_desc* params, int64_t n_params, int32_t world_size,
+                          const mfsdp_cost_model* model, int64_t workspace_cap_bytes,
+                          mfsdp_segment* seg_out, int32_t* policy_out);
 
 /* ------------------------------------------------------------------------------------------
  * The owned-matrix set.  Built once from the owner's matrix table; its launch tables, tensor

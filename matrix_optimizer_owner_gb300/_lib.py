@@ -33,12 +33,28 @@ class Matrix(C.Structure):
     _fields_ = [("rows", C.c_int64), ("cols", C.c_int64), ("offset", C.c_int64)]
 
 
+class CostModel(C.Structure):
+    _fields_ = [("param_bytes", C.c_int32), ("grad_bytes", C.c_int32),
+                ("state_bytes", C.c_int32), ("ns_steps", C.c_int32)]
+
+
+class RankResources(C.Structure):
+    _fields_ = [("param_bytes", C.c_int64), ("grad_bytes", C.c_int64),
+                ("state_bytes", C.c_int64), ("comm_bytes", C.c_int64),
+                ("workspace_bytes", C.c_int64), ("optimizer_flops", C.c_double)]
+
+
 _vp = C.c_void_p
 _i32, _i64, _f32, _u64 = C.c_int32, C.c_int64, C.c_float, C.c_uint64
 
 SIGNATURES = {
     "mfsdp_plan_owner_set": (C.c_int, [C.POINTER(ParamDesc), _i64, _i32, _i32,
                                        C.POINTER(Segment), C.POINTER(_i64), C.POINTER(_i64)]),
+    "mfsdp_score_plan": (C.c_int, [C.POINTER(ParamDesc), _i64, _i32, C.POINTER(Segment),
+                                   C.POINTER(CostModel), C.POINTER(RankResources),
+                                   C.POINTER(C.c_double), C.POINTER(_i64)]),
+    "mfsdp_plan_cost_aware": (C.c_int, [C.POINTER(ParamDesc), _i64, _i32, C.POINTER(CostModel),
+                                        _i64, C.POINTER(Segment), C.POINTER(_i32)]),
     "mfsdp_owner_set_create": (C.c_int, [C.POINTER(Matrix), _i32, _i64, C.POINTER(_vp)]),
     "mfsdp_owner_set_destroy": (C.c_int, [_vp]),
     "mfsdp_owner_set_workspace_bytes": (C.c_int, [_vp, C.POINTER(C.c_size_t)]),

@@ -159,3 +159,132 @@ extern "C" int mfsdp_plan_owner_set(const mfsdp_param_desc* params, int64_t n_pa
   if (n_blocks_out) *n_blocks_out = nb;
   return MFSDP_OK;
 }
+
+// ------------------------------------------------------------------------------------------
+// Resource scorer and CostAware (§4.1), with the §4.2 quantities O_{B,r}, P_B and gamma_B.
+// The pages name the estimates but give no formulas; the ones used here are stated with the
+// declarations: one owner-segment collective's send + receive bytes, the gradient-reduce
+// receive buffers as workspace, nominal Newton–Schulz FLOPs as optimizer compute.
+// ------------------------------------------------------------------------------------------
+namespace {
+
+bool add_overflows(int64_t a, int64_t b) { return b > std::numeric_limits<int64_t>::max() - a; }
+
+int score_impl(const mfsdp_param_desc* params, int64_t n_params, int32_t world_size,
+               const mfsdp_segment* segs, const mfsdp_cost_model* model,
+               mfsdp_rank_resources* ranks_out, double* gamma_out, int64_t* n_blocks_out) {
+  if (n_params < 0 || world_size <= 0 || model == nullptr || ranks_out == nullptr)
+    return MFSDP_EINVAL;
+  if (n_params > 0 && (params == nullptr || segs == nullptr)) return MFSDP_EINVAL;
+  if (model->param_bytes < 1 || model->grad_bytes < 1 || model->state_bytes < 1 ||
+      model->ns_steps < 0)
+    return MFSDP_EINVAL;
+  const int64_t W = world_size;
+  std::unordered_map<int32_t, int32_t> block_pos;
+  std::vector<int64_t> pb;  // P_B
+  std::vector<int32_t> pos(n_params);
+  for (int64_t i = 0; i < n_params; ++i) {
+    const mfsdp_param_desc& p = params[i];
+    if (p.rows < 0 || p.cols < 0 || mul_overflows(p.rows, p.cols)) return MFSDP_ESHAPE;
+    if (segs[i].numel != p.rows * p.cols) return MFSDP_ESHAPE;
+    if (segs[i].owner < 0 || segs[i].owner >= world_size) return MFSDP_EINVAL;
+    auto it = block_pos.emplace(p.block, (int32_t)pb.size());
+    if (it.second) pb.push_back(0);
+    pos[i] = it.first->second;
+    if (add_overflows(pb[pos[i]], segs[i].numel)) return MFSDP_ESHAPE;
+    pb[pos[i]] += segs[i].numel;
+  }
+  const int64_t nb = (int64_t)pb.size();
+  std::vector<int64_t> o((size_t)(nb * W), 0);  // O_{B,r}
+  std::vector<int64_t> mat(W, 0), tail(W, 0);
+  std::vector<double> flops(W, 0.0);
+  for (int64_t i = 0; i < n_params; ++i) {
+    const int32_t r = segs[i].owner;
+    const int64_t ne = segs[i].numel;
+    o[(size_t)(pos[i] * W + r)] += ne;
+    if (params[i].is_matrix) {
+      mat[r] += ne;
+      if (ne > 0) {
+        const int64_t m = std::min(params[i].rows, params[i].cols);
+        const int64_t n = std::max(params[i].rows, params[i].cols);
+        flops[r] += (double)model->ns_steps *
+                    (4.0 * (double)m * (double)m * (double)n + 2.0 * (double)(m * m * m));
+      }
+    } else {
+      tail[r] += ne;
+    }
+  }
+  const int64_t big = std::numeric_limits<int64_t>::max() / 4;
+  for (int32_t r = 0; r < world_size; ++r) {
+    const int64_t own = mat[r] + tail[r];
+    int64_t comm = 0, ws = 0;
+    for (int64_t b = 0; b < nb; ++b) {
+      const int64_t obr = o[(size_t)(b * W + r)];
+      if (obr > big / W) return MFSDP_ESHAPE;
+      comm += (W - 1) * obr + (pb[b] - obr);
+      if (comm > big) return MFSDP_ESHAPE;
+      ws = std::max(ws, (W - 1) * obr);
+    }
+    if (own > big / 8 || comm > big / 8 || ws > big / 8) return MFSDP_ESHAPE;
+    mfsdp_rank_resources& x = ranks_out[r];
+    x.param_bytes = own * model->param_bytes;
+    x.grad_bytes = own * model->grad_bytes;
+    x.state_bytes = (mat[r] + 2 * tail[r]) * model->state_bytes;
+    x.comm_bytes = comm * model->param_bytes;
+    x.workspace_bytes = ws * model->grad_bytes;
+    x.optimizer_flops = flops[r];
+  }
+  if (gamma_out) {
+    for (int64_t b = 0; b < nb; ++b) {
+      int64_t mx = 0;
+      for (int32_t r = 0; r < world_size; ++r) mx = std::max(mx, o[(size_t)(b * W + r)]);
+      gamma_out[b] = pb[b] > 0 ? (double)mx / ((double)pb[b] / (double)W) : 0.0;
+    }
+  }
+  if (n_blocks_out) *n_blocks_out = nb;
+  return MFSDP_OK;
+}
+
+int64_t max_workspace(const std::vector<mfsdp_rank_resources>& rs) {
+  int64_t m = 0;
+  for (const mfsdp_rank_resources& x : rs) m = std::max(m, x.workspace_bytes);
+  return m;
+}
+
+}  // namespace
+
+extern "C" int mfsdp_score_plan(const mfsdp_param_desc* params, int64_t n_params,
+                                int32_t world_size, const mfsdp_segment* segs,
+                                const mfsdp_cost_model* model, mfsdp_rank_resources* ranks_out,
+                                double* gamma_out, int64_t* n_blocks_out) {
+  return score_impl(params, n_params, world_size, segs, model, ranks_out, gamma_out,
+                    n_blocks_out);
+}
+
+extern "C" int mfsdp_plan_cost_aware(const mfsdp_param_desc* params, int64_t n_params,
+                                     int32_t world_size, const mfsdp_cost_model* model,
+                                     int64_t workspace_cap_bytes, mfsdp_segment* seg_out,
+                                     int32_t* policy_out) {
+  if (n_params < 0 || world_size <= 0 || model == nullptr) return MFSDP_EINVAL;
+  if (n_params > 0 && (params == nullptr || seg_out == nullptr)) return MFSDP_EINVAL;
+  std::vector<mfsdp_segment> role((size_t)n_params), scope((size_t)n_params);
+  int st = mfsdp_plan_owner_set(params, n_params, world_size, MFSDP_POLICY_ROLE_GREEDY,
+                                role.data(), nullptr, nullptr);
+  if (st != MFSDP_OK) return st;
+  st = mfsdp_plan_owner_set(params, n_params, world_size, MFSDP_POLICY_SCOPE_GREEDY,
+                            scope.data(), nullptr, nullptr);
+  if (st != MFSDP_OK) return st;
+  std::vector<mfsdp_rank_resources> rs_role(world_size), rs_scope(world_size);
+  st = score_impl(params, n_params, world_size, role.data(), model, rs_role.data(), nullptr,
+                  nullptr);
+  if (st != MFSDP_OK) return st;
+  st = score_impl(params, n_params, world_size, scope.data(), model, rs_scope.data(), nullptr,
+                  nullptr);
+  if (st != MFSDP_OK) return st;
+  const int64_t cap = workspace_cap_bytes > 0 ? workspace_cap_bytes : max_workspace(rs_role);
+  const bool take_scope = max_workspace(rs_scope) <= cap;
+  const std::vector<mfsdp_segment>& pick = take_scope ? scope : role;
+  std::copy(pick.begin(), pick.end(), seg_out);
+  if (policy_out) *policy_out = take_scope ? MFSDP_POLICY_SCOPE_GREEDY : MFSDP_POLICY_ROLE_GREEDY;
+  return MFSDP_OK;
+}

@@ -12,7 +12,7 @@ import ctypes as C
 from typing import Optional, Sequence, Tuple
 
 from . import _lib
-from ._lib import Matrix, ParamDesc, Segment
+from ._lib import CostModel, Matrix, ParamDesc, RankResources, Segment
 
 POLICY_ROLE_GREEDY = 0
 POLICY_SCOPE_GREEDY = 1
@@ -87,6 +87,55 @@ def mfsdp_plan_owner_set(params: Sequence[Tuple[int, int, int, bool]], world_siz
              "rank_offset": s.rank_offset, "numel": s.numel} for s in seg[:n]]
     table = [[brn[k * world_size + r] for r in range(world_size)] for k in range(nb.value)]
     return segs, table, nb.value
+
+
+def _param_array(params):
+    n = len(params)
+    pd = (ParamDesc * max(n, 1))()
+    for i, (r, c, b, m) in enumerate(params):
+        pd[i] = ParamDesc(r, c, b, 1 if m else 0)
+    return pd
+
+
+def _cost_model(param_bytes, grad_bytes, state_bytes, ns_steps):
+    return CostModel(param_bytes, grad_bytes, state_bytes, ns_steps)
+
+
+def mfsdp_score_plan(params: Sequence[Tuple[int, int, int, bool]], world_size: int,
+                     segments: Sequence[dict], param_bytes: int = 2, grad_bytes: int = 2,
+                     state_bytes: int = 4, ns_steps: int = 5):
+    """Per-rank resource estimates and gamma_B of a plan (segments as returned by
+    ``mfsdp_plan_owner_set``).  Returns (list of per-rank dicts, gamma per block)."""
+    lib = _lib.load()
+    n = len(params)
+    seg = (Segment * max(n, 1))()
+    for i, s in enumerate(segments):
+        seg[i] = Segment(s["owner"], s["role"], s["local_offset"], s["rank_offset"], s["numel"])
+    out = (RankResources * world_size)()
+    gam = (C.c_double * max(n, 1))()
+    nb = C.c_int64(0)
+    model = _cost_model(param_bytes, grad_bytes, state_bytes, ns_steps)
+    _check("mfsdp_score_plan", lib.mfsdp_score_plan(_param_array(params), n, world_size, seg,
+                                                    C.byref(model), out, gam, C.byref(nb)))
+    ranks = [{k: getattr(x, k) for k, _ in RankResources._fields_} for x in out]
+    return ranks, [gam[k] for k in range(nb.value)]
+
+
+def mfsdp_plan_cost_aware(params: Sequence[Tuple[int, int, int, bool]], world_size: int,
+                          workspace_cap_bytes: int = 0, param_bytes: int = 2, grad_bytes: int = 2,
+                          state_bytes: int = 4, ns_steps: int = 5):
+    """CostAware plan.  Returns (segments, policy taken)."""
+    lib = _lib.load()
+    n = len(params)
+    seg = (Segment * max(n, 1))()
+    pol = C.c_int32(-1)
+    model = _cost_model(param_bytes, grad_bytes, state_bytes, ns_steps)
+    _check("mfsdp_plan_cost_aware",
+           lib.mfsdp_plan_cost_aware(_param_array(params), n, world_size, C.byref(model),
+                                     workspace_cap_bytes, seg, C.byref(pol)))
+    segs = [{"owner": s.owner, "role": s.role, "local_offset": s.local_offset,
+             "rank_offset": s.rank_offset, "numel": s.numel} for s in seg[:n]]
+    return segs, pol.value
 
 
 # ------------------------------------------------------------------------------- owner set

@@ -193,3 +193,88 @@ def owned(params: Sequence[Param], segs: Sequence[Segment], rank: int):
     tails = sorted((s.rank_offset, i) for i, s in enumerate(segs)
                    if s.owner == rank and not params[i].is_matrix)
     return [i for _, i in mats], [i for _, i in tails]
+
+
+# ---------------------------------------------------------------------------------------------
+# Resource scorer and the cost-aware policy (§4.1, §4.2).
+#
+# The pages name the scorer's outputs (per-rank parameter, gradient, optimizer-state,
+# communication and workspace estimates) and the CostAware rule (take the ScopeGreedy plan
+# only when its balance gain stays within workspace caps) but print no formulas for them.
+# Readings, each the plainest one the §4.2 bandwidth model supports:
+#
+# * parameter / gradient bytes of rank r: its owned numel times the element size;
+# * optimizer-state bytes: one momentum buffer per owned matrix element (Muon), two moments
+#   per owned tail element (AdamW), at the state element size;
+# * communication bytes of rank r for one owner-segment collective over every block
+#   (materialise, or gradient reduce: the two move the same bytes in opposite directions):
+#   sum over blocks of (W - 1) O_{B,r} sent (its segment to every other rank) plus
+#   P_B - O_{B,r} received (everyone else's segments), times the element size;
+# * workspace bytes of rank r: the receive buffers of the gradient reduce into its owner
+#   segments, (W - 1) O_{B,r} gradient elements, for the block where that is largest;
+# * optimizer compute of rank r: nominal Newton–Schulz FLOPs of its owned matrices,
+#   steps * (4 m^2 n + 2 m^3) with m = min(rows, cols), n = max(rows, cols);
+# * CostAware: plan with RoleGreedy and with ScopeGreedy; take the scope plan if its largest
+#   per-rank workspace is at most the cap, else keep the role plan.  A cap <= 0 means the
+#   role plan's own largest workspace (the scope plan may not need more).
+# ---------------------------------------------------------------------------------------------
+
+COST_AWARE = 2
+
+
+@dataclass(frozen=True)
+class RankResources:
+    param_bytes: int
+    grad_bytes: int
+    state_bytes: int
+    comm_bytes: int
+    workspace_bytes: int
+    optimizer_flops: float
+
+
+def score_plan(params: Sequence[Param], segs: Sequence[Segment], world_size: int,
+               param_bytes: int = 2, grad_bytes: int = 2, state_bytes: int = 4,
+               ns_steps: int = 5) -> List[RankResources]:
+    """Per-rank resource estimates of a completed plan (§4.1 resource scorer)."""
+    W = world_size
+    o = block_rank_numel(params, segs, W)
+    blocks = block_order(params)
+    pb = {b: sum(p.numel for p in params if p.block == b) for b in blocks}
+    out = []
+    for r in range(W):
+        own = [i for i, s in enumerate(segs) if s.owner == r]
+        numel = sum(params[i].numel for i in own)
+        mat = sum(params[i].numel for i in own if params[i].is_matrix)
+        tail = numel - mat
+        comm = sum((W - 1) * o[(b, r)] + (pb[b] - o[(b, r)]) for b in blocks) * param_bytes
+        ws = max([(W - 1) * o[(b, r)] for b in blocks] + [0]) * grad_bytes
+        flops = 0.0
+        for i in own:
+            p = params[i]
+            if p.is_matrix and p.numel > 0:
+                m, n = min(p.rows, p.cols), max(p.rows, p.cols)
+                flops += ns_steps * (4.0 * m * m * n + 2.0 * m ** 3)
+        out.append(RankResources(numel * param_bytes, numel * grad_bytes,
+                                 (mat + 2 * tail) * state_bytes, comm, ws, flops))
+    return out
+
+
+def imbalance(values: Sequence[float]) -> float:
+    """max / mean over ranks (1 = flat); 0 when every value is 0."""
+    tot = float(sum(values))
+    return (max(values) / (tot / len(values))) if tot > 0 else 0.0
+
+
+def plan_cost_aware(params: Sequence[Param], world_size: int, workspace_cap_bytes: int = 0,
+                    param_bytes: int = 2, grad_bytes: int = 2, state_bytes: int = 4,
+                    ns_steps: int = 5) -> Tuple[List[Segment], int]:
+    """CostAware (§4.1): the ScopeGreedy plan if its largest workspace is within the cap,
+    else the RoleGreedy plan.  Returns (segments, the policy taken)."""
+    role = plan(params, world_size, ROLE_GREEDY)
+    scope = plan(params, world_size, SCOPE_GREEDY)
+    kw = dict(param_bytes=param_bytes, grad_bytes=grad_bytes, state_bytes=state_bytes,
+              ns_steps=ns_steps)
+    ws_role = max(x.workspace_bytes for x in score_plan(params, role, world_size, **kw))
+    ws_scope = max(x.workspace_bytes for x in score_plan(params, scope, world_size, **kw))
+    cap = workspace_cap_bytes if workspace_cap_bytes > 0 else ws_role
+    return (scope, SCOPE_GREEDY) if ws_scope <= cap else (role, ROLE_GREEDY)

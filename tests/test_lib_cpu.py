@@ -98,6 +98,76 @@ def test_planner_bit_exact_on_random_sets(lib):
             assert table == otable
 
 
+def _oracle_score(params, W, segs, **kw):
+    ps = [oplan.Param(r, c, b, m) for r, c, b, m in params]
+    osegs = [oplan.Segment(s["owner"], s["role"], s["local_offset"], s["rank_offset"],
+                           s["numel"]) for s in segs]
+    ranks = [x.__dict__ for x in oplan.score_plan(ps, osegs, W, **kw)]
+    gam = oplan.gamma(ps, osegs, W)
+    return ranks, [gam[b] for b in oplan.block_order(ps)]
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+def test_scorer_and_cost_aware_bit_exact_on_workloads(lib, cfg):
+    from matrix_optimizer_owner_gb300 import mfsdp
+    wl = get_config(cfg)
+    params = _params(wl)
+    ps = [oplan.Param(r, c, b, m) for r, c, b, m in params]
+    for W in sorted({1, 2, 3, 8, wl.world_size}):
+        for policy in (0, 1):
+            segs, _, _ = mfsdp.mfsdp_plan_owner_set(params, W, policy)
+            for kw in ({}, dict(param_bytes=4, grad_bytes=4, state_bytes=8, ns_steps=2)):
+                ranks, gam = mfsdp.mfsdp_score_plan(params, W, segs, **kw)
+                oranks, ogam = _oracle_score(params, W, segs, **kw)
+                assert ranks == oranks
+                assert gam == ogam
+        for cap in (0, 1, 1 << 40):
+            segs, pol = mfsdp.mfsdp_plan_cost_aware(params, W, cap)
+            osegs, opol = oplan.plan_cost_aware(ps, W, cap)
+            assert pol == opol
+            assert segs == [s.__dict__ for s in osegs]
+
+
+def test_scorer_bit_exact_on_random_sets(lib):
+    from matrix_optimizer_owner_gb300 import mfsdp
+    rng = np.random.default_rng(321)
+    for trial in range(200):
+        n = int(rng.integers(0, 25))
+        params = []
+        for _ in range(n):
+            is_mat = bool(rng.random() < 0.6)
+            r = int(rng.integers(0, 300))
+            c = int(rng.integers(0, 300)) if is_mat else 1
+            params.append((r, c, int(rng.integers(0, 4)), is_mat))
+        W = int(rng.integers(1, 6))
+        segs, _, _ = mfsdp.mfsdp_plan_owner_set(params, W, int(rng.integers(0, 2)))
+        ranks, gam = mfsdp.mfsdp_score_plan(params, W, segs)
+        assert (ranks, gam) == _oracle_score(params, W, segs), trial
+        ps = [oplan.Param(r, c, b, m) for r, c, b, m in params]
+        cap = int(rng.integers(0, 4000))
+        segs, pol = mfsdp.mfsdp_plan_cost_aware(params, W, cap)
+        osegs, opol = oplan.plan_cost_aware(ps, W, cap)
+        assert pol == opol and segs == [s.__dict__ for s in osegs], trial
+
+
+def test_scorer_error_codes(lib):
+    from matrix_optimizer_owner_gb300 import _lib as L
+    pd = (L.ParamDesc * 1)(L.ParamDesc(2, 2, 0, 1))
+    seg = (L.Segment * 1)(L.Segment(0, 0, 0, 0, 4))
+    out = (L.RankResources * 2)()
+    good = L.CostModel(2, 2, 4, 5)
+    assert lib.mfsdp_score_plan(pd, 1, 2, seg, C.byref(good), out, None, None) == 0
+    assert lib.mfsdp_score_plan(pd, 1, 2, seg, None, out, None, None) == -1       # no model
+    bad_model = L.CostModel(0, 2, 4, 5)
+    assert lib.mfsdp_score_plan(pd, 1, 2, seg, C.byref(bad_model), out, None, None) == -1
+    bad_owner = (L.Segment * 1)(L.Segment(2, 0, 0, 0, 4))
+    assert lib.mfsdp_score_plan(pd, 1, 2, bad_owner, C.byref(good), out, None, None) == -1
+    bad_numel = (L.Segment * 1)(L.Segment(0, 0, 0, 0, 5))
+    assert lib.mfsdp_score_plan(pd, 1, 2, bad_numel, C.byref(good), out, None, None) == -2
+    assert lib.mfsdp_plan_cost_aware(pd, 1, 0, C.byref(good), 0, seg, None) == -1  # world size
+    assert lib.mfsdp_plan_cost_aware(pd, 1, 2, None, 0, seg, None) == -1           # no model
+
+
 def test_planner_error_codes(lib):
     from matrix_optimizer_owner_gb300 import _lib as L
     pd = (L.ParamDesc * 1)(L.ParamDesc(2, 2, 0, 1))

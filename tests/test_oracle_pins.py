@@ -366,3 +366,60 @@ def test_gamma_model():
     assert plan.gamma(ps, segs, 4)[0] == pytest.approx(4.0)
     ps = [plan.Param(4, 4, 0, True) for _ in range(4)]
     assert plan.gamma(ps, plan.plan(ps, 4), 4)[0] == pytest.approx(1.0)
+
+
+def test_score_plan_hand_worked():
+    # One block: matrices 4x2 (8) and 2x3 (6), then a tail vector of 5.  Two ranks, RoleGreedy:
+    # 8 -> r0; 6 -> r1; tail 5 -> r1 (6 < 8): O_{B,0} = 8, O_{B,1} = 11, P_B = 19.
+    ps = [plan.Param(4, 2, 0, True), plan.Param(2, 3, 0, True), plan.Param(5, 1, 0, False)]
+    segs = plan.plan(ps, 2)
+    assert [s.owner for s in segs] == [0, 1, 1]
+    r0, r1 = plan.score_plan(ps, segs, 2, param_bytes=2, grad_bytes=2, state_bytes=4,
+                             ns_steps=5)
+    # params/grads: owned numel x 2 B; state: matrices x 4 B + tail x 2 moments x 4 B
+    assert (r0.param_bytes, r0.grad_bytes, r0.state_bytes) == (16, 16, 32)
+    assert (r1.param_bytes, r1.grad_bytes, r1.state_bytes) == (22, 22, 64)
+    # one collective: send (W-1) O + receive P - O, x 2 B: r0 (8 + 11) * 2, r1 (11 + 8) * 2
+    assert r0.comm_bytes == 38 and r1.comm_bytes == 38
+    # reduce receive buffers (W-1) O x 2 B
+    assert r0.workspace_bytes == 16 and r1.workspace_bytes == 22
+    # Newton-Schulz: 4x2 -> m=2, n=4: 5 (4*4*4 + 2*8) = 400; 2x3 -> m=2, n=3: 5 (48 + 16) = 320
+    assert r0.optimizer_flops == 400.0 and r1.optimizer_flops == 320.0
+    assert plan.gamma(ps, segs, 2)[0] == pytest.approx(22 / 19)
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3])
+def test_score_plan_sums_over_ranks(cfg):
+    wl = get_config(cfg)
+    ps = _params(wl)
+    total = sum(p.numel for p in ps)
+    mats = sum(p.numel for p in ps if p.is_matrix)
+    nominal = sum(5 * (4 * min(p.rows, p.cols) ** 2 * max(p.rows, p.cols)
+                       + 2 * min(p.rows, p.cols) ** 3) for p in ps if p.is_matrix)
+    for W in (1, 3, 8):
+        for pol in (plan.ROLE_GREEDY, plan.SCOPE_GREEDY):
+            sc = plan.score_plan(ps, plan.plan(ps, W, pol), W)
+            assert sum(x.param_bytes for x in sc) == 2 * total
+            assert sum(x.state_bytes for x in sc) == 4 * (mats + 2 * (total - mats))
+            # every block's elements are sent W-1 times and received W-1 times in all
+            assert sum(x.comm_bytes for x in sc) == 2 * (W - 1) * total * 2
+            assert sum(x.optimizer_flops for x in sc) == pytest.approx(nominal, rel=1e-12)
+            if W == 1:
+                assert all(x.comm_bytes == 0 and x.workspace_bytes == 0 for x in sc)
+
+
+def test_cost_aware_takes_scope_only_within_the_cap():
+    wl = get_config(2)
+    ps = _params(wl)
+    role = plan.plan(ps, 8, plan.ROLE_GREEDY)
+    scope = plan.plan(ps, 8, plan.SCOPE_GREEDY)
+    ws_role = max(x.workspace_bytes for x in plan.score_plan(ps, role, 8))
+    ws_scope = max(x.workspace_bytes for x in plan.score_plan(ps, scope, 8))
+    assert ws_scope > ws_role  # pooling stacks more of one block on a rank
+    assert plan.plan_cost_aware(ps, 8) == (role, plan.ROLE_GREEDY)
+    assert plan.plan_cost_aware(ps, 8, ws_scope) == (scope, plan.SCOPE_GREEDY)
+    assert plan.plan_cost_aware(ps, 8, ws_scope - 1) == (role, plan.ROLE_GREEDY)
+    # a flatter plan with no workspace cost is taken
+    same = [plan.Param(4, 4, b, True) for b in range(6)]
+    assert plan.plan_cost_aware(same, 3)[1] == plan.SCOPE_GREEDY
+    assert plan.imbalance([2.0, 2.0]) == 1.0 and plan.imbalance([3.0, 1.0]) == 1.5
