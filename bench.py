@@ -58,6 +58,8 @@ NS_TRAFFIC_SOURCES = ("matrix_optimizer_owner_gb300/csrc/ns_gemm.cu",
                       "matrix_optimizer_owner_gb300/csrc/mfsdp_internal.h")
 NS_TRAFFIC = {
     # config index: (sources sha256, bytes per launch, profile summary)
+    1: ("0a763903af3477bd49aaf702376cffc49a1457ac0db4903cfc115ae1accbc724", 208507716,
+        "profiles/owner_step_gpt2_small_launch_list.md"),
 }
 
 
@@ -334,6 +336,34 @@ def time_e2e(wb, steps, stream):
     return s.elapsed_time(e) / steps, h2d, norm_h.numel() * 4
 
 
+def time_repack(wb, reps, stream, world=8):
+    """Owner-segment repacking of the workload's whole parameter list (2-byte elements): pack
+    the canonical buffer into the owner shards of a RoleGreedy plan over ``world`` ranks, all
+    held on this GPU.  HBM traffic = read + write of every parameter byte."""
+    from matrix_optimizer_owner_gb300 import mfsdp
+    params = [(p.rows, p.cols, p.block, p.is_matrix) for p in wb.wl.params]
+    segs, table, _ = mfsdp.mfsdp_plan_owner_set(params, world, mfsdp.POLICY_ROLE_GREEDY)
+    sizes = [sum(row[r] for row in table) for r in range(world)]
+    total = sum(sizes)
+    canon = torch.empty(total, dtype=torch.bfloat16, device=stream.device)
+    canon.view(torch.int16).random_()
+    shards = [torch.empty(n, dtype=torch.bfloat16, device=stream.device) for n in sizes]
+    ws = torch.empty(mfsdp.mfsdp_repack_workspace_bytes(len(params)), dtype=torch.uint8,
+                     device=stream.device)
+    for _ in range(3):
+        mfsdp.mfsdp_pack_owner_shards(params, segs, world, canon, shards, ws, stream)
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(reps):
+        mfsdp.mfsdp_pack_owner_shards(params, segs, world, canon, shards, ws, stream)
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / reps
+    return ms, 2 * total * 2, len(params)
+
+
 def config_block(wb, cfg):
     wl = wb.wl
     return {"workload": wl.name, "config_index": cfg, "owner_rank": wb.rank,
@@ -413,6 +443,14 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": wb.launches_per_step() * args.steps,
         "clocks": clocks, "device_status": status,
     }
+    if not args.no_repack:
+        rms, rbytes, nparams = time_repack(wb, 10, stream)
+        line["repack"] = {
+            "kernel": "segment_copy_kernel", "what": f"pack {nparams} parameters (2-byte "
+            "elements) from the canonical axis into 8-rank RoleGreedy owner shards",
+            "ms": round(rms, 4), "bytes": rbytes, "bound": "hbm",
+            "achieved_gbs": round(rbytes / (rms * 1e-3) / 1e9, 1), "peak_gbs": peaks["hbm_gbs"],
+            "frac": round(rbytes / (rms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 4)}
     if rank == 0 and not args.no_cpu_baseline:
         spent, flops, elems, sample = oracle_sample(wb, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(extrapolated_ms(wb, spent, flops), 1), "unit": "ms",
@@ -493,6 +531,8 @@ def main():
     ap.add_argument("--ref-mats", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-repack", action="store_true",
+                    help="skip the owner-shard repacking measurement")
     ap.add_argument("--clock-window-s", type=float, default=1.0)
     args = ap.parse_args()
 

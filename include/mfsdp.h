@@ -10,6 +10,8 @@
  *   mfsdp_plan_owner_set          owner assignment + segment table (host only)   §4.1
  *   mfsdp_score_plan              per-rank resource estimates, gamma_B (host)     §4.1, §4.2
  *   mfsdp_plan_cost_aware         CostAware: scope plan within a workspace cap    §4.1
+ *   mfsdp_pack_owner_shards /     canonical axis <-> owner shards (reshard load)  §4.4
+ *   mfsdp_unpack_owner_shards
  *   mfsdp_owner_reduce_momentum   W-way gradient deposit + Nesterov momentum + norm  §3, §4.2
  *   mfsdp_newton_schulz           quintic Newton–Schulz of every owned matrix      §2
  *   mfsdp_apply_update            scaled update with decoupled weight decay        §5.1
@@ -159,6 +161,52 @@ int mfsdp_score_plan(const mfsdp_param_desc* params, int64_t n_params, int32_t w
 int mfsdp_plan_cost_aware(const mfsdp_param_desc* params, int64_t n_params, int32_t world_size,
                           const mfsdp_cost_model* model, int64_t workspace_cap_bytes,
                           mfsdp_segment* seg_out, int32_t* policy_out);
+
+/* ------------------------------------------------------------------------------------------
+ * Owner-segment repacking (§4.1, §4.2, §4.4): moving parameters (or gradients, or optimizer
+ * state of the same shape) between the canonical axis and owner shards.
+ *
+ * Layouts.  Canonical buffer: the parameters back to back in declaration order, parameter i
+ * at sum_{j<i} numel_j elements.  Owner shard of rank r: r's block-local shards back to back
+ * in block order (first appearance), parameter i (owned by r) at
+ * sum_{B' before B} O_{B',r} + segs[i].local_offset elements — the concatenation of the
+ * FSDP block shards a plan from mfsdp_plan_owner_set gives rank r.
+ *
+ * Reshard load (§4.4) is mfsdp_unpack_owner_shards under the saved plan followed by
+ * mfsdp_pack_owner_shards under the target plan and world size.
+ *
+ * Common arguments:
+ *   params, segs   [n_params] host arrays; segs as written by mfsdp_plan_owner_set (owner,
+ *                  local_offset, numel are read; numel must equal rows x cols and each
+ *                  segment must lie inside its block-local shard).
+ *   elem_bytes     element size: 1, 2, 4 or 8.  Elements are copied bit for bit.
+ *   shards         host array of world_size DEVICE pointers, one owner shard per rank; a NULL
+ *                  entry skips that rank (a rank that holds only its own shard passes the
+ *                  others as NULL).
+ *   canonical      DEVICE pointer to the canonical buffer.
+ *   workspace      DEVICE buffer of at least mfsdp_repack_workspace_bytes(n_params) bytes for
+ *                  the copy table; reused by the next call on the same stream.
+ * Buffers may start at any element boundary; ranges whose source and destination share their
+ * alignment mod 16 bytes move as 16-byte vectors.  Source and destination must not overlap.
+ * Errors: MFSDP_EINVAL (null arrays, world_size <= 0, bad elem_bytes, owner out of range),
+ *         MFSDP_ESHAPE (numel mismatch, a segment outside its shard), MFSDP_EWORKSPACE,
+ *         MFSDP_ECUDA.  Enqueued on `stream`; returns without synchronising.
+ * ------------------------------------------------------------------------------------------ */
+
+int mfsdp_repack_workspace_bytes(int64_t n_params, size_t* bytes_out);
+
+/* Canonical buffer -> the owner shard of every rank whose shards[r] is not NULL. */
+int mfsdp_pack_owner_shards(const mfsdp_param_desc* params, int64_t n_params,
+                            const mfsdp_segment* segs, int32_t world_size, int32_t elem_bytes,
+                            const void* canonical, void* const* shards, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Owner shards of the ranks whose shards[r] is not NULL -> their parameters' places in the
+ * canonical buffer (the rest of the canonical buffer is left as it was). */
+int mfsdp_unpack_owner_shards(const mfsdp_param_desc* params, int64_t n_params,
+                              const mfsdp_segment* segs, int32_t world_size, int32_t elem_bytes,
+                              const void* const* shards, void* canonical, void* workspace,
+                              size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------
  * The owned-matrix set.  Built once from the owner's matrix table; its launch tables, tensor

@@ -55,6 +55,12 @@ SIGNATURES = {
                                    C.POINTER(C.c_double), C.POINTER(_i64)]),
     "mfsdp_plan_cost_aware": (C.c_int, [C.POINTER(ParamDesc), _i64, _i32, C.POINTER(CostModel),
                                         _i64, C.POINTER(Segment), C.POINTER(_i32)]),
+    "mfsdp_repack_workspace_bytes": (C.c_int, [_i64, C.POINTER(C.c_size_t)]),
+    "mfsdp_pack_owner_shards": (C.c_int, [C.POINTER(ParamDesc), _i64, C.POINTER(Segment), _i32,
+                                          _i32, _vp, C.POINTER(_vp), _vp, C.c_size_t, _vp]),
+    "mfsdp_unpack_owner_shards": (C.c_int, [C.POINTER(ParamDesc), _i64, C.POINTER(Segment),
+                                            _i32, _i32, C.POINTER(_vp), _vp, _vp, C.c_size_t,
+                                            _vp]),
     "mfsdp_owner_set_create": (C.c_int, [C.POINTER(Matrix), _i32, _i64, C.POINTER(_vp)]),
     "mfsdp_owner_set_destroy": (C.c_int, [_vp]),
     "mfsdp_owner_set_workspace_bytes": (C.c_int, [_vp, C.POINTER(C.c_size_t)]),

@@ -687,20 +687,6 @@ __device__ __forceinline__ uint4 load_granule(const uint16_t* p, int64_t ld, int
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Store eight bf16 at (r, c); elements outside M x N are not written.
-__device__ __forceinline__ void store_granule(uint16_t* p, int64_t ld, int r, int c, int M, int N,
-                                              uint4 v) {
-  if (r >= M || c >= N) return;
-  uint16_t* dst = p + (int64_t)r * ld + c;
-  if (c + 8 <= N) {
-    *reinterpret_cast<uint4*>(dst) = v;
-    return;
-  }
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  for (int e = 0; e < 8; ++e)
-    if (c + e < N) dst[e] = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
-}
-
 // tcgen05.ld of 32 consecutive fp32 columns of this thread's TMEM lane, split in issue and
 // wait so that other work overlaps the load; the registers are read-write operands of the
 // wait, so no use of them can move above it.

@@ -236,14 +236,20 @@ reduce_momentum_kernel(const __grid_constant__ ReduceParams P) {
 // Owner gradient deposit + Nesterov momentum + norm partials, bulk-copy path.
 // A persistent grid walks the same per-matrix chunk partition (chunk c = CTA c of the
 // partition; CTA b takes chunks b, b + grid, ...).  Each chunk is split into sub-chunks of
-// E elements; warp 0 streams every sub-chunk's W contribution slices and momentum slice
-// (one slice per lane) into a ring of shared-memory stages with cp.async.bulk (completion
-// counted on one mbarrier per stage) several stages ahead, and all 256 threads consume a
-// stage from shared memory and write the new momentum and the bf16 NS input straight to
-// global memory.  A chunk is always
-// processed by one CTA with the same element-to-thread mapping, so its norm partial does not
-// depend on the grid size.  Waits are bounded; on expiry the kernel records a timeout, stops
-// issuing, drains its copies in flight and exits.
+// E elements that flow through a ring of S shared-memory stages:
+//   warp 8 (producer)  for each sub-chunk, once all consumer warps have released the stage
+//                      (its empty mbarrier), copies the W contribution slices and the momentum
+//                      slice in with cp.async.bulk, one slice per lane (a thread's bulk copies
+//                      run one after another), completion counted on the stage's full
+//                      mbarrier;
+//   warps 0-7          wait for the stage, form G, the new momentum and the bf16 NS input for
+//                      their 8-element vectors, write them to global memory, add u^2 to a
+//                      per-thread sum, and release the stage (one arrival per warp).
+// Warps are only coupled through the ring, never by a CTA-wide barrier.  At the end of a chunk
+// each warp reduces its sum (xor-shuffle tree) into a per-chunk slot; the last warp to finish
+// the chunk adds the eight warp sums in warp order and writes the chunk's partial, so the
+// partial is the same for any grid size and any warp timing.  Waits are bounded; on expiry
+// the kernel records a timeout, stops, waits for its copies in flight and exits.
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ bool bulk_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -287,124 +293,150 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+constexpr int kConsumerWarps = kStreamThreads / 32;
+constexpr int kBulkThreads = kStreamThreads + 32;  // consumers + the producer warp
+constexpr int kChunkSlots = 16;                     // > stages: a warp runs at most S ahead
+
 template <typename T>
-__global__ void __launch_bounds__(kStreamThreads, 1)
+__global__ void __launch_bounds__(kBulkThreads, 1)
 reduce_momentum_bulk_kernel(const __grid_constant__ ReduceParams P,
                             const __grid_constant__ BulkCfg C) {
   extern __shared__ __align__(128) uint8_t sm[];
-  __shared__ float red[kStreamThreads / 32];
-  __shared__ int abort_flag;
   __shared__ __align__(8) uint64_t full[kMaxBulkStages];
-  const int tid = threadIdx.x;
+  __shared__ __align__(8) uint64_t empty[kMaxBulkStages];
+  __shared__ float wsum[kChunkSlots][kConsumerWarps];
+  __shared__ int wdone[kChunkSlots];
+  __shared__ int abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int W = P.W, E = C.sub_elems, S = C.stages;
   const uint32_t cbytes = (uint32_t)sizeof(T);
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(sm);
-  auto fbar = [&](int s) { return (uint32_t)__cvta_generic_to_shared(&full[s]); };
+  auto fbar = [&](int st) { return (uint32_t)__cvta_generic_to_shared(&full[st]); };
+  auto ebar = [&](int st) { return (uint32_t)__cvta_generic_to_shared(&empty[st]); };
   if (tid == 0) {
-    for (int s = 0; s < S; ++s)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(fbar(s)), "r"(1u));
+    for (int st = 0; st < S; ++st) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(fbar(st)), "r"(1u));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(ebar(st)),
+                   "r"((uint32_t)kConsumerWarps));
+    }
+    for (int k = 0; k < kChunkSlots; ++k) wdone[k] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     abort_flag = 0;
   }
   __syncthreads();
 
-  const int lane = tid & 31;
-  const bool producer = tid < 32;  // warp 0 walks the producer cursor, every lane alike
-  // Producer cursor (warp 0): the next (chunk, sub-chunk) to fetch.
-  int pc = blockIdx.x, psub = 0, issued = 0;
-  uint32_t armed = 0, last_parity = 0;
-  auto issue_next = [&]() {
-    if (pc >= P.total_ctas) return;
-    const int mi = find_matrix(P.mats, P.n_mats, pc);
-    const DevMat dm = P.mats[mi];
-    const int64_t rel0 = (int64_t)(pc - dm.cta_begin) * kChunk;
-    const int64_t ccnt = min((int64_t)kChunk, dm.numel - rel0);
-    const int64_t e0 = dm.offset + rel0 + (int64_t)psub * E;
-    const int n = (int)min((int64_t)E, ccnt - (int64_t)psub * E);
-    const int n8 = n & ~7;
-    const int st = issued % S;
-    const uint32_t bar = fbar(st);
-    const uint32_t dst = sbase + (uint32_t)st * C.stage_bytes;
-    const uint32_t bytes = (uint32_t)n8 * (cbytes * W + 4u);
-    if (lane == 0)
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                   : "memory");
-    if (n8 > 0) {
-      // one slice per lane: a thread's bulk copies run one after another, so the W + 1 copies
-      // of a stage are spread over the lanes of warp 0 to run side by side
-      for (int w = lane; w <= W; w += 32) {
-        if (w < W)
-          bulk_copy(dst + (uint32_t)(w * E) * cbytes,
-                    static_cast<const uint8_t*>(P.contrib.p[w]) + e0 * cbytes,
-                    (uint32_t)n8 * cbytes, bar);
-        else
-          bulk_copy(dst + (uint32_t)(W * E) * cbytes, P.momentum + e0, (uint32_t)n8 * 4u, bar);
-      }
-    }
-    armed |= 1u << st;
-    last_parity = (last_parity & ~(1u << st)) | ((uint32_t)((issued / S) & 1) << st);
-    ++issued;
-    if ((int64_t)(++psub) * E >= ccnt) {
-      psub = 0;
-      pc += gridDim.x;
-    }
-  };
-  if (producer)
-    for (int k = 0; k < S - 1; ++k) issue_next();
-
-  float ss = 0.f;
-  int q = 0;  // consumer sub-chunk counter
-  bool stop = false;
-  for (int c = blockIdx.x; c < P.total_ctas && !stop; c += gridDim.x) {
-    const int mi = find_matrix(P.mats, P.n_mats, c);
-    const DevMat dm = P.mats[mi];
-    const int64_t rel0 = (int64_t)(c - dm.cta_begin) * kChunk;
-    const int64_t ccnt = min((int64_t)kChunk, dm.numel - rel0);
-    const int64_t cbase = dm.offset + rel0;
-    const bool lo_out = dm.split && P.uhat_lo != nullptr;
-    for (int64_t sub0 = 0; sub0 < ccnt; sub0 += E, ++q) {
-      if (producer) issue_next();  // stage (q + S - 1) % S was freed by the last barrier
-      const int st = q % S;
-      const bool ok = bulk_wait(fbar(st), (uint32_t)((q / S) & 1), C.wait_limit_ns, P.status,
-                                &abort_flag, true);
-      const int n = ok ? (int)min((int64_t)E, ccnt - sub0) : 0;  // nothing to read on a failure
-      const int n8 = n & ~7;
-      const int64_t e0 = cbase + sub0;
-      const uint8_t* stage = sm + (size_t)st * C.stage_bytes;
-      const float4* mo = reinterpret_cast<const float4*>(stage + (size_t)(W * E) * cbytes);
-      for (int v = tid; v < (n8 >> 3); v += kStreamThreads) {
-        float g[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int w = 0; w < W; ++w) {
-          const uint8_t* cw = stage + (size_t)(w * E) * cbytes;
-          Raw8<T> r;
-          if (sizeof(T) == 2) {
-            reinterpret_cast<uint4*>(&r)[0] = reinterpret_cast<const uint4*>(cw)[v];
-          } else {
-            reinterpret_cast<float4*>(&r)[0] = reinterpret_cast<const float4*>(cw)[2 * v];
-            reinterpret_cast<float4*>(&r)[1] = reinterpret_cast<const float4*>(cw)[2 * v + 1];
-          }
-          r.add_to(g);
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------------ producer warp
+    uint32_t armed = 0, last_parity = 0;
+    uint32_t q = 0;
+    bool ok = true;
+    for (int pc = blockIdx.x; pc < P.total_ctas && ok; pc += gridDim.x) {
+      const int mi = find_matrix(P.mats, P.n_mats, pc);
+      const DevMat dm = P.mats[mi];
+      const int64_t rel0 = (int64_t)(pc - dm.cta_begin) * kChunk;
+      const int64_t ccnt = min((int64_t)kChunk, dm.numel - rel0);
+      for (int64_t sub0 = 0; sub0 < ccnt; sub0 += E, ++q) {
+        const int st = (int)(q % (uint32_t)S);
+        const uint32_t round = q / (uint32_t)S;
+        // the stage's previous contents (round - 1) have been released by every consumer
+        if (round > 0) {
+          if (lane == 0)
+            ok = bulk_wait(ebar(st), (round - 1) & 1u, C.wait_limit_ns, P.status, &abort_flag,
+                           true);
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+          if (!ok) break;
         }
-        const float4 m0 = mo[2 * v], m1 = mo[2 * v + 1];
-        const float m8[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-        finish8(P, lo_out, e0 + (int64_t)v * 8, g, m8, ss);
+        const int64_t e0 = dm.offset + rel0 + sub0;
+        const int n = (int)min((int64_t)E, ccnt - sub0);
+        const int n8 = n & ~7;
+        const uint32_t bar = fbar(st);
+        const uint32_t dst = sbase + (uint32_t)st * C.stage_bytes;
+        if (lane == 0)
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                       "r"((uint32_t)n8 * (cbytes * W + 4u))
+                       : "memory");
+        if (n8 > 0) {
+          for (int w = lane; w <= W; w += 32) {
+            if (w < W)
+              bulk_copy(dst + (uint32_t)(w * E) * cbytes,
+                        static_cast<const uint8_t*>(P.contrib.p[w]) + e0 * cbytes,
+                        (uint32_t)n8 * cbytes, bar);
+            else
+              bulk_copy(dst + (uint32_t)(W * E) * cbytes, P.momentum + e0, (uint32_t)n8 * 4u,
+                        bar);
+          }
+        }
+        armed |= 1u << st;
+        last_parity = (last_parity & ~(1u << st)) | ((round & 1u) << st);
       }
-      if (tid < n - n8) finish1<T>(P, lo_out, e0 + n8 + tid, ss);  // last < 8 elements
-      // every thread is done with the stage (the producer may refill it), and all stop together
-      // if any wait failed
-      if (__syncthreads_or(!ok)) { stop = true; break; }
     }
-    if (stop) break;
-    const float tot = block_sum(ss, red);
-    if (tid == 0) P.partials[c] = tot;
-    ss = 0.f;
-    __syncthreads();
+    // every copy this CTA issued has landed before it exits
+    if (lane == 0)
+      for (int st = 0; st < S; ++st)
+        if (armed & (1u << st))
+          bulk_wait(fbar(st), (last_parity >> st) & 1u, C.wait_limit_ns, P.status, &abort_flag,
+                    false);
+  } else {
+    // ------------------------------------------------------------------ consumer warps
+    uint32_t q = 0, slot = 0;
+    bool ok = true;
+    for (int c = blockIdx.x; c < P.total_ctas && ok; c += gridDim.x, slot = (slot + 1) % kChunkSlots) {
+      const int mi = find_matrix(P.mats, P.n_mats, c);
+      const DevMat dm = P.mats[mi];
+      const int64_t rel0 = (int64_t)(c - dm.cta_begin) * kChunk;
+      const int64_t ccnt = min((int64_t)kChunk, dm.numel - rel0);
+      const int64_t cbase = dm.offset + rel0;
+      const bool lo_out = dm.split && P.uhat_lo != nullptr;
+      float ss = 0.f;
+      for (int64_t sub0 = 0; sub0 < ccnt; sub0 += E, ++q) {
+        const int st = (int)(q % (uint32_t)S);
+        ok = bulk_wait(fbar(st), (q / (uint32_t)S) & 1u, C.wait_limit_ns, P.status, &abort_flag,
+                       true);
+        if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+        const int n = (int)min((int64_t)E, ccnt - sub0);
+        const int n8 = n & ~7;
+        const int64_t e0 = cbase + sub0;
+        const uint8_t* stage = sm + (size_t)st * C.stage_bytes;
+        const float4* mo = reinterpret_cast<const float4*>(stage + (size_t)(W * E) * cbytes);
+        for (int v = tid; v < (n8 >> 3); v += kStreamThreads) {
+          float g[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          for (int w = 0; w < W; ++w) {
+            const uint8_t* cw = stage + (size_t)(w * E) * cbytes;
+            Raw8<T> r;
+            if (sizeof(T) == 2) {
+              reinterpret_cast<uint4*>(&r)[0] = reinterpret_cast<const uint4*>(cw)[v];
+            } else {
+              reinterpret_cast<float4*>(&r)[0] = reinterpret_cast<const float4*>(cw)[2 * v];
+              reinterpret_cast<float4*>(&r)[1] = reinterpret_cast<const float4*>(cw)[2 * v + 1];
+            }
+            r.add_to(g);
+          }
+          const float4 m0 = mo[2 * v], m1 = mo[2 * v + 1];
+          const float m8[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+          finish8(P, lo_out, e0 + (int64_t)v * 8, g, m8, ss);
+        }
+        if (tid < n - n8) finish1<T>(P, lo_out, e0 + n8 + tid, ss);  // last < 8 elements
+        __syncwarp();
+        if (lane == 0)
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ebar(st)) : "memory");
+      }
+      if (!ok) break;
+      // chunk partial: warp sums in a slot, the last warp adds them in warp order
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+      if (lane == 0) {
+        wsum[slot][warp] = ss;
+        __threadfence_block();
+        if (atomicAdd(&wdone[slot], 1) == kConsumerWarps - 1) {
+          __threadfence_block();
+          float tot = 0.f;
+          for (int k = 0; k < kConsumerWarps; ++k) tot += wsum[slot][k];
+          P.partials[c] = tot;
+          atomicExch(&wdone[slot], 0);
+        }
+      }
+    }
   }
-  // every copy this CTA issued has landed before it exits
-  if (tid == 0)
-    for (int s = 0; s < S; ++s)
-      if (armed & (1u << s))
-        bulk_wait(fbar(s), (last_parity >> s) & 1u, C.wait_limit_ns, P.status, &abort_flag, false);
 }
 
 // One CTA per matrix: nu = sqrt(sum of its CTA partials), summed in fp64 in index order.
@@ -589,11 +621,11 @@ cudaError_t launch_reduce_momentum(const ReduceParams& p, int contrib_dtype, cud
     e = cudaFuncSetAttribute(reduce_momentum_bulk_kernel<__nv_bfloat16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess)
-      reduce_momentum_bulk_kernel<__nv_bfloat16><<<grid, kStreamThreads, smem, s>>>(p, c);
+      reduce_momentum_bulk_kernel<__nv_bfloat16><<<grid, kBulkThreads, smem, s>>>(p, c);
   } else {
     e = cudaFuncSetAttribute(reduce_momentum_bulk_kernel<float>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) reduce_momentum_bulk_kernel<float><<<grid, kStreamThreads, smem, s>>>(p, c);
+    if (e == cudaSuccess) reduce_momentum_bulk_kernel<float><<<grid, kBulkThreads, smem, s>>>(p, c);
   }
   return e == cudaSuccess ? cudaGetLastError() : e;
 }

@@ -138,6 +138,46 @@ def mfsdp_plan_cost_aware(params: Sequence[Tuple[int, int, int, bool]], world_si
     return segs, pol.value
 
 
+# ------------------------------------------------------------------------------- repacking
+def _segment_array(segments):
+    seg = (Segment * max(len(segments), 1))()
+    for i, s in enumerate(segments):
+        seg[i] = Segment(s["owner"], s["role"], s["local_offset"], s["rank_offset"], s["numel"])
+    return seg
+
+
+def mfsdp_repack_workspace_bytes(n_params: int) -> int:
+    out = C.c_size_t(0)
+    _check("mfsdp_repack_workspace_bytes",
+           _lib.load().mfsdp_repack_workspace_bytes(n_params, C.byref(out)))
+    return out.value
+
+
+def mfsdp_pack_owner_shards(params, segments, world_size: int, canonical, shards, workspace,
+                            stream=None) -> None:
+    """Canonical tensor -> owner shard tensors (``shards[r]`` may be None to skip rank r).
+    All tensors share one element size; ``workspace`` is a uint8 device tensor."""
+    eb = canonical.element_size()
+    ptrs = (C.c_void_p * world_size)(*[_ptr(t) for t in shards])
+    _check("mfsdp_pack_owner_shards",
+           _lib.load().mfsdp_pack_owner_shards(_param_array(params), len(params),
+                                               _segment_array(segments), world_size, eb,
+                                               _ptr(canonical), ptrs, _ptr(workspace),
+                                               workspace.numel(), _stream(stream)))
+
+
+def mfsdp_unpack_owner_shards(params, segments, world_size: int, shards, canonical, workspace,
+                              stream=None) -> None:
+    """Owner shard tensors (None entries skipped) -> canonical tensor."""
+    eb = canonical.element_size()
+    ptrs = (C.c_void_p * world_size)(*[_ptr(t) for t in shards])
+    _check("mfsdp_unpack_owner_shards",
+           _lib.load().mfsdp_unpack_owner_shards(_param_array(params), len(params),
+                                                 _segment_array(segments), world_size, eb, ptrs,
+                                                 _ptr(canonical), _ptr(workspace),
+                                                 workspace.numel(), _stream(stream)))
+
+
 # ------------------------------------------------------------------------------- owner set
 class OwnerSet:
     """Handle of ``mfsdp_owner_set``: create, query workspace, bind, destroy."""

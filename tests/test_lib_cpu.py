@@ -168,6 +168,31 @@ def test_scorer_error_codes(lib):
     assert lib.mfsdp_plan_cost_aware(pd, 1, 2, None, 0, seg, None) == -1           # no model
 
 
+def test_repack_validation_before_any_launch(lib):
+    from matrix_optimizer_owner_gb300 import _lib as L
+    pd = (L.ParamDesc * 2)(L.ParamDesc(2, 2, 0, 1), L.ParamDesc(3, 1, 0, 0))
+    seg = (L.Segment * 2)(L.Segment(0, 0, 0, 0, 4), L.Segment(1, 1, 0, 0, 3))
+    sh = (C.c_void_p * 2)(1 << 20, 2 << 20)     # never dereferenced: every case fails first
+    canon, ws = C.c_void_p(3 << 20), C.c_void_p(4 << 20)
+    need = C.c_size_t(0)
+    assert lib.mfsdp_repack_workspace_bytes(2, C.byref(need)) == 0 and need.value >= 64
+    assert lib.mfsdp_repack_workspace_bytes(-1, C.byref(need)) == -1
+    pack, unpack = lib.mfsdp_pack_owner_shards, lib.mfsdp_unpack_owner_shards
+    assert pack(pd, 2, seg, 0, 2, canon, sh, ws, need.value, None) == -1        # world size
+    assert pack(pd, 2, seg, 2, 3, canon, sh, ws, need.value, None) == -1        # element size
+    assert pack(pd, 2, seg, 2, 2, None, sh, ws, need.value, None) == -1         # no canonical
+    assert unpack(pd, 2, seg, 2, 2, None, canon, ws, need.value, None) == -1    # no shards
+    bad_owner = (L.Segment * 2)(L.Segment(0, 0, 0, 0, 4), L.Segment(2, 1, 0, 0, 3))
+    assert pack(pd, 2, bad_owner, 2, 2, canon, sh, ws, need.value, None) == -1
+    bad_numel = (L.Segment * 2)(L.Segment(0, 0, 0, 0, 5), L.Segment(1, 1, 0, 0, 3))
+    assert pack(pd, 2, bad_numel, 2, 2, canon, sh, ws, need.value, None) == -2
+    outside = (L.Segment * 2)(L.Segment(0, 0, 1, 0, 4), L.Segment(1, 1, 0, 0, 3))
+    assert pack(pd, 2, outside, 2, 2, canon, sh, ws, need.value, None) == -2    # past its shard
+    assert pack(pd, 2, seg, 2, 2, canon, sh, None, need.value, None) == -5      # no workspace
+    assert pack(pd, 2, seg, 2, 2, canon, sh, ws, 8, None) == -5                 # too small
+    assert pack(None, 0, None, 2, 2, None, None, None, 0, None) == 0            # empty model
+
+
 def test_planner_error_codes(lib):
     from matrix_optimizer_owner_gb300 import _lib as L
     pd = (L.ParamDesc * 1)(L.ParamDesc(2, 2, 0, 1))

@@ -423,3 +423,39 @@ def test_cost_aware_takes_scope_only_within_the_cap():
     same = [plan.Param(4, 4, b, True) for b in range(6)]
     assert plan.plan_cost_aware(same, 3)[1] == plan.SCOPE_GREEDY
     assert plan.imbalance([2.0, 2.0]) == 1.0 and plan.imbalance([3.0, 1.0]) == 1.5
+
+
+# ----------------------------------------------------------------------------- repacking
+def test_repack_hand_worked_layout():
+    from oracle import repack
+    # block 0: m0 4x2 (8) -> r0, m1 2x3 (6) -> r1, tail 5 -> r1; block 1: m3 3x3 (9) -> r0
+    # (loads 8 < 11), tail 2 -> r1.  Shards: r0 = [m0 | m3], r1 = [m1, tail0 | tail1].
+    ps = [plan.Param(4, 2, 0, True), plan.Param(2, 3, 0, True), plan.Param(5, 1, 0, False),
+          plan.Param(3, 3, 1, True), plan.Param(2, 1, 1, False)]
+    segs = plan.plan(ps, 2)
+    assert [s.owner for s in segs] == [0, 1, 1, 0, 1]
+    offs, size = repack.shard_offsets(ps, segs, 2)
+    assert offs == [0, 0, 6, 8, 11] and size == [17, 13]
+    canon = np.arange(30, dtype=np.int32)
+    r0, r1 = repack.pack(ps, segs, 2, canon)
+    assert r0.tolist() == list(range(0, 8)) + list(range(19, 28))
+    assert r1.tolist() == list(range(8, 14)) + list(range(14, 19)) + list(range(28, 30))
+
+
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_repack_round_trips(cfg):
+    from oracle import repack
+    ps = _params(get_config(cfg))
+    total = sum(p.numel for p in ps)
+    canon = np.random.default_rng(cfg).integers(0, 1 << 16, size=total).astype(np.uint16)
+    for W in (1, 3, 8):
+        segs = plan.plan(ps, W)
+        shards = repack.pack(ps, segs, W, canon)
+        assert sum(len(s) for s in shards) == total
+        assert np.array_equal(repack.unpack(ps, segs, W, shards), canon)
+    # reshard 8 -> 3 ranks under another policy equals packing the canonical buffer directly
+    a = plan.plan(ps, 8, plan.ROLE_GREEDY)
+    b = plan.plan(ps, 3, plan.SCOPE_GREEDY)
+    out = repack.reshard(ps, a, 8, repack.pack(ps, a, 8, canon), b, 3)
+    for x, y in zip(out, repack.pack(ps, b, 3, canon)):
+        assert np.array_equal(x, y)
