@@ -185,6 +185,11 @@ __device__ __forceinline__ uint16_t f2bf(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+// Two floats rounded to nearest-even bf16 in one conversion: lo in bits 0-15, hi in 16-31.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 
 // 32 consecutive bf16 of row r starting at column c0 (c0 % 8 == 0, pitch % 8 == 0) as fp32.
 __device__ __forceinline__ void load_row32(const uint16_t* p, int64_t ld, int r, int c0, int N,
@@ -919,6 +924,13 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
     auto load_d = [&](const DSrc& ds, int q, uint4 (&dst)[4]) {
       if (!((ds.bits >> q) & 1u)) return;
       const int rows = (int)((ds.bits >> 4) & 63u), cols = (int)(ds.bits >> 10);
+      if (rows == 32 && cols == 128) {  // the warp's whole 32 x 128 region is inside
+        const uint16_t* src = ds.p + (int64_t)crow * ds.ld + 32 * q + 8 * cchunk;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)(8 * i) * ds.ld));
+        return;
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         dst[i] = load_granule(ds.p, ds.ld, 8 * i + crow, 32 * q + 8 * cchunk, rows, cols);
@@ -1010,7 +1022,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
             v0 *= alpha;
             v1 *= alpha;
           }
-          hw[k] = (uint32_t)f2bf(v0) | ((uint32_t)f2bf(v1) << 16);
+          hw[k] = pack_bf16x2(v0, v1);
         }
         if (sym && c0 == rw) {
           // block on the diagonal: row r stores columns >= r and mirrors columns > r
