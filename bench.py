@@ -58,7 +58,7 @@ NS_TRAFFIC_SOURCES = ("matrix_optimizer_owner_gb300/csrc/ns_gemm.cu",
                       "matrix_optimizer_owner_gb300/csrc/mfsdp_internal.h")
 NS_TRAFFIC = {
     # config index: (sources sha256, bytes per launch, profile summary)
-    1: ("0a763903af3477bd49aaf702376cffc49a1457ac0db4903cfc115ae1accbc724", 208507716,
+    1: ("16861d43a1380ef4005f910f26ebc4847ef4fc6d0205066d0bb98dc7cfab22f2", 208922948,
         "profiles/owner_step_gpt2_small_launch_list.md"),
 }
 
@@ -350,18 +350,57 @@ def time_repack(wb, reps, stream, world=8):
     shards = [torch.empty(n, dtype=torch.bfloat16, device=stream.device) for n in sizes]
     ws = torch.empty(mfsdp.mfsdp_repack_workspace_bytes(len(params)), dtype=torch.uint8,
                      device=stream.device)
+    plan = mfsdp.RepackPlan(params, segs, world)
     for _ in range(3):
-        mfsdp.mfsdp_pack_owner_shards(params, segs, world, canon, shards, ws, stream)
+        plan.pack(canon, shards, ws, stream)
     torch.cuda.synchronize()
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
     s.record(stream)
     for _ in range(reps):
-        mfsdp.mfsdp_pack_owner_shards(params, segs, world, canon, shards, ws, stream)
+        plan.pack(canon, shards, ws, stream)
     e.record(stream)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / reps
     return ms, 2 * total * 2, len(params)
+
+
+FFMA_PEAK_NOTE = "152 SMs x 128 fp32 lanes x 2 FLOP x the sampled SM clock"
+
+
+def time_shampoo(device, reps=2, root_iters=30):
+    """Owner Shampoo step on one GPT-2-small layer's matrices (2304x768, 768x768, 3072x768,
+    768x3072), fp32: statistics, 30 coupled-Newton steps for every inverse fourth root, the
+    preconditioned update.  Returns (ms per step, FLOPs per step)."""
+    from matrix_optimizer_owner_gb300 import mfsdp
+    shapes = [(2304, 768), (768, 768), (3072, 768), (768, 3072)]
+    offs, o = [], 0
+    for r, c in shapes:
+        offs.append(o)
+        o += r * c
+    sset = mfsdp.ShampooSet([(r, c, off) for (r, c), off in zip(shapes, offs)])
+    ws = torch.empty(sset.workspace_bytes, dtype=torch.uint8, device=device)
+    l = torch.empty(sset.l_numel, dtype=torch.float32, device=device)
+    r_ = torch.empty(sset.r_numel, dtype=torch.float32, device=device)
+    sset.init_state(1e-6, l, r_, ws)
+    g = torch.randn(o, device=device) * 1e-3
+    w = torch.randn(o, device=device) * 0.02
+    sset.step(g, l, r_, w, 0.02, 0.01, root_iters, ws)
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        sset.step(g, l, r_, w, 0.02, 0.01, root_iters, ws)
+    e.record()
+    torch.cuda.synchronize()
+    flops = 0
+    for r, c in shapes:
+        flops += 2 * r * r * c + 2 * r * c * c          # statistics
+        flops += root_iters * 4 * 2 * (r ** 3 + c ** 3)  # roots
+        flops += 2 * r * r * c + 2 * r * c * c          # P
+    sset.close()
+    return s.elapsed_time(e) / reps, flops
 
 
 def config_block(wb, cfg):
@@ -443,6 +482,18 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": wb.launches_per_step() * args.steps,
         "clocks": clocks, "device_status": status,
     }
+    if not args.no_shampoo and rank == 0:
+        sms_, sflops = time_shampoo(dev)
+        sm_mhz = (clocks or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+        ffma_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+        line["shampoo"] = {
+            "kernel": "sgemm_batched_kernel (fp32 FFMA) + root and update kernels",
+            "what": "one owner Shampoo step of one GPT-2-small layer (2304x768, 768x768, "
+                    "3072x768, 768x3072), 30 coupled-Newton steps per inverse fourth root",
+            "ms": round(sms_, 3), "flops": sflops, "bound": "alu",
+            "achieved_tflops": round(sflops / (sms_ * 1e-3) / 1e12, 2),
+            "peak_tflops": round(ffma_peak, 1), "peak_source": FFMA_PEAK_NOTE,
+            "frac": round(sflops / (sms_ * 1e-3) / 1e12 / ffma_peak, 4)}
     if not args.no_repack:
         rms, rbytes, nparams = time_repack(wb, 10, stream)
         line["repack"] = {
@@ -545,6 +596,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-repack", action="store_true",
                     help="skip the owner-shard repacking measurement")
+    ap.add_argument("--no-shampoo", action="store_true",
+                    help="skip the owner Shampoo measurement")
     ap.add_argument("--clock-window-s", type=float, default=1.0)
     args = ap.parse_args()
 

@@ -12,6 +12,7 @@
  *   mfsdp_plan_cost_aware         CostAware: scope plan within a workspace cap    §4.1
  *   mfsdp_pack_owner_shards /     canonical axis <-> owner shards (reshard load)  §4.4
  *   mfsdp_unpack_owner_shards
+ *   mfsdp_shampoo_step            owner Shampoo (L/R inverse fourth roots)         §5.7
  *   mfsdp_owner_reduce_momentum   W-way gradient deposit + Nesterov momentum + norm  §3, §4.2
  *   mfsdp_newton_schulz           quintic Newton–Schulz of every owned matrix      §2
  *   mfsdp_apply_update            scaled update with decoupled weight decay        §5.1
@@ -217,6 +218,44 @@ typedef struct {
   int64_t rows, cols;  /* >= 0; an empty matrix is skipped by every call */
   int64_t offset;      /* element offset of the matrix in the flat owner buffers */
 } mfsdp_matrix;
+
+/* ------------------------------------------------------------------------------------------
+ * Owner Shampoo (§5.7): the owner's whole matrices preconditioned with full left and right
+ * statistics and their inverse fourth roots, in place of Muon.  For every matrix G (rows x
+ * cols) of the set, one step is
+ *     L += G G^T,   R += G^T G                     (L, R start at eps I)
+ *     P  = L^{-1/4} G R^{-1/4}
+ *     W  = W (1 - lr weight_decay) - lr P
+ * The pages name the preconditioners and the inverse fourth root only; this is the original
+ * Shampoo update.  The roots come from `root_iters` steps of the coupled Newton iteration for
+ * the inverse p-th root (p = 4), started from X = c^{-1/4} I, M = A / c with c = ||A||_F; an
+ * eigenvalue ratio of 1e-8 converges within 26 steps.  Every product is an fp32 GEMM on the
+ * CUDA cores.
+ *
+ * Buffers (DEVICE, fp32, caller-owned): `grad` and `weights` are the flat owner buffers the
+ * matrix table's offsets index (grad = the deposited gradient, e.g. the reduced_grad_out of
+ * mfsdp_owner_reduce_momentum); `l` / `r` hold every matrix's L (rows^2) / R (cols^2) back to
+ * back in table order (sizes from mfsdp_shampoo_set_sizes).  The workspace holds the root
+ * iteration's buffers (7 x (rows^2 + cols^2) floats per matrix), P and the launch tables.
+ * Errors: MFSDP_EINVAL (null pointers, eps <= 0, root_iters outside [1, 200]), MFSDP_ESHAPE
+ * (rows or cols outside [1, 65536], negative offset), MFSDP_EWORKSPACE, MFSDP_ECUDA.
+ * ------------------------------------------------------------------------------------------ */
+
+typedef struct mfsdp_shampoo_set mfsdp_shampoo_set;
+
+int mfsdp_shampoo_set_create(const mfsdp_matrix* mats, int32_t n_mats, mfsdp_shampoo_set** out);
+int mfsdp_shampoo_set_destroy(mfsdp_shampoo_set* set);
+/* Workspace bytes and the numel of the flat L and R buffers (any output may be NULL). */
+int mfsdp_shampoo_set_sizes(const mfsdp_shampoo_set* set, size_t* workspace_bytes,
+                            int64_t* l_numel, int64_t* r_numel);
+/* L = R = eps I for every matrix. */
+int mfsdp_shampoo_init_state(const mfsdp_shampoo_set* set, float eps, float* l, float* r,
+                             void* workspace, size_t workspace_bytes, void* stream);
+/* One Shampoo step of every matrix in the set (enqueued on `stream`). */
+int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* grad, float* l, float* r,
+                       float* weights, float lr, float weight_decay, int32_t root_iters,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
 
 typedef struct mfsdp_owner_set_s mfsdp_owner_set;
 

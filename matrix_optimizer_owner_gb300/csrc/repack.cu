@@ -22,6 +22,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <limits>
+#include <mutex>
 #include <unordered_map>
 #include <vector>
 
@@ -42,12 +43,18 @@ struct CopyDesc {
   int64_t start;  // offset of this range in the concatenated byte stream
 };
 
+// Up to kInlineDescs ranges travel in the launch's parameter space (no upload, no host wait);
+// longer lists go through the caller's workspace.
+constexpr int kInlineDescs = 800;
+
 struct CopyParams {
-  const CopyDesc* descs;
+  const CopyDesc* descs;  // the workspace table, or nullptr when the ranges are inline
   int64_t n_descs;
   int64_t total;  // bytes
   int32_t elem_bytes;
+  CopyDesc inline_descs[kInlineDescs];
 };
+static_assert(sizeof(CopyParams) <= 32000, "kernel parameter space");
 
 __device__ __forceinline__ int64_t find_desc(const CopyDesc* d, int64_t n, int64_t pos) {
   int64_t lo = 0, hi = n - 1;
@@ -107,12 +114,13 @@ __device__ void copy_part(const CopyDesc& d, int64_t a, int64_t b, int eb) {
 
 __global__ void __launch_bounds__(kCopyThreads) segment_copy_kernel(
     const __grid_constant__ CopyParams P) {
+  const CopyDesc* descs = P.descs ? P.descs : P.inline_descs;
   const int64_t npieces = (P.total + kPiece - 1) / kPiece;
   for (int64_t pc = blockIdx.x; pc < npieces; pc += gridDim.x) {
     const int64_t p0 = pc * kPiece, p1 = P.total < p0 + kPiece ? P.total : p0 + kPiece;
-    int64_t k = find_desc(P.descs, P.n_descs, p0);
+    int64_t k = find_desc(descs, P.n_descs, p0);
     for (int64_t pos = p0; pos < p1 && k < P.n_descs; ++k) {
-      const CopyDesc d = P.descs[k];
+      const CopyDesc d = descs[k];
       const int64_t a = pos - d.start, b = d.bytes < p1 - d.start ? d.bytes : p1 - d.start;
       if (b > a) copy_part(d, a, b, P.elem_bytes);
       pos = d.start + d.bytes;
@@ -176,14 +184,25 @@ int run_copies(std::vector<CopyDesc>& d, int32_t eb, void* ws, size_t ws_bytes, 
   if (live.empty()) return MFSDP_OK;
   if (ws_bytes < desc_bytes((int64_t)live.size())) return MFSDP_EWORKSPACE;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(ws, live.data(), live.size() * sizeof(CopyDesc), cudaMemcpyHostToDevice,
-                      st) != cudaSuccess)
-    return MFSDP_ECUDA;
+  static CopyParams p;  // large: kept off the stack; filled and launched under one lock
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  p.n_descs = (int64_t)live.size();
+  p.total = total;
+  p.elem_bytes = eb;
+  if (live.size() <= (size_t)kInlineDescs) {
+    p.descs = nullptr;
+    std::copy(live.begin(), live.end(), p.inline_descs);
+  } else {
+    if (cudaMemcpyAsync(ws, live.data(), live.size() * sizeof(CopyDesc), cudaMemcpyHostToDevice,
+                        st) != cudaSuccess)
+      return MFSDP_ECUDA;
+    p.descs = static_cast<const CopyDesc*>(ws);
+  }
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return MFSDP_ECUDA;
-  CopyParams p{static_cast<const CopyDesc*>(ws), (int64_t)live.size(), total, eb};
   const int64_t npieces = (total + kPiece - 1) / kPiece;
   const int grid = (int)std::min<int64_t>(npieces, (int64_t)sms * kCopyCtasPerSm);
   segment_copy_kernel<<<grid, kCopyThreads, 0, st>>>(p);

@@ -1,0 +1,481 @@
+// Owner Shampoo: full left / right preconditioners with an inverse fourth root, on the owner's
+// whole matrices (fp32).
+//
+// "MatrixFSDP: communication-free matrix optimizers under ZeRO-3 parameter sharding", §5.7:
+// with every 2D matrix whole on its owner, the owner can run Shampoo ("full L/R
+// preconditioners with inverse fourth root") in place of Muon.  Per owned matrix G (rows x
+// cols), the original Shampoo update:
+//     L += G G^T,  R += G^T G             (L_0 = R_0 = eps I)
+//     P  = L^{-1/4} G R^{-1/4}
+//     W  = W (1 - lr wd) - lr P
+// The inverse fourth roots come from the coupled Newton iteration for the inverse p-th root
+// (Guo and Higham, "A Schur–Newton method for the matrix p-th root and its inverse", 2006):
+// with c = ||A||_F,  X_0 = c^{-1/4} I,  M_0 = A / c, and for k = 0 .. iters-1
+//     T_k = (5 I - M_k) / 4,  X_{k+1} = X_k T_k,  M_{k+1} = T_k^4 M_k,
+// so M_k -> I and X_k -> A^{-1/4}; an eigenvalue ratio of 1e-8 converges in 26 iterations.
+//
+// Everything is a dense fp32 product, run by one batched SGEMM kernel on the CUDA cores
+// (fp32 FFMA, 128 x 128 output tiles, 8 x 8 outputs per thread, double-buffered shared
+// memory): a launch runs the same product for every owned matrix (blockIdx.z = matrix).
+// The iteration's T = (5I - M) / 4 is written by the epilogue of the product that forms M.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "mfsdp.h"
+#include "mfsdp_internal.h"
+
+namespace mfsdp {
+namespace {
+
+constexpr int kGemmThreads = 256;
+constexpr int kTM = 128, kTN = 128, kTK = 8;
+
+struct GemmDesc {
+  const float* a;
+  const float* b;
+  float* c;
+  float* t_out;  // nullable: also write (5 delta_ij - C_ij) / 4 here
+  int32_t m, n, k;
+  int32_t lda, ldb, ldc;
+  float alpha, beta;
+};
+
+// C = alpha op(A) op(B) + beta C for every descriptor (blockIdx.z).  op(A) is m x k: A stored
+// m x k row-major (ta = 0) or k x m (ta = 1); op(B) is k x n: B stored k x n (tb = 0) or
+// n x k (tb = 1).  Thread (ty, tx) of the 16 x 16 grid computes rows {4ty + i, 64 + 4ty + i}
+// and columns {4tx + j, 64 + 4tx + j}, i, j < 4.
+template <int TA, int TB>
+__global__ void __launch_bounds__(kGemmThreads, 2) sgemm_batched_kernel(const GemmDesc* descs) {
+  __shared__ __align__(16) float As[2][kTK][kTM];
+  __shared__ __align__(16) float Bs[2][kTK][kTN];
+  const GemmDesc d = descs[blockIdx.z];
+  const int m0 = blockIdx.y * kTM, n0 = blockIdx.x * kTN;
+  if (m0 >= d.m || n0 >= d.n) return;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+
+  // global -> register loads of one k-tile (4 floats per thread per operand)
+  float ra[4], rb[4];
+  auto load_tile = [&](int k0) {
+    if (TA == 0) {  // A[m][k]: thread -> row tid / 2, k (tid % 2) * 4 .. + 3
+      const int mm = m0 + (tid >> 1), kk = k0 + (tid & 1) * 4;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        ra[u] = (mm < d.m && kk + u < d.k) ? d.a[(int64_t)mm * d.lda + kk + u] : 0.f;
+    } else {        // A[k][m]: thread -> k tid / 32, m (tid % 32) * 4 .. + 3
+      const int kk = k0 + (tid >> 5), mm = m0 + (tid & 31) * 4;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        ra[u] = (kk < d.k && mm + u < d.m) ? d.a[(int64_t)kk * d.lda + mm + u] : 0.f;
+    }
+    if (TB == 0) {  // B[k][n]: thread -> k tid / 32, n (tid % 32) * 4 .. + 3
+      const int kk = k0 + (tid >> 5), nn = n0 + (tid & 31) * 4;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        rb[u] = (kk < d.k && nn + u < d.n) ? d.b[(int64_t)kk * d.ldb + nn + u] : 0.f;
+    } else {        // B[n][k]: thread -> n tid / 2, k (tid % 2) * 4 .. + 3
+      const int nn = n0 + (tid >> 1), kk = k0 + (tid & 1) * 4;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        rb[u] = (nn < d.n && kk + u < d.k) ? d.b[(int64_t)nn * d.ldb + kk + u] : 0.f;
+    }
+  };
+  auto store_tile = [&](int buf) {
+    if (TA == 0) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) As[buf][(tid & 1) * 4 + u][tid >> 1] = ra[u];
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) As[buf][tid >> 5][(tid & 31) * 4 + u] = ra[u];
+    }
+    if (TB == 0) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) Bs[buf][tid >> 5][(tid & 31) * 4 + u] = rb[u];
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) Bs[buf][(tid & 1) * 4 + u][tid >> 1] = rb[u];
+    }
+  };
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+  const int ntiles = (d.k + kTK - 1) / kTK;
+  load_tile(0);
+  store_tile(0);
+  __syncthreads();
+  for (int kt = 0; kt < ntiles; ++kt) {
+    const int buf = kt & 1;
+    if (kt + 1 < ntiles) load_tile((kt + 1) * kTK);
+#pragma unroll
+    for (int kk = 0; kk < kTK; ++kk) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][4 * ty]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + 4 * ty]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][4 * tx]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + 4 * tx]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    if (kt + 1 < ntiles) store_tile(buf ^ 1);
+    __syncthreads();
+  }
+
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int mm = m0 + (i < 4 ? 4 * ty + i : 64 + 4 * ty + i - 4);
+    if (mm >= d.m) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int nn = n0 + (j < 4 ? 4 * tx + j : 64 + 4 * tx + j - 4);
+      if (nn >= d.n) continue;
+      float* cp = d.c + (int64_t)mm * d.ldc + nn;
+      float v = d.alpha * acc[i][j];
+      if (d.beta != 0.f) v = fmaf(d.beta, *cp, v);
+      *cp = v;
+      if (d.t_out) d.t_out[(int64_t)mm * d.ldc + nn] = ((mm == nn ? 5.f : 0.f) - v) * 0.25f;
+    }
+  }
+}
+
+// ||A||_F of each matrix (fp64, fixed order: per-thread strided sums, then a tree).
+struct NormDesc {
+  const float* a;
+  int64_t numel;
+  double* out;
+};
+
+__global__ void __launch_bounds__(1024) frob_kernel(const NormDesc* descs) {
+  __shared__ double red[1024];
+  const NormDesc d = descs[blockIdx.x];
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < d.numel; i += blockDim.x) {
+    const double v = d.a[i];
+    s += v * v;
+  }
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *d.out = sqrt(red[0]);
+}
+
+// Start of the iteration for each matrix: X = c^{-1/4} I, M = A / c, T = (5I - M) / 4.
+struct PrepDesc {
+  const float* a;
+  float* x;
+  float* m;
+  float* t;
+  const double* norm;
+  int32_t dim;
+};
+
+__global__ void root_prep_kernel(const PrepDesc* descs) {
+  const PrepDesc d = descs[blockIdx.y];
+  const int64_t n = (int64_t)d.dim * d.dim;
+  const double c = *d.norm;
+  const float inv_c = (float)(1.0 / c), x0 = (float)pow(c, -0.25);
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const bool diag = (e / d.dim) == (e % d.dim);
+    const float mv = d.a[e] * inv_c;
+    d.m[e] = mv;
+    d.t[e] = ((diag ? 5.f : 0.f) - mv) * 0.25f;
+    d.x[e] = diag ? x0 : 0.f;
+  }
+}
+
+// A = eps I for every state matrix.
+__global__ void scaled_identity_kernel(float* base, const int64_t* offs, const int32_t* dims,
+                                       float eps) {
+  const int i = blockIdx.y;
+  const int64_t n = (int64_t)dims[i] * dims[i];
+  float* a = base + offs[i];
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x)
+    a[e] = (e / dims[i]) == (e % dims[i]) ? eps : 0.f;
+}
+
+// W = W (1 - lr wd) - lr P over the flat owner buffer.
+__global__ void shampoo_update_kernel(float* w, const float* p, int64_t n, float decay,
+                                      float lr) {
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x)
+    w[e] = fmaf(w[e], decay, -lr * p[e]);
+}
+
+}  // namespace
+}  // namespace mfsdp
+
+using namespace mfsdp;
+
+// ------------------------------------------------------------------------------------------
+// The owned-matrix set of the Shampoo step and its workspace layout.
+// ------------------------------------------------------------------------------------------
+struct mfsdp_shampoo_set {
+  struct Mat {
+    int64_t rows, cols, offset;  // in the flat owner buffers (weights, gradient, P)
+    int64_t l_off, r_off;        // in the flat L and R state buffers
+  };
+  std::vector<Mat> mats;
+  int64_t numel = 0, l_numel = 0, r_numel = 0;
+  // workspace: per side (L of every matrix, then R of every matrix) X0, X1, M0, M1, T, T2, T4
+  // (dim^2 floats each), then P and Y (numel floats each), norms, descriptor tables
+  std::vector<int64_t> side_off;  // float offset of each side's seven buffers
+  std::vector<int32_t> side_dim;
+  int64_t floats = 0;
+  size_t off_norms = 0, off_tables = 0, table_bytes = 0, ws_bytes = 0;
+};
+
+namespace {
+
+constexpr int kSideBufs = 7;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int launch_gemm(const GemmDesc* dev_descs, int nprob, int max_m, int max_n, int ta, int tb,
+                cudaStream_t st) {
+  if (nprob <= 0) return MFSDP_OK;
+  const dim3 grid((unsigned)((max_n + kTN - 1) / kTN), (unsigned)((max_m + kTM - 1) / kTM),
+                  (unsigned)nprob);
+  if (ta == 0 && tb == 0) sgemm_batched_kernel<0, 0><<<grid, kGemmThreads, 0, st>>>(dev_descs);
+  else if (ta == 0 && tb == 1) sgemm_batched_kernel<0, 1><<<grid, kGemmThreads, 0, st>>>(dev_descs);
+  else if (ta == 1 && tb == 0) sgemm_batched_kernel<1, 0><<<grid, kGemmThreads, 0, st>>>(dev_descs);
+  else sgemm_batched_kernel<1, 1><<<grid, kGemmThreads, 0, st>>>(dev_descs);
+  return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
+}
+
+}  // namespace
+
+extern "C" int mfsdp_shampoo_set_create(const mfsdp_matrix* mats, int32_t n_mats,
+                                        mfsdp_shampoo_set** out) {
+  if (out == nullptr || n_mats < 0 || (n_mats > 0 && mats == nullptr)) return MFSDP_EINVAL;
+  auto* s = new mfsdp_shampoo_set();
+  int64_t lo = 0, ro = 0;
+  for (int32_t i = 0; i < n_mats; ++i) {
+    const mfsdp_matrix& m = mats[i];
+    if (m.rows <= 0 || m.cols <= 0 || m.offset < 0 || m.rows > (1 << 16) || m.cols > (1 << 16)) {
+      delete s;
+      return MFSDP_ESHAPE;
+    }
+    s->mats.push_back({m.rows, m.cols, m.offset, lo, ro});
+    lo += m.rows * m.rows;
+    ro += m.cols * m.cols;
+    s->numel = std::max(s->numel, m.offset + m.rows * m.cols);
+  }
+  s->l_numel = lo;
+  s->r_numel = ro;
+  int64_t f = 0;
+  for (int side = 0; side < 2; ++side)
+    for (const auto& m : s->mats) {
+      const int64_t d = side == 0 ? m.rows : m.cols;
+      s->side_off.push_back(f);
+      s->side_dim.push_back((int32_t)d);
+      f += kSideBufs * d * d;
+    }
+  f += 2 * s->numel;  // P and Y
+  s->floats = f;
+  const int n = n_mats;
+  s->off_norms = align256((size_t)f * sizeof(float));
+  s->off_tables = align256(s->off_norms + sizeof(double) * 2 * (size_t)std::max(n, 1));
+  // tables: stats (2n), the iteration's 4 products x 2n for each parity, P (2n), norms (2n),
+  // prep (2n); the state-initialisation offsets and dims fit in the same space
+  s->table_bytes = sizeof(GemmDesc) * (size_t)(20 * std::max(n, 1)) +
+                   sizeof(NormDesc) * 2 * (size_t)std::max(n, 1) +
+                   sizeof(PrepDesc) * 2 * (size_t)std::max(n, 1);
+  s->ws_bytes = align256(s->off_tables + s->table_bytes);
+  *out = s;
+  return MFSDP_OK;
+}
+
+extern "C" int mfsdp_shampoo_set_destroy(mfsdp_shampoo_set* set) {
+  delete set;
+  return MFSDP_OK;
+}
+
+extern "C" int mfsdp_shampoo_set_sizes(const mfsdp_shampoo_set* set, size_t* workspace_bytes,
+                                       int64_t* l_numel, int64_t* r_numel) {
+  if (set == nullptr) return MFSDP_EINVAL;
+  if (workspace_bytes) *workspace_bytes = set->ws_bytes;
+  if (l_numel) *l_numel = set->l_numel;
+  if (r_numel) *r_numel = set->r_numel;
+  return MFSDP_OK;
+}
+
+extern "C" int mfsdp_shampoo_init_state(const mfsdp_shampoo_set* set, float eps, float* l,
+                                        float* r, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  if (set == nullptr || !(eps > 0.f) || l == nullptr || r == nullptr) return MFSDP_EINVAL;
+  const int n = (int)set->mats.size();
+  if (n == 0) return MFSDP_OK;
+  if (workspace == nullptr || workspace_bytes < set->ws_bytes) return MFSDP_EWORKSPACE;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // offsets and dims of L then R, staged in the workspace's table area
+  std::vector<int64_t> offs(2 * (size_t)n);
+  std::vector<int32_t> dims(2 * (size_t)n);
+  for (int i = 0; i < n; ++i) {
+    offs[i] = set->mats[i].l_off;
+    dims[i] = (int32_t)set->mats[i].rows;
+    offs[n + i] = set->mats[i].r_off;
+    dims[n + i] = (int32_t)set->mats[i].cols;
+  }
+  uint8_t* tab = static_cast<uint8_t*>(workspace) + set->off_tables;
+  const size_t ob = offs.size() * sizeof(int64_t);
+  if (ob + dims.size() * sizeof(int32_t) > set->table_bytes) return MFSDP_EWORKSPACE;
+  if (cudaMemcpyAsync(tab, offs.data(), ob, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(tab + ob, dims.data(), dims.size() * sizeof(int32_t),
+                      cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MFSDP_ECUDA;
+  const auto* doffs = reinterpret_cast<const int64_t*>(tab);
+  const auto* ddims = reinterpret_cast<const int32_t*>(tab + ob);
+  scaled_identity_kernel<<<dim3(64, (unsigned)n), 256, 0, st>>>(l, doffs, ddims, eps);
+  scaled_identity_kernel<<<dim3(64, (unsigned)n), 256, 0, st>>>(r, doffs + n, ddims + n, eps);
+  return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
+}
+
+extern "C" int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* grad, float* l,
+                                  float* r, float* weights, float lr, float weight_decay,
+                                  int32_t root_iters, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  if (set == nullptr || grad == nullptr || l == nullptr || r == nullptr || weights == nullptr)
+    return MFSDP_EINVAL;
+  if (root_iters < 1 || root_iters > 200) return MFSDP_EINVAL;
+  const int n = (int)set->mats.size();
+  if (n == 0) return MFSDP_OK;
+  if (workspace == nullptr || workspace_bytes < set->ws_bytes) return MFSDP_EWORKSPACE;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* wsf = static_cast<float*>(workspace);
+  double* norms = reinterpret_cast<double*>(static_cast<uint8_t*>(workspace) + set->off_norms);
+  float* pbuf = wsf + (set->floats - 2 * set->numel);
+  float* ybuf = pbuf + set->numel;
+  auto side = [&](int sd, int i, int b) {  // buffer b of side sd (0 = L, 1 = R) of matrix i
+    return wsf + set->side_off[(size_t)(sd * n + i)] +
+           (int64_t)b * set->side_dim[(size_t)(sd * n + i)] * set->side_dim[(size_t)(sd * n + i)];
+  };
+  enum { X0 = 0, X1 = 1, M0 = 2, M1 = 3, T = 4, T2 = 5, T4 = 6 };
+  int max_rows = 0, max_cols = 0;
+  for (const auto& m : set->mats) {
+    max_rows = std::max(max_rows, (int)m.rows);
+    max_cols = std::max(max_cols, (int)m.cols);
+  }
+  const int max_dim = std::max(max_rows, max_cols);
+
+  // Host tables, uploaded once per step.
+  std::vector<GemmDesc> stats(2 * (size_t)n), iter(4 * 2 * (size_t)n), pre(2 * (size_t)n);
+  std::vector<NormDesc> nd(2 * (size_t)n);
+  std::vector<PrepDesc> pd(2 * (size_t)n);
+  for (int i = 0; i < n; ++i) {
+    const auto& m = set->mats[i];
+    const float* g = grad + m.offset;
+    const int rows = (int)m.rows, cols = (int)m.cols;
+    // L += G G^T (A = G, op(B) = G^T)   R += G^T G (op(A) = G^T, B = G)
+    stats[i] = {g, g, l + m.l_off, nullptr, rows, rows, cols, cols, cols, rows, 1.f, 1.f};
+    stats[n + i] = {g, g, r + m.r_off, nullptr, cols, cols, rows, cols, cols, cols, 1.f, 1.f};
+    for (int sd = 0; sd < 2; ++sd) {
+      const int k = sd * n + i, d = sd == 0 ? rows : cols;
+      nd[k] = {sd == 0 ? l + m.l_off : r + m.r_off, (int64_t)d * d, norms + k};
+      pd[k] = {sd == 0 ? l + m.l_off : r + m.r_off, side(sd, i, X0), side(sd, i, M0),
+               side(sd, i, T), norms + k, d};
+    }
+    // P = X_L G X_R: Y = X_L G, P = Y X_R (root buffers chosen below by iteration parity)
+  }
+  // the iteration ping-pongs X and M: after `root_iters` iterations the result is in
+  // X[root_iters & 1]
+  const int xf = root_iters & 1;
+  for (int i = 0; i < n; ++i) {
+    const auto& m = set->mats[i];
+    const int rows = (int)m.rows, cols = (int)m.cols;
+    pre[i] = {side(0, i, xf), grad + m.offset, ybuf + m.offset, nullptr, rows, cols, rows, rows,
+              cols, cols, 1.f, 0.f};
+    pre[n + i] = {ybuf + m.offset, side(1, i, xf), pbuf + m.offset, nullptr, rows, cols, cols,
+                  cols, cols, cols, 1.f, 0.f};
+  }
+  // Iteration products for both parities of k: even k reads X0 / M0 and writes X1 / M1, odd
+  // k the reverse.
+  std::vector<GemmDesc> iter_odd(4 * 2 * (size_t)n);
+  for (int par = 0; par < 2; ++par) {
+    std::vector<GemmDesc>& tbl = par == 0 ? iter : iter_odd;
+    const int xi = par == 0 ? X0 : X1, xo = par == 0 ? X1 : X0;
+    const int mi = par == 0 ? M0 : M1, mo = par == 0 ? M1 : M0;
+    for (int sd = 0; sd < 2; ++sd)
+      for (int i = 0; i < n; ++i) {
+        const int k = sd * n + i;
+        const int d = set->side_dim[(size_t)k];
+        // X_{k+1} = X_k T,  T2 = T T,  T4 = T2 T2,  M_{k+1} = T4 M_k (and T = (5I - M)/4)
+        tbl[0 * 2 * n + k] = {side(sd, i, xi), side(sd, i, T), side(sd, i, xo), nullptr,
+                              d, d, d, d, d, d, 1.f, 0.f};
+        tbl[1 * 2 * n + k] = {side(sd, i, T), side(sd, i, T), side(sd, i, T2), nullptr,
+                              d, d, d, d, d, d, 1.f, 0.f};
+        tbl[2 * 2 * n + k] = {side(sd, i, T2), side(sd, i, T2), side(sd, i, T4), nullptr,
+                              d, d, d, d, d, d, 1.f, 0.f};
+        tbl[3 * 2 * n + k] = {side(sd, i, T4), side(sd, i, mi), side(sd, i, mo),
+                              side(sd, i, T), d, d, d, d, d, d, 1.f, 0.f};
+      }
+  }
+  // One upload of every table: stats | even iteration | odd iteration | P | norms | prep.
+  const size_t g_bytes = sizeof(GemmDesc) * (size_t)(20 * n);
+  std::vector<uint8_t> host(g_bytes + sizeof(NormDesc) * 2 * (size_t)n +
+                            sizeof(PrepDesc) * 2 * (size_t)n);
+  if (host.size() > set->table_bytes) return MFSDP_EWORKSPACE;
+  {
+    uint8_t* h = host.data();
+    auto put = [&](const void* src, size_t bytes) {
+      std::memcpy(h, src, bytes);
+      h += bytes;
+    };
+    put(stats.data(), sizeof(GemmDesc) * stats.size());
+    put(iter.data(), sizeof(GemmDesc) * iter.size());
+    put(iter_odd.data(), sizeof(GemmDesc) * iter_odd.size());
+    put(pre.data(), sizeof(GemmDesc) * pre.size());
+    put(nd.data(), sizeof(NormDesc) * nd.size());
+    put(pd.data(), sizeof(PrepDesc) * pd.size());
+  }
+  uint8_t* tab = static_cast<uint8_t*>(workspace) + set->off_tables;
+  if (cudaMemcpyAsync(tab, host.data(), host.size(), cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MFSDP_ECUDA;
+  const GemmDesc* d_stats = reinterpret_cast<const GemmDesc*>(tab);
+  const GemmDesc* d_even = d_stats + 2 * n;
+  const GemmDesc* d_odd = d_even + 8 * n;
+  const GemmDesc* d_pre = d_odd + 8 * n;
+  const NormDesc* d_norm = reinterpret_cast<const NormDesc*>(d_pre + 2 * n);
+  const PrepDesc* d_prep = reinterpret_cast<const PrepDesc*>(d_norm + 2 * n);
+
+  int e;
+  // statistics: L += G G^T, R += G^T G
+  if ((e = launch_gemm(d_stats, n, max_rows, max_rows, 0, 1, st)) != MFSDP_OK) return e;
+  if ((e = launch_gemm(d_stats + n, n, max_cols, max_cols, 1, 0, st)) != MFSDP_OK) return e;
+  // inverse fourth roots of every L and R
+  frob_kernel<<<2 * n, 1024, 0, st>>>(d_norm);
+  root_prep_kernel<<<dim3(256, (unsigned)(2 * n)), 256, 0, st>>>(d_prep);
+  if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
+  for (int it = 0; it < root_iters; ++it) {
+    const GemmDesc* tbl = (it & 1) ? d_odd : d_even;
+    for (int prod = 0; prod < 4; ++prod)
+      if ((e = launch_gemm(tbl + prod * 2 * n, 2 * n, max_dim, max_dim, 0, 0, st)) != MFSDP_OK)
+        return e;
+  }
+  // P = L^{-1/4} G R^{-1/4}
+  if ((e = launch_gemm(d_pre, n, max_rows, max_cols, 0, 0, st)) != MFSDP_OK) return e;
+  if ((e = launch_gemm(d_pre + n, n, max_rows, max_cols, 0, 0, st)) != MFSDP_OK) return e;
+  // W = W (1 - lr wd) - lr P, matrix by matrix
+  const float decay = (float)(1.0 - (double)lr * (double)weight_decay);
+  for (const auto& m : set->mats) {
+    const int64_t cnt = m.rows * m.cols;
+    const int blocks = (int)std::min<int64_t>((cnt + 255) / 256, 4096);
+    shampoo_update_kernel<<<blocks, 256, 0, st>>>(weights + m.offset, pbuf + m.offset, cnt,
+                                                  decay, lr);
+  }
+  return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
+}

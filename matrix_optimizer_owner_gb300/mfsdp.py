@@ -153,6 +153,34 @@ def mfsdp_repack_workspace_bytes(n_params: int) -> int:
     return out.value
 
 
+class RepackPlan:
+    """A parameter list and its segment table marshalled once, for repeated pack / unpack
+    calls (the per-call marshalling of a long list costs more host time than the copy)."""
+
+    def __init__(self, params, segments, world_size: int):
+        self.n = len(params)
+        self.world_size = world_size
+        self._pd = _param_array(params)
+        self._seg = _segment_array(segments)
+
+    def _ptrs(self, shards):
+        return (C.c_void_p * self.world_size)(*[_ptr(t) for t in shards])
+
+    def pack(self, canonical, shards, workspace, stream=None) -> None:
+        _check("mfsdp_pack_owner_shards",
+               _lib.load().mfsdp_pack_owner_shards(
+                   self._pd, self.n, self._seg, self.world_size, canonical.element_size(),
+                   _ptr(canonical), self._ptrs(shards), _ptr(workspace), workspace.numel(),
+                   _stream(stream)))
+
+    def unpack(self, shards, canonical, workspace, stream=None) -> None:
+        _check("mfsdp_unpack_owner_shards",
+               _lib.load().mfsdp_unpack_owner_shards(
+                   self._pd, self.n, self._seg, self.world_size, canonical.element_size(),
+                   self._ptrs(shards), _ptr(canonical), _ptr(workspace), workspace.numel(),
+                   _stream(stream)))
+
+
 def mfsdp_pack_owner_shards(params, segments, world_size: int, canonical, shards, workspace,
                             stream=None) -> None:
     """Canonical tensor -> owner shard tensors (``shards[r]`` may be None to skip rank r).
@@ -176,6 +204,46 @@ def mfsdp_unpack_owner_shards(params, segments, world_size: int, shards, canonic
                                                  _segment_array(segments), world_size, eb, ptrs,
                                                  _ptr(canonical), _ptr(workspace),
                                                  workspace.numel(), _stream(stream)))
+
+
+# ------------------------------------------------------------------------------- Shampoo
+class ShampooSet:
+    """Handle of ``mfsdp_shampoo_set``: the owned matrices of an owner Shampoo step."""
+
+    def __init__(self, mats: Sequence[Tuple[int, int, int]]):
+        lib = _lib.load()
+        n = len(mats)
+        arr = (Matrix * max(n, 1))()
+        for i, (r, c, off) in enumerate(mats):
+            arr[i] = Matrix(r, c, off)
+        h = C.c_void_p()
+        _check("mfsdp_shampoo_set_create", lib.mfsdp_shampoo_set_create(arr, n, C.byref(h)))
+        self._h = h
+        ws, ln, rn = C.c_size_t(0), C.c_int64(0), C.c_int64(0)
+        _check("mfsdp_shampoo_set_sizes",
+               lib.mfsdp_shampoo_set_sizes(h, C.byref(ws), C.byref(ln), C.byref(rn)))
+        self.workspace_bytes, self.l_numel, self.r_numel = ws.value, ln.value, rn.value
+
+    def close(self) -> None:
+        if self._h:
+            _lib.load().mfsdp_shampoo_set_destroy(self._h)
+            self._h = None
+
+    __del__ = close
+
+    def init_state(self, eps: float, l, r, workspace, stream=None) -> None:
+        _check("mfsdp_shampoo_init_state",
+               _lib.load().mfsdp_shampoo_init_state(self._h, eps, _ptr(l), _ptr(r),
+                                                    _ptr(workspace), workspace.numel(),
+                                                    _stream(stream)))
+
+    def step(self, grad, l, r, weights, lr: float, weight_decay: float, root_iters: int,
+             workspace, stream=None) -> None:
+        _check("mfsdp_shampoo_step",
+               _lib.load().mfsdp_shampoo_step(self._h, _ptr(grad), _ptr(l), _ptr(r),
+                                              _ptr(weights), lr, weight_decay, root_iters,
+                                              _ptr(workspace), workspace.numel(),
+                                              _stream(stream)))
 
 
 # ------------------------------------------------------------------------------- owner set

@@ -159,3 +159,25 @@ def test_llama3_8b_full_model_pack_and_reshard():
         got = dst[s["owner"]][offs_b[i]:offs_b[i] + s["numel"]]
         assert torch.equal(got, canon[coff[i]:coff[i] + s["numel"]]), i
     assert mfsdp.mfsdp_query_status() == 0
+
+
+def test_repack_plan_matches_the_plain_calls():
+    from matrix_optimizer_owner_gb300 import mfsdp
+    torch.cuda.set_device(0)
+    params = _odd_params(13)
+    ps = _oparams(params)
+    total = sum(p.numel for p in ps)
+    canon = _random(total, torch.int16, 5)
+    segs = _segs(params, 5, 1)
+    _, size = orepack.shard_offsets(ps, _osegs(segs), 5)
+    ws = _ws(len(params))
+    plan = mfsdp.RepackPlan(params, segs, 5)
+    a = [torch.zeros(n, dtype=torch.int16, device="cuda") for n in size]
+    b = [torch.zeros(n, dtype=torch.int16, device="cuda") for n in size]
+    plan.pack(canon, a, ws)
+    mfsdp.mfsdp_pack_owner_shards(params, segs, 5, canon, b, ws)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    back = torch.zeros_like(canon)
+    plan.unpack(a, back, ws)
+    assert torch.equal(back, canon)

@@ -243,3 +243,26 @@ def test_owner_set_validation_and_workspace(lib):
                                 0.01, nul) == -3                         # misaligned
     assert lib.mfsdp_adamw_tail(ptrs, 1, 1, 1.0, 0, 0, 0, 0, 1, 1e-3, 0.9, 0.95, 1e-8,
                                 0.01, nul) == 0                          # empty tail
+
+
+def test_shampoo_validation_before_any_launch(lib):
+    from matrix_optimizer_owner_gb300 import _lib as L
+    mats = (L.Matrix * 2)(L.Matrix(4, 3, 0), L.Matrix(2, 5, 12))
+    h = C.c_void_p()
+    assert lib.mfsdp_shampoo_set_create(mats, 2, C.byref(h)) == 0
+    ws, ln, rn = C.c_size_t(0), C.c_int64(0), C.c_int64(0)
+    assert lib.mfsdp_shampoo_set_sizes(h, C.byref(ws), C.byref(ln), C.byref(rn)) == 0
+    assert (ln.value, rn.value) == (16 + 4, 9 + 25)
+    # 7 root buffers per side, P and Y, norms and tables
+    assert ws.value >= 4 * (7 * (16 + 9 + 4 + 25) + 2 * 22)
+    p = C.c_void_p(1 << 20)  # never dereferenced: every case fails first
+    st = lib.mfsdp_shampoo_step
+    assert st(h, None, p, p, p, 0.1, 0.0, 30, p, ws.value, None) == -1         # no gradient
+    assert st(h, p, p, p, p, 0.1, 0.0, 0, p, ws.value, None) == -1             # iterations
+    assert st(h, p, p, p, p, 0.1, 0.0, 30, None, ws.value, None) == -5         # no workspace
+    assert st(h, p, p, p, p, 0.1, 0.0, 30, p, ws.value - 1, None) == -5        # too small
+    assert lib.mfsdp_shampoo_init_state(h, 0.0, p, p, p, ws.value, None) == -1  # eps
+    assert lib.mfsdp_shampoo_set_destroy(h) == 0
+    bad = (L.Matrix * 1)(L.Matrix(0, 3, 0))
+    assert lib.mfsdp_shampoo_set_create(bad, 1, C.byref(h)) == -2
+    assert lib.mfsdp_shampoo_set_create(None, 1, C.byref(h)) == -1

@@ -459,3 +459,70 @@ def test_repack_round_trips(cfg):
     out = repack.reshard(ps, a, 8, repack.pack(ps, a, 8, canon), b, 3)
     for x, y in zip(out, repack.pack(ps, b, 3, canon)):
         assert np.array_equal(x, y)
+
+
+# ----------------------------------------------------------------------------- Shampoo
+def test_shampoo_inverse_root_closed_forms():
+    from oracle import shampoo
+    lam = np.array([16.0, 1.0, 1e-4, 81.0])
+    np.testing.assert_allclose(shampoo.inverse_root(np.diag(lam)), np.diag(lam ** -0.25),
+                               rtol=1e-12)
+    rng = np.random.default_rng(4)
+    q, _ = np.linalg.qr(rng.normal(size=(6, 6)))
+    lam = rng.uniform(1e-3, 10.0, size=6)
+    a = (q * lam) @ q.T
+    x = shampoo.inverse_root(a)
+    np.testing.assert_allclose(x, (q * lam ** -0.25) @ q.T, rtol=1e-10, atol=1e-12)
+    # X^4 A = I, and the square root variant is different (a planted -1/2 fails the pin)
+    np.testing.assert_allclose(np.linalg.matrix_power(x, 4) @ a, np.eye(6), atol=1e-9)
+    assert not np.allclose(shampoo.inverse_root(a, p=2) @ shampoo.inverse_root(a, p=2) @
+                           shampoo.inverse_root(a, p=2) @ shampoo.inverse_root(a, p=2) @ a,
+                           np.eye(6), atol=1e-3)
+
+
+def test_shampoo_scalar_step_closed_form():
+    # 1 x 1: L = R = eps + g^2, P = g / sqrt(eps + g^2); W = W (1 - lr wd) - lr P
+    from oracle import shampoo
+    eps, g, w = 1e-4, 0.03, 0.5
+    out = shampoo.shampoo_matrix_step(np.array([[w]]), np.array([[eps]]), np.array([[eps]]),
+                                      [np.array([[g / 2]]), np.array([[g / 2]])],
+                                      grad_scale=1.0, lr=0.1, weight_decay=0.01)
+    assert out["L"][0, 0] == pytest.approx(eps + g * g, rel=1e-14)
+    assert out["P"][0, 0] == pytest.approx(g / math.sqrt(eps + g * g), rel=1e-12)
+    assert out["W"][0, 0] == pytest.approx(w * (1 - 0.1 * 0.01) - 0.1 * g / math.sqrt(eps + g * g),
+                                           rel=1e-12)
+
+
+def test_shampoo_rank_one_and_orthogonal_invariance():
+    from oracle import shampoo
+    rng = np.random.default_rng(6)
+    # G = s u v^T: L = eps I + s^2 u u^T, R = eps I + s^2 v v^T, so
+    # P = s (eps + s^2)^{-1/2} u v^T exactly.
+    u = rng.normal(size=5); u /= np.linalg.norm(u)
+    v = rng.normal(size=7); v /= np.linalg.norm(v)
+    s, eps = 0.2, 1e-3
+    g = s * np.outer(u, v)
+    l, r = shampoo.statistics_update(eps * np.eye(5), eps * np.eye(7), g)
+    np.testing.assert_allclose(shampoo.preconditioned(l, r, g),
+                               s / math.sqrt(eps + s * s) * np.outer(u, v), atol=1e-12)
+    # rotating G on both sides rotates P the same way
+    g = rng.normal(size=(5, 7))
+    qa, _ = np.linalg.qr(rng.normal(size=(5, 5)))
+    qb, _ = np.linalg.qr(rng.normal(size=(7, 7)))
+    p1 = shampoo.preconditioned(*shampoo.statistics_update(eps * np.eye(5), eps * np.eye(7), g), g)
+    g2 = qa @ g @ qb
+    p2 = shampoo.preconditioned(*shampoo.statistics_update(eps * np.eye(5), eps * np.eye(7), g2),
+                                g2)
+    np.testing.assert_allclose(p2, qa @ p1 @ qb, atol=1e-10)
+
+
+def test_coupled_newton_root_matches_the_definition():
+    from oracle import shampoo
+    rng = np.random.default_rng(8)
+    for n, spread in ((8, 1e-2), (20, 1e-6), (33, 1e-8)):
+        q, _ = np.linalg.qr(rng.normal(size=(n, n)))
+        lam = np.exp(rng.uniform(np.log(spread), 0.0, size=n))
+        a = (q * lam) @ q.T
+        x = shampoo.coupled_newton_inverse_root(a, iters=30)
+        ref = shampoo.inverse_root(a)
+        assert np.linalg.norm(x - ref) / np.linalg.norm(ref) < 1e-9, n
