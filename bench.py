@@ -58,17 +58,24 @@ NS_TRAFFIC_SOURCES = ("matrix_optimizer_owner_gb300/csrc/ns_gemm.cu",
                       "matrix_optimizer_owner_gb300/csrc/mfsdp_internal.h")
 NS_TRAFFIC = {
     # config index: (sources sha256, bytes per launch, profile summary)
-    1: ("16861d43a1380ef4005f910f26ebc4847ef4fc6d0205066d0bb98dc7cfab22f2", 208922948,
+    1: ("cd2a2668010435c8a6c48f0bbc7356f821d851a0f037264a33c3fcfa51cf6075", 208922948,
         "profiles/owner_step_gpt2_small_launch_list.md"),
 }
 
 
 def ns_sources_sha():
+    """SHA-256 of the kernel sources with comments and blank lines removed (a comment edit
+    does not change the kernel)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for rel in NS_TRAFFIC_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        lines = [ln.rstrip() for ln in src.splitlines() if ln.strip()]
+        h.update("\n".join(lines).encode())
     return h.hexdigest()
 
 

@@ -84,7 +84,7 @@ typedef enum {
 
 /*
  * Assign every role (one per 2D matrix, one packed non-2D tail per block; §3) to an owner
- * rank and lay out the owned segments (§4.1).  The load is owner-resident numel; ties go to
+ * rank and lay out the owned segments (§4.1).  The load is the numel resident on the owner; ties go to
  * the lowest rank.  Within each (block, rank) the owned roles are laid out by first
  * declaration index, a role's parameters in declaration order, unpadded, so every parameter
  * has one contiguous local segment and a tail is one whole segment.

@@ -1,8 +1,8 @@
 // Newton–Schulz phases as one persistent, grouped tcgen05 GEMM launch per phase.
 //
 // "MatrixFSDP: communication-free matrix optimizers under ZeRO-3 parameter sharding", §2: Muon
-// orthogonalises each whole 2D matrix with Newton–Schulz steps built from products such as
-// X X^T.  One quintic iteration, X of shape m x n with m <= n, is three products:
+// orthogonalises each whole 2D matrix with Newton–Schulz steps whose products include X X^T.
+// One quintic iteration, X of shape m x n with m <= n, is three products:
 //     gram  A  = X X^T            (m x m, K = n, symmetric: upper-triangle tiles only)
 //     poly  B  = b*A + c*A A      (m x m, K = m, symmetric: upper-triangle tiles only)
 //     apply X' = a*X + B X        (m x n, K = m)

@@ -3,7 +3,7 @@
 // "MatrixFSDP: communication-free matrix optimizers under ZeRO-3 parameter sharding":
 //   §3   one role per data-parallel-sharded 2D matrix, one packed non-2D tail role per FSDP
 //        unit, each whole on one owner;
-//   §4.1 the planner sees every block; the greedy load is owner-resident numel; RoleGreedy
+//   §4.1 the planner sees every block; the greedy load is the numel resident on the owner; RoleGreedy
 //        (the memory-conservative default) and ScopeGreedy (roles of all blocks pooled); each
 //        block layout gives every parameter one contiguous local segment;
 //   §4.2 O_{B,r}, the bytes of block B owned by rank r, drives the bandwidth model.

@@ -2,8 +2,8 @@
 // whole matrices (fp32).
 //
 // "MatrixFSDP: communication-free matrix optimizers under ZeRO-3 parameter sharding", §5.7:
-// with every 2D matrix whole on its owner, the owner can run Shampoo ("full L/R
-// preconditioners with inverse fourth root") in place of Muon.  Per owned matrix G (rows x
+// with every 2D matrix whole on its owner, the owner can run Shampoo, with full left and
+// right preconditioners and their inverse fourth roots, in place of Muon.  Per owned matrix G (rows x
 // cols), the original Shampoo update:
 //     L += G G^T,  R += G^T G             (L_0 = R_0 = eps I)
 //     P  = L^{-1/4} G R^{-1/4}
@@ -33,7 +33,8 @@ namespace mfsdp {
 namespace {
 
 constexpr int kGemmThreads = 256;
-constexpr int kTM = 128, kTN = 128, kTK = 8;
+constexpr int kTM = 128, kTN = 128, kTK = 16;
+constexpr int kPad = 4;  // shared-memory row padding (keeps 16-byte alignment)
 
 struct GemmDesc {
   const float* a;
@@ -45,59 +46,65 @@ struct GemmDesc {
   float alpha, beta;
 };
 
+// 8 consecutive floats of a row at (r, c0) of a row-major buffer, zero outside rows x cols;
+// 16-byte loads when the 8 are inside and aligned.
+__device__ __forceinline__ void load8(const float* p, int64_t ld, int r, int c0, int rows,
+                                      int cols, float (&v)[8]) {
+  if (r < rows && c0 + 8 <= cols && ((reinterpret_cast<uintptr_t>(p + (int64_t)r * ld + c0) &
+                                      15u) == 0)) {
+    const float4* q = reinterpret_cast<const float4*>(p + (int64_t)r * ld + c0);
+    const float4 x = __ldg(q), y = __ldg(q + 1);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+    return;
+  }
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    v[u] = (r < rows && c0 + u < cols) ? p[(int64_t)r * ld + c0 + u] : 0.f;
+}
+
 // C = alpha op(A) op(B) + beta C for every descriptor (blockIdx.z).  op(A) is m x k: A stored
 // m x k row-major (ta = 0) or k x m (ta = 1); op(B) is k x n: B stored k x n (tb = 0) or
-// n x k (tb = 1).  Thread (ty, tx) of the 16 x 16 grid computes rows {4ty + i, 64 + 4ty + i}
-// and columns {4tx + j, 64 + 4tx + j}, i, j < 4.
+// n x k (tb = 1).  Tiles of op(A) and op(B) are kept k-major in shared memory; thread
+// (ty, tx) of the 16 x 16 grid computes rows {4ty + i, 64 + 4ty + i} and columns
+// {4tx + j, 64 + 4tx + j}, i, j < 4.  A k-tile is 16 deep; each thread moves 8 floats of each
+// operand per k-tile, mapped so that consecutive lanes write consecutive shared-memory words.
 template <int TA, int TB>
 __global__ void __launch_bounds__(kGemmThreads, 2) sgemm_batched_kernel(const GemmDesc* descs) {
-  __shared__ __align__(16) float As[2][kTK][kTM];
-  __shared__ __align__(16) float Bs[2][kTK][kTN];
+  __shared__ __align__(16) float As[2][kTK][kTM + kPad];
+  __shared__ __align__(16) float Bs[2][kTK][kTN + kPad];
   const GemmDesc d = descs[blockIdx.z];
   const int m0 = blockIdx.y * kTM, n0 = blockIdx.x * kTN;
   if (m0 >= d.m || n0 >= d.n) return;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  // k-major operand (A with ta = 0, B with tb = 1): lane -> row tid & 127, k half tid >> 7;
+  // mn-major operand (A with ta = 1, B with tb = 0): k tid >> 4, 8 columns from (tid & 15) * 8
+  const int kr_row = tid & 127, kr_k = (tid >> 7) * 8;
+  const int mr_k = tid >> 4, mr_c = (tid & 15) * 8;
 
-  // global -> register loads of one k-tile (4 floats per thread per operand)
-  float ra[4], rb[4];
+  float ra[8], rb[8];
   auto load_tile = [&](int k0) {
-    if (TA == 0) {  // A[m][k]: thread -> row tid / 2, k (tid % 2) * 4 .. + 3
-      const int mm = m0 + (tid >> 1), kk = k0 + (tid & 1) * 4;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        ra[u] = (mm < d.m && kk + u < d.k) ? d.a[(int64_t)mm * d.lda + kk + u] : 0.f;
-    } else {        // A[k][m]: thread -> k tid / 32, m (tid % 32) * 4 .. + 3
-      const int kk = k0 + (tid >> 5), mm = m0 + (tid & 31) * 4;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        ra[u] = (kk < d.k && mm + u < d.m) ? d.a[(int64_t)kk * d.lda + mm + u] : 0.f;
-    }
-    if (TB == 0) {  // B[k][n]: thread -> k tid / 32, n (tid % 32) * 4 .. + 3
-      const int kk = k0 + (tid >> 5), nn = n0 + (tid & 31) * 4;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        rb[u] = (kk < d.k && nn + u < d.n) ? d.b[(int64_t)kk * d.ldb + nn + u] : 0.f;
-    } else {        // B[n][k]: thread -> n tid / 2, k (tid % 2) * 4 .. + 3
-      const int nn = n0 + (tid >> 1), kk = k0 + (tid & 1) * 4;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        rb[u] = (nn < d.n && kk + u < d.k) ? d.b[(int64_t)nn * d.ldb + kk + u] : 0.f;
-    }
+    if (TA == 0) load8(d.a, d.lda, m0 + kr_row, k0 + kr_k, d.m, d.k, ra);
+    else load8(d.a, d.lda, k0 + mr_k, m0 + mr_c, d.k, d.m, ra);
+    if (TB == 0) load8(d.b, d.ldb, k0 + mr_k, n0 + mr_c, d.k, d.n, rb);
+    else load8(d.b, d.ldb, n0 + kr_row, k0 + kr_k, d.n, d.k, rb);
   };
   auto store_tile = [&](int buf) {
     if (TA == 0) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) As[buf][(tid & 1) * 4 + u][tid >> 1] = ra[u];
+      for (int u = 0; u < 8; ++u) As[buf][kr_k + u][kr_row] = ra[u];
     } else {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) As[buf][tid >> 5][(tid & 31) * 4 + u] = ra[u];
+      *reinterpret_cast<float4*>(&As[buf][mr_k][mr_c]) = make_float4(ra[0], ra[1], ra[2], ra[3]);
+      *reinterpret_cast<float4*>(&As[buf][mr_k][mr_c + 4]) =
+          make_float4(ra[4], ra[5], ra[6], ra[7]);
     }
     if (TB == 0) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) Bs[buf][tid >> 5][(tid & 31) * 4 + u] = rb[u];
+      *reinterpret_cast<float4*>(&Bs[buf][mr_k][mr_c]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
+      *reinterpret_cast<float4*>(&Bs[buf][mr_k][mr_c + 4]) =
+          make_float4(rb[4], rb[5], rb[6], rb[7]);
     } else {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) Bs[buf][(tid & 1) * 4 + u][tid >> 1] = rb[u];
+      for (int u = 0; u < 8; ++u) Bs[buf][kr_k + u][kr_row] = rb[u];
     }
   };
 

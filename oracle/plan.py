@@ -5,7 +5,7 @@
 * §3 — each data-parallel-sharded 2D weight is whole on one owner rank and empty elsewhere;
   the non-2D tensors of one FSDP unit are packed into one tail role, whole on a tail owner.
 * §4.1 — planning sees every FSDP block; each block becomes roles (one per 2D matrix, one
-  packed non-2D tail); the greedy load is owner-resident numel; RoleGreedy is the
+  packed non-2D tail); the greedy load is the numel resident on the owner; RoleGreedy is the
   memory-conservative default and ScopeGreedy pools the roles of all blocks for global
   balance; each block layout must give every parameter one contiguous local segment.
 * §4.2 — the bandwidth model gamma_B = max_r O_{B,r} / (P_B / W).
@@ -200,7 +200,7 @@ def owned(params: Sequence[Param], segs: Sequence[Segment], rank: int):
 #
 # The pages name the scorer's outputs (per-rank parameter, gradient, optimizer-state,
 # communication and workspace estimates) and the CostAware rule (take the ScopeGreedy plan
-# only when its balance gain stays within workspace caps) but print no formulas for them.
+# when its better balance does not cost more workspace than a cap) but print no formulas.
 # Readings, each the plainest one the §4.2 bandwidth model supports:
 #
 # * parameter / gradient bytes of rank r: its owned numel times the element size;
