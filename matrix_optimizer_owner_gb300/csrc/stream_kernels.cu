@@ -607,8 +607,10 @@ cudaError_t launch_reduce_momentum(const ReduceParams& p, int contrib_dtype, cud
   const int per_elem = p.W * esz + 4;
   // E is a power of two from 256 up: it divides the chunk, and for E >= 2048 every thread of
   // the CTA gets the same number of 8-element vectors per stage.
+  // (one or two contributions: 64 KB stages, three of them, so each copy is longer)
+  const size_t budget = p.W <= 2 ? (size_t)64 * 1024 : kBulkStageBudget;
   int E = 256;
-  while (2 * E <= kChunk && (size_t)(2 * E) * per_elem <= kBulkStageBudget) E *= 2;
+  while (2 * E <= kChunk && (size_t)(2 * E) * per_elem <= budget) E *= 2;
   BulkCfg c{};
   c.sub_elems = E;
   c.stage_bytes = E * per_elem;

@@ -113,5 +113,26 @@ class OwnerStep:
         self.apply_update(hyper, stream)
         self.adamw_tail(tail_contribs, hyper, self.t, stream)
 
+    def capture(self, contribs, hyper, reduced_grad=None):
+        """Capture deposit + momentum + norm, Newton–Schulz and the update of this owner step
+        (18 launches for a bf16 owned set) in one CUDA graph on a side stream, reading the
+        given contribution buffers; returns the graph.  The AdamW tail stays outside (its
+        bias correction changes every step): ``graph_step`` replays the graph and launches
+        it."""
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize(self.device)
+        with torch.cuda.graph(g):
+            stream = torch.cuda.current_stream(self.device)
+            self.reduce_momentum(contribs, hyper, reduced_grad, stream)
+            self.newton_schulz(hyper, stream)
+            self.apply_update(hyper, stream)
+        return g
+
+    def graph_step(self, graph, tail_contribs, hyper, stream=None):
+        """One owner step through a graph from ``capture`` plus the AdamW tail."""
+        self.t += 1
+        graph.replay()
+        self.adamw_tail(tail_contribs, hyper, self.t, stream)
+
     def close(self):
         self.oset.close()
