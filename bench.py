@@ -337,28 +337,47 @@ def time_graph(wb, steps, warmup):
     return s.elapsed_time(e) / steps
 
 
-def time_e2e(wb, steps, stream):
-    """Same step through the C ABI with host buffers: H2D of the step's contributions from
-    pinned memory, the step, D2H of the per-matrix update norms."""
+def time_e2e(wb, steps, stream, n_copy_streams=2):
+    """Same step through the C ABI with host buffers: every step copies its contributions
+    host->device from pinned memory, runs, and reads the per-matrix update norms back.  The
+    copies of step k+1 run on copy streams into a second set of device buffers while step k
+    computes (each waits until the step that last used its buffers has finished)."""
     hp = wb.wl.hyper
     r = wb.runner
-    host_c = [c.cpu().pin_memory() for c in wb.contrib]
-    host_t = [c.cpu().pin_memory() for c in wb.tail_contrib]
+    host = [c.cpu().pin_memory() for c in wb.contrib + wb.tail_contrib]
+    n_c = len(wb.contrib)
+    sets = [wb.contrib + wb.tail_contrib,
+            [torch.empty_like(c) for c in wb.contrib + wb.tail_contrib]]
     norm_h = torch.empty(r.norm.numel(), dtype=torch.float32).pin_memory()
+    copy_streams = [torch.cuda.Stream() for _ in range(n_copy_streams)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    copied = [[torch.cuda.Event() for _ in copy_streams] for _ in range(2)]
+
+    def issue_copies(b):
+        for k, cs in enumerate(copy_streams):
+            cs.wait_event(done[b])
+            with torch.cuda.stream(cs):
+                for d, h in list(zip(sets[b], host))[k::n_copy_streams]:
+                    d.copy_(h, non_blocking=True)
+            copied[b][k].record(cs)
+
     torch.cuda.synchronize()
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
     s.record(stream)
-    for _ in range(steps):
-        for d, h in zip(wb.contrib, host_c):
-            d.copy_(h, non_blocking=True)
-        for d, h in zip(wb.tail_contrib, host_t):
-            d.copy_(h, non_blocking=True)
-        r.step(wb.contrib, wb.tail_contrib, hp)
+    issue_copies(0)
+    for i in range(steps):
+        b = i & 1
+        for ev in copied[b]:
+            stream.wait_event(ev)
+        if i + 1 < steps:
+            issue_copies(b ^ 1)
+        r.step(sets[b][:n_c], sets[b][n_c:], hp)
+        done[b].record(stream)
         norm_h.copy_(r.norm, non_blocking=True)
     e.record(stream)
     torch.cuda.synchronize()
-    h2d = sum(c.numel() * c.element_size() for c in host_c + host_t)
+    h2d = sum(c.numel() * c.element_size() for c in host)
     return s.elapsed_time(e) / steps, h2d, norm_h.numel() * 4
 
 
