@@ -1,0 +1,60 @@
+"""bench.py's JSON line: the keys and types every run must print.
+
+The reference arm runs on the CPU (it times the oracle), so its line is checked here without a
+GPU; our arm's line is checked on the GPU with a short run.
+"""
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+BASE_KEYS = {"metric": str, "value": (int, float), "unit": str, "n_gpus": int, "steps": int,
+             "warmup": int, "ms_per_step": (int, float), "higher_is_better": bool,
+             "scaling": str, "dtype": str, "data": str, "config": dict}
+
+
+def _run(args, timeout):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, cwd=ROOT,
+                         capture_output=True, text=True, timeout=timeout)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1, out.stdout
+    return json.loads(lines[0])
+
+
+def _check_base(d):
+    for k, t in BASE_KEYS.items():
+        assert isinstance(d[k], t), k
+    assert "vs_baseline" in d and d["higher_is_better"] is False
+    assert d["config"]["workload"]
+
+
+def test_reference_arm_line():
+    d = _run(["--impl", "reference", "--config", "0", "--steps", "1", "--warmup", "0"], 600)
+    _check_base(d)
+    assert d["impl"] == "reference" and d["dtype"] == "f64"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.gpu
+def test_our_arm_line():
+    d = _run(["--steps", "3", "--warmup", "3", "--cpu-seconds", "2", "--clock-window-s", "0.2"],
+             900)
+    _check_base(d)
+    r = d["roofline"]
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert 0 < r["frac"] < 1.5 and r["achieved"] > 0 and r["peak"] > 0
+    assert "traffic" in r
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert d["gpu_launches"] == 19 * 3
+    assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    assert d["device_status"] == 0
+    assert d["repack"]["bound"] == "hbm" and d["shampoo"]["bound"] == "alu"
