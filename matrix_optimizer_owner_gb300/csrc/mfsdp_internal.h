@@ -163,7 +163,6 @@ struct NsLaunchParams {
   int* status;
 };
 
-size_t ns_smem_bytes(bool split);
 cudaError_t ns_prepare_kernels();  // set the dynamic shared memory attribute once per device
 int ns_pair_max_clusters(int num_sms);  // co-resident CTA pairs of the pair kernel (-1: error)
 // split: single-CTA kernel, `grid` CTAs; else the CTA-pair kernel, `grid` pairs.

@@ -1084,16 +1084,11 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
 
 }  // namespace
 
-size_t ns_smem_bytes(bool split) { return split ? Cfg<true>::kSmem : Cfg<false>::kSmem; }
 
 cudaError_t ns_prepare_kernels() {
   cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)PairCfg::kSmem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(ns_gemm_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)Cfg<false>::kSmem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(ns_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)Cfg<true>::kSmem);
