@@ -58,7 +58,7 @@ NS_TRAFFIC_SOURCES = ("matrix_optimizer_owner_gb300/csrc/ns_gemm.cu",
                       "matrix_optimizer_owner_gb300/csrc/mfsdp_internal.h")
 NS_TRAFFIC = {
     # config index: (sources sha256, bytes per launch, profile summary)
-    1: ("cd2a2668010435c8a6c48f0bbc7356f821d851a0f037264a33c3fcfa51cf6075", 208922948,
+    1: ("55e2b1c500f6b58b8be0231d6700a06f84b08f885f67a0ced6c74f5da2b01dc6", 209561190,
         "profiles/owner_step_gpt2_small_launch_list.md"),
 }
 
