@@ -320,21 +320,22 @@ def time_steps(wb, steps, warmup, stream, clock_window_s=0.0):
 
 def time_graph(wb, steps, warmup):
     """The same step with deposit, Newton–Schulz and update replayed from one CUDA graph
-    (AdamW tail launched after it); returns ms per step."""
+    (AdamW tail launched after it); returns (ms per step over the timed region, the K
+    per-step times)."""
     hp = wb.wl.hyper
     r = wb.runner
     g = r.capture(wb.contrib, hp)
     for _ in range(warmup):
         r.graph_step(g, wb.tail_contrib, hp)
     torch.cuda.synchronize()
-    s = torch.cuda.Event(enable_timing=True)
-    e = torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record()
+    for k in range(steps):
         r.graph_step(g, wb.tail_contrib, hp)
-    e.record()
+        ev[k + 1].record()
     torch.cuda.synchronize()
-    return s.elapsed_time(e) / steps
+    per_step = [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
+    return ev[0].elapsed_time(ev[steps]) / steps, per_step
 
 
 def time_e2e(wb, steps, stream, n_copy_streams=2):
@@ -473,7 +474,8 @@ def run_ours(args, rank, world, local_rank):
                                       args.clock_window_s)
         # the product's launch path: deposit, Newton–Schulz and update replayed from one
         # CUDA graph, the AdamW tail launched after it
-        graph_ms = None if args.no_graph else time_graph(wb, args.steps, max(args.warmup, 3))
+        graph_ms, graph_steps = (None, None) if args.no_graph else \
+            time_graph(wb, args.steps, max(args.warmup, 3))
     clocks = clk.summary()
     if clocks is not None:
         clocks["window"] = (f"{args.clock_window_s:.1f} s of untimed steps + the timed "
@@ -517,6 +519,8 @@ def run_ours(args, rank, world, local_rank):
                        launch=("CUDA graph (deposit, Newton–Schulz, update) + AdamW tail"
                                if graph_ms is not None else "call by call")),
         "eager_ms_per_step": round(eager_ms, 4),
+        "step_ms_median": round(statistics.median(graph_steps), 4) if graph_steps else None,
+        "step_ms_max": round(max(graph_steps), 4) if graph_steps else None,
         "ns_tflops": round(ns_tf_nominal, 1), "ns_tflops_executed": round(ns_tf_exec, 1),
         "ns_frac_of_peak": round(ns_tf_exec / peak_tf, 4),
         "phases_ms_per_step": {k: round(v / args.steps, 4) for k, v in phases.items()},
