@@ -58,7 +58,7 @@ NS_TRAFFIC_SOURCES = ("matrix_optimizer_owner_gb300/csrc/ns_gemm.cu",
                       "matrix_optimizer_owner_gb300/csrc/mfsdp_internal.h")
 NS_TRAFFIC = {
     # config index: (sources sha256, bytes per launch, profile summary)
-    1: ("55e2b1c500f6b58b8be0231d6700a06f84b08f885f67a0ced6c74f5da2b01dc6", 209561190,
+    1: ("1411d0098b5646a5e85b08c266047908082bd3000fe769244611453089739e22", 208988228,
         "profiles/owner_step_gpt2_small_launch_list.md"),
 }
 
@@ -414,10 +414,12 @@ def time_repack(wb, reps, stream, world=8):
 FFMA_PEAK_NOTE = "152 SMs x 128 fp32 lanes x 2 FLOP x the sampled SM clock"
 
 
-def time_shampoo(device, reps=2, root_iters=30):
+def time_shampoo(device, reps=2, root_iters=30, precision=0):
     """Owner Shampoo step on one GPT-2-small layer's matrices (2304x768, 768x768, 3072x768,
-    768x3072), fp32: statistics, 30 coupled-Newton steps for every inverse fourth root, the
-    preconditioned update.  Returns (ms per step, FLOPs per step)."""
+    768x3072): statistics, 30 coupled-Newton steps for every inverse fourth root, the
+    preconditioned update; precision 0 = fp32 products on the CUDA cores, 1 = the root
+    iteration and P on the tensor cores with split-bf16 operands.  Returns (ms per step,
+    nominal FLOPs per step, tensor-core FLOPs executed per step)."""
     from matrix_optimizer_owner_gb300 import mfsdp
     shapes = [(2304, 768), (768, 768), (3072, 768), (768, 3072)]
     offs, o = [], 0
@@ -431,22 +433,26 @@ def time_shampoo(device, reps=2, root_iters=30):
     sset.init_state(1e-6, l, r_, ws)
     g = torch.randn(o, device=device) * 1e-3
     w = torch.randn(o, device=device) * 0.02
-    sset.step(g, l, r_, w, 0.02, 0.01, root_iters, ws)
+    sset.step(g, l, r_, w, 0.02, 0.01, root_iters, ws, precision=precision)
     torch.cuda.synchronize()
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
     s.record()
     for _ in range(reps):
-        sset.step(g, l, r_, w, 0.02, 0.01, root_iters, ws)
+        sset.step(g, l, r_, w, 0.02, 0.01, root_iters, ws, precision=precision)
     e.record()
     torch.cuda.synchronize()
-    flops = 0
+    flops = tensor = 0
     for r, c in shapes:
         flops += 2 * r * r * c + 2 * r * c * c          # statistics
         flops += root_iters * 4 * 2 * (r ** 3 + c ** 3)  # roots
         flops += 2 * r * r * c + 2 * r * c * c          # P
+        # tensor path: symmetric side products keep the upper triangle, the last iteration
+        # forms X only, three MMAs per split product
+        sym = sum(d * (d + 1) * d for d in (r, c))
+        tensor += 3 * ((4 * (root_iters - 1) + 1) * sym + 2 * r * r * c + 2 * r * c * c)
     sset.close()
-    return s.elapsed_time(e) / reps, flops
+    return s.elapsed_time(e) / reps, flops, tensor
 
 
 def config_block(wb, cfg):
@@ -542,17 +548,31 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks, "device_status": status,
     }
     if not args.no_shampoo and rank == 0:
-        sms_, sflops = time_shampoo(dev)
+        what = ("one owner Shampoo step of one GPT-2-small layer (2304x768, 768x768, "
+                "3072x768, 768x3072), 30 coupled-Newton steps per inverse fourth root")
+        sms_, sflops, _ = time_shampoo(dev)
         sm_mhz = (clocks or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
         ffma_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
         line["shampoo"] = {
             "kernel": "sgemm_batched_kernel (fp32 FFMA) + root and update kernels",
-            "what": "one owner Shampoo step of one GPT-2-small layer (2304x768, 768x768, "
-                    "3072x768, 768x3072), 30 coupled-Newton steps per inverse fourth root",
+            "what": what, "precision": "fp32",
             "ms": round(sms_, 3), "flops": sflops, "bound": "alu",
             "achieved_tflops": round(sflops / (sms_ * 1e-3) / 1e12, 2),
             "peak_tflops": round(ffma_peak, 1), "peak_source": FFMA_PEAK_NOTE,
             "frac": round(sflops / (sms_ * 1e-3) / 1e12 / ffma_peak, 4)}
+        tms, tflops, texec = time_shampoo(dev, precision=1)
+        line["shampoo_tc"] = {
+            "kernel": "ns_gemm_kernel<split> (tcgen05, split-bf16) for the roots and P; "
+                      "sgemm_batched_kernel for the statistics",
+            "what": what, "precision": "split_bf16",
+            "ms": round(tms, 3), "flops": tflops, "bound": "tensor",
+            "tensor_flops_executed": texec,
+            "achieved_tflops": round(texec / (tms * 1e-3) / 1e12, 1),
+            "peak_tflops": float(peaks["bf16_tflops"]),
+            "peak_source": f"{peak_src} bf16 burst",
+            "frac": round(texec / (tms * 1e-3) / 1e12 / float(peaks["bf16_tflops"]), 4),
+            "frac_note": "executed tensor FLOPs over the whole step time (statistics, norms "
+                         "and elementwise kernels included)"}
     if not args.no_repack:
         rms, rbytes, nparams = time_repack(wb, 10, stream)
         line["repack"] = {

@@ -229,19 +229,31 @@ typedef struct {
  * The pages name the preconditioners and the inverse fourth root only; this is the original
  * Shampoo update.  The roots come from `root_iters` steps of the coupled Newton iteration for
  * the inverse p-th root (p = 4), started from X = c^{-1/4} I, M = A / c with c = ||A||_F; an
- * eigenvalue ratio of 1e-8 converges within 26 steps.  Every product is an fp32 GEMM on the
- * CUDA cores.
+ * eigenvalue ratio of 1e-8 converges within 26 steps.
+ *
+ * `precision` selects where the products run:
+ *   MFSDP_SHAMPOO_FP32        every product an fp32 GEMM on the CUDA cores;
+ *   MFSDP_SHAMPOO_SPLIT_BF16  the statistics as above; the root iteration and P = X_L G X_R on
+ *                             the tcgen05 tensor cores with split-bf16 operands (value = hi +
+ *                             lo, three products per multiply, fp32 accumulation: about 16
+ *                             significant bits per stored value, so the roots carry a relative
+ *                             error near 1e-4 where the fp32 path reaches 1e-6).
  *
  * Buffers (DEVICE, fp32, caller-owned): `grad` and `weights` are the flat owner buffers the
  * matrix table's offsets index (grad = the deposited gradient, e.g. the reduced_grad_out of
  * mfsdp_owner_reduce_momentum); `l` / `r` hold every matrix's L (rows^2) / R (cols^2) back to
  * back in table order (sizes from mfsdp_shampoo_set_sizes).  The workspace holds the root
- * iteration's buffers (7 x (rows^2 + cols^2) floats per matrix), P and the launch tables.
- * Errors: MFSDP_EINVAL (null pointers, eps <= 0, root_iters outside [1, 200]), MFSDP_ESHAPE
+ * iteration's buffers (7 x (rows^2 + cols^2) values per matrix), P, the tensor maps and the
+ * launch tables; its size covers both precisions.
+ * Errors: MFSDP_EINVAL (null pointers, eps <= 0, root_iters outside [1, 200], unknown
+ * precision), MFSDP_ESHAPE
  * (rows or cols outside [1, 65536], negative offset), MFSDP_EWORKSPACE, MFSDP_ECUDA.
  * ------------------------------------------------------------------------------------------ */
 
 typedef struct mfsdp_shampoo_set mfsdp_shampoo_set;
+
+#define MFSDP_SHAMPOO_FP32 0
+#define MFSDP_SHAMPOO_SPLIT_BF16 1
 
 int mfsdp_shampoo_set_create(const mfsdp_matrix* mats, int32_t n_mats, mfsdp_shampoo_set** out);
 int mfsdp_shampoo_set_destroy(mfsdp_shampoo_set* set);
@@ -254,7 +266,8 @@ int mfsdp_shampoo_init_state(const mfsdp_shampoo_set* set, float eps, float* l, 
 /* One Shampoo step of every matrix in the set (enqueued on `stream`). */
 int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* grad, float* l, float* r,
                        float* weights, float lr, float weight_decay, int32_t root_iters,
-                       void* workspace, size_t workspace_bytes, void* stream);
+                       int32_t precision, void* workspace, size_t workspace_bytes,
+                       void* stream);
 
 
 typedef struct mfsdp_owner_set_s mfsdp_owner_set;

@@ -66,8 +66,8 @@ SIGNATURES = {
     "mfsdp_shampoo_set_sizes": (C.c_int, [_vp, C.POINTER(C.c_size_t), C.POINTER(_i64),
                                           C.POINTER(_i64)]),
     "mfsdp_shampoo_init_state": (C.c_int, [_vp, _f32, _vp, _vp, _vp, C.c_size_t, _vp]),
-    "mfsdp_shampoo_step": (C.c_int, [_vp, _vp, _vp, _vp, _vp, _f32, _f32, _i32, _vp, C.c_size_t,
-                                     _vp]),
+    "mfsdp_shampoo_step": (C.c_int, [_vp, _vp, _vp, _vp, _vp, _f32, _f32, _i32, _i32, _vp,
+                                     C.c_size_t, _vp]),
     "mfsdp_owner_set_create": (C.c_int, [C.POINTER(Matrix), _i32, _i64, C.POINTER(_vp)]),
     "mfsdp_owner_set_destroy": (C.c_int, [_vp]),
     "mfsdp_owner_set_workspace_bytes": (C.c_int, [_vp, C.POINTER(C.c_size_t)]),

@@ -73,7 +73,7 @@ struct mfsdp_owner_set_s {
   void* ortho_lo = nullptr;
 };
 
-namespace {
+namespace mfsdp {
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -109,7 +109,7 @@ bool encode_map3d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
 // box_cols with a 128-byte swizzle (operand loads) or a 64-byte swizzle (the epilogue's
 // 32 x 32 staging blocks).
 bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
-                uint32_t box_rows, uint32_t box_cols = 64, bool swizzle128 = true) {
+                uint32_t box_rows, uint32_t box_cols, bool swizzle128) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -137,6 +137,10 @@ void add_tiles(std::vector<NsTile>& out, int32_t prob, int64_t M, int64_t N, boo
       }
   }
 }
+
+}  // namespace mfsdp
+
+namespace {
 
 int check_device(const mfsdp_owner_set* set) {
   int dev = -1;

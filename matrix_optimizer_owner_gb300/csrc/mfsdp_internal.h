@@ -6,6 +6,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <vector>
 
 namespace mfsdp {
 
@@ -134,8 +135,8 @@ struct NsProblem {         // one output matrix of one Newton–Schulz phase
   int32_t first;           // first iteration: fold s = 1/(norm + eps) into alpha / beta
   int32_t mat;             // matrix index (norm)
   int32_t map_a, map_b;    // tensor-map indices of the hi operands (2D 64x64 box); +1: 2D
-                           // 64x128 box, +2: 3D 64x64x2 MN-major view, +3: 2D 32x32 unswizzled
-                           // box (stores), +kMapsPerHalf: the lo half's maps
+                           // 64x128 box, +2: 3D 64x64x2 MN-major view, +3: 2D 32x32 box with
+                           // 64-byte swizzle (stores), +kMapsPerHalf: the lo half's maps
   int32_t mn3d;            // bit 0 / bit 1: the A / B operand is MN-major and has the 3D view
   int32_t map_o;           // tensor-map index of the output's 32x32 store box (hi, 64B swizzle)
   int32_t pad2_;
@@ -167,5 +168,16 @@ cudaError_t ns_prepare_kernels();  // set the dynamic shared memory attribute on
 int ns_pair_max_clusters(int num_sms);  // co-resident CTA pairs of the pair kernel (-1: error)
 // split: single-CTA kernel, `grid` CTAs; else the CTA-pair kernel, `grid` pairs.
 cudaError_t launch_ns_phase(const NsLaunchParams& p, bool split, int grid, cudaStream_t s);
+
+// 2D bf16 tensor map over a rows x cols row-major buffer of pitch ld elements (box_rows x
+// box_cols boxes; 128-byte swizzle, or 64-byte for the epilogue's store boxes) and the 3D
+// MN-major view; false when the driver refuses the map.
+bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
+                uint32_t box_rows, uint32_t box_cols = 64, bool swizzle128 = true);
+bool encode_map3d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld);
+// Output tiles (bm x kBN) of one problem in the rasterised order; `sym` keeps the tiles that
+// reach the upper triangle.
+void add_tiles(std::vector<NsTile>& out, int32_t prob, int64_t M, int64_t N, bool sym,
+               int64_t bm);
 
 }  // namespace mfsdp

@@ -18,6 +18,7 @@
 // (fp32 FFMA, 128 x 128 output tiles, 8 x 8 outputs per thread, double-buffered shared
 // memory): a launch runs the same product for every owned matrix (blockIdx.z = matrix).
 // The iteration's T = (5I - M) / 4 is written by the epilogue of the product that forms M.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -223,6 +224,103 @@ __global__ void shampoo_update_kernel(float* w, const float* p, int64_t n, float
     w[e] = fmaf(w[e], decay, -lr * p[e]);
 }
 
+// ---------------------------------------------------------------- split-bf16 root path
+// A value v is held as two bf16, hi = rn(v) and lo = rn(v - hi) (16 significant bits); the
+// Newton–Schulz GEMM's split mode multiplies such pairs with three tensor-core products
+// (hi*hi + hi*lo + lo*hi, fp32 accumulation) and writes its output the same way.
+__device__ __forceinline__ void split_bf16(float v, uint16_t& hi, uint16_t& lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  hi = __bfloat16_as_ushort(h);
+  lo = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(h)));
+}
+__device__ __forceinline__ float join_bf16(uint16_t hi, uint16_t lo) {
+  return __uint_as_float((uint32_t)hi << 16) + __uint_as_float((uint32_t)lo << 16);
+}
+
+struct SplitDesc {   // a rows x cols fp32 matrix (pitch lds) to / from a split pair (pitch ldd)
+  const float* src;  // nullable (prep, T-update): see the kernels
+  uint16_t* hi;
+  uint16_t* lo;
+  int32_t rows, cols, lds, ldd;
+};
+
+// hi / lo of a fp32 matrix (the gradient G).
+__global__ void to_split_kernel(const SplitDesc* descs) {
+  const SplitDesc d = descs[blockIdx.y];
+  const int64_t n = (int64_t)d.rows * d.cols;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / d.cols, c = e % d.cols;
+    uint16_t h, l;
+    split_bf16(d.src[r * d.lds + c], h, l);
+    d.hi[r * d.ldd + c] = h;
+    d.lo[r * d.ldd + c] = l;
+  }
+}
+
+struct RootPrepDesc {
+  const float* a;        // the statistics matrix, dim x dim, pitch dim
+  const double* norm;    // ||A||_F
+  uint16_t *x_hi, *x_lo, *m_hi, *m_lo, *t_hi, *t_lo;  // pitch ld
+  int32_t dim, ld;
+};
+
+// X = c^{-1/4} I, M = A / c, T = (5I - M) / 4 as split pairs.
+__global__ void root_prep_split_kernel(const RootPrepDesc* descs) {
+  const RootPrepDesc d = descs[blockIdx.y];
+  const int64_t n = (int64_t)d.dim * d.dim;
+  const double c = *d.norm;
+  const float inv_c = (float)(1.0 / c), x0 = (float)pow(c, -0.25);
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / d.dim, col = e % d.dim, o = r * d.ld + col;
+    const bool diag = r == col;
+    uint16_t h, l;
+    split_bf16(d.a[e] * inv_c, h, l);
+    d.m_hi[o] = h;
+    d.m_lo[o] = l;
+    const float mv = join_bf16(h, l);
+    split_bf16(((diag ? 5.f : 0.f) - mv) * 0.25f, h, l);
+    d.t_hi[o] = h;
+    d.t_lo[o] = l;
+    split_bf16(diag ? x0 : 0.f, h, l);
+    d.x_hi[o] = h;
+    d.x_lo[o] = l;
+  }
+}
+
+// T = (5I - M) / 4 from the split M (hi, lo in `src` slots reinterpreted: see the host).
+struct TDesc {
+  const uint16_t *m_hi, *m_lo;
+  uint16_t *t_hi, *t_lo;
+  int32_t dim, ld;
+};
+
+__global__ void t_from_m_kernel(const TDesc* descs) {
+  const TDesc d = descs[blockIdx.y];
+  const int64_t n = (int64_t)d.dim * d.dim;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / d.dim, col = e % d.dim, o = r * d.ld + col;
+    uint16_t h, l;
+    split_bf16(((r == col ? 5.f : 0.f) - join_bf16(d.m_hi[o], d.m_lo[o])) * 0.25f, h, l);
+    d.t_hi[o] = h;
+    d.t_lo[o] = l;
+  }
+}
+
+// W = W (1 - lr wd) - lr (P_hi + P_lo) for one matrix (P pitch ldp).
+__global__ void update_split_kernel(float* w, const uint16_t* p_hi, const uint16_t* p_lo,
+                                    int32_t rows, int32_t cols, int32_t ldp, float decay,
+                                    float lr) {
+  const int64_t n = (int64_t)rows * cols;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / cols, c = e % cols, o = r * ldp + c;
+    w[e] = fmaf(w[e], decay, -lr * join_bf16(p_hi[o], p_lo[o]));
+  }
+}
+
 }  // namespace
 }  // namespace mfsdp
 
@@ -244,6 +342,23 @@ struct mfsdp_shampoo_set {
   std::vector<int32_t> side_dim;
   int64_t floats = 0;
   size_t off_norms = 0, off_tables = 0, table_bytes = 0, ws_bytes = 0;
+  // split-bf16 (tensor-core) layout: per side the same seven buffers as (hi, lo) bf16 pairs of
+  // pitch side_ld; per matrix G, Y, P as pairs of pitch mat_ld; then norms, the epilogue's
+  // (unused) per-problem scale array, tensor maps and launch tables
+  std::vector<size_t> tc_side_off, tc_mat_off;
+  std::vector<int32_t> side_ld, mat_ld;
+  size_t tc_off_norms = 0, tc_off_fnorm = 0, tc_off_tables = 0, tc_table_bytes = 0;
+  size_t tc_ws_bytes = 0;
+  int max_rows() const {
+    int64_t v = 0;
+    for (const auto& m : mats) v = std::max(v, m.rows);
+    return (int)v;
+  }
+  int max_cols() const {
+    int64_t v = 0;
+    for (const auto& m : mats) v = std::max(v, m.cols);
+    return (int)v;
+  }
 };
 
 namespace {
@@ -262,6 +377,127 @@ int launch_gemm(const GemmDesc* dev_descs, int nprob, int max_m, int max_n, int 
   else if (ta == 1 && tb == 0) sgemm_batched_kernel<1, 0><<<grid, kGemmThreads, 0, st>>>(dev_descs);
   else sgemm_batched_kernel<1, 1><<<grid, kGemmThreads, 0, st>>>(dev_descs);
   return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
+}
+
+}  // namespace
+
+namespace {
+
+// Split-kernel launches of a step.  One root iteration is three launches over every side:
+// kXT (X' = T X and T2 = T T, both from the current T), kT4 (T4 = T2 T2) and kTM (M' = T4 M),
+// then T = (5I - M') / 4 elementwise; the last iteration runs only the X' tiles of kXT.
+// Every side product is a polynomial in the statistics matrix, so symmetric: only the tiles
+// touching the upper triangle run and the epilogue mirrors them.
+constexpr int kTcLaunches = 7;
+enum TcLaunch { kXT0, kXT1, kT4, kTM0, kTM1, kY, kP };
+
+int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
+
+// Tensor-map index of buffer b of side k (hi half; +kMapsPerHalf: lo) or of matrix i's G, Y, P.
+int tc_side_map(int k, int b) { return (k * kSideBufs + b) * 2 * kMapsPerHalf; }
+int tc_mat_map(int n, int i, int b) { return (2 * n * kSideBufs + i * 3 + b) * 2 * kMapsPerHalf; }
+int tc_n_maps(int n) { return (2 * n * kSideBufs + 3 * n) * 2 * kMapsPerHalf; }
+
+struct TcTables {
+  std::vector<NsProblem> probs[kTcLaunches];
+  std::vector<NsTile> tiles[kTcLaunches];
+  int32_t x_tiles[2] = {0, 0};  // leading X' tiles of kXT0 / kXT1
+};
+
+// Problems and tiles of every split-kernel launch; buffer addresses from the workspace `base`,
+// or null when only the counts are wanted.
+void tc_tables(const mfsdp_shampoo_set* s, uint8_t* base, int root_iters, TcTables& tt) {
+  const int n = (int)s->mats.size();
+  auto sbuf = [&](int k, int b, int h) -> uint16_t* {
+    if (!base) return nullptr;
+    const int64_t d = s->side_dim[(size_t)k], p = s->side_ld[(size_t)k];
+    return reinterpret_cast<uint16_t*>(base + s->tc_side_off[(size_t)k]) + (b * 2 + h) * d * p;
+  };
+  auto mbuf = [&](int i, int b, int h) -> uint16_t* {
+    if (!base) return nullptr;
+    const auto& m = s->mats[(size_t)i];
+    return reinterpret_cast<uint16_t*>(base + s->tc_mat_off[(size_t)i]) +
+           (b * 2 + h) * m.rows * s->mat_ld[(size_t)i];
+  };
+  enum { X0 = 0, X1 = 1, M0 = 2, M1 = 3, T = 4, T2 = 5, T4 = 6 };
+  // out (M x N) = A B: A as K-major rows (M x K), B as MN-major rows (K x N) when b_mn = 1,
+  // as K-major rows (N x K, i.e. B^T stored) when b_mn = 0
+  auto prob = [&](int M, int N, int K, int b_mn, int sym, int mat, int ma, int mb, uint16_t* oh,
+                  uint16_t* ol, int64_t ldo) {
+    NsProblem p{};
+    p.M = M; p.N = N; p.K = K;
+    p.a_mn = 0; p.b_mn = b_mn; p.sym = sym; p.kind = kApply; p.first = 0; p.mat = mat;
+    p.map_a = ma; p.map_b = mb; p.mn3d = 0; p.map_o = 0;
+    p.d_hi = nullptr; p.d_lo = nullptr; p.ldd = 0;  // no addend: the launches run with a = 0
+    p.o_hi = oh; p.o_lo = ol; p.ldo = ldo;
+    return p;
+  };
+  auto side = [&](int k, int a, int b, int o) {  // side product o = a b of side k
+    const int d = s->side_dim[(size_t)k], p = s->side_ld[(size_t)k];
+    return prob(d, d, d, 1, 1, k, tc_side_map(k, a), tc_side_map(k, b), sbuf(k, o, 0),
+                sbuf(k, o, 1), p);
+  };
+  for (int par = 0; par < 2; ++par) {
+    const int xi = par ? X1 : X0, xo = par ? X0 : X1, mi = par ? M1 : M0, mo = par ? M0 : M1;
+    auto& xt = tt.probs[par ? kXT1 : kXT0];
+    for (int k = 0; k < 2 * n; ++k) xt.push_back(side(k, T, xi, xo));
+    for (int k = 0; k < 2 * n; ++k) xt.push_back(side(k, T, T, T2));
+    for (int k = 0; k < 2 * n; ++k) tt.probs[par ? kTM1 : kTM0].push_back(side(k, T4, mi, mo));
+  }
+  for (int k = 0; k < 2 * n; ++k) tt.probs[kT4].push_back(side(k, T2, T2, T4));
+  // P = X_L G X_R with the roots in X[root_iters & 1]: Y = X_L G, P = Y X_R
+  const int xf = root_iters & 1;
+  for (int i = 0; i < n; ++i) {
+    const auto& m = s->mats[(size_t)i];
+    const int rows = (int)m.rows, cols = (int)m.cols, pc = s->mat_ld[(size_t)i];
+    tt.probs[kY].push_back(prob(rows, cols, rows, 1, 0, i, tc_side_map(i, xf),
+                                tc_mat_map(n, i, 0), mbuf(i, 1, 0), mbuf(i, 1, 1), pc));
+    tt.probs[kP].push_back(prob(rows, cols, cols, 1, 0, i, tc_mat_map(n, i, 1),
+                                tc_side_map(n + i, xf), mbuf(i, 2, 0), mbuf(i, 2, 1), pc));
+  }
+  for (int l = 0; l < kTcLaunches; ++l)
+    for (size_t q = 0; q < tt.probs[l].size(); ++q) {
+      const NsProblem& p = tt.probs[l][q];
+      add_tiles(tt.tiles[l], (int32_t)q, p.M, p.N, p.sym != 0, kBM);
+      if ((l == kXT0 || l == kXT1) && q + 1 == (size_t)(2 * n))
+        tt.x_tiles[l == kXT1] = (int32_t)tt.tiles[l].size();
+    }
+}
+
+size_t tc_table_bytes(const TcTables& tt, int n) {
+  size_t b = align256(sizeof(CUtensorMap) * (size_t)tc_n_maps(n));
+  for (int l = 0; l < kTcLaunches; ++l)
+    b += align256(sizeof(NsProblem) * std::max<size_t>(tt.probs[l].size(), 1)) +
+         align256(sizeof(NsTile) * std::max<size_t>(tt.tiles[l].size(), 1));
+  b += align256(sizeof(GemmDesc) * 2 * (size_t)n) + align256(sizeof(NormDesc) * 2 * (size_t)n) +
+       align256(sizeof(RootPrepDesc) * 2 * (size_t)n) + align256(sizeof(TDesc) * 4 * (size_t)n) +
+       align256(sizeof(SplitDesc) * (size_t)n);
+  return b;
+}
+
+void tc_layout(mfsdp_shampoo_set* s) {
+  const int n = (int)s->mats.size();
+  size_t off = 0;
+  for (int sd = 0; sd < 2; ++sd)
+    for (const auto& m : s->mats) {
+      const int64_t d = sd == 0 ? m.rows : m.cols;
+      s->side_ld.push_back((int32_t)round8(d));
+      s->tc_side_off.push_back(off);
+      off = align256(off + sizeof(uint16_t) * 2 * kSideBufs * (size_t)d * (size_t)round8(d));
+    }
+  for (const auto& m : s->mats) {
+    s->mat_ld.push_back((int32_t)round8(m.cols));
+    s->tc_mat_off.push_back(off);
+    off = align256(off + sizeof(uint16_t) * 6 * (size_t)m.rows * (size_t)round8(m.cols));
+  }
+  s->tc_off_norms = off;
+  s->tc_off_fnorm = align256(off + sizeof(double) * 2 * (size_t)std::max(n, 1));
+  s->tc_off_tables = align256(s->tc_off_fnorm + sizeof(float) * 2 * (size_t)std::max(n, 1));
+  s->tc_off_tables = (s->tc_off_tables + 1023) & ~size_t(1023);  // tensor maps: 64-byte aligned
+  TcTables tt;
+  tc_tables(s, nullptr, 1, tt);
+  s->tc_table_bytes = tc_table_bytes(tt, std::max(n, 1));
+  s->tc_ws_bytes = align256(s->tc_off_tables + s->tc_table_bytes);
 }
 
 }  // namespace
@@ -303,6 +539,8 @@ extern "C" int mfsdp_shampoo_set_create(const mfsdp_matrix* mats, int32_t n_mats
                    sizeof(NormDesc) * 2 * (size_t)std::max(n, 1) +
                    sizeof(PrepDesc) * 2 * (size_t)std::max(n, 1);
   s->ws_bytes = align256(s->off_tables + s->table_bytes);
+  tc_layout(s);
+  s->ws_bytes = std::max(s->ws_bytes, s->tc_ws_bytes);
   *out = s;
   return MFSDP_OK;
 }
@@ -352,17 +590,180 @@ extern "C" int mfsdp_shampoo_init_state(const mfsdp_shampoo_set* set, float eps,
   return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
 }
 
+namespace {
+
+// The Shampoo step with the root iterations and the preconditioning on the tensor cores
+// (split-bf16 operands, fp32 accumulation); statistics and norms as in the fp32 path.
+int shampoo_step_split(const mfsdp_shampoo_set* set, const float* grad, float* l, float* r,
+                       float* weights, float lr, float weight_decay, int32_t root_iters,
+                       uint8_t* ws, cudaStream_t st) {
+  const int n = (int)set->mats.size();
+  TcTables tt;
+  tc_tables(set, ws, root_iters, tt);
+  double* norms = reinterpret_cast<double*>(ws + set->tc_off_norms);
+  float* fnorm = reinterpret_cast<float*>(ws + set->tc_off_fnorm);
+  auto sbuf = [&](int k, int b, int h) {
+    const int64_t d = set->side_dim[(size_t)k], p = set->side_ld[(size_t)k];
+    return reinterpret_cast<uint16_t*>(ws + set->tc_side_off[(size_t)k]) + (b * 2 + h) * d * p;
+  };
+  auto mbuf = [&](int i, int b, int h) {
+    return reinterpret_cast<uint16_t*>(ws + set->tc_mat_off[(size_t)i]) +
+           (b * 2 + h) * set->mats[(size_t)i].rows * set->mat_ld[(size_t)i];
+  };
+  enum { X0 = 0, X1 = 1, M0 = 2, M1 = 3, T = 4 };
+
+  // tensor maps: the 64 x 64 box (MN-major operand) and the 128 x 64 box (K-major operand) of
+  // every hi and lo half
+  std::vector<CUtensorMap> maps((size_t)tc_n_maps(n));
+  std::memset(maps.data(), 0, maps.size() * sizeof(CUtensorMap));
+  auto put_maps = [&](int idx, const uint16_t* hi, const uint16_t* lo, int64_t rows, int64_t cols,
+                      int64_t ld) {
+    for (int h = 0; h < 2; ++h) {
+      CUtensorMap* mp = maps.data() + idx + h * kMapsPerHalf;
+      const uint16_t* b = h ? lo : hi;
+      if (!encode_map(mp, b, rows, cols, ld, 64u) || !encode_map(mp + 1, b, rows, cols, ld, 128u))
+        return false;
+    }
+    return true;
+  };
+  for (int k = 0; k < 2 * n; ++k)
+    for (int b = 0; b < kSideBufs; ++b)
+      if (!put_maps(tc_side_map(k, b), sbuf(k, b, 0), sbuf(k, b, 1), set->side_dim[(size_t)k],
+                    set->side_dim[(size_t)k], set->side_ld[(size_t)k]))
+        return MFSDP_ECUDA;
+  for (int i = 0; i < n; ++i)
+    for (int b = 0; b < 2; ++b)  // G and Y are operands; P only an output
+      if (!put_maps(tc_mat_map(n, i, b), mbuf(i, b, 0), mbuf(i, b, 1), set->mats[(size_t)i].rows,
+                    set->mats[(size_t)i].cols, set->mat_ld[(size_t)i]))
+        return MFSDP_ECUDA;
+
+  std::vector<GemmDesc> stats(2 * (size_t)n);
+  std::vector<NormDesc> nd(2 * (size_t)n);
+  std::vector<RootPrepDesc> pd(2 * (size_t)n);
+  std::vector<TDesc> td(4 * (size_t)n);
+  std::vector<SplitDesc> sp((size_t)n);
+  for (int i = 0; i < n; ++i) {
+    const auto& m = set->mats[(size_t)i];
+    const float* g = grad + m.offset;
+    const int rows = (int)m.rows, cols = (int)m.cols;
+    stats[i] = {g, g, l + m.l_off, nullptr, rows, rows, cols, cols, cols, rows, 1.f, 1.f};
+    stats[n + i] = {g, g, r + m.r_off, nullptr, cols, cols, rows, cols, cols, cols, 1.f, 1.f};
+    sp[i] = {g, mbuf(i, 0, 0), mbuf(i, 0, 1), rows, cols, cols, set->mat_ld[(size_t)i]};
+  }
+  for (int k = 0; k < 2 * n; ++k) {
+    const int i = k % n, d = set->side_dim[(size_t)k], ld = set->side_ld[(size_t)k];
+    const auto& m = set->mats[(size_t)i];
+    float* a = k < n ? l + m.l_off : r + m.r_off;
+    nd[k] = {a, (int64_t)d * d, norms + k};
+    pd[k] = {a, norms + k, sbuf(k, X0, 0), sbuf(k, X0, 1), sbuf(k, M0, 0), sbuf(k, M0, 1),
+             sbuf(k, T, 0), sbuf(k, T, 1), d, ld};
+    // after an even iteration M is in M1, after an odd one in M0
+    td[k] = {sbuf(k, M1, 0), sbuf(k, M1, 1), sbuf(k, T, 0), sbuf(k, T, 1), d, ld};
+    td[2 * n + k] = {sbuf(k, M0, 0), sbuf(k, M0, 1), sbuf(k, T, 0), sbuf(k, T, 1), d, ld};
+  }
+
+  // one upload, in the layout the table area is sized for
+  std::vector<uint8_t> host(set->tc_table_bytes, 0);
+  size_t at = 0;
+  auto put = [&](const void* src, size_t bytes) {
+    const size_t o = at;
+    std::memcpy(host.data() + at, src, bytes);
+    at += align256(std::max<size_t>(bytes, 1));
+    return o;
+  };
+  const size_t o_maps = put(maps.data(), maps.size() * sizeof(CUtensorMap));
+  size_t o_probs[kTcLaunches], o_tiles[kTcLaunches];
+  for (int q = 0; q < kTcLaunches; ++q) {
+    o_probs[q] = put(tt.probs[q].data(), tt.probs[q].size() * sizeof(NsProblem));
+    o_tiles[q] = put(tt.tiles[q].data(), tt.tiles[q].size() * sizeof(NsTile));
+  }
+  const size_t o_stats = put(stats.data(), stats.size() * sizeof(GemmDesc));
+  const size_t o_norm = put(nd.data(), nd.size() * sizeof(NormDesc));
+  const size_t o_prep = put(pd.data(), pd.size() * sizeof(RootPrepDesc));
+  const size_t o_t = put(td.data(), td.size() * sizeof(TDesc));
+  const size_t o_split = put(sp.data(), sp.size() * sizeof(SplitDesc));
+  if (at > set->tc_table_bytes) return MFSDP_EWORKSPACE;
+  uint8_t* tab = ws + set->tc_off_tables;
+  if (cudaMemcpyAsync(tab, host.data(), at, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemsetAsync(fnorm, 0, sizeof(float) * 2 * (size_t)n, st) != cudaSuccess)
+    return MFSDP_ECUDA;
+  if (ns_prepare_kernels() != cudaSuccess) return MFSDP_ECUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MFSDP_ECUDA;
+  int* status = status_word_address();
+  if (status == nullptr) return MFSDP_ECUDA;
+
+  auto ns = [&](int q, int32_t ntiles) {
+    NsLaunchParams lp{};
+    lp.probs = reinterpret_cast<const NsProblem*>(tab + o_probs[q]);
+    lp.tiles = reinterpret_cast<const NsTile*>(tab + o_tiles[q]);
+    lp.ntiles = ntiles;
+    lp.maps = reinterpret_cast<const CUtensorMap*>(tab + o_maps);
+    lp.norm = fnorm;
+    lp.eps = 1.f;
+    lp.a = 0.f;  // out = acc: no addend
+    lp.b = 0.f;
+    lp.c = 1.f;
+    lp.wait_limit_ns = wait_limit_ns();
+    lp.status = status;
+    return launch_ns_phase(lp, true, std::min(ntiles, sms), st) == cudaSuccess;
+  };
+  auto all = [&](int q) { return (int32_t)tt.tiles[q].size(); };
+  const unsigned nb = (unsigned)n;
+  int e;
+  // statistics: L += G G^T, R += G^T G (fp32), and G as a split pair
+  const GemmDesc* d_stats = reinterpret_cast<const GemmDesc*>(tab + o_stats);
+  if ((e = launch_gemm(d_stats, n, set->max_rows(), set->max_rows(), 0, 1, st)) != MFSDP_OK)
+    return e;
+  if ((e = launch_gemm(d_stats + n, n, set->max_cols(), set->max_cols(), 1, 0, st)) != MFSDP_OK)
+    return e;
+  to_split_kernel<<<dim3(128, nb), 256, 0, st>>>(reinterpret_cast<const SplitDesc*>(tab + o_split));
+  frob_kernel<<<2 * n, 1024, 0, st>>>(reinterpret_cast<const NormDesc*>(tab + o_norm));
+  root_prep_split_kernel<<<dim3(256, 2 * nb), 256, 0, st>>>(
+      reinterpret_cast<const RootPrepDesc*>(tab + o_prep));
+  if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
+  const TDesc* d_t = reinterpret_cast<const TDesc*>(tab + o_t);
+  for (int it = 0; it < root_iters; ++it) {
+    const int par = it & 1;
+    const bool last = it + 1 == root_iters;
+    if (!ns(par ? kXT1 : kXT0, last ? tt.x_tiles[par] : all(par ? kXT1 : kXT0))) return MFSDP_ECUDA;
+    if (last) break;
+    if (!ns(kT4, all(kT4)) || !ns(par ? kTM1 : kTM0, all(par ? kTM1 : kTM0))) return MFSDP_ECUDA;
+    t_from_m_kernel<<<dim3(256, 2 * nb), 256, 0, st>>>(d_t + par * 2 * n);
+  }
+  // P = X_L G X_R
+  if (!ns(kY, all(kY)) || !ns(kP, all(kP))) return MFSDP_ECUDA;
+  const float decay = (float)(1.0 - (double)lr * (double)weight_decay);
+  for (int i = 0; i < n; ++i) {
+    const auto& m = set->mats[(size_t)i];
+    const int blocks = (int)std::min<int64_t>((m.rows * m.cols + 255) / 256, 4096);
+    update_split_kernel<<<blocks, 256, 0, st>>>(weights + m.offset, mbuf(i, 2, 0), mbuf(i, 2, 1),
+                                                (int32_t)m.rows, (int32_t)m.cols,
+                                                set->mat_ld[(size_t)i], decay, lr);
+  }
+  return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
+}
+
+}  // namespace
+
 extern "C" int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* grad, float* l,
                                   float* r, float* weights, float lr, float weight_decay,
-                                  int32_t root_iters, void* workspace, size_t workspace_bytes,
-                                  void* stream) {
+                                  int32_t root_iters, int32_t precision, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
   if (set == nullptr || grad == nullptr || l == nullptr || r == nullptr || weights == nullptr)
     return MFSDP_EINVAL;
   if (root_iters < 1 || root_iters > 200) return MFSDP_EINVAL;
+  if (precision != MFSDP_SHAMPOO_FP32 && precision != MFSDP_SHAMPOO_SPLIT_BF16)
+    return MFSDP_EINVAL;
   const int n = (int)set->mats.size();
   if (n == 0) return MFSDP_OK;
   if (workspace == nullptr || workspace_bytes < set->ws_bytes) return MFSDP_EWORKSPACE;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (precision == MFSDP_SHAMPOO_SPLIT_BF16)
+    return shampoo_step_split(set, grad, l, r, weights, lr, weight_decay, root_iters,
+                              static_cast<uint8_t*>(workspace), st);
   float* wsf = static_cast<float*>(workspace);
   double* norms = reinterpret_cast<double*>(static_cast<uint8_t*>(workspace) + set->off_norms);
   float* pbuf = wsf + (set->floats - 2 * set->numel);

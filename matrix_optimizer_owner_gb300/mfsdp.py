@@ -207,6 +207,9 @@ def mfsdp_unpack_owner_shards(params, segments, world_size: int, shards, canonic
 
 
 # ------------------------------------------------------------------------------- Shampoo
+SHAMPOO_FP32 = 0
+SHAMPOO_SPLIT_BF16 = 1
+
 class ShampooSet:
     """Handle of ``mfsdp_shampoo_set``: the owned matrices of an owner Shampoo step."""
 
@@ -238,11 +241,13 @@ class ShampooSet:
                                                     _stream(stream)))
 
     def step(self, grad, l, r, weights, lr: float, weight_decay: float, root_iters: int,
-             workspace, stream=None) -> None:
+             workspace, stream=None, precision: int = 0) -> None:
+        """``precision``: SHAMPOO_FP32 (CUDA-core fp32 products) or SHAMPOO_SPLIT_BF16 (root
+        iteration and preconditioning on the tensor cores, split-bf16 operands)."""
         _check("mfsdp_shampoo_step",
                _lib.load().mfsdp_shampoo_step(self._h, _ptr(grad), _ptr(l), _ptr(r),
                                               _ptr(weights), lr, weight_decay, root_iters,
-                                              _ptr(workspace), workspace.numel(),
+                                              precision, _ptr(workspace), workspace.numel(),
                                               _stream(stream)))
 
 

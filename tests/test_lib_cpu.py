@@ -253,14 +253,19 @@ def test_shampoo_validation_before_any_launch(lib):
     ws, ln, rn = C.c_size_t(0), C.c_int64(0), C.c_int64(0)
     assert lib.mfsdp_shampoo_set_sizes(h, C.byref(ws), C.byref(ln), C.byref(rn)) == 0
     assert (ln.value, rn.value) == (16 + 4, 9 + 25)
-    # 7 root buffers per side, P and Y, norms and tables
+    # 7 root buffers per side, P and Y, norms and tables; the split-bf16 mode's buffers (hi and
+    # lo halves, rows padded to 8 elements) and its tensor maps (8 per buffer) fit as well
     assert ws.value >= 4 * (7 * (16 + 9 + 4 + 25) + 2 * 22)
+    assert ws.value >= 4 * 7 * (4 * 8 + 3 * 8 + 2 * 8 + 5 * 8) + 128 * 8 * (7 * 4 + 3 * 2)
     p = C.c_void_p(1 << 20)  # never dereferenced: every case fails first
     st = lib.mfsdp_shampoo_step
-    assert st(h, None, p, p, p, 0.1, 0.0, 30, p, ws.value, None) == -1         # no gradient
-    assert st(h, p, p, p, p, 0.1, 0.0, 0, p, ws.value, None) == -1             # iterations
-    assert st(h, p, p, p, p, 0.1, 0.0, 30, None, ws.value, None) == -5         # no workspace
-    assert st(h, p, p, p, p, 0.1, 0.0, 30, p, ws.value - 1, None) == -5        # too small
+    for prec in (0, 1):
+        assert st(h, None, p, p, p, 0.1, 0.0, 30, prec, p, ws.value, None) == -1  # no gradient
+        assert st(h, p, p, p, p, 0.1, 0.0, 0, prec, p, ws.value, None) == -1      # iterations
+        assert st(h, p, p, p, p, 0.1, 0.0, 30, prec, None, ws.value, None) == -5  # no workspace
+        assert st(h, p, p, p, p, 0.1, 0.0, 30, prec, p, ws.value - 1, None) == -5  # too small
+    assert st(h, p, p, p, p, 0.1, 0.0, 30, 2, p, ws.value, None) == -1          # precision
+    assert st(h, p, p, p, p, 0.1, 0.0, 30, -1, p, ws.value, None) == -1
     assert lib.mfsdp_shampoo_init_state(h, 0.0, p, p, p, ws.value, None) == -1  # eps
     assert lib.mfsdp_shampoo_set_destroy(h) == 0
     bad = (L.Matrix * 1)(L.Matrix(0, 3, 0))
