@@ -526,3 +526,120 @@ def test_coupled_newton_root_matches_the_definition():
         x = shampoo.coupled_newton_inverse_root(a, iters=30)
         ref = shampoo.inverse_root(a)
         assert np.linalg.norm(x - ref) / np.linalg.norm(ref) < 1e-9, n
+
+
+# ----------------------------------------------------------------------------- SOAP
+SOAP_HYPER = dict(grad_scale=1.0, lr=1e-3, weight_decay=1e-2, beta1=0.9, beta2=0.95, eps=1e-8,
+                  beta_stats=0.95)
+
+
+def _soap_run(gs, w0, **over):
+    from oracle import soap
+    h = dict(SOAP_HYPER, **over)
+    rows, cols = gs[0].shape
+    st = {"W": w0, "L": np.zeros((rows, rows)), "R": np.zeros((cols, cols)),
+          "M": np.zeros((rows, cols)), "V": np.zeros((rows, cols))}
+    outs = []
+    for t, g in enumerate(gs, start=1):
+        st = soap.soap_matrix_step(st["W"], st["L"], st["R"], st["M"], st["V"], [g], t=t, **h)
+        outs.append(st)
+    return outs
+
+
+def test_soap_scalar_is_the_hand_worked_adamw_run():
+    # 1 x 1: the eigenbasis is +-1, so SOAP is AdamW on the single element; p0 = 1,
+    # lr 1e-3, wd 1e-2, betas (0.9, 0.95), eps 1e-8, gradients 0.5, -0.25, 0 (fp64 by hand)
+    outs = _soap_run([np.array([[0.5]]), np.array([[-0.25]]), np.array([[0.0]])],
+                     np.array([[1.0]]))
+    expect = [(0.05, 0.0125, 0.99899000002), (0.02, 0.015, 0.99871164067875817),
+              (0.018, 0.01425, 0.9984915208835361)]
+    for o, (m, v, p) in zip(outs, expect):
+        assert o["M"][0, 0] == pytest.approx(m, rel=1e-12)
+        assert o["V"][0, 0] == pytest.approx(v, rel=1e-12)
+        assert o["W"][0, 0] == pytest.approx(p, rel=1e-13)
+
+
+def test_soap_diagonal_gradients_are_elementwise_adamw():
+    # diagonal G with |g_11| > |g_22| > |g_33| at every step: L and R stay diagonal in that
+    # order, the eigenbases are signed identities, and each diagonal entry runs its own AdamW
+    # (the independent coordinate-wise oracle); off-diagonal entries only decay
+    rng = np.random.default_rng(21)
+    gs = [np.diag(np.array([3.0, 2.0, 1.0]) * rng.uniform(0.5, 0.6, 3) *
+                  rng.choice([-1.0, 1.0], 3)) for _ in range(4)]
+    w0 = rng.normal(size=(3, 3))
+    outs = _soap_run(gs, w0)
+    p, m, v = np.diag(w0).copy(), np.zeros(3), np.zeros(3)
+    for t, (g, o) in enumerate(zip(gs, outs), start=1):
+        p, m, v = adamw.adamw_step(p, m, v, np.diag(g), t, 1e-3, 0.9, 0.95, 1e-8, 1e-2)
+        np.testing.assert_allclose(np.diag(o["W"]), p, rtol=1e-12)
+        off = ~np.eye(3, dtype=bool)
+        np.testing.assert_allclose(o["W"][off], w0[off] * (1 - 1e-5) ** t, rtol=1e-12)
+
+
+def test_soap_rank_one_closed_form():
+    # first step, G = s u v^T (unit u, v): the top eigenvectors are +-u and +-v, G' = +-s e1 e1^T,
+    # N' = +-s / (s + eps) at (1, 1) and 0 elsewhere, so N = s / (s + eps) u v^T
+    from oracle import soap
+    rng = np.random.default_rng(22)
+    u = rng.normal(size=5); u /= np.linalg.norm(u)
+    v = rng.normal(size=7); v /= np.linalg.norm(v)
+    s, eps = 0.2, 1e-3
+    o = _soap_run([s * np.outer(u, v)], np.zeros((5, 7)), eps=eps)[0]
+    np.testing.assert_allclose(o["N"], s / (s + eps) * np.outer(u, v), atol=1e-12)
+    assert o["lamL"][0] == pytest.approx(0.05 * s * s, rel=1e-12)
+    assert np.all(np.diff(o["lamL"]) <= 0) and np.all(np.diff(o["lamR"]) <= 0)
+
+
+def test_soap_orthogonal_equivariance_and_transpose():
+    # G -> A G B^T (A, B orthogonal) for every step and W0 -> A W0 B^T: W, M rotate the same
+    # way, L -> A L A^T, R -> B R B^T, and V (eigenbasis coordinates) is unchanged.  G -> G^T
+    # swaps L and R and transposes W, M and V.
+    rng = np.random.default_rng(23)
+    gs = [rng.normal(size=(5, 7)) * 1e-2 for _ in range(3)]
+    w0 = rng.normal(size=(5, 7))
+    a, _ = np.linalg.qr(rng.normal(size=(5, 5)))
+    b, _ = np.linalg.qr(rng.normal(size=(7, 7)))
+    base = _soap_run(gs, w0, eps=1e-6)
+    rot = _soap_run([a @ g @ b.T for g in gs], a @ w0 @ b.T, eps=1e-6)
+    tr = _soap_run([g.T for g in gs], w0.T, eps=1e-6)
+    for o, orot, otr in zip(base, rot, tr):
+        np.testing.assert_allclose(orot["W"], a @ o["W"] @ b.T, atol=1e-10)
+        np.testing.assert_allclose(orot["M"], a @ o["M"] @ b.T, atol=1e-12)
+        np.testing.assert_allclose(orot["L"], a @ o["L"] @ a.T, atol=1e-12)
+        np.testing.assert_allclose(orot["V"], o["V"], rtol=1e-8, atol=1e-16)
+        np.testing.assert_allclose(otr["W"], o["W"].T, atol=1e-10)
+        np.testing.assert_allclose(otr["V"], o["V"].T, rtol=1e-8, atol=1e-16)
+        np.testing.assert_allclose(otr["L"], o["R"], atol=1e-12)
+
+
+def test_soap_direction_ignores_eigenvector_signs():
+    from oracle import soap
+    rng = np.random.default_rng(24)
+    g, m, v = rng.normal(size=(4, 6)), rng.normal(size=(4, 6)), rng.uniform(size=(4, 6))
+    ql, _ = np.linalg.qr(rng.normal(size=(4, 4)))
+    qr, _ = np.linalg.qr(rng.normal(size=(6, 6)))
+    kw = dict(t=3, beta1=0.9, beta2=0.95, eps=1e-8)
+    n1, _, v1 = soap.soap_direction(g, m, v, ql, qr, **kw)
+    sl, sr = np.array([1, -1, -1, 1]), np.array([-1, 1, 1, 1, -1, 1])
+    n2, _, v2 = soap.soap_direction(g, m, v, ql * sl, qr * sr, **kw)
+    np.testing.assert_allclose(n2, n1, atol=1e-12)
+    np.testing.assert_allclose(v2, v1, rtol=1e-14)
+
+
+def test_planted_soap_mistakes_are_caught():
+    # back-rotation without the transpose, and the second moment kept in parameter
+    # coordinates: both fail the rank-one closed form
+    rng = np.random.default_rng(25)
+    u = rng.normal(size=5); u /= np.linalg.norm(u)
+    v = rng.normal(size=7); v /= np.linalg.norm(v)
+    s, eps = 0.2, 1e-3
+    g = s * np.outer(u, v)
+    from oracle import soap
+    _, ql = soap.eigenbasis(g @ g.T)
+    _, qr = soap.eigenbasis(g.T @ g)
+    want = s / (s + eps) * np.outer(u, v)
+    n_rot = (ql.T @ g @ qr) / (np.abs(ql.T @ g @ qr) + eps)
+    assert np.abs(ql @ n_rot @ qr - want).max() > 1e-2                  # Q_R instead of Q_R^T
+    assert np.abs(ql @ n_rot @ qr.T - want).max() < 1e-12
+    n_param = g / (np.abs(g) + eps)                                       # Adam in W coordinates
+    assert np.abs(n_param - want).max() > 1e-2
