@@ -13,6 +13,7 @@
  *   mfsdp_pack_owner_shards /     canonical axis <-> owner shards (reshard load)  §4.4
  *   mfsdp_unpack_owner_shards
  *   mfsdp_shampoo_step            owner Shampoo (L/R inverse fourth roots)         §5.7
+ *   mfsdp_soap_step               owner SOAP (Adam in the Shampoo eigenbasis)      §5.7
  *   mfsdp_owner_reduce_momentum   W-way gradient deposit + Nesterov momentum + norm  §3, §4.2
  *   mfsdp_newton_schulz           quintic Newton–Schulz of every owned matrix      §2
  *   mfsdp_apply_update            scaled update with decoupled weight decay        §5.1
@@ -269,6 +270,68 @@ int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* grad, float* l
                        int32_t precision, void* workspace, size_t workspace_bytes,
                        void* stream);
 
+
+/* ------------------------------------------------------------------------------------------
+ * Owner SOAP (§5.7): Adam run in the eigenbasis of the Shampoo statistics, on the owner's
+ * whole matrices, in place of Muon.  For every matrix G (rows x cols) of the set and step
+ * t >= 1 (the pages name the method only; this is the SOAP update with the eigenbasis taken
+ * exactly at every step):
+ *     L = bs L + (1 - bs) G G^T,   R = bs R + (1 - bs) G^T G
+ *     Q_L, Q_R = eigenvectors of L, R (columns), in descending eigenvalue order
+ *     M = b1 M + (1 - b1) G                      (parameter coordinates)
+ *     G' = Q_L^T G Q_R,  M' = Q_L^T M Q_R
+ *     V = b2 V + (1 - b2) G'^2                   (eigenbasis coordinates)
+ *     N = Q_L [ (M' / (1 - b1^t)) / (sqrt(V / (1 - b2^t)) + eps) ] Q_R^T
+ *     W = W (1 - lr weight_decay) - lr N
+ * The eigenbases come from cyclic block Jacobi on Q^T L Q, started from the basis the state
+ * holds (the previous step's), until a sweep rotates nothing or `max_sweeps` sweeps ran;
+ * every product is fp32 on the CUDA cores.  Eigenvectors are fixed up to sign, and N does not
+ * depend on the signs.
+ *
+ * State (DEVICE, fp32, caller-owned, updated in place): `l`, `q_l` hold every matrix's L and
+ * Q_L (rows^2 each) back to back in table order, `r`, `q_r` its R and Q_R (cols^2); `eig_l`
+ * (sum of rows) and `eig_r` (sum of cols) the eigenvalues, descending per matrix;
+ * `exp_avg` (M) and `exp_avg_sq` (V) are flat owner buffers indexed like the weights.
+ * mfsdp_soap_init_state sets L = R = 0, Q = I, eigenvalues, M and V to 0; a caller may write
+ * any symmetric positive semi-definite L, R and any orthogonal Q there instead.
+ * `grad` and `weights` are the flat owner buffers (fp32).  `info` (DEVICE, nullable,
+ * 2 x n_mats int32: L sides, then R sides) receives the sweeps each solve used, negated when
+ * it stopped at max_sweeps.
+ * Errors: MFSDP_EINVAL (null pointers, t < 1, max_sweeps outside [1, 100], a beta outside
+ * [0, 1), eps < 0, jacobi_tol outside [0, 1e-2)), MFSDP_ESHAPE (rows or cols outside [1, 65536], negative offset),
+ * MFSDP_EWORKSPACE, MFSDP_ECUDA.
+ * ------------------------------------------------------------------------------------------ */
+
+typedef struct mfsdp_soap_set mfsdp_soap_set;
+
+typedef struct {
+  float* l;
+  float* r;
+  float* q_l;
+  float* q_r;
+  float* eig_l;
+  float* eig_r;
+  float* exp_avg;
+  float* exp_avg_sq;
+} mfsdp_soap_state;
+
+typedef struct {
+  float lr, beta1, beta2, beta_stats, eps, weight_decay;
+  int32_t max_sweeps;
+  float jacobi_tol;  /* couplings below jacobi_tol * ||L|| are not rotated; 0: 1e-6 */
+} mfsdp_soap_hyper;
+
+int mfsdp_soap_set_create(const mfsdp_matrix* mats, int32_t n_mats, mfsdp_soap_set** out);
+int mfsdp_soap_set_destroy(mfsdp_soap_set* set);
+/* Workspace bytes and the numel of the flat L (= Q_L), R (= Q_R) and eigenvalue buffers. */
+int mfsdp_soap_set_sizes(const mfsdp_soap_set* set, size_t* workspace_bytes, int64_t* l_numel,
+                         int64_t* r_numel, int64_t* eig_l_numel, int64_t* eig_r_numel);
+int mfsdp_soap_init_state(const mfsdp_soap_set* set, const mfsdp_soap_state* state,
+                          void* workspace, size_t workspace_bytes, void* stream);
+/* One SOAP step of every matrix in the set (enqueued on `stream`). */
+int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, float* weights,
+                    const mfsdp_soap_state* state, int64_t t, const mfsdp_soap_hyper* hyper,
+                    int32_t* info, void* workspace, size_t workspace_bytes, void* stream);
 
 typedef struct mfsdp_owner_set_s mfsdp_owner_set;
 

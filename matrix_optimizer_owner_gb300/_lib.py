@@ -33,6 +33,17 @@ class Matrix(C.Structure):
     _fields_ = [("rows", C.c_int64), ("cols", C.c_int64), ("offset", C.c_int64)]
 
 
+class SoapState(C.Structure):
+    _fields_ = [(name, C.c_void_p) for name in
+                ("l", "r", "q_l", "q_r", "eig_l", "eig_r", "exp_avg", "exp_avg_sq")]
+
+
+class SoapHyper(C.Structure):
+    _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float),
+                ("beta_stats", C.c_float), ("eps", C.c_float), ("weight_decay", C.c_float),
+                ("max_sweeps", C.c_int32), ("jacobi_tol", C.c_float)]
+
+
 class CostModel(C.Structure):
     _fields_ = [("param_bytes", C.c_int32), ("grad_bytes", C.c_int32),
                 ("state_bytes", C.c_int32), ("ns_steps", C.c_int32)]
@@ -68,6 +79,13 @@ SIGNATURES = {
     "mfsdp_shampoo_init_state": (C.c_int, [_vp, _f32, _vp, _vp, _vp, C.c_size_t, _vp]),
     "mfsdp_shampoo_step": (C.c_int, [_vp, _vp, _vp, _vp, _vp, _f32, _f32, _i32, _i32, _vp,
                                      C.c_size_t, _vp]),
+    "mfsdp_soap_set_create": (C.c_int, [C.POINTER(Matrix), _i32, C.POINTER(_vp)]),
+    "mfsdp_soap_set_destroy": (C.c_int, [_vp]),
+    "mfsdp_soap_set_sizes": (C.c_int, [_vp, C.POINTER(C.c_size_t), C.POINTER(_i64),
+                                       C.POINTER(_i64), C.POINTER(_i64), C.POINTER(_i64)]),
+    "mfsdp_soap_init_state": (C.c_int, [_vp, C.POINTER(SoapState), _vp, C.c_size_t, _vp]),
+    "mfsdp_soap_step": (C.c_int, [_vp, _vp, _vp, C.POINTER(SoapState), _i64,
+                                  C.POINTER(SoapHyper), _vp, _vp, C.c_size_t, _vp]),
     "mfsdp_owner_set_create": (C.c_int, [C.POINTER(Matrix), _i32, _i64, C.POINTER(_vp)]),
     "mfsdp_owner_set_destroy": (C.c_int, [_vp]),
     "mfsdp_owner_set_workspace_bytes": (C.c_int, [_vp, C.POINTER(C.c_size_t)]),

@@ -117,6 +117,21 @@ cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int* status, cudaStr
 int* status_word_address();  // device address of this device's status word (nullptr on error)
 uint64_t wait_limit_ns();    // limit of every bounded device-side wait (mfsdp_set_wait_limit_ns)
 
+// ---- batched fp32 GEMM on the CUDA cores (second-order optimizers) ------------------------
+struct GemmDesc {          // C = alpha op(A) op(B) + beta C, row-major, one problem
+  const float* a;
+  const float* b;
+  float* c;
+  float* t_out;            // nullable: also write (5 delta_ij - C_ij) / 4 here
+  int32_t m, n, k;
+  int32_t lda, ldb, ldc;
+  float alpha, beta;
+};
+// Every problem of the table in one launch (blockIdx.z = problem); ta / tb: op = transpose.
+// Returns an MFSDP status.
+int launch_gemm(const GemmDesc* dev_descs, int nprob, int max_m, int max_n, int ta, int tb,
+                cudaStream_t st);
+
 // ---- Newton–Schulz grouped GEMM (tcgen05 / TMEM / TMA) ------------------------------------
 constexpr int kBM = 128;   // tile rows    = UMMA M (one CTA, TMEM lanes 0..127)
 constexpr int kBN = 256;   // tile columns = UMMA N

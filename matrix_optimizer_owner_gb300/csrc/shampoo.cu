@@ -37,15 +37,6 @@ constexpr int kGemmThreads = 256;
 constexpr int kTM = 128, kTN = 128, kTK = 16;
 constexpr int kPad = 4;  // shared-memory row padding (keeps 16-byte alignment)
 
-struct GemmDesc {
-  const float* a;
-  const float* b;
-  float* c;
-  float* t_out;  // nullable: also write (5 delta_ij - C_ij) / 4 here
-  int32_t m, n, k;
-  int32_t lda, ldb, ldc;
-  float alpha, beta;
-};
 
 // 8 consecutive floats of a row at (r, c0) of a row-major buffer, zero outside rows x cols;
 // 16-byte loads when the 8 are inside and aligned.
@@ -322,6 +313,19 @@ __global__ void update_split_kernel(float* w, const uint16_t* p_hi, const uint16
 }
 
 }  // namespace
+
+int launch_gemm(const GemmDesc* dev_descs, int nprob, int max_m, int max_n, int ta, int tb,
+                cudaStream_t st) {
+  if (nprob <= 0) return MFSDP_OK;
+  const dim3 grid((unsigned)((max_n + kTN - 1) / kTN), (unsigned)((max_m + kTM - 1) / kTM),
+                  (unsigned)nprob);
+  if (ta == 0 && tb == 0) sgemm_batched_kernel<0, 0><<<grid, kGemmThreads, 0, st>>>(dev_descs);
+  else if (ta == 0 && tb == 1) sgemm_batched_kernel<0, 1><<<grid, kGemmThreads, 0, st>>>(dev_descs);
+  else if (ta == 1 && tb == 0) sgemm_batched_kernel<1, 0><<<grid, kGemmThreads, 0, st>>>(dev_descs);
+  else sgemm_batched_kernel<1, 1><<<grid, kGemmThreads, 0, st>>>(dev_descs);
+  return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
+}
+
 }  // namespace mfsdp
 
 using namespace mfsdp;
@@ -366,18 +370,6 @@ namespace {
 constexpr int kSideBufs = 7;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
-int launch_gemm(const GemmDesc* dev_descs, int nprob, int max_m, int max_n, int ta, int tb,
-                cudaStream_t st) {
-  if (nprob <= 0) return MFSDP_OK;
-  const dim3 grid((unsigned)((max_n + kTN - 1) / kTN), (unsigned)((max_m + kTM - 1) / kTM),
-                  (unsigned)nprob);
-  if (ta == 0 && tb == 0) sgemm_batched_kernel<0, 0><<<grid, kGemmThreads, 0, st>>>(dev_descs);
-  else if (ta == 0 && tb == 1) sgemm_batched_kernel<0, 1><<<grid, kGemmThreads, 0, st>>>(dev_descs);
-  else if (ta == 1 && tb == 0) sgemm_batched_kernel<1, 0><<<grid, kGemmThreads, 0, st>>>(dev_descs);
-  else sgemm_batched_kernel<1, 1><<<grid, kGemmThreads, 0, st>>>(dev_descs);
-  return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
-}
 
 }  // namespace
 

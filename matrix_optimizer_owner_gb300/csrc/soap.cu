@@ -1,0 +1,859 @@
+// Owner SOAP: Adam in the eigenbasis of the Shampoo statistics, on the owner's whole matrices
+// (fp32).
+//
+// "MatrixFSDP: communication-free matrix optimizers under ZeRO-3 parameter sharding", §5.7:
+// with every 2D matrix whole on its owner, the owner can run SOAP (Adam in the Shampoo
+// eigenbasis) in place of Muon.  Per owned matrix G (rows x cols) and step t >= 1, the SOAP
+// update of Vyas et al. (2024) with the eigenbasis taken exactly at every step:
+//     L = bs L + (1 - bs) G G^T,   R = bs R + (1 - bs) G^T G
+//     Q_L, Q_R = eigenvectors of L, R (columns, descending eigenvalue)
+//     M = b1 M + (1 - b1) G;   G' = Q_L^T G Q_R;   M' = Q_L^T M Q_R
+//     V = b2 V + (1 - b2) G'^2                   (V in eigenbasis coordinates)
+//     N = Q_L [ (M' / (1 - b1^t)) / (sqrt(V / (1 - b2^t)) + eps) ] Q_R^T
+//     W = W (1 - lr wd) - lr N
+//
+// Eigenbases: cyclic two-sided block Jacobi, warm-started from the previous step's basis Q:
+// A = Q^T L Q (nearly diagonal once the statistics move slowly), Z = Q, then sweeps over all
+// pairs of 32-index blocks in round-robin order.  In one round every pair (P, Q) of blocks
+// forms a 64 x 64 subproblem [A_PP A_PQ; A_QP A_QQ], diagonalised exactly by a CTA in shared
+// memory (cyclic Jacobi with plane rotations, Golub & Van Loan §8.5), giving a 64 x 64
+// orthogonal J; a second launch applies all of the round's J to A (A <- J^T A J, block by
+// block) and to Z (Z <- Z J).  A sweep in which no subproblem rotated ends the solve for that
+// matrix.  The eigenvalues are then sorted (descending, ties by index) and Z's columns
+// scattered into Q in that order.  Plane rotations are skipped where the coupling is at
+// rounding level, |a_pq| <= tol max_i |a_ii| (tol = 1e-6, about 16u, by default): the rotations
+// of a block are 64-term fp32 sums, whose rounding leaves couplings of a few u ||L|| between
+// nearly equal eigenvalues, and eigenvectors are accurate to about tol ||L|| / gap.
+//
+// Every product (statistics, A = Q^T L Q, the rotations into and out of the eigenbasis) is
+// the batched fp32 SGEMM on the CUDA cores; the Jacobi rotations are fp32 FFMA as well: the
+// accumulated basis must stay orthogonal to fp32 precision over hundreds of rounds.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "mfsdp.h"
+#include "mfsdp_internal.h"
+
+namespace mfsdp {
+namespace {
+
+constexpr int kJB = 32;           // Jacobi block (indices)
+constexpr int kJP = 2 * kJB;      // a pair of blocks: one 64 x 64 subproblem
+constexpr int kJLd = kJP + 1;     // shared-memory pitch (conflict-free column access)
+constexpr int kJThreads = 256;
+constexpr int kSubSweeps = 12;    // sweeps of one 64 x 64 subproblem at most
+constexpr float kDefaultJacobiTol = 1e-6f;  // couplings below tol * max_i a_ii are not rotated
+
+struct SideDev {           // one statistics matrix of the Jacobi solve ("side")
+  float* stat;             // L or R, d x d (pitch d)
+  float* q;                // basis state, d x d (pitch d): previous basis in, sorted basis out
+  float* eig;              // eigenvalue state, d (descending)
+  float* a;                // dp x dp working matrix (pitch dp)
+  float* zt;               // dp x dp accumulated eigenvectors, one per ROW (pitch dp)
+  float* t;                // d x d scratch (pitch d)
+  float* j;                // dp / 64 rotations of the current round, 64 x 64 row-major each
+  int32_t* rot;            // per pair of the round: 1 unless its rotation is the identity
+  int32_t* rank;           // d: position of eigenvalue i in descending order
+  float* diag_max;         // max_i |a_ii| of the working matrix (refreshed every sweep)
+  float tol;               // relative rotation threshold
+  int32_t d, dp;
+};
+
+struct JacobiCtl {
+  int32_t converged, rotated, sweeps, pad_;
+};
+
+struct MatDev {            // one owned matrix in the flat owner buffers
+  int64_t offset, numel;
+};
+
+// Pair i of round r of the round-robin ("circle") schedule over n (even) indices: every index
+// once per round, every pair once in n - 1 rounds.
+__device__ __forceinline__ void circle_pair(int n, int r, int i, int& x, int& y) {
+  if (i == 0) {
+    x = n - 1;
+    y = r;
+  } else {
+    x = (r + i) % (n - 1);
+    y = (r - i + (n - 1)) % (n - 1);
+  }
+}
+
+// Global index of local index c (0..63) of pair-block p in round r.
+__device__ __forceinline__ int pair_index(int nb, int r, int p, int c) {
+  int b0, b1;
+  circle_pair(nb, r, p, b0, b1);
+  return (c < kJB ? b0 : b1) * kJB + (c & (kJB - 1));
+}
+
+// Z^T = Q^T padded with the identity, A's padding = 0, the solve's control words reset.
+__global__ void jacobi_setup_kernel(const SideDev* sides, JacobiCtl* ctl) {
+  const SideDev s = sides[blockIdx.y];
+  const int64_t n = (int64_t)s.dp * s.dp;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(e / s.dp), c = (int)(e % s.dp);
+    const bool in = r < s.d && c < s.d;
+    s.zt[e] = in ? s.q[(int64_t)c * s.d + r] : (r == c ? 1.f : 0.f);
+    if (!in) s.a[e] = 0.f;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) ctl[blockIdx.y] = JacobiCtl{0, 0, 0, 0};
+}
+
+// max_i |a_ii|: a lower bound of ||L||_2 that is tight once A is nearly diagonal, so it is
+// refreshed after every sweep (converged sides keep theirs).
+__global__ void __launch_bounds__(1024) diag_max_kernel(const SideDev* sides,
+                                                        const JacobiCtl* ctl) {
+  __shared__ float red[1024];
+  const SideDev s = sides[blockIdx.x];
+  if (ctl && ctl[blockIdx.x].converged) return;
+  float m = 0.f;
+  for (int i = threadIdx.x; i < s.d; i += blockDim.x)
+    m = fmaxf(m, fabsf(s.a[(int64_t)i * s.dp + i]));
+  red[threadIdx.x] = m;
+  __syncthreads();
+  for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + o]);
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *s.diag_max = red[0];
+}
+
+// out (64 x 64, registers: rows ty + 16 ii, columns tx + 16 jj) = op(X) Y with
+// op(X)[i][k] = X[k][i] (XT) or X[i][k].
+template <bool XT>
+__device__ __forceinline__ void mm64(const float (*X)[kJLd], const float (*Y)[kJLd], int ty,
+                                     int tx, float (&acc)[4][4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
+  for (int kk = 0; kk < kJP; ++kk) {
+    float xv[4], yv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) xv[i] = XT ? X[kk][ty + 16 * i] : X[ty + 16 * i][kk];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) yv[j] = Y[kk][tx + 16 * j];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], yv[j], acc[i][j]);
+  }
+}
+
+// One round's subproblems: CTA (pair, side) diagonalises the 64 x 64 block of its pair.
+__global__ void __launch_bounds__(kJThreads) jacobi_solve_kernel(const SideDev* sides,
+                                                                 JacobiCtl* ctl, int round) {
+  const int k = blockIdx.y;
+  const SideDev s = sides[k];
+  const int nb = s.dp / kJB;
+  if (ctl[k].converged || round >= nb - 1 || (int)blockIdx.x >= nb / 2) return;
+  __shared__ float S[kJP][kJLd];
+  __shared__ float V[kJP][kJLd];
+  __shared__ float cs[kJP / 2], sn[kJP / 2];
+  __shared__ int pp[kJP / 2], qq[kJP / 2];
+  __shared__ int sweep_rot, any_rot;
+  const int tid = threadIdx.x, pb = blockIdx.x;
+  for (int e = tid; e < kJP * kJP; e += kJThreads) {
+    const int r = e / kJP, c = e % kJP;
+    S[r][c] = s.a[(int64_t)pair_index(nb, round, pb, r) * s.dp + pair_index(nb, round, pb, c)];
+    V[r][c] = r == c ? 1.f : 0.f;
+  }
+  const float tol = s.tol * *s.diag_max;
+  if (tid == 0) any_rot = 0;
+  for (int sw = 0; sw < kSubSweeps; ++sw) {
+    __syncthreads();  // every thread has read the previous sweep's flag
+    if (tid == 0) sweep_rot = 0;
+    __syncthreads();
+    for (int r = 0; r < kJP - 1; ++r) {
+      if (tid < kJP / 2) {
+        int p, q;
+        circle_pair(kJP, r, tid, p, q);
+        if (p > q) { const int t = p; p = q; q = t; }
+        const float app = S[p][p], aqq = S[q][q], apq = S[p][q];
+        float c = 1.f, sv = 0.f;
+        if (fabsf(apq) > tol) {
+          // the rotation that zeroes a_pq (symmetric Schur decomposition of the 2 x 2 block)
+          const float tau = (aqq - app) / (2.f * apq);
+          const float t = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
+          c = 1.f / sqrtf(1.f + t * t);
+          sv = t * c;
+          sweep_rot = 1;
+        }
+        cs[tid] = c;
+        sn[tid] = sv;
+        pp[tid] = p;
+        qq[tid] = q;
+      }
+      __syncthreads();
+      // S <- J^T S J: the 2 x 2 blocks of (pair a rows, pair b columns) are disjoint
+      for (int e = tid; e < (kJP / 2) * (kJP / 2); e += kJThreads) {
+        const int a = e / (kJP / 2), b = e % (kJP / 2);
+        const float sa = sn[a], sb = sn[b];
+        if (sa == 0.f && sb == 0.f) continue;
+        const float ca = cs[a], cb = cs[b];
+        const int p = pp[a], p2 = qq[a], q = pp[b], q2 = qq[b];
+        const float x11 = S[p][q], x12 = S[p][q2], x21 = S[p2][q], x22 = S[p2][q2];
+        const float y11 = ca * x11 - sa * x21, y12 = ca * x12 - sa * x22;
+        const float y21 = sa * x11 + ca * x21, y22 = sa * x12 + ca * x22;
+        float z11 = cb * y11 - sb * y12, z12 = sb * y11 + cb * y12;
+        float z21 = cb * y21 - sb * y22, z22 = sb * y21 + cb * y22;
+        if (a == b) z12 = z21 = 0.f;  // the coupling this rotation removes
+        S[p][q] = z11;
+        S[p][q2] = z12;
+        S[p2][q] = z21;
+        S[p2][q2] = z22;
+      }
+      // V <- V J
+      for (int e = tid; e < kJP * (kJP / 2); e += kJThreads) {
+        const int i = e / (kJP / 2), a = e % (kJP / 2);
+        const float sa = sn[a];
+        if (sa == 0.f) continue;
+        const float ca = cs[a];
+        const int p = pp[a], p2 = qq[a];
+        const float v1 = V[i][p], v2 = V[i][p2];
+        V[i][p] = ca * v1 - sa * v2;
+        V[i][p2] = sa * v1 + ca * v2;
+      }
+      __syncthreads();
+    }
+    const bool more = sweep_rot != 0;
+    if (tid == 0 && more) any_rot = 1;
+    if (!more) break;
+  }
+  __syncthreads();
+  if (any_rot) {
+    // one polar (Newton–Schulz) step, V <- V (3I - V^T V) / 2: the rotations' rounding leaves
+    // V^T V = I + E with |E| ~ 1e-5 (a bias of ~1e-8 per rotation in c^2 + s^2), the step
+    // leaves O(E^2)
+    const int ty = tid >> 4, tx = tid & 15;
+    float acc[4][4];
+    mm64<true>(V, V, ty, tx, acc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = ty + 16 * i, c = tx + 16 * j;
+        S[r][c] = ((r == c ? 3.f : 0.f) - acc[i][j]) * 0.5f;
+      }
+    __syncthreads();
+    mm64<false>(V, S, ty, tx, acc);
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) V[ty + 16 * i][tx + 16 * j] = acc[i][j];
+    __syncthreads();
+  }
+  float* jout = s.j + (int64_t)pb * kJP * kJP;
+  for (int e = tid; e < kJP * kJP; e += kJThreads) jout[e] = V[e / kJP][e % kJP];
+  if (tid == 0) {
+    s.rot[pb] = any_rot;
+    if (any_rot) ctl[k].rotated = 1;
+  }
+}
+
+constexpr int kALd = kJP + 4;  // apply kernel's shared-memory pitch: rows 16-byte aligned
+constexpr size_t kApplySmem = 4 * sizeof(float) * kJP * kALd;
+
+// acc (rows 4ty + i, columns 4tx + j of a 64 x 64 tile) = P^T Q, i.e. sum_k P[k][.] Q[k][.]:
+// both operands read along rows with 128-bit loads.
+__device__ __forceinline__ void mm64_tn(const float (*P)[kALd], const float (*Q)[kALd], int ty,
+                                        int tx, float (&acc)[4][4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 8
+  for (int kk = 0; kk < kJP; ++kk) {
+    const float4 pv = *reinterpret_cast<const float4*>(&P[kk][4 * ty]);
+    const float4 qv = *reinterpret_cast<const float4*>(&Q[kk][4 * tx]);
+    const float pa[4] = {pv.x, pv.y, pv.z, pv.w}, qa[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(pa[i], qa[j], acc[i][j]);
+  }
+}
+
+// 64 x 64 block of a row-major global matrix (pitch ld) into shared memory: rows rowi(r),
+// columns coli(c), 4 consecutive columns at a time (they never straddle a 32-block).
+template <typename RowF, typename ColF>
+__device__ __forceinline__ void load_block(float (*dst)[kALd], const float* src, int64_t ld,
+                                           RowF rowi, ColF coli) {
+  for (int e = threadIdx.x; e < kJP * kJP / 4; e += kJThreads) {
+    const int r = e / (kJP / 4), c = (e % (kJP / 4)) * 4;
+    *reinterpret_cast<float4*>(&dst[r][c]) =
+        *reinterpret_cast<const float4*>(src + (int64_t)rowi(r) * ld + coli(c));
+  }
+}
+
+// The round's rotations applied.  Blocks [0, P(P+1)/2) of a side update A's block pair (p, q),
+// p <= q: Y = Jp^T (A_pq Jq), with A_pq Jq formed from the mirrored block (A is symmetric), Y
+// written to (p, q) and Y^T to (q, p).  Blocks [P(P+1)/2, P(P+1)/2 + P^2) update the rows I_p
+// of Z^T over one 64-column tile: Z^T <- Jp^T Z^T.
+__global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* sides,
+                                                                 const JacobiCtl* ctl,
+                                                                 int round) {
+  const int k = blockIdx.y;
+  const SideDev s = sides[k];
+  const int nb = s.dp / kJB, P = nb / 2;
+  if (ctl[k].converged || round >= nb - 1) return;
+  const int na = P * (P + 1) / 2;
+  const int bid = blockIdx.x;
+  if (bid >= na + P * P) return;
+  extern __shared__ __align__(16) float smem[];
+  float (*B0)[kALd] = reinterpret_cast<float (*)[kALd]>(smem);
+  float (*B1)[kALd] = B0 + kJP;
+  float (*B2)[kALd] = B1 + kJP;
+  float (*B3)[kALd] = B2 + kJP;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  float acc[4][4];
+  auto idx = [&](int pb, int c) { return pair_index(nb, round, pb, c); };
+  if (bid < na) {
+    int p = 0, rem = bid;
+    while (rem >= P - p) { rem -= P - p; ++p; }
+    const int q = p + rem;
+    if (!s.rot[p] && !s.rot[q]) return;
+    const float* jp = s.j + (int64_t)p * kJP * kJP;
+    const float* jq = s.j + (int64_t)q * kJP * kJP;
+    // B0[k][i] = A[I_q(k)][I_p(i)] = A_pq[i][k]
+    load_block(B0, s.a, s.dp, [&](int r) { return idx(q, r); }, [&](int c) { return idx(p, c); });
+    load_block(B1, jp, kJP, [](int r) { return r; }, [](int c) { return c; });
+    load_block(B2, jq, kJP, [](int r) { return r; }, [](int c) { return c; });
+    __syncthreads();
+    mm64_tn(B0, B2, ty, tx, acc);  // W = A_pq Jq
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(&B3[4 * ty + i][4 * tx]) =
+          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    __syncthreads();
+    mm64_tn(B1, B3, ty, tx, acc);  // Y = Jp^T W
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int gr = idx(p, 4 * ty + i), gc = idx(q, 4 * tx);
+      *reinterpret_cast<float4*>(s.a + (int64_t)gr * s.dp + gc) =
+          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    }
+    if (p != q) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int gr = idx(q, 4 * tx + j), gc = idx(p, 4 * ty);
+        *reinterpret_cast<float4*>(s.a + (int64_t)gr * s.dp + gc) =
+            make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
+      }
+    }
+  } else {
+    const int e0 = bid - na, t = e0 / P, p = e0 % P;
+    if (!s.rot[p]) return;
+    const float* jp = s.j + (int64_t)p * kJP * kJP;
+    // B0[k][j] = Z^T[I_p(k)][64 t + j]
+    load_block(B0, s.zt, s.dp, [&](int r) { return idx(p, r); },
+               [&](int c) { return t * kJP + c; });
+    load_block(B1, jp, kJP, [](int r) { return r; }, [](int c) { return c; });
+    __syncthreads();
+    mm64_tn(B1, B0, ty, tx, acc);  // Jp^T Z^T_p
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int gr = idx(p, 4 * ty + i);
+      *reinterpret_cast<float4*>(s.zt + (int64_t)gr * s.dp + t * kJP + 4 * tx) =
+          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    }
+  }
+}
+
+// End of a sweep: a side whose sweep rotated nothing is converged.
+__global__ void jacobi_sweep_end_kernel(JacobiCtl* ctl, int nsides) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= nsides) return;
+  JacobiCtl c = ctl[k];
+  if (!c.converged) {
+    ++c.sweeps;
+    if (!c.rotated) c.converged = 1;
+  }
+  c.rotated = 0;
+  ctl[k] = c;
+}
+
+// Rayleigh quotients of the final basis: lambda_i = z_i^T L z_i / z_i^T z_i, with T = Z^T L
+// (rows z_i^T L) formed by the SGEMM; one warp per eigenvector.  They replace diag(A), whose
+// entries carry the rounding of every rotation applied to A.
+__global__ void rayleigh_kernel(const SideDev* sides) {
+  const SideDev s = sides[blockIdx.y];
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int i = warp; i < s.d; i += nw) {
+    const float* z = s.zt + (int64_t)i * s.dp;
+    const float* t = s.t + (int64_t)i * s.d;
+    double num = 0.0, den = 0.0;
+    for (int c = lane; c < s.d; c += 32) {
+      num += (double)t[c] * z[c];
+      den += (double)z[c] * z[c];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      num += __shfl_xor_sync(0xffffffffu, num, o);
+      den += __shfl_xor_sync(0xffffffffu, den, o);
+    }
+    if (lane == 0) s.a[(int64_t)i * s.dp + i] = (float)(num / den);
+  }
+}
+
+// rank[i] = position of diag(A)_i in descending order (ties by index); eig[rank[i]] = diag_i.
+__global__ void eig_rank_kernel(const SideDev* sides) {
+  const SideDev s = sides[blockIdx.y];
+  __shared__ float lam[256];
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if ((int)(blockIdx.x * blockDim.x) >= s.d) return;  // block-uniform
+  const float li = i < s.d ? s.a[(int64_t)i * s.dp + i] : 0.f;
+  int rank = 0;
+  for (int j0 = 0; j0 < s.d; j0 += 256) {
+    __syncthreads();
+    const int jj = j0 + threadIdx.x;
+    lam[threadIdx.x] = jj < s.d ? s.a[(int64_t)jj * s.dp + jj] : 0.f;
+    __syncthreads();
+    const int cnt = min(256, s.d - j0);
+    for (int u = 0; u < cnt; ++u) {
+      const float lj = lam[u];
+      rank += (lj > li || (lj == li && j0 + u < i)) ? 1 : 0;
+    }
+  }
+  if (i < s.d) {
+    s.rank[i] = rank;
+    s.eig[rank] = li;
+  }
+}
+
+// Q[r][rank[i]] = Z^T[i][r], through 32 x 32 shared-memory tiles (reads along rows of Z^T,
+// writes along rows of Q).
+__global__ void eig_scatter_kernel(const SideDev* sides) {
+  const SideDev s = sides[blockIdx.z];
+  __shared__ float tile[32][33];
+  const int i0 = blockIdx.y * 32, r0 = blockIdx.x * 32;
+  if (i0 >= s.d || r0 >= s.d) return;  // block-uniform
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  for (int u = ty; u < 32; u += 8) {
+    const int i = i0 + u, r = r0 + tx;
+    tile[u][tx] = (i < s.d && r < s.d) ? s.zt[(int64_t)i * s.dp + r] : 0.f;
+  }
+  __syncthreads();
+  for (int u = ty; u < 32; u += 8) {
+    const int r = r0 + u, i = i0 + tx;
+    if (r < s.d && i < s.d) s.q[(int64_t)r * s.d + s.rank[i]] = tile[tx][u];
+  }
+}
+
+// Per-side solve report: sweeps used, negative when the sweep limit was reached first.
+__global__ void jacobi_info_kernel(const JacobiCtl* ctl, int nsides, int32_t* info) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k < nsides) info[k] = ctl[k].converged ? ctl[k].sweeps : -ctl[k].sweeps;
+}
+
+// M = b1 M + (1 - b1) G.
+__global__ void soap_moment_kernel(const MatDev* mats, float* m, const float* g, float beta1) {
+  const MatDev d = mats[blockIdx.y];
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < d.numel;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t o = d.offset + e;
+    m[o] = fmaf(beta1, m[o], (1.f - beta1) * g[o]);
+  }
+}
+
+// In the eigenbasis: V = b2 V + (1 - b2) G'^2; N' = (M' / bc1) / (sqrt(V / bc2) + eps) -> mrot.
+__global__ void soap_adam_kernel(const MatDev* mats, const float* grot, float* mrot, float* v,
+                                 float beta2, float bc1, float bc2, float eps) {
+  const MatDev d = mats[blockIdx.y];
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < d.numel;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t o = d.offset + e;
+    const float gr = grot[o];
+    const float vn = fmaf(beta2, v[o], (1.f - beta2) * gr * gr);
+    v[o] = vn;
+    mrot[o] = (mrot[o] / bc1) / (sqrtf(vn / bc2) + eps);
+  }
+}
+
+// W = W (1 - lr wd) - lr N.
+__global__ void soap_update_kernel(const MatDev* mats, float* w, const float* nbuf, float decay,
+                                   float lr) {
+  const MatDev d = mats[blockIdx.y];
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < d.numel;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t o = d.offset + e;
+    w[o] = fmaf(w[o], decay, -lr * nbuf[o]);
+  }
+}
+
+// L = R = 0, Q = I, eigenvalues 0 for every side; M = V = 0 over every matrix.
+__global__ void soap_init_side_kernel(const SideDev* sides) {
+  const SideDev s = sides[blockIdx.y];
+  const int64_t n = (int64_t)s.d * s.d;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    s.stat[e] = 0.f;
+    s.q[e] = (e / s.d) == (e % s.d) ? 1.f : 0.f;
+    if (e < s.d) s.eig[e] = 0.f;
+  }
+}
+
+__global__ void soap_zero_kernel(const MatDev* mats, float* m, float* v) {
+  const MatDev d = mats[blockIdx.y];
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < d.numel;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    m[d.offset + e] = 0.f;
+    v[d.offset + e] = 0.f;
+  }
+}
+
+}  // namespace
+}  // namespace mfsdp
+
+using namespace mfsdp;
+
+// ------------------------------------------------------------------------------------------
+// The owned-matrix set of the SOAP step and its workspace layout.
+// ------------------------------------------------------------------------------------------
+struct mfsdp_soap_set {
+  struct Mat {
+    int64_t rows, cols, offset;  // in the flat owner buffers (weights, gradient, M, V)
+    int64_t l_off, r_off;        // in the flat L / R (and Q_L / Q_R) state buffers
+    int64_t el_off, er_off;      // in the flat eigenvalue state buffers
+  };
+  struct Side {
+    int32_t d, dp;
+    size_t a, z, t, j, rot, rank;  // workspace byte offsets
+  };
+  std::vector<Mat> mats;
+  std::vector<Side> sides;         // L of every matrix, then R of every matrix
+  int64_t numel = 0, l_numel = 0, r_numel = 0, el_numel = 0, er_numel = 0;
+  int32_t dp_max = 0, d_max = 0;
+  size_t off_tmp_g = 0, off_tmp_m = 0, off_g_rot = 0, off_m_rot = 0;
+  size_t off_dmax = 0, off_ctl = 0, off_tables = 0, table_bytes = 0, ws_bytes = 0;
+};
+
+namespace {
+
+size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+constexpr int kGemmsPerMat = 14;  // stats 2, T 2, A 2, Rayleigh 2, into the basis 4, back 2
+
+// Device tables of one step, in upload order.
+struct SoapTables {
+  std::vector<SideDev> sides;
+  std::vector<MatDev> mats;
+  std::vector<GemmDesc> stats_l, stats_r, t, a, ray, rot1, rot2, back1, back2;
+};
+
+size_t soap_table_bytes(size_t n) {
+  return al256(sizeof(SideDev) * 2 * n) + al256(sizeof(MatDev) * n) +
+         al256(sizeof(GemmDesc) * kGemmsPerMat * n) + 12 * 256;
+}
+
+}  // namespace
+
+extern "C" int mfsdp_soap_set_create(const mfsdp_matrix* mats, int32_t n_mats,
+                                     mfsdp_soap_set** out) {
+  if (out == nullptr || n_mats < 0 || (n_mats > 0 && mats == nullptr)) return MFSDP_EINVAL;
+  auto* s = new mfsdp_soap_set();
+  int64_t lo = 0, ro = 0, elo = 0, ero = 0;
+  for (int32_t i = 0; i < n_mats; ++i) {
+    const mfsdp_matrix& m = mats[i];
+    if (m.rows <= 0 || m.cols <= 0 || m.offset < 0 || m.rows > (1 << 16) || m.cols > (1 << 16)) {
+      delete s;
+      return MFSDP_ESHAPE;
+    }
+    s->mats.push_back({m.rows, m.cols, m.offset, lo, ro, elo, ero});
+    lo += m.rows * m.rows;
+    ro += m.cols * m.cols;
+    elo += m.rows;
+    ero += m.cols;
+    s->numel = std::max(s->numel, m.offset + m.rows * m.cols);
+  }
+  s->l_numel = lo;
+  s->r_numel = ro;
+  s->el_numel = elo;
+  s->er_numel = ero;
+  size_t off = 0;
+  for (int side = 0; side < 2; ++side)
+    for (const auto& m : s->mats) {
+      mfsdp_soap_set::Side sd{};
+      sd.d = (int32_t)(side == 0 ? m.rows : m.cols);
+      sd.dp = (sd.d + 63) / 64 * 64;
+      const size_t dp2 = (size_t)sd.dp * sd.dp * sizeof(float);
+      sd.a = off; off = al256(off + dp2);
+      sd.z = off; off = al256(off + dp2);
+      sd.t = off; off = al256(off + (size_t)sd.d * sd.d * sizeof(float));
+      sd.j = off; off = al256(off + (size_t)(sd.dp / 64) * 64 * 64 * sizeof(float));
+      sd.rot = off; off = al256(off + (size_t)(sd.dp / 64) * sizeof(int32_t));
+      sd.rank = off; off = al256(off + (size_t)sd.d * sizeof(int32_t));
+      s->dp_max = std::max(s->dp_max, sd.dp);
+      s->d_max = std::max(s->d_max, sd.d);
+      s->sides.push_back(sd);
+    }
+  const size_t flat = (size_t)s->numel * sizeof(float);
+  s->off_tmp_g = off; off = al256(off + flat);
+  s->off_tmp_m = off; off = al256(off + flat);
+  s->off_g_rot = off; off = al256(off + flat);
+  s->off_m_rot = off; off = al256(off + flat);
+  const size_t n = std::max<size_t>(s->mats.size(), 1);
+  s->off_dmax = off; off = al256(off + sizeof(float) * 2 * n);
+  s->off_ctl = off; off = al256(off + sizeof(JacobiCtl) * 2 * n);
+  s->off_tables = off;
+  s->table_bytes = soap_table_bytes(n);
+  s->ws_bytes = al256(off + s->table_bytes);
+  *out = s;
+  return MFSDP_OK;
+}
+
+extern "C" int mfsdp_soap_set_destroy(mfsdp_soap_set* set) {
+  delete set;
+  return MFSDP_OK;
+}
+
+extern "C" int mfsdp_soap_set_sizes(const mfsdp_soap_set* set, size_t* workspace_bytes,
+                                    int64_t* l_numel, int64_t* r_numel, int64_t* eig_l_numel,
+                                    int64_t* eig_r_numel) {
+  if (set == nullptr) return MFSDP_EINVAL;
+  if (workspace_bytes) *workspace_bytes = set->ws_bytes;
+  if (l_numel) *l_numel = set->l_numel;
+  if (r_numel) *r_numel = set->r_numel;
+  if (eig_l_numel) *eig_l_numel = set->el_numel;
+  if (eig_r_numel) *eig_r_numel = set->er_numel;
+  return MFSDP_OK;
+}
+
+namespace {
+
+bool state_ok(const mfsdp_soap_state* st) {
+  return st && st->l && st->r && st->q_l && st->q_r && st->eig_l && st->eig_r && st->exp_avg &&
+         st->exp_avg_sq;
+}
+
+// Side and matrix tables for the given state and workspace.
+void soap_fill(const mfsdp_soap_set* set, const mfsdp_soap_state* st, uint8_t* ws, float tol,
+               SoapTables& tb) {
+  const int n = (int)set->mats.size();
+  float* dmax = reinterpret_cast<float*>(ws + set->off_dmax);
+  for (int k = 0; k < 2 * n; ++k) {
+    const auto& sd = set->sides[(size_t)k];
+    const auto& m = set->mats[(size_t)(k % n)];
+    const bool left = k < n;
+    SideDev d{};
+    d.stat = (left ? st->l : st->r) + (left ? m.l_off : m.r_off);
+    d.q = (left ? st->q_l : st->q_r) + (left ? m.l_off : m.r_off);
+    d.eig = (left ? st->eig_l : st->eig_r) + (left ? m.el_off : m.er_off);
+    d.a = reinterpret_cast<float*>(ws + sd.a);
+    d.zt = reinterpret_cast<float*>(ws + sd.z);
+    d.t = reinterpret_cast<float*>(ws + sd.t);
+    d.j = reinterpret_cast<float*>(ws + sd.j);
+    d.rot = reinterpret_cast<int32_t*>(ws + sd.rot);
+    d.rank = reinterpret_cast<int32_t*>(ws + sd.rank);
+    d.diag_max = dmax + k;
+    d.d = sd.d;
+    d.dp = sd.dp;
+    d.tol = tol;
+    tb.sides.push_back(d);
+  }
+  for (const auto& m : set->mats) tb.mats.push_back(MatDev{m.offset, m.rows * m.cols});
+}
+
+// Upload `tb`'s vectors back to back (256-byte aligned) and return their device addresses.
+template <typename T>
+const T* put(std::vector<uint8_t>& host, size_t& at, uint8_t* dev, const std::vector<T>& v) {
+  const size_t bytes = v.size() * sizeof(T);
+  if (bytes) std::memcpy(host.data() + at, v.data(), bytes);
+  const T* p = reinterpret_cast<const T*>(dev + at);
+  at += al256(std::max<size_t>(bytes, 1));
+  return p;
+}
+
+int gemm_max(const std::vector<GemmDesc>& v, int& mm, int& mn) {
+  mm = mn = 0;
+  for (const auto& g : v) {
+    mm = std::max(mm, g.m);
+    mn = std::max(mn, g.n);
+  }
+  return (int)v.size();
+}
+
+int run_gemms(const std::vector<GemmDesc>& v, const GemmDesc* dev, int ta, int tb,
+              cudaStream_t st) {
+  int mm, mn;
+  const int cnt = gemm_max(v, mm, mn);
+  return launch_gemm(dev, cnt, mm, mn, ta, tb, st);
+}
+
+}  // namespace
+
+extern "C" int mfsdp_soap_init_state(const mfsdp_soap_set* set, const mfsdp_soap_state* state,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (set == nullptr || !state_ok(state)) return MFSDP_EINVAL;
+  const int n = (int)set->mats.size();
+  if (n == 0) return MFSDP_OK;
+  if (workspace == nullptr || workspace_bytes < set->ws_bytes) return MFSDP_EWORKSPACE;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  SoapTables tb;
+  soap_fill(set, state, ws, kDefaultJacobiTol, tb);
+  std::vector<uint8_t> host(set->table_bytes);
+  size_t at = 0;
+  uint8_t* dev = ws + set->off_tables;
+  const SideDev* d_sides = put(host, at, dev, tb.sides);
+  const MatDev* d_mats = put(host, at, dev, tb.mats);
+  if (cudaMemcpyAsync(dev, host.data(), at, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MFSDP_ECUDA;
+  soap_init_side_kernel<<<dim3(64, 2 * (unsigned)n), 256, 0, st>>>(d_sides);
+  soap_zero_kernel<<<dim3(64, (unsigned)n), 256, 0, st>>>(d_mats, state->exp_avg,
+                                                          state->exp_avg_sq);
+  return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
+}
+
+extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, float* weights,
+                               const mfsdp_soap_state* state, int64_t t,
+                               const mfsdp_soap_hyper* h, int32_t* info, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (set == nullptr || grad == nullptr || weights == nullptr || !state_ok(state) ||
+      h == nullptr)
+    return MFSDP_EINVAL;
+  if (t < 1 || h->max_sweeps < 1 || h->max_sweeps > 100 || !(h->eps >= 0.f) ||
+      !(h->beta1 >= 0.f && h->beta1 < 1.f) || !(h->beta2 >= 0.f && h->beta2 < 1.f) ||
+      !(h->beta_stats >= 0.f && h->beta_stats < 1.f) ||
+      !(h->jacobi_tol >= 0.f && h->jacobi_tol < 1e-2f))
+    return MFSDP_EINVAL;
+  const int n = (int)set->mats.size();
+  if (n == 0) return MFSDP_OK;
+  if (workspace == nullptr || workspace_bytes < set->ws_bytes) return MFSDP_EWORKSPACE;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* tmp_g = reinterpret_cast<float*>(ws + set->off_tmp_g);
+  float* tmp_m = reinterpret_cast<float*>(ws + set->off_tmp_m);
+  float* g_rot = reinterpret_cast<float*>(ws + set->off_g_rot);
+  float* m_rot = reinterpret_cast<float*>(ws + set->off_m_rot);
+  JacobiCtl* ctl = reinterpret_cast<JacobiCtl*>(ws + set->off_ctl);
+
+  SoapTables tb;
+  soap_fill(set, state, ws, h->jacobi_tol > 0.f ? h->jacobi_tol : kDefaultJacobiTol, tb);
+  const float bs = h->beta_stats;
+  for (int i = 0; i < n; ++i) {
+    const auto& m = set->mats[(size_t)i];
+    const int rows = (int)m.rows, cols = (int)m.cols;
+    const int64_t o = m.offset;
+    float* l = state->l + m.l_off;
+    float* r = state->r + m.r_off;
+    float* ql = state->q_l + m.l_off;
+    float* qr = state->q_r + m.r_off;
+    float* tl = reinterpret_cast<float*>(ws + set->sides[(size_t)i].t);
+    float* tr = reinterpret_cast<float*>(ws + set->sides[(size_t)(n + i)].t);
+    float* al = reinterpret_cast<float*>(ws + set->sides[(size_t)i].a);
+    float* ar = reinterpret_cast<float*>(ws + set->sides[(size_t)(n + i)].a);
+    const int dpl = set->sides[(size_t)i].dp, dpr = set->sides[(size_t)(n + i)].dp;
+    // L = bs L + (1 - bs) G G^T;  R = bs R + (1 - bs) G^T G
+    tb.stats_l.push_back({grad + o, grad + o, l, nullptr, rows, rows, cols, cols, cols, rows,
+                          1.f - bs, bs});
+    tb.stats_r.push_back({grad + o, grad + o, r, nullptr, cols, cols, rows, cols, cols, cols,
+                          1.f - bs, bs});
+    // T = L Q;  A = Q^T T  (the statistics in the previous basis)
+    tb.t.push_back({l, ql, tl, nullptr, rows, rows, rows, rows, rows, rows, 1.f, 0.f});
+    tb.t.push_back({r, qr, tr, nullptr, cols, cols, cols, cols, cols, cols, 1.f, 0.f});
+    tb.a.push_back({ql, tl, al, nullptr, rows, rows, rows, rows, rows, dpl, 1.f, 0.f});
+    tb.a.push_back({qr, tr, ar, nullptr, cols, cols, cols, cols, cols, dpr, 1.f, 0.f});
+    // after the solve: T = Z^T L (rows z_i^T L) for the Rayleigh quotients
+    float* ztl = reinterpret_cast<float*>(ws + set->sides[(size_t)i].z);
+    float* ztr = reinterpret_cast<float*>(ws + set->sides[(size_t)(n + i)].z);
+    tb.ray.push_back({ztl, l, tl, nullptr, rows, rows, rows, dpl, rows, rows, 1.f, 0.f});
+    tb.ray.push_back({ztr, r, tr, nullptr, cols, cols, cols, dpr, cols, cols, 1.f, 0.f});
+    // into the new basis: Q_L^T G, Q_L^T M, then times Q_R
+    tb.rot1.push_back({ql, grad + o, tmp_g + o, nullptr, rows, cols, rows, rows, cols, cols,
+                       1.f, 0.f});
+    tb.rot1.push_back({ql, state->exp_avg + o, tmp_m + o, nullptr, rows, cols, rows, rows, cols,
+                       cols, 1.f, 0.f});
+    tb.rot2.push_back({tmp_g + o, qr, g_rot + o, nullptr, rows, cols, cols, cols, cols, cols,
+                       1.f, 0.f});
+    tb.rot2.push_back({tmp_m + o, qr, m_rot + o, nullptr, rows, cols, cols, cols, cols, cols,
+                       1.f, 0.f});
+    // back out: Q_L N', then times Q_R^T (N into g_rot)
+    tb.back1.push_back({ql, m_rot + o, tmp_g + o, nullptr, rows, cols, rows, rows, cols, cols,
+                        1.f, 0.f});
+    tb.back2.push_back({tmp_g + o, qr, g_rot + o, nullptr, rows, cols, cols, cols, cols, cols,
+                        1.f, 0.f});
+  }
+  std::vector<uint8_t> host(set->table_bytes);
+  size_t at = 0;
+  uint8_t* dev = ws + set->off_tables;
+  const SideDev* d_sides = put(host, at, dev, tb.sides);
+  const MatDev* d_mats = put(host, at, dev, tb.mats);
+  const GemmDesc* d_stats_l = put(host, at, dev, tb.stats_l);
+  const GemmDesc* d_stats_r = put(host, at, dev, tb.stats_r);
+  const GemmDesc* d_t = put(host, at, dev, tb.t);
+  const GemmDesc* d_a = put(host, at, dev, tb.a);
+  const GemmDesc* d_ray = put(host, at, dev, tb.ray);
+  const GemmDesc* d_rot1 = put(host, at, dev, tb.rot1);
+  const GemmDesc* d_rot2 = put(host, at, dev, tb.rot2);
+  const GemmDesc* d_back1 = put(host, at, dev, tb.back1);
+  const GemmDesc* d_back2 = put(host, at, dev, tb.back2);
+  if (at > set->table_bytes) return MFSDP_EWORKSPACE;
+  if (cudaMemcpyAsync(dev, host.data(), at, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MFSDP_ECUDA;
+  if (cudaFuncSetAttribute(jacobi_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kApplySmem) != cudaSuccess)
+    return MFSDP_ECUDA;
+
+  const unsigned ns = 2u * (unsigned)n;
+  const int sweep_blocks = (int)((ns + 255) / 256);
+  int e;
+  // statistics
+  if ((e = run_gemms(tb.stats_l, d_stats_l, 0, 1, st)) != MFSDP_OK) return e;
+  if ((e = run_gemms(tb.stats_r, d_stats_r, 1, 0, st)) != MFSDP_OK) return e;
+  // the statistics in the previous basis, A = Q^T L Q, and Z = Q
+  jacobi_setup_kernel<<<dim3(128, ns), 256, 0, st>>>(d_sides, ctl);
+  if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
+  if ((e = run_gemms(tb.t, d_t, 0, 0, st)) != MFSDP_OK) return e;
+  if ((e = run_gemms(tb.a, d_a, 1, 0, st)) != MFSDP_OK) return e;
+  diag_max_kernel<<<ns, 1024, 0, st>>>(d_sides, nullptr);
+  // block Jacobi sweeps; converged sides return at once
+  const int nb_max = set->dp_max / kJB, pairs_max = nb_max / 2;
+  const unsigned apply_blocks = (unsigned)(pairs_max * (pairs_max + 1) / 2 + pairs_max * pairs_max);
+  for (int sw = 0; sw < h->max_sweeps; ++sw) {
+    for (int r = 0; r < nb_max - 1; ++r) {
+      jacobi_solve_kernel<<<dim3((unsigned)pairs_max, ns), kJThreads, 0, st>>>(d_sides, ctl, r);
+      jacobi_apply_kernel<<<dim3(apply_blocks, ns), kJThreads, kApplySmem, st>>>(d_sides, ctl,
+                                                                                  r);
+    }
+    jacobi_sweep_end_kernel<<<sweep_blocks, 256, 0, st>>>(ctl, (int)ns);
+    diag_max_kernel<<<ns, 1024, 0, st>>>(d_sides, ctl);
+  }
+  if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
+  // eigenvalues (Rayleigh quotients) in descending order, the basis columns with them
+  if ((e = run_gemms(tb.ray, d_ray, 0, 0, st)) != MFSDP_OK) return e;
+  rayleigh_kernel<<<dim3(64, ns), 256, 0, st>>>(d_sides);
+  eig_rank_kernel<<<dim3((unsigned)((set->d_max + 255) / 256), ns), 256, 0, st>>>(d_sides);
+  {
+    const unsigned tiles = (unsigned)((set->d_max + 31) / 32);
+    eig_scatter_kernel<<<dim3(tiles, tiles, ns), 256, 0, st>>>(d_sides);
+  }
+  if (info) jacobi_info_kernel<<<sweep_blocks, 256, 0, st>>>(ctl, (int)ns, info);
+  // Adam in the eigenbasis
+  soap_moment_kernel<<<dim3(128, (unsigned)n), 256, 0, st>>>(d_mats, state->exp_avg, grad,
+                                                             h->beta1);
+  if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
+  if ((e = run_gemms(tb.rot1, d_rot1, 1, 0, st)) != MFSDP_OK) return e;
+  if ((e = run_gemms(tb.rot2, d_rot2, 0, 0, st)) != MFSDP_OK) return e;
+  const float bc1 = (float)(1.0 - std::pow((double)h->beta1, (double)t));
+  const float bc2 = (float)(1.0 - std::pow((double)h->beta2, (double)t));
+  soap_adam_kernel<<<dim3(128, (unsigned)n), 256, 0, st>>>(d_mats, g_rot, m_rot,
+                                                           state->exp_avg_sq, h->beta2, bc1,
+                                                           bc2, h->eps);
+  if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
+  if ((e = run_gemms(tb.back1, d_back1, 0, 0, st)) != MFSDP_OK) return e;
+  if ((e = run_gemms(tb.back2, d_back2, 0, 1, st)) != MFSDP_OK) return e;
+  const float decay = (float)(1.0 - (double)h->lr * (double)h->weight_decay);
+  soap_update_kernel<<<dim3(128, (unsigned)n), 256, 0, st>>>(d_mats, weights, g_rot, decay,
+                                                             h->lr);
+  return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
+}

@@ -251,6 +251,68 @@ class ShampooSet:
                                               _stream(stream)))
 
 
+# ------------------------------------------------------------------------------- SOAP
+class SoapSet:
+    """Handle of ``mfsdp_soap_set``: the owned matrices of an owner SOAP step.  ``state``
+    arguments are dicts of fp32 device tensors with the keys of ``SOAP_STATE_KEYS``."""
+
+    SOAP_STATE_KEYS = ("l", "r", "q_l", "q_r", "eig_l", "eig_r", "exp_avg", "exp_avg_sq")
+
+    def __init__(self, mats: Sequence[Tuple[int, int, int]]):
+        lib = _lib.load()
+        n = len(mats)
+        arr = (Matrix * max(n, 1))()
+        for i, (r, c, off) in enumerate(mats):
+            arr[i] = Matrix(r, c, off)
+        h = C.c_void_p()
+        _check("mfsdp_soap_set_create", lib.mfsdp_soap_set_create(arr, n, C.byref(h)))
+        self._h = h
+        ws, ln, rn, el, er = (C.c_size_t(0), C.c_int64(0), C.c_int64(0), C.c_int64(0),
+                              C.c_int64(0))
+        _check("mfsdp_soap_set_sizes",
+               lib.mfsdp_soap_set_sizes(h, C.byref(ws), C.byref(ln), C.byref(rn), C.byref(el),
+                                        C.byref(er)))
+        self.workspace_bytes = ws.value
+        self.l_numel, self.r_numel = ln.value, rn.value
+        self.eig_l_numel, self.eig_r_numel = el.value, er.value
+        self.n_mats = n
+
+    def close(self) -> None:
+        if self._h:
+            _lib.load().mfsdp_soap_set_destroy(self._h)
+            self._h = None
+
+    __del__ = close
+
+    def state_sizes(self, numel: int):
+        """numel of every state buffer for owner buffers of ``numel`` elements."""
+        return {"l": self.l_numel, "r": self.r_numel, "q_l": self.l_numel,
+                "q_r": self.r_numel, "eig_l": self.eig_l_numel, "eig_r": self.eig_r_numel,
+                "exp_avg": numel, "exp_avg_sq": numel}
+
+    @staticmethod
+    def _state(state) -> "_lib.SoapState":
+        return _lib.SoapState(*[_ptr(state[k]) for k in SoapSet.SOAP_STATE_KEYS])
+
+    def init_state(self, state, workspace, stream=None) -> None:
+        st = self._state(state)
+        _check("mfsdp_soap_init_state",
+               _lib.load().mfsdp_soap_init_state(self._h, C.byref(st), _ptr(workspace),
+                                                 workspace.numel(), _stream(stream)))
+
+    def step(self, grad, weights, state, t: int, *, lr: float, beta1: float, beta2: float,
+             beta_stats: float, eps: float, weight_decay: float, max_sweeps: int, workspace,
+             info=None, stream=None, jacobi_tol: float = 0.0) -> None:
+        st = self._state(state)
+        hy = _lib.SoapHyper(lr, beta1, beta2, beta_stats, eps, weight_decay, max_sweeps,
+                            jacobi_tol)
+        _check("mfsdp_soap_step",
+               _lib.load().mfsdp_soap_step(self._h, _ptr(grad), _ptr(weights), C.byref(st), t,
+                                           C.byref(hy), _ptr(info) if info is not None else None,
+                                           _ptr(workspace), workspace.numel(),
+                                           _stream(stream)))
+
+
 # ------------------------------------------------------------------------------- owner set
 class OwnerSet:
     """Handle of ``mfsdp_owner_set``: create, query workspace, bind, destroy."""

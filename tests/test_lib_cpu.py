@@ -271,3 +271,44 @@ def test_shampoo_validation_before_any_launch(lib):
     bad = (L.Matrix * 1)(L.Matrix(0, 3, 0))
     assert lib.mfsdp_shampoo_set_create(bad, 1, C.byref(h)) == -2
     assert lib.mfsdp_shampoo_set_create(None, 1, C.byref(h)) == -1
+
+
+def test_soap_validation_before_any_launch(lib):
+    from matrix_optimizer_owner_gb300 import _lib as L
+    mats = (L.Matrix * 2)(L.Matrix(4, 3, 0), L.Matrix(2, 70, 12))
+    h = C.c_void_p()
+    assert lib.mfsdp_soap_set_create(mats, 2, C.byref(h)) == 0
+    ws, ln, rn, el, er = (C.c_size_t(0), C.c_int64(0), C.c_int64(0), C.c_int64(0),
+                          C.c_int64(0))
+    assert lib.mfsdp_soap_set_sizes(h, C.byref(ws), C.byref(ln), C.byref(rn), C.byref(el),
+                                    C.byref(er)) == 0
+    assert (ln.value, rn.value, el.value, er.value) == (16 + 4, 9 + 4900, 4 + 2, 3 + 70)
+    # per side a padded working matrix and basis (dims rounded up to 64: 64, 64, 64, 128)
+    assert ws.value >= 4 * 2 * (3 * 64 * 64 + 128 * 128)
+    p = C.c_void_p(1 << 20)  # never dereferenced: every case fails first
+    st = L.SoapState(*([p.value] * 8))
+    good = L.SoapHyper(1e-3, 0.9, 0.95, 0.95, 1e-8, 0.01, 10, 0.0)
+    step = lib.mfsdp_soap_step
+    assert step(h, None, p, C.byref(st), 1, C.byref(good), None, p, ws.value, None) == -1
+    assert step(h, p, p, None, 1, C.byref(good), None, p, ws.value, None) == -1
+    assert step(h, p, p, C.byref(st), 0, C.byref(good), None, p, ws.value, None) == -1  # t
+    for field, bad in (("max_sweeps", 0), ("max_sweeps", 101), ("beta1", 1.0),
+                       ("beta2", -0.1), ("beta_stats", 1.0), ("eps", -1.0),
+                       ("jacobi_tol", -1e-6), ("jacobi_tol", 0.5)):
+        hb = L.SoapHyper(1e-3, 0.9, 0.95, 0.95, 1e-8, 0.01, 10, 0.0)
+        setattr(hb, field, bad)
+        assert step(h, p, p, C.byref(st), 1, C.byref(hb), None, p, ws.value, None) == -1, field
+    assert step(h, p, p, C.byref(st), 1, C.byref(good), None, None, ws.value, None) == -5
+    assert step(h, p, p, C.byref(st), 1, C.byref(good), None, p, ws.value - 1, None) == -5
+    missing = L.SoapState(*([p.value] * 7 + [None]))
+    assert step(h, p, p, C.byref(missing), 1, C.byref(good), None, p, ws.value, None) == -1
+    assert lib.mfsdp_soap_init_state(h, C.byref(missing), p, ws.value, None) == -1
+    assert lib.mfsdp_soap_init_state(h, C.byref(st), p, ws.value - 1, None) == -5
+    assert lib.mfsdp_soap_set_destroy(h) == 0
+    bad = (L.Matrix * 1)(L.Matrix(3, 0, 0))
+    assert lib.mfsdp_soap_set_create(bad, 1, C.byref(h)) == -2
+    assert lib.mfsdp_soap_set_create(None, 1, C.byref(h)) == -1
+    # the empty set is a no-op
+    assert lib.mfsdp_soap_set_create(None, 0, C.byref(h)) == 0
+    assert step(h, p, p, C.byref(st), 1, C.byref(good), None, None, 0, None) == 0
+    assert lib.mfsdp_soap_set_destroy(h) == 0
