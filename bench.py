@@ -455,6 +455,57 @@ def time_shampoo(device, reps=2, root_iters=30, precision=0):
     return s.elapsed_time(e) / reps, flops, tensor
 
 
+def time_soap(device, warm=3, reps=2, max_sweeps=20):
+    """Owner SOAP step on one GPT-2-small layer's matrices (2304x768, 768x768, 3072x768,
+    768x3072), eigenbases exact every step: `warm` untimed steps (the first starts the Jacobi
+    solves from Q = I, later ones from the previous basis), then `reps` timed steps on fresh
+    gradients.  Returns (ms per step, sweeps per side of the last step, SGEMM FLOPs per step,
+    Jacobi FLOPs of the last step counting every block of every rotating sweep)."""
+    from matrix_optimizer_owner_gb300 import mfsdp
+    shapes = [(2304, 768), (768, 768), (3072, 768), (768, 3072)]
+    offs, o = [], 0
+    for r, c in shapes:
+        offs.append(o)
+        o += r * c
+    sset = mfsdp.SoapSet([(r, c, off) for (r, c), off in zip(shapes, offs)])
+    ws = torch.empty(sset.workspace_bytes, dtype=torch.uint8, device=device)
+    st = {k: torch.empty(n, dtype=torch.float32, device=device)
+          for k, n in sset.state_sizes(o).items()}
+    sset.init_state(st, ws)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(11)
+    w = torch.randn(o, generator=gen, device=device) * 0.02
+    grads = [torch.randn(o, generator=gen, device=device) * 1e-3 for _ in range(warm + reps)]
+    info = torch.zeros(2 * len(shapes), dtype=torch.int32, device=device)
+    hyper = dict(lr=1e-3, beta1=0.9, beta2=0.95, beta_stats=0.95, eps=1e-8, weight_decay=1e-2,
+                 max_sweeps=max_sweeps)
+    for t in range(1, warm + 1):
+        sset.step(grads[t - 1], w, st, t, workspace=ws, info=info, **hyper)
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for t in range(warm + 1, warm + reps + 1):
+        sset.step(grads[t - 1], w, st, t, workspace=ws, info=info, **hyper)
+    e.record()
+    torch.cuda.synchronize()
+    sweeps = [int(x) for x in info.cpu().tolist()]
+    sides = [r for r, _ in shapes] + [c for _, c in shapes]
+    gemm = 0
+    for r, c in shapes:
+        gemm += 2 * r * r * c + 2 * r * c * c            # statistics
+        gemm += 2 * (2 * r ** 3 + 2 * c ** 3)            # Q^T L Q
+        gemm += 2 * r ** 3 + 2 * c ** 3                  # Rayleigh quotients
+        gemm += 2 * (2 * r * r * c + 2 * r * c * c)      # G', M' into the eigenbasis
+        gemm += 2 * r * r * c + 2 * r * c * c            # N back out
+    jac = 0
+    for d, sw in zip(sides, sweeps):
+        dp = (d + 63) // 64 * 64
+        jac += 8 * dp ** 3 * max(abs(sw) - 1, 0)         # the last sweep only checks
+    sset.close()
+    return s.elapsed_time(e) / reps, sweeps, gemm, jac
+
+
 def config_block(wb, cfg):
     wl = wb.wl
     return {"workload": wl.name, "config_index": cfg, "owner_rank": wb.rank,
@@ -573,6 +624,23 @@ def run_ours(args, rank, world, local_rank):
             "frac": round(texec / (tms * 1e-3) / 1e12 / float(peaks["bf16_tflops"]), 4),
             "frac_note": "executed tensor FLOPs over the whole step time (statistics, norms "
                          "and elementwise kernels included)"}
+    if not args.no_soap and rank == 0:
+        sms_, sweeps, gemm, jac = time_soap(dev)
+        sm_mhz = (clocks or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+        ffma_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+        ach = (gemm + jac) / (sms_ * 1e-3) / 1e12
+        line["soap"] = {
+            "kernel": "jacobi_apply_kernel + jacobi_solve_kernel (block Jacobi eigenbases, fp32) "
+                      "+ sgemm_batched_kernel",
+            "what": "one owner SOAP step of one GPT-2-small layer (2304x768, 768x768, 3072x768, "
+                    "768x3072), exact eigenbases every step, warm-started",
+            "ms": round(sms_, 3), "sweeps_per_side": sweeps, "bound": "alu",
+            "flops": gemm + jac, "achieved_tflops": round(ach, 2),
+            "peak_tflops": round(ffma_peak, 1), "peak_source": FFMA_PEAK_NOTE,
+            "frac": round(ach / ffma_peak, 4),
+            "flops_counted": "SGEMMs + 8 dp^3 per side per rotating sweep (every 64x64 block "
+                             "product of the rotations): an upper bound, since pairs whose "
+                             "rotation is the identity skip their blocks"}
     if not args.no_repack:
         rms, rbytes, nparams = time_repack(wb, 10, stream)
         line["repack"] = {
@@ -675,6 +743,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-repack", action="store_true",
                     help="skip the owner-shard repacking measurement")
+    ap.add_argument("--no-soap", action="store_true",
+                    help="skip the owner SOAP measurement (one GPT-2-small layer)")
     ap.add_argument("--no-shampoo", action="store_true",
                     help="skip the owner Shampoo measurement")
     ap.add_argument("--no-graph", action="store_true",

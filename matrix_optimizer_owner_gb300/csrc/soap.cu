@@ -16,7 +16,7 @@
 // A = Q^T L Q (nearly diagonal once the statistics move slowly), Z = Q, then sweeps over all
 // pairs of 32-index blocks in round-robin order.  In one round every pair (P, Q) of blocks
 // forms a 64 x 64 subproblem [A_PP A_PQ; A_QP A_QQ], diagonalised exactly by a CTA in shared
-// memory (cyclic Jacobi with plane rotations, Golub & Van Loan §8.5), giving a 64 x 64
+// memory (one cyclic sweep of plane rotations, Golub & Van Loan §8.5), giving a 64 x 64
 // orthogonal J; a second launch applies all of the round's J to A (A <- J^T A J, block by
 // block) and to Z (Z <- Z J).  A sweep in which no subproblem rotated ends the solve for that
 // matrix.  The eigenvalues are then sorted (descending, ties by index) and Z's columns
@@ -45,8 +45,13 @@ namespace {
 constexpr int kJB = 32;           // Jacobi block (indices)
 constexpr int kJP = 2 * kJB;      // a pair of blocks: one 64 x 64 subproblem
 constexpr int kJLd = kJP + 1;     // shared-memory pitch (conflict-free column access)
-constexpr int kJThreads = 256;
-constexpr int kSubSweeps = 12;    // sweeps of one 64 x 64 subproblem at most
+constexpr int kJThreads = 256;      // apply kernel (4 x 4 outputs per thread)
+constexpr int kSolveThreads = 512;  // solve kernel
+// Sweeps of one 64 x 64 subproblem per round.  One suffices: the subproblem need not be
+// diagonalised exactly for the outer iteration to converge (an emulation of the solve on
+// rank-deficient statistics takes the same number of outer sweeps with 1, 2, 3 or 12), and
+// near convergence a single sweep does diagonalise it.
+constexpr int kSubSweeps = 1;
 constexpr float kDefaultJacobiTol = 1e-6f;  // couplings below tol * max_i a_ii are not rotated
 
 struct SideDev {           // one statistics matrix of the Jacobi solve ("side")
@@ -89,6 +94,17 @@ __device__ __forceinline__ int pair_index(int nb, int r, int p, int c) {
   int b0, b1;
   circle_pair(nb, r, p, b0, b1);
   return (c < kJB ? b0 : b1) * kJB + (c & (kJB - 1));
+}
+
+// The side whose range [begin[k], begin[k + 1]) of a compact grid holds block `bid`.
+__device__ __forceinline__ int side_of(const int32_t* begin, int nsides, int bid) {
+  int lo = 0, hi = nsides - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (begin[mid] <= bid) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
 }
 
 // Z^T = Q^T padded with the identity, A's padding = 0, the solve's control words reset.
@@ -148,21 +164,38 @@ __device__ __forceinline__ void mm64(const float (*X)[kJLd], const float (*Y)[kJ
 }
 
 // One round's subproblems: CTA (pair, side) diagonalises the 64 x 64 block of its pair.
-__global__ void __launch_bounds__(kJThreads) jacobi_solve_kernel(const SideDev* sides,
-                                                                 JacobiCtl* ctl, int round) {
-  const int k = blockIdx.y;
+// Compact grid: blocks [begin[k], begin[k + 1]) are the dp_k / 64 pairs of side k.
+__global__ void __launch_bounds__(kSolveThreads) jacobi_solve_kernel(const SideDev* sides,
+                                                                     const int32_t* begin,
+                                                                     int nsides, JacobiCtl* ctl,
+                                                                     int round) {
+  const int k = side_of(begin, nsides, blockIdx.x);
   const SideDev s = sides[k];
   const int nb = s.dp / kJB;
-  if (ctl[k].converged || round >= nb - 1 || (int)blockIdx.x >= nb / 2) return;
+  if (ctl[k].converged || round >= nb - 1) return;
   __shared__ float S[kJP][kJLd];
   __shared__ float V[kJP][kJLd];
   __shared__ float cs[kJP / 2], sn[kJP / 2];
-  __shared__ int pp[kJP / 2], qq[kJP / 2];
   __shared__ int sweep_rot, any_rot;
-  const int tid = threadIdx.x, pb = blockIdx.x;
-  for (int e = tid; e < kJP * kJP; e += kJThreads) {
+  __shared__ int gi[kJP];
+  __shared__ uint16_t ptab[(kJP - 1) * (kJP / 2)];  // round r, pair a: p | q << 8, p < q
+  __shared__ uint16_t ttab[(kJP / 2) * (kJP / 2 + 1) / 2];  // upper-triangle block: a | b << 8
+  const int tid = threadIdx.x, pb = blockIdx.x - begin[k];
+  if (tid < kJP) gi[tid] = pair_index(nb, round, pb, tid);
+  for (int e = tid; e < (kJP - 1) * (kJP / 2); e += kSolveThreads) {
+    int p, q;
+    circle_pair(kJP, e / (kJP / 2), e % (kJP / 2), p, q);
+    ptab[e] = (uint16_t)(min(p, q) | (max(p, q) << 8));
+  }
+  for (int e = tid; e < (kJP / 2) * (kJP / 2 + 1) / 2; e += kSolveThreads) {
+    int a = 0, rem = e;  // e-th (a, b), a <= b, row by row
+    while (rem >= kJP / 2 - a) { rem -= kJP / 2 - a; ++a; }
+    ttab[e] = (uint16_t)(a | ((a + rem) << 8));
+  }
+  __syncthreads();
+  for (int e = tid; e < kJP * kJP; e += kSolveThreads) {
     const int r = e / kJP, c = e % kJP;
-    S[r][c] = s.a[(int64_t)pair_index(nb, round, pb, r) * s.dp + pair_index(nb, round, pb, c)];
+    S[r][c] = s.a[(int64_t)gi[r] * s.dp + gi[c]];
     V[r][c] = r == c ? 1.f : 0.f;
   }
   const float tol = s.tol * *s.diag_max;
@@ -173,9 +206,7 @@ __global__ void __launch_bounds__(kJThreads) jacobi_solve_kernel(const SideDev* 
     __syncthreads();
     for (int r = 0; r < kJP - 1; ++r) {
       if (tid < kJP / 2) {
-        int p, q;
-        circle_pair(kJP, r, tid, p, q);
-        if (p > q) { const int t = p; p = q; q = t; }
+        const int pq = ptab[r * (kJP / 2) + tid], p = pq & 0xff, q = pq >> 8;
         const float app = S[p][p], aqq = S[q][q], apq = S[p][q];
         float c = 1.f, sv = 0.f;
         if (fabsf(apq) > tol) {
@@ -188,38 +219,80 @@ __global__ void __launch_bounds__(kJThreads) jacobi_solve_kernel(const SideDev* 
         }
         cs[tid] = c;
         sn[tid] = sv;
-        pp[tid] = p;
-        qq[tid] = q;
       }
       __syncthreads();
-      // S <- J^T S J: the 2 x 2 blocks of (pair a rows, pair b columns) are disjoint
-      for (int e = tid; e < (kJP / 2) * (kJP / 2); e += kJThreads) {
-        const int a = e / (kJP / 2), b = e % (kJP / 2);
-        const float sa = sn[a], sb = sn[b];
+      // S <- J^T S J over the 2 x 2 blocks (pair a rows, pair b columns), a <= b, mirrored
+      // (S stays symmetric), and V <- V J: all disjoint.  A thread's blocks and V row-pairs
+      // are loaded first, then rotated, then stored, so that their latencies overlap.
+      const uint16_t* pr = ptab + r * (kJP / 2);
+      constexpr int kTri = (kJP / 2) * (kJP / 2 + 1) / 2;  // 528 blocks
+      constexpr int kTriPer = (kTri + kSolveThreads - 1) / kSolveThreads;
+      float sval[kTriPer][4], csv[kTriPer][4];
+      int sidx[kTriPer][4];
+      bool sact[kTriPer], sdiag[kTriPer];
+#pragma unroll
+      for (int u = 0; u < kTriPer; ++u) {
+        const int e = tid + u * kSolveThreads;
+        sact[u] = e < kTri;
+        if (!sact[u]) continue;
+        const int a = ttab[e] & 0xff, b = ttab[e] >> 8;
+        const int pa = pr[a], pb = pr[b];
+        const int p = pa & 0xff, p2 = pa >> 8, q = pb & 0xff, q2 = pb >> 8;
+        csv[u][0] = cs[a]; csv[u][1] = sn[a]; csv[u][2] = cs[b]; csv[u][3] = sn[b];
+        sdiag[u] = a == b;
+        sidx[u][0] = p * kJLd + q; sidx[u][1] = p * kJLd + q2;
+        sidx[u][2] = p2 * kJLd + q; sidx[u][3] = p2 * kJLd + q2;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) sval[u][w] = (&S[0][0])[sidx[u][w]];
+      }
+      float vv[4][2], vcs[4][2];
+      int vidx[4][2];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = tid + u * kSolveThreads, i = e % kJP, a = e / kJP;
+        const int pa = pr[a], p = pa & 0xff, p2 = pa >> 8;
+        vcs[u][0] = cs[a]; vcs[u][1] = sn[a];
+        vidx[u][0] = i * kJLd + p; vidx[u][1] = i * kJLd + p2;
+        vv[u][0] = (&V[0][0])[vidx[u][0]];
+        vv[u][1] = (&V[0][0])[vidx[u][1]];
+      }
+#pragma unroll
+      for (int u = 0; u < kTriPer; ++u) {
+        if (!sact[u]) continue;
+        const float ca = csv[u][0], sa = csv[u][1], cb = csv[u][2], sb = csv[u][3];
         if (sa == 0.f && sb == 0.f) continue;
-        const float ca = cs[a], cb = cs[b];
-        const int p = pp[a], p2 = qq[a], q = pp[b], q2 = qq[b];
-        const float x11 = S[p][q], x12 = S[p][q2], x21 = S[p2][q], x22 = S[p2][q2];
+        const float x11 = sval[u][0], x12 = sval[u][1], x21 = sval[u][2], x22 = sval[u][3];
         const float y11 = ca * x11 - sa * x21, y12 = ca * x12 - sa * x22;
         const float y21 = sa * x11 + ca * x21, y22 = sa * x12 + ca * x22;
         float z11 = cb * y11 - sb * y12, z12 = sb * y11 + cb * y12;
         float z21 = cb * y21 - sb * y22, z22 = sb * y21 + cb * y22;
-        if (a == b) z12 = z21 = 0.f;  // the coupling this rotation removes
-        S[p][q] = z11;
-        S[p][q2] = z12;
-        S[p2][q] = z21;
-        S[p2][q2] = z22;
+        float* S0 = &S[0][0];
+        if (sdiag[u]) {
+          z12 = z21 = 0.f;  // the coupling this rotation removes
+          S0[sidx[u][0]] = z11;
+          S0[sidx[u][1]] = 0.f;
+          S0[sidx[u][2]] = 0.f;
+          S0[sidx[u][3]] = z22;
+        } else {
+          // block (a, b) and its mirror (b, a): S[q][p] = z11, S[q2][p] = z12, ...
+          const int p = sidx[u][0] / kJLd, p2 = sidx[u][2] / kJLd;
+          const int q = sidx[u][0] % kJLd, q2 = sidx[u][1] % kJLd;
+          S0[sidx[u][0]] = z11;
+          S0[sidx[u][1]] = z12;
+          S0[sidx[u][2]] = z21;
+          S0[sidx[u][3]] = z22;
+          S0[q * kJLd + p] = z11;
+          S0[q2 * kJLd + p] = z12;
+          S0[q * kJLd + p2] = z21;
+          S0[q2 * kJLd + p2] = z22;
+        }
       }
-      // V <- V J
-      for (int e = tid; e < kJP * (kJP / 2); e += kJThreads) {
-        const int i = e / (kJP / 2), a = e % (kJP / 2);
-        const float sa = sn[a];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float ca = vcs[u][0], sa = vcs[u][1];
         if (sa == 0.f) continue;
-        const float ca = cs[a];
-        const int p = pp[a], p2 = qq[a];
-        const float v1 = V[i][p], v2 = V[i][p2];
-        V[i][p] = ca * v1 - sa * v2;
-        V[i][p2] = sa * v1 + ca * v2;
+        (&V[0][0])[vidx[u][0]] = ca * vv[u][0] - sa * vv[u][1];
+        (&V[0][0])[vidx[u][1]] = sa * vv[u][0] + ca * vv[u][1];
       }
       __syncthreads();
     }
@@ -232,27 +305,33 @@ __global__ void __launch_bounds__(kJThreads) jacobi_solve_kernel(const SideDev* 
     // one polar (Newton–Schulz) step, V <- V (3I - V^T V) / 2: the rotations' rounding leaves
     // V^T V = I + E with |E| ~ 1e-5 (a bias of ~1e-8 per rotation in c^2 + s^2), the step
     // leaves O(E^2)
-    const int ty = tid >> 4, tx = tid & 15;
+    // (the first 256 threads compute, 4 x 4 outputs each)
+    const int ty = (tid >> 4) & 15, tx = tid & 15;
+    const bool worker = tid < 256;
     float acc[4][4];
-    mm64<true>(V, V, ty, tx, acc);
+    if (worker) {
+      mm64<true>(V, V, ty, tx, acc);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int r = ty + 16 * i, c = tx + 16 * j;
-        S[r][c] = ((r == c ? 3.f : 0.f) - acc[i][j]) * 0.5f;
-      }
+        for (int j = 0; j < 4; ++j) {
+          const int r = ty + 16 * i, c = tx + 16 * j;
+          S[r][c] = ((r == c ? 3.f : 0.f) - acc[i][j]) * 0.5f;
+        }
+    }
     __syncthreads();
-    mm64<false>(V, S, ty, tx, acc);
+    if (worker) mm64<false>(V, S, ty, tx, acc);
     __syncthreads();
+    if (worker) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) V[ty + 16 * i][tx + 16 * j] = acc[i][j];
+        for (int j = 0; j < 4; ++j) V[ty + 16 * i][tx + 16 * j] = acc[i][j];
+    }
     __syncthreads();
   }
   float* jout = s.j + (int64_t)pb * kJP * kJP;
-  for (int e = tid; e < kJP * kJP; e += kJThreads) jout[e] = V[e / kJP][e % kJP];
+  for (int e = tid; e < kJP * kJP; e += kSolveThreads) jout[e] = V[e / kJP][e % kJP];
   if (tid == 0) {
     s.rot[pb] = any_rot;
     if (any_rot) ctl[k].rotated = 1;
@@ -260,7 +339,7 @@ __global__ void __launch_bounds__(kJThreads) jacobi_solve_kernel(const SideDev* 
 }
 
 constexpr int kALd = kJP + 4;  // apply kernel's shared-memory pitch: rows 16-byte aligned
-constexpr size_t kApplySmem = 4 * sizeof(float) * kJP * kALd;
+constexpr size_t kApplySmem = 3 * sizeof(float) * kJP * kALd;  // 4 CTAs per SM
 
 // acc (rows 4ty + i, columns 4tx + j of a 64 x 64 tile) = P^T Q, i.e. sum_k P[k][.] Q[k][.]:
 // both operands read along rows with 128-bit loads.
@@ -294,33 +373,38 @@ __device__ __forceinline__ void load_block(float (*dst)[kALd], const float* src,
   }
 }
 
-// The round's rotations applied.  Blocks [0, P(P+1)/2) of a side update A's block pair (p, q),
-// p <= q: Y = Jp^T (A_pq Jq), with A_pq Jq formed from the mirrored block (A is symmetric), Y
-// written to (p, q) and Y^T to (q, p).  Blocks [P(P+1)/2, P(P+1)/2 + P^2) update the rows I_p
-// of Z^T over one 64-column tile: Z^T <- Jp^T Z^T.
+// The round's rotations applied; compact grid, blocks [begin[k], begin[k + 1]) for side k.
+// Its blocks [0, P(P+1)/2) update A's block pair (p, q), p <= q: Y = Jp^T (A_pq Jq), with
+// A_pq Jq formed from the mirrored block (A is symmetric), Y written to (p, q) and Y^T to
+// (q, p).  Blocks [P(P+1)/2, P(P+1)/2 + P^2) update the rows I_p of Z^T over one 64-column
+// tile: Z^T <- Jp^T Z^T.
 __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* sides,
+                                                                 const int32_t* begin,
+                                                                 int nsides,
                                                                  const JacobiCtl* ctl,
                                                                  int round) {
-  const int k = blockIdx.y;
+  const int k = side_of(begin, nsides, blockIdx.x);
   const SideDev s = sides[k];
   const int nb = s.dp / kJB, P = nb / 2;
   if (ctl[k].converged || round >= nb - 1) return;
   const int na = P * (P + 1) / 2;
-  const int bid = blockIdx.x;
-  if (bid >= na + P * P) return;
+  const int bid = blockIdx.x - begin[k];
   extern __shared__ __align__(16) float smem[];
   float (*B0)[kALd] = reinterpret_cast<float (*)[kALd]>(smem);
   float (*B1)[kALd] = B0 + kJP;
   float (*B2)[kALd] = B1 + kJP;
-  float (*B3)[kALd] = B2 + kJP;
+  __shared__ int ip[kJP], iq[kJP];  // global indices of the two pair-blocks
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   float acc[4][4];
-  auto idx = [&](int pb, int c) { return pair_index(nb, round, pb, c); };
   if (bid < na) {
     int p = 0, rem = bid;
     while (rem >= P - p) { rem -= P - p; ++p; }
     const int q = p + rem;
     if (!s.rot[p] && !s.rot[q]) return;
+    if (tid < kJP) ip[tid] = pair_index(nb, round, p, tid);
+    else if (tid < 2 * kJP) iq[tid - kJP] = pair_index(nb, round, q, tid - kJP);
+    __syncthreads();
+    auto idx = [&](int pb, int c) { return pb == p ? ip[c] : iq[c]; };
     const float* jp = s.j + (int64_t)p * kJP * kJP;
     const float* jq = s.j + (int64_t)q * kJP * kJP;
     // B0[k][i] = A[I_q(k)][I_p(i)] = A_pq[i][k]
@@ -329,12 +413,13 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
     load_block(B2, jq, kJP, [](int r) { return r; }, [](int c) { return c; });
     __syncthreads();
     mm64_tn(B0, B2, ty, tx, acc);  // W = A_pq Jq
+    __syncthreads();               // B0 is free: W goes there
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      *reinterpret_cast<float4*>(&B3[4 * ty + i][4 * tx]) =
+      *reinterpret_cast<float4*>(&B0[4 * ty + i][4 * tx]) =
           make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
     __syncthreads();
-    mm64_tn(B1, B3, ty, tx, acc);  // Y = Jp^T W
+    mm64_tn(B1, B0, ty, tx, acc);  // Y = Jp^T W
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int gr = idx(p, 4 * ty + i), gc = idx(q, 4 * tx);
@@ -352,6 +437,9 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
   } else {
     const int e0 = bid - na, t = e0 / P, p = e0 % P;
     if (!s.rot[p]) return;
+    if (tid < kJP) ip[tid] = pair_index(nb, round, p, tid);
+    __syncthreads();
+    auto idx = [&](int, int c) { return ip[c]; };
     const float* jp = s.j + (int64_t)p * kJP * kJP;
     // B0[k][j] = Z^T[I_p(k)][64 t + j]
     load_block(B0, s.zt, s.dp, [&](int r) { return idx(p, r); },
@@ -391,11 +479,12 @@ __global__ void rayleigh_kernel(const SideDev* sides) {
   for (int i = warp; i < s.d; i += nw) {
     const float* z = s.zt + (int64_t)i * s.dp;
     const float* t = s.t + (int64_t)i * s.d;
-    double num = 0.0, den = 0.0;
+    float nf = 0.f, df = 0.f;  // per lane: d / 32 terms in fp32, then the lanes in fp64
     for (int c = lane; c < s.d; c += 32) {
-      num += (double)t[c] * z[c];
-      den += (double)z[c] * z[c];
+      nf = fmaf(t[c], z[c], nf);
+      df = fmaf(z[c], z[c], df);
     }
+    double num = nf, den = df;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       num += __shfl_xor_sync(0xffffffffu, num, o);
@@ -546,13 +635,15 @@ constexpr int kGemmsPerMat = 14;  // stats 2, T 2, A 2, Rayleigh 2, into the bas
 // Device tables of one step, in upload order.
 struct SoapTables {
   std::vector<SideDev> sides;
+  std::vector<int32_t> solve_begin, apply_begin;  // compact-grid prefix sums, 2n + 1 entries
   std::vector<MatDev> mats;
   std::vector<GemmDesc> stats_l, stats_r, t, a, ray, rot1, rot2, back1, back2;
 };
 
 size_t soap_table_bytes(size_t n) {
   return al256(sizeof(SideDev) * 2 * n) + al256(sizeof(MatDev) * n) +
-         al256(sizeof(GemmDesc) * kGemmsPerMat * n) + 12 * 256;
+         2 * al256(sizeof(int32_t) * (2 * n + 1)) + al256(sizeof(GemmDesc) * kGemmsPerMat * n) +
+         16 * 256;
 }
 
 }  // namespace
@@ -661,6 +752,16 @@ void soap_fill(const mfsdp_soap_set* set, const mfsdp_soap_state* st, uint8_t* w
     tb.sides.push_back(d);
   }
   for (const auto& m : set->mats) tb.mats.push_back(MatDev{m.offset, m.rows * m.cols});
+  int32_t sb = 0, ab = 0;
+  for (int k = 0; k < 2 * n; ++k) {
+    const int32_t P = set->sides[(size_t)k].dp / 64;
+    tb.solve_begin.push_back(sb);
+    tb.apply_begin.push_back(ab);
+    sb += P;
+    ab += P * (P + 1) / 2 + P * P;
+  }
+  tb.solve_begin.push_back(sb);
+  tb.apply_begin.push_back(ab);
 }
 
 // Upload `tb`'s vectors back to back (256-byte aligned) and return their device addresses.
@@ -788,6 +889,8 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
   uint8_t* dev = ws + set->off_tables;
   const SideDev* d_sides = put(host, at, dev, tb.sides);
   const MatDev* d_mats = put(host, at, dev, tb.mats);
+  const int32_t* d_solve_begin = put(host, at, dev, tb.solve_begin);
+  const int32_t* d_apply_begin = put(host, at, dev, tb.apply_begin);
   const GemmDesc* d_stats_l = put(host, at, dev, tb.stats_l);
   const GemmDesc* d_stats_r = put(host, at, dev, tb.stats_r);
   const GemmDesc* d_t = put(host, at, dev, tb.t);
@@ -817,13 +920,15 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
   if ((e = run_gemms(tb.a, d_a, 1, 0, st)) != MFSDP_OK) return e;
   diag_max_kernel<<<ns, 1024, 0, st>>>(d_sides, nullptr);
   // block Jacobi sweeps; converged sides return at once
-  const int nb_max = set->dp_max / kJB, pairs_max = nb_max / 2;
-  const unsigned apply_blocks = (unsigned)(pairs_max * (pairs_max + 1) / 2 + pairs_max * pairs_max);
+  const int nb_max = set->dp_max / kJB;
+  const unsigned solve_blocks = (unsigned)tb.solve_begin.back();
+  const unsigned apply_blocks = (unsigned)tb.apply_begin.back();
   for (int sw = 0; sw < h->max_sweeps; ++sw) {
     for (int r = 0; r < nb_max - 1; ++r) {
-      jacobi_solve_kernel<<<dim3((unsigned)pairs_max, ns), kJThreads, 0, st>>>(d_sides, ctl, r);
-      jacobi_apply_kernel<<<dim3(apply_blocks, ns), kJThreads, kApplySmem, st>>>(d_sides, ctl,
-                                                                                  r);
+      jacobi_solve_kernel<<<solve_blocks, kSolveThreads, 0, st>>>(d_sides, d_solve_begin,
+                                                                  (int)ns, ctl, r);
+      jacobi_apply_kernel<<<apply_blocks, kJThreads, kApplySmem, st>>>(d_sides, d_apply_begin,
+                                                                      (int)ns, ctl, r);
     }
     jacobi_sweep_end_kernel<<<sweep_blocks, 256, 0, st>>>(ctl, (int)ns);
     diag_max_kernel<<<ns, 1024, 0, st>>>(d_sides, ctl);
