@@ -286,7 +286,10 @@ int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* grad, float* l
  * The eigenbases come from cyclic block Jacobi on Q^T L Q, started from the basis the state
  * holds (the previous step's), until a sweep rotates nothing or `max_sweeps` sweeps ran;
  * every product is fp32 on the CUDA cores.  Eigenvectors are fixed up to sign, and N does not
- * depend on the signs.
+ * depend on the signs.  The solves run on `stream` and on one internal stream of the set,
+ * forked from and joined back into `stream` with events (created at the first step, on the
+ * device current then), so a capture of `stream` takes both; a set serves one host thread at
+ * a time.
  *
  * State (DEVICE, fp32, caller-owned, updated in place): `l`, `q_l` hold every matrix's L and
  * Q_L (rows^2 each) back to back in table order, `r`, `q_r` its R and Q_R (cols^2); `eig_l`

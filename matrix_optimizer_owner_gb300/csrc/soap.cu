@@ -66,6 +66,7 @@ struct SideDev {           // one statistics matrix of the Jacobi solve ("side")
   int32_t* rank;           // d: position of eigenvalue i in descending order
   float* diag_max;         // max_i |a_ii| of the working matrix (refreshed every sweep)
   float tol;               // relative rotation threshold
+  int32_t orig;            // index of the side in table order (L of every matrix, then R)
   int32_t d, dp;
 };
 
@@ -539,9 +540,10 @@ __global__ void eig_scatter_kernel(const SideDev* sides) {
 }
 
 // Per-side solve report: sweeps used, negative when the sweep limit was reached first.
-__global__ void jacobi_info_kernel(const JacobiCtl* ctl, int nsides, int32_t* info) {
+__global__ void jacobi_info_kernel(const SideDev* sides, const JacobiCtl* ctl, int nsides,
+                                   int32_t* info) {
   const int k = blockIdx.x * blockDim.x + threadIdx.x;
-  if (k < nsides) info[k] = ctl[k].converged ? ctl[k].sweeps : -ctl[k].sweeps;
+  if (k < nsides) info[sides[k].orig] = ctl[k].converged ? ctl[k].sweeps : -ctl[k].sweeps;
 }
 
 // M = b1 M + (1 - b1) G.
@@ -624,6 +626,19 @@ struct mfsdp_soap_set {
   int32_t dp_max = 0, d_max = 0;
   size_t off_tmp_g = 0, off_tmp_m = 0, off_g_rot = 0, off_m_rot = 0;
   size_t off_dmax = 0, off_ctl = 0, off_tables = 0, table_bytes = 0, ws_bytes = 0;
+  // The Jacobi solves run as two independent groups of sides, the second on an internal
+  // stream, so that one group's (latency-bound) subproblem launches overlap the other's
+  // (throughput-bound) rotation launches.  `order` lists the sides group by group.
+  std::vector<int32_t> order;
+  int32_t split = 0;             // sides in group 0
+  int32_t nb_max_group[2] = {0, 0};
+  mutable cudaStream_t aux = nullptr;
+  mutable cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  ~mfsdp_soap_set() {
+    if (aux) cudaStreamDestroy(aux);
+    if (ev_fork) cudaEventDestroy(ev_fork);
+    if (ev_join) cudaEventDestroy(ev_join);
+  }
 };
 
 namespace {
@@ -635,15 +650,15 @@ constexpr int kGemmsPerMat = 14;  // stats 2, T 2, A 2, Rayleigh 2, into the bas
 // Device tables of one step, in upload order.
 struct SoapTables {
   std::vector<SideDev> sides;
-  std::vector<int32_t> solve_begin, apply_begin;  // compact-grid prefix sums, 2n + 1 entries
+  std::vector<int32_t> solve_begin[2], apply_begin[2];  // compact grids of the two groups
   std::vector<MatDev> mats;
   std::vector<GemmDesc> stats_l, stats_r, t, a, ray, rot1, rot2, back1, back2;
 };
 
 size_t soap_table_bytes(size_t n) {
   return al256(sizeof(SideDev) * 2 * n) + al256(sizeof(MatDev) * n) +
-         2 * al256(sizeof(int32_t) * (2 * n + 1)) + al256(sizeof(GemmDesc) * kGemmsPerMat * n) +
-         16 * 256;
+         4 * al256(sizeof(int32_t) * (2 * n + 1)) + al256(sizeof(GemmDesc) * kGemmsPerMat * n) +
+         20 * 256;
 }
 
 }  // namespace
@@ -687,6 +702,30 @@ extern "C" int mfsdp_soap_set_create(const mfsdp_matrix* mats, int32_t n_mats,
       s->d_max = std::max(s->d_max, sd.d);
       s->sides.push_back(sd);
     }
+  {
+    // two groups balanced by Jacobi work (~dp^3), largest first (the two largest sides land
+    // in different groups)
+    std::vector<int32_t> idx(s->sides.size());
+    for (size_t k = 0; k < idx.size(); ++k) idx[k] = (int32_t)k;
+    std::stable_sort(idx.begin(), idx.end(), [&](int32_t x, int32_t y) {
+      return s->sides[(size_t)x].dp > s->sides[(size_t)y].dp;
+    });
+    double load[2] = {0.0, 0.0};
+    std::vector<int> grp(s->sides.size(), 0);
+    for (int32_t k : idx) {
+      const int g = load[1] < load[0] ? 1 : 0;
+      const double dp = s->sides[(size_t)k].dp;
+      load[g] += dp * dp * dp;
+      grp[(size_t)k] = g;
+    }
+    for (int g = 0; g < 2; ++g)
+      for (size_t k = 0; k < grp.size(); ++k)
+        if (grp[k] == g) {
+          s->order.push_back((int32_t)k);
+          s->nb_max_group[g] = std::max(s->nb_max_group[g], s->sides[k].dp / kJB);
+        }
+    s->split = (int32_t)std::count(grp.begin(), grp.end(), 0);
+  }
   const size_t flat = (size_t)s->numel * sizeof(float);
   s->off_tmp_g = off; off = al256(off + flat);
   s->off_tmp_m = off; off = al256(off + flat);
@@ -731,11 +770,13 @@ void soap_fill(const mfsdp_soap_set* set, const mfsdp_soap_state* st, uint8_t* w
                SoapTables& tb) {
   const int n = (int)set->mats.size();
   float* dmax = reinterpret_cast<float*>(ws + set->off_dmax);
-  for (int k = 0; k < 2 * n; ++k) {
+  for (int pos = 0; pos < 2 * n; ++pos) {
+    const int k = set->order[(size_t)pos];
     const auto& sd = set->sides[(size_t)k];
     const auto& m = set->mats[(size_t)(k % n)];
     const bool left = k < n;
     SideDev d{};
+    d.orig = k;
     d.stat = (left ? st->l : st->r) + (left ? m.l_off : m.r_off);
     d.q = (left ? st->q_l : st->q_r) + (left ? m.l_off : m.r_off);
     d.eig = (left ? st->eig_l : st->eig_r) + (left ? m.el_off : m.er_off);
@@ -752,16 +793,19 @@ void soap_fill(const mfsdp_soap_set* set, const mfsdp_soap_state* st, uint8_t* w
     tb.sides.push_back(d);
   }
   for (const auto& m : set->mats) tb.mats.push_back(MatDev{m.offset, m.rows * m.cols});
-  int32_t sb = 0, ab = 0;
-  for (int k = 0; k < 2 * n; ++k) {
-    const int32_t P = set->sides[(size_t)k].dp / 64;
-    tb.solve_begin.push_back(sb);
-    tb.apply_begin.push_back(ab);
-    sb += P;
-    ab += P * (P + 1) / 2 + P * P;
+  for (int g = 0; g < 2; ++g) {
+    const int lo = g ? set->split : 0, hi = g ? 2 * n : set->split;
+    int32_t sb = 0, ab = 0;
+    for (int pos = lo; pos < hi; ++pos) {
+      const int32_t P = set->sides[(size_t)set->order[(size_t)pos]].dp / 64;
+      tb.solve_begin[g].push_back(sb);
+      tb.apply_begin[g].push_back(ab);
+      sb += P;
+      ab += P * (P + 1) / 2 + P * P;
+    }
+    tb.solve_begin[g].push_back(sb);
+    tb.apply_begin[g].push_back(ab);
   }
-  tb.solve_begin.push_back(sb);
-  tb.apply_begin.push_back(ab);
 }
 
 // Upload `tb`'s vectors back to back (256-byte aligned) and return their device addresses.
@@ -889,8 +933,10 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
   uint8_t* dev = ws + set->off_tables;
   const SideDev* d_sides = put(host, at, dev, tb.sides);
   const MatDev* d_mats = put(host, at, dev, tb.mats);
-  const int32_t* d_solve_begin = put(host, at, dev, tb.solve_begin);
-  const int32_t* d_apply_begin = put(host, at, dev, tb.apply_begin);
+  const int32_t* d_solve_begin[2] = {put(host, at, dev, tb.solve_begin[0]),
+                                      put(host, at, dev, tb.solve_begin[1])};
+  const int32_t* d_apply_begin[2] = {put(host, at, dev, tb.apply_begin[0]),
+                                      put(host, at, dev, tb.apply_begin[1])};
   const GemmDesc* d_stats_l = put(host, at, dev, tb.stats_l);
   const GemmDesc* d_stats_r = put(host, at, dev, tb.stats_r);
   const GemmDesc* d_t = put(host, at, dev, tb.t);
@@ -919,20 +965,39 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
   if ((e = run_gemms(tb.t, d_t, 0, 0, st)) != MFSDP_OK) return e;
   if ((e = run_gemms(tb.a, d_a, 1, 0, st)) != MFSDP_OK) return e;
   diag_max_kernel<<<ns, 1024, 0, st>>>(d_sides, nullptr);
-  // block Jacobi sweeps; converged sides return at once
-  const int nb_max = set->dp_max / kJB;
-  const unsigned solve_blocks = (unsigned)tb.solve_begin.back();
-  const unsigned apply_blocks = (unsigned)tb.apply_begin.back();
-  for (int sw = 0; sw < h->max_sweeps; ++sw) {
-    for (int r = 0; r < nb_max - 1; ++r) {
-      jacobi_solve_kernel<<<solve_blocks, kSolveThreads, 0, st>>>(d_sides, d_solve_begin,
-                                                                  (int)ns, ctl, r);
-      jacobi_apply_kernel<<<apply_blocks, kJThreads, kApplySmem, st>>>(d_sides, d_apply_begin,
-                                                                      (int)ns, ctl, r);
-    }
-    jacobi_sweep_end_kernel<<<sweep_blocks, 256, 0, st>>>(ctl, (int)ns);
-    diag_max_kernel<<<ns, 1024, 0, st>>>(d_sides, ctl);
+  // block Jacobi sweeps, the two groups of sides on two streams (forked from and joined back
+  // into `st`); converged sides return at once
+  if (!set->aux) {
+    if (cudaStreamCreateWithFlags(&set->aux, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&set->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&set->ev_join, cudaEventDisableTiming) != cudaSuccess)
+      return MFSDP_ECUDA;
   }
+  if (cudaEventRecord(set->ev_fork, st) != cudaSuccess ||
+      cudaStreamWaitEvent(set->aux, set->ev_fork, 0) != cudaSuccess)
+    return MFSDP_ECUDA;
+  const cudaStream_t gst[2] = {st, set->aux};
+  const int goff[2] = {0, set->split}, gn[2] = {set->split, (int)ns - set->split};
+  const int nb_max = std::max(set->nb_max_group[0], set->nb_max_group[1]);
+  for (int sw = 0; sw < h->max_sweeps; ++sw) {
+    for (int r = 0; r < nb_max - 1; ++r)
+      for (int g = 0; g < 2; ++g) {
+        if (gn[g] == 0 || r >= set->nb_max_group[g] - 1) continue;
+        jacobi_solve_kernel<<<(unsigned)tb.solve_begin[g].back(), kSolveThreads, 0, gst[g]>>>(
+            d_sides + goff[g], d_solve_begin[g], gn[g], ctl + goff[g], r);
+        jacobi_apply_kernel<<<(unsigned)tb.apply_begin[g].back(), kJThreads, kApplySmem,
+                              gst[g]>>>(d_sides + goff[g], d_apply_begin[g], gn[g],
+                                        ctl + goff[g], r);
+      }
+    for (int g = 0; g < 2; ++g) {
+      if (gn[g] == 0) continue;
+      jacobi_sweep_end_kernel<<<(gn[g] + 255) / 256, 256, 0, gst[g]>>>(ctl + goff[g], gn[g]);
+      diag_max_kernel<<<(unsigned)gn[g], 1024, 0, gst[g]>>>(d_sides + goff[g], ctl + goff[g]);
+    }
+  }
+  if (cudaEventRecord(set->ev_join, set->aux) != cudaSuccess ||
+      cudaStreamWaitEvent(st, set->ev_join, 0) != cudaSuccess)
+    return MFSDP_ECUDA;
   if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
   // eigenvalues (Rayleigh quotients) in descending order, the basis columns with them
   if ((e = run_gemms(tb.ray, d_ray, 0, 0, st)) != MFSDP_OK) return e;
@@ -942,7 +1007,7 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
     const unsigned tiles = (unsigned)((set->d_max + 31) / 32);
     eig_scatter_kernel<<<dim3(tiles, tiles, ns), 256, 0, st>>>(d_sides);
   }
-  if (info) jacobi_info_kernel<<<sweep_blocks, 256, 0, st>>>(ctl, (int)ns, info);
+  if (info) jacobi_info_kernel<<<sweep_blocks, 256, 0, st>>>(d_sides, ctl, (int)ns, info);
   // Adam in the eigenbasis
   soap_moment_kernel<<<dim3(128, (unsigned)n), 256, 0, st>>>(d_mats, state->exp_avg, grad,
                                                              h->beta1);
