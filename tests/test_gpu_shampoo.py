@@ -97,3 +97,16 @@ def test_ragged_shapes(precision):
 @PRECISIONS
 def test_gpt2_small_shapes_one_step(precision):
     _check([(2304, 768), (768, 768), (3072, 768), (768, 3072)], 1, 3, precision)
+
+
+@PRECISIONS
+def test_empty_set_is_a_no_op(precision):
+    from matrix_optimizer_owner_gb300 import mfsdp
+    torch.cuda.set_device(0)
+    sset = mfsdp.ShampooSet([])
+    ws = torch.empty(max(sset.workspace_bytes, 1), dtype=torch.uint8, device="cuda")
+    x = torch.zeros(4, device="cuda")
+    sset.init_state(EPS, x, x, ws)
+    sset.step(x, x, x, x, LR, WD, ITERS, ws, precision=precision)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(x) == 0

@@ -180,3 +180,42 @@ def test_gpt2_layer_properties():
                      w_new[off:off + n].reshape(rows, cols)) / hyper["lr"]
             assert _rel(n_gpu, nn) < 1e-3, ((rows, cols), t, _rel(n_gpu, nn))
     sset.close()
+
+
+def test_zero_gradient_and_sweep_limit():
+    """A zero gradient leaves N = 0 (M' = 0, V = 0: N' = 0 / (0 + eps)), so the weights only
+    decay; a solve stopped by max_sweeps reports its sweeps negated, and a later step warm-starts
+    from the basis it left (still orthogonal)."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    from matrix_optimizer_owner_gb300 import mfsdp
+    shapes = [(96, 130), (64, 64)]
+    sset, ws, state, offs, numel = _setup(shapes, dev)
+    info = torch.zeros(2 * len(shapes), dtype=torch.int32, device=dev)
+    w = torch.randn(numel, device=dev) * 0.02
+    w0 = w.clone()
+    sset.step(torch.zeros(numel, device=dev), w, state, 1, max_sweeps=SWEEPS, workspace=ws,
+              info=info, **H)
+    torch.cuda.synchronize()
+    assert mfsdp.mfsdp_query_status() == 0
+    torch.testing.assert_close(w, w0 * (1 - H["lr"] * H["weight_decay"]), rtol=1e-7, atol=0)
+    assert (info.cpu().numpy() == 1).all()  # nothing to rotate: one checking sweep
+    rng = np.random.default_rng(9)
+    views = _views(shapes, state)
+    for v, (r, c) in zip(views, shapes):
+        state["l"][v["L"]] = torch.from_numpy(_spd(r, rng).astype(np.float32).ravel()).to(dev)
+        state["r"][v["R"]] = torch.from_numpy(_spd(c, rng).astype(np.float32).ravel()).to(dev)
+    g = torch.randn(numel, device=dev) * 1e-3
+    sset.step(g, w, state, 2, max_sweeps=1, workspace=ws, info=info, **H)
+    torch.cuda.synchronize()
+    assert (info.cpu().numpy() == -1).all(), info.cpu().numpy()
+    st = {k: v.double().cpu().numpy() for k, v in state.items()}
+    for v, (r, c) in zip(views, shapes):
+        for key, d, sl in (("q_l", r, v["L"]), ("q_r", c, v["R"])):
+            q = st[key][sl].reshape(d, d)
+            assert np.abs(q.T @ q - np.eye(d)).max() < 1e-4
+    sset.step(g, w, state, 3, max_sweeps=SWEEPS, workspace=ws, info=info, **H)
+    torch.cuda.synchronize()
+    assert (info.cpu().numpy() > 0).all()
+    assert mfsdp.mfsdp_query_status() == 0
+    sset.close()
