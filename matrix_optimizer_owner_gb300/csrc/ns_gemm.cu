@@ -290,6 +290,9 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
   using C = Cfg<SPLIT>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
+  // the next phase may launch now: its CTAs take SMs as ours leave and stop in
+  // griddepcontrol.wait until this grid has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -324,6 +327,9 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // everything above touched only this CTA's shared and tensor memory; from here on the
+  // previous phase's outputs are read
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t tmem_base = *tmem_slot;
   const Guard g{abort_flag, P.wait_limit_ns, P.status};
 
@@ -740,6 +746,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
   using C = PairCfg;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // as in ns_gemm_kernel
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -777,6 +784,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
   __syncthreads();
   cluster_sync_all();
   tc_fence_after();
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous phase has completed
   const uint32_t tmem_base = *tmem_slot;
   uint32_t peer_base;
   asm volatile("ld.shared::cluster.u32 %0, [%1];"
@@ -1113,24 +1121,30 @@ int ns_pair_max_clusters(int num_sms) {
 
 cudaError_t launch_ns_phase(const NsLaunchParams& p, bool split, int grid, cudaStream_t s) {
   if (p.ntiles <= 0) return cudaSuccess;
+  // Programmatic dependent launch: a phase's grid may start while the previous one drains
+  // (its prologue overlaps that tail; the kernel waits for the previous grid before it reads).
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.blockDim = dim3(kNsThreads, 1, 1);
+  cfg.stream = s;
+  cfg.attrs = attr;
   if (split) {
-    ns_gemm_kernel<true><<<grid, kNsThreads, Cfg<true>::kSmem, s>>>(p);
-    return cudaGetLastError();
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<true>::kSmem;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ns_gemm_kernel<true>, p);
   }
   // bf16 operands: CTA pairs; `grid` is the number of co-resident pairs
   const int pairs = std::max(1, std::min(p.ntiles, grid));
-  cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cfg.blockDim = dim3(kNsThreads, 1, 1);
   cfg.dynamicSmemBytes = PairCfg::kSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel, p);
 }
 
