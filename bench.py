@@ -58,7 +58,7 @@ NS_TRAFFIC_SOURCES = ("matrix_optimizer_owner_gb300/csrc/ns_gemm.cu",
                       "matrix_optimizer_owner_gb300/csrc/mfsdp_internal.h")
 NS_TRAFFIC = {
     # config index: (sources sha256, bytes per launch, profile summary)
-    1: ("1411d0098b5646a5e85b08c266047908082bd3000fe769244611453089739e22", 208988228,
+    1: ("54b95f322b77846271c864618e2edeedab9a6d6d5313bd086cbea5b6b7454f00", 208958703,
         "profiles/owner_step_gpt2_small_launch_list.md"),
 }
 
