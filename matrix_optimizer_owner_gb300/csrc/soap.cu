@@ -15,12 +15,13 @@
 // Eigenbases: cyclic two-sided block Jacobi, warm-started from the previous step's basis Q:
 // A = Q^T L Q (nearly diagonal once the statistics move slowly), Z = Q, then sweeps over all
 // pairs of 32-index blocks in round-robin order.  In one round every pair (P, Q) of blocks
-// forms a 64 x 64 subproblem [A_PP A_PQ; A_QP A_QQ], diagonalised exactly by a CTA in shared
-// memory (one cyclic sweep of plane rotations, Golub & Van Loan §8.5), giving a 64 x 64
-// orthogonal J; a second launch applies all of the round's J to A (A <- J^T A J, block by
-// block) and to Z (Z <- Z J).  A sweep in which no subproblem rotated ends the solve for that
-// matrix.  The eigenvalues are then sorted (descending, ties by index) and Z's columns
-// scattered into Q in that order.  Plane rotations are skipped where the coupling is at
+// forms a 64 x 64 subproblem [A_PP A_PQ; A_QP A_QQ], reduced by a CTA in shared memory (one
+// cyclic sweep of plane rotations, Golub & Van Loan §8.5, then one polar step), giving a
+// 64 x 64 orthogonal J; a second launch applies all of the round's J to A (A <- J^T A J, block
+// by block) and to Z, kept transposed (Z^T <- J^T Z^T: eigenvectors as rows).  A sweep in
+// which no subproblem rotated ends the solve for that matrix.  The eigenvalues are the
+// Rayleigh quotients of the final basis, sorted (descending, ties by index), and Z's columns
+// are scattered into Q in that order.  Plane rotations are skipped where the coupling is at
 // rounding level, |a_pq| <= tol max_i |a_ii| (tol = 1e-6, about 16u, by default): the rotations
 // of a block are 64-term fp32 sums, whose rounding leaves couplings of a few u ||L|| between
 // nearly equal eigenvalues, and eigenvectors are accurate to about tol ||L|| / gap.
