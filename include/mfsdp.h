@@ -54,7 +54,8 @@ typedef enum {
   MFSDP_EWORKSPACE = -5,  /* workspace smaller than mfsdp_owner_set_workspace_bytes() */
   MFSDP_ECUDA = -6,       /* a CUDA runtime / driver call failed */
   MFSDP_ETIMEOUT = -7,    /* device status: a bounded device-side wait ran out */
-  MFSDP_ENONFINITE = -8,  /* device status: a matrix norm was NaN or Inf */
+  MFSDP_ENONFINITE = -8,  /* device status: a matrix norm (Muon) or update (Shampoo, SOAP) was
+                             NaN or Inf */
   MFSDP_ENODEVICE = -9    /* no usable sm_103 device for a device call */
 } mfsdp_status;
 
@@ -246,6 +247,7 @@ typedef struct {
  * back in table order (sizes from mfsdp_shampoo_set_sizes).  The workspace holds the root
  * iteration's buffers (7 x (rows^2 + cols^2) values per matrix), P, the tensor maps and the
  * launch tables; its size covers both precisions.
+ * A non-finite P sets MFSDP_ENONFINITE in the device status word (mfsdp_query_status).
  * Errors: MFSDP_EINVAL (null pointers, eps <= 0, root_iters outside [1, 200], unknown
  * precision), MFSDP_ESHAPE
  * (rows or cols outside [1, 65536], negative offset), MFSDP_EWORKSPACE, MFSDP_ECUDA.
@@ -299,7 +301,7 @@ int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* grad, float* l
  * any symmetric positive semi-definite L, R and any orthogonal Q there instead.
  * `grad` and `weights` are the flat owner buffers (fp32).  `info` (DEVICE, nullable,
  * 2 x n_mats int32: L sides, then R sides) receives the sweeps each solve used, negated when
- * it stopped at max_sweeps.
+ * it stopped at max_sweeps.  A non-finite N sets MFSDP_ENONFINITE in the device status word.
  * Errors: MFSDP_EINVAL (null pointers, t < 1, max_sweeps outside [1, 100], a beta outside
  * [0, 1), eps < 0, jacobi_tol outside [0, 1e-2)), MFSDP_ESHAPE (rows or cols outside [1, 65536], negative offset),
  * MFSDP_EWORKSPACE, MFSDP_ECUDA.

@@ -169,7 +169,7 @@ const char* mfsdp_status_string(int st) {
     case MFSDP_EWORKSPACE: return "workspace too small";
     case MFSDP_ECUDA: return "CUDA error";
     case MFSDP_ETIMEOUT: return "device wait timed out";
-    case MFSDP_ENONFINITE: return "non-finite norm";
+    case MFSDP_ENONFINITE: return "non-finite norm or update";
     case MFSDP_ENODEVICE: return "no usable sm_103 device";
     default: return "unknown status";
   }

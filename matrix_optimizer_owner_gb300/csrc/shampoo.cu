@@ -207,12 +207,22 @@ __global__ void scaled_identity_kernel(float* base, const int64_t* offs, const i
     a[e] = (e / dims[i]) == (e % dims[i]) ? eps : 0.f;
 }
 
+// One atomic per warp whose lanes saw a non-finite update (the device status word).
+__device__ __forceinline__ void flag_non_finite(bool bad, int* status) {
+  if (__any_sync(__activemask(), bad) && (threadIdx.x & 31) == 0)
+    atomicOr(status, kStatusNonFinite);
+}
+
 // W = W (1 - lr wd) - lr P over the flat owner buffer.
 __global__ void shampoo_update_kernel(float* w, const float* p, int64_t n, float decay,
-                                      float lr) {
+                                      float lr, int* status) {
+  bool bad = false;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
-       e += (int64_t)gridDim.x * blockDim.x)
+       e += (int64_t)gridDim.x * blockDim.x) {
+    bad |= !isfinite(p[e]);
     w[e] = fmaf(w[e], decay, -lr * p[e]);
+  }
+  flag_non_finite(bad, status);
 }
 
 // ---------------------------------------------------------------- split-bf16 root path
@@ -303,13 +313,17 @@ __global__ void t_from_m_kernel(const TDesc* descs) {
 // W = W (1 - lr wd) - lr (P_hi + P_lo) for one matrix (P pitch ldp).
 __global__ void update_split_kernel(float* w, const uint16_t* p_hi, const uint16_t* p_lo,
                                     int32_t rows, int32_t cols, int32_t ldp, float decay,
-                                    float lr) {
+                                    float lr, int* status) {
   const int64_t n = (int64_t)rows * cols;
+  bool bad = false;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = e / cols, c = e % cols, o = r * ldp + c;
-    w[e] = fmaf(w[e], decay, -lr * join_bf16(p_hi[o], p_lo[o]));
+    const float pv = join_bf16(p_hi[o], p_lo[o]);
+    bad |= !isfinite(pv);
+    w[e] = fmaf(w[e], decay, -lr * pv);
   }
+  flag_non_finite(bad, status);
 }
 
 }  // namespace
@@ -733,7 +747,7 @@ int shampoo_step_split(const mfsdp_shampoo_set* set, const float* grad, float* l
     const int blocks = (int)std::min<int64_t>((m.rows * m.cols + 255) / 256, 4096);
     update_split_kernel<<<blocks, 256, 0, st>>>(weights + m.offset, mbuf(i, 2, 0), mbuf(i, 2, 1),
                                                 (int32_t)m.rows, (int32_t)m.cols,
-                                                set->mat_ld[(size_t)i], decay, lr);
+                                                set->mat_ld[(size_t)i], decay, lr, status);
   }
   return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
 }
@@ -870,12 +884,14 @@ extern "C" int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* gra
   if ((e = launch_gemm(d_pre, n, max_rows, max_cols, 0, 0, st)) != MFSDP_OK) return e;
   if ((e = launch_gemm(d_pre + n, n, max_rows, max_cols, 0, 0, st)) != MFSDP_OK) return e;
   // W = W (1 - lr wd) - lr P, matrix by matrix
+  int* status = status_word_address();
+  if (status == nullptr) return MFSDP_ECUDA;
   const float decay = (float)(1.0 - (double)lr * (double)weight_decay);
   for (const auto& m : set->mats) {
     const int64_t cnt = m.rows * m.cols;
     const int blocks = (int)std::min<int64_t>((cnt + 255) / 256, 4096);
     shampoo_update_kernel<<<blocks, 256, 0, st>>>(weights + m.offset, pbuf + m.offset, cnt,
-                                                  decay, lr);
+                                                  decay, lr, status);
   }
   return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
 }

@@ -571,15 +571,19 @@ __global__ void soap_adam_kernel(const MatDev* mats, const float* grot, float* m
   }
 }
 
-// W = W (1 - lr wd) - lr N.
+// W = W (1 - lr wd) - lr N; a non-finite N sets the device status word (one atomic per warp).
 __global__ void soap_update_kernel(const MatDev* mats, float* w, const float* nbuf, float decay,
-                                   float lr) {
+                                   float lr, int* status) {
   const MatDev d = mats[blockIdx.y];
+  bool bad = false;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < d.numel;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t o = d.offset + e;
+    bad |= !isfinite(nbuf[o]);
     w[o] = fmaf(w[o], decay, -lr * nbuf[o]);
   }
+  if (__any_sync(__activemask(), bad) && (threadIdx.x & 31) == 0)
+    atomicOr(status, kStatusNonFinite);
 }
 
 // L = R = 0, Q = I, eigenvalues 0 for every side; M = V = 0 over every matrix.
@@ -1024,7 +1028,9 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
   if ((e = run_gemms(tb.back1, d_back1, 0, 0, st)) != MFSDP_OK) return e;
   if ((e = run_gemms(tb.back2, d_back2, 0, 1, st)) != MFSDP_OK) return e;
   const float decay = (float)(1.0 - (double)h->lr * (double)h->weight_decay);
+  int* status = status_word_address();
+  if (status == nullptr) return MFSDP_ECUDA;
   soap_update_kernel<<<dim3(128, (unsigned)n), 256, 0, st>>>(d_mats, weights, g_rot, decay,
-                                                             h->lr);
+                                                             h->lr, status);
   return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
 }

@@ -110,3 +110,22 @@ def test_empty_set_is_a_no_op(precision):
     sset.step(x, x, x, x, LR, WD, ITERS, ws, precision=precision)
     torch.cuda.synchronize()
     assert torch.count_nonzero(x) == 0
+
+
+@PRECISIONS
+def test_non_finite_gradient_sets_the_status(precision):
+    from matrix_optimizer_owner_gb300 import mfsdp
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    sset = mfsdp.ShampooSet([(64, 96, 0)])
+    ws = torch.empty(sset.workspace_bytes, dtype=torch.uint8, device=dev)
+    l = torch.empty(sset.l_numel, device=dev)
+    r = torch.empty(sset.r_numel, device=dev)
+    sset.init_state(EPS, l, r, ws)
+    g = torch.randn(64 * 96, device=dev) * 1e-3
+    g[17] = float("nan")
+    w = torch.zeros(64 * 96, device=dev)
+    assert mfsdp.mfsdp_query_status() == 0
+    sset.step(g, l, r, w, LR, WD, ITERS, ws, precision=precision)
+    assert mfsdp.mfsdp_query_status() == -8   # MFSDP_ENONFINITE, then cleared
+    assert mfsdp.mfsdp_query_status() == 0

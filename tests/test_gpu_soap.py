@@ -219,3 +219,18 @@ def test_zero_gradient_and_sweep_limit():
     assert (info.cpu().numpy() > 0).all()
     assert mfsdp.mfsdp_query_status() == 0
     sset.close()
+
+
+def test_non_finite_gradient_sets_the_status():
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    from matrix_optimizer_owner_gb300 import mfsdp
+    sset, ws, state, offs, numel = _setup([(64, 96)], dev)
+    g = torch.randn(numel, device=dev) * 1e-3
+    g[5] = float("inf")
+    w = torch.zeros(numel, device=dev)
+    assert mfsdp.mfsdp_query_status() == 0
+    sset.step(g, w, state, 1, max_sweeps=SWEEPS, workspace=ws, **H)
+    assert mfsdp.mfsdp_query_status() == -8   # MFSDP_ENONFINITE, then cleared
+    assert mfsdp.mfsdp_query_status() == 0
+    sset.close()
