@@ -58,7 +58,7 @@ NS_TRAFFIC_SOURCES = ("matrix_optimizer_owner_gb300/csrc/ns_gemm.cu",
                       "matrix_optimizer_owner_gb300/csrc/mfsdp_internal.h")
 NS_TRAFFIC = {
     # config index: (sources sha256, bytes per launch, profile summary)
-    1: ("54b95f322b77846271c864618e2edeedab9a6d6d5313bd086cbea5b6b7454f00", 208958703,
+    1: ("6a63a09e508998d8c4f12dd71c25f05a2484edfe6fde69933d067fec2418e4a1", 208883128,
         "profiles/owner_step_gpt2_small_launch_list.md"),
 }
 
