@@ -301,9 +301,10 @@ int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* grad, float* l
  * any symmetric positive semi-definite L, R and any orthogonal Q there instead.
  * `grad` and `weights` are the flat owner buffers (fp32).  `info` (DEVICE, nullable,
  * 2 x n_mats int32: L sides, then R sides) receives the sweeps each solve used, negated when
- * it stopped at max_sweeps.  A non-finite N sets MFSDP_ENONFINITE in the device status word.
+ * it stopped at max_sweeps (0 for every side when the step does not refresh).  A non-finite
+ * N sets MFSDP_ENONFINITE in the device status word.
  * Errors: MFSDP_EINVAL (null pointers, t < 1, max_sweeps outside [1, 100], a beta outside
- * [0, 1), eps < 0, jacobi_tol outside [0, 1e-2)), MFSDP_ESHAPE (rows or cols outside [1, 65536], negative offset),
+ * [0, 1), eps < 0, jacobi_tol outside [0, 1e-2), refresh not 0 or 1), MFSDP_ESHAPE (rows or cols outside [1, 65536], negative offset),
  * MFSDP_EWORKSPACE, MFSDP_ECUDA.
  * ------------------------------------------------------------------------------------------ */
 
@@ -324,6 +325,8 @@ typedef struct {
   float lr, beta1, beta2, beta_stats, eps, weight_decay;
   int32_t max_sweeps;
   float jacobi_tol;  /* couplings below jacobi_tol * ||L|| are not rotated; 0: 1e-6 */
+  int32_t refresh;   /* 1: recompute the eigenbases this step; 0: keep the state's Q and
+                        eigenvalues (SOAP's preconditioning frequency: refresh every f steps) */
 } mfsdp_soap_hyper;
 
 int mfsdp_soap_set_create(const mfsdp_matrix* mats, int32_t n_mats, mfsdp_soap_set** out);

@@ -41,7 +41,7 @@ class SoapState(C.Structure):
 class SoapHyper(C.Structure):
     _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float),
                 ("beta_stats", C.c_float), ("eps", C.c_float), ("weight_decay", C.c_float),
-                ("max_sweeps", C.c_int32), ("jacobi_tol", C.c_float)]
+                ("max_sweeps", C.c_int32), ("jacobi_tol", C.c_float), ("refresh", C.c_int32)]
 
 
 class CostModel(C.Structure):

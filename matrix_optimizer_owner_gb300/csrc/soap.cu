@@ -874,7 +874,7 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
   if (t < 1 || h->max_sweeps < 1 || h->max_sweeps > 100 || !(h->eps >= 0.f) ||
       !(h->beta1 >= 0.f && h->beta1 < 1.f) || !(h->beta2 >= 0.f && h->beta2 < 1.f) ||
       !(h->beta_stats >= 0.f && h->beta_stats < 1.f) ||
-      !(h->jacobi_tol >= 0.f && h->jacobi_tol < 1e-2f))
+      !(h->jacobi_tol >= 0.f && h->jacobi_tol < 1e-2f) || (h->refresh != 0 && h->refresh != 1))
     return MFSDP_EINVAL;
   const int n = (int)set->mats.size();
   if (n == 0) return MFSDP_OK;
@@ -964,55 +964,59 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
   // statistics
   if ((e = run_gemms(tb.stats_l, d_stats_l, 0, 1, st)) != MFSDP_OK) return e;
   if ((e = run_gemms(tb.stats_r, d_stats_r, 1, 0, st)) != MFSDP_OK) return e;
-  // the statistics in the previous basis, A = Q^T L Q, and Z = Q
-  jacobi_setup_kernel<<<dim3(128, ns), 256, 0, st>>>(d_sides, ctl);
-  if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
-  if ((e = run_gemms(tb.t, d_t, 0, 0, st)) != MFSDP_OK) return e;
-  if ((e = run_gemms(tb.a, d_a, 1, 0, st)) != MFSDP_OK) return e;
-  diag_max_kernel<<<ns, 1024, 0, st>>>(d_sides, nullptr);
-  // block Jacobi sweeps, the two groups of sides on two streams (forked from and joined back
-  // into `st`); converged sides return at once
-  if (!set->aux) {
-    if (cudaStreamCreateWithFlags(&set->aux, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&set->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&set->ev_join, cudaEventDisableTiming) != cudaSuccess)
-      return MFSDP_ECUDA;
-  }
-  if (cudaEventRecord(set->ev_fork, st) != cudaSuccess ||
-      cudaStreamWaitEvent(set->aux, set->ev_fork, 0) != cudaSuccess)
-    return MFSDP_ECUDA;
-  const cudaStream_t gst[2] = {st, set->aux};
-  const int goff[2] = {0, set->split}, gn[2] = {set->split, (int)ns - set->split};
-  const int nb_max = std::max(set->nb_max_group[0], set->nb_max_group[1]);
-  for (int sw = 0; sw < h->max_sweeps; ++sw) {
-    for (int r = 0; r < nb_max - 1; ++r)
-      for (int g = 0; g < 2; ++g) {
-        if (gn[g] == 0 || r >= set->nb_max_group[g] - 1) continue;
-        jacobi_solve_kernel<<<(unsigned)tb.solve_begin[g].back(), kSolveThreads, 0, gst[g]>>>(
-            d_sides + goff[g], d_solve_begin[g], gn[g], ctl + goff[g], r);
-        jacobi_apply_kernel<<<(unsigned)tb.apply_begin[g].back(), kJThreads, kApplySmem,
-                              gst[g]>>>(d_sides + goff[g], d_apply_begin[g], gn[g],
-                                        ctl + goff[g], r);
-      }
-    for (int g = 0; g < 2; ++g) {
-      if (gn[g] == 0) continue;
-      jacobi_sweep_end_kernel<<<(gn[g] + 255) / 256, 256, 0, gst[g]>>>(ctl + goff[g], gn[g]);
-      diag_max_kernel<<<(unsigned)gn[g], 1024, 0, gst[g]>>>(d_sides + goff[g], ctl + goff[g]);
+  if (h->refresh) {
+    // the statistics in the previous basis, A = Q^T L Q, and Z = Q
+    jacobi_setup_kernel<<<dim3(128, ns), 256, 0, st>>>(d_sides, ctl);
+    if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
+    if ((e = run_gemms(tb.t, d_t, 0, 0, st)) != MFSDP_OK) return e;
+    if ((e = run_gemms(tb.a, d_a, 1, 0, st)) != MFSDP_OK) return e;
+    diag_max_kernel<<<ns, 1024, 0, st>>>(d_sides, nullptr);
+    // block Jacobi sweeps, the two groups of sides on two streams (forked from and joined back
+    // into `st`); converged sides return at once
+    if (!set->aux) {
+      if (cudaStreamCreateWithFlags(&set->aux, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&set->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&set->ev_join, cudaEventDisableTiming) != cudaSuccess)
+        return MFSDP_ECUDA;
     }
-  }
-  if (cudaEventRecord(set->ev_join, set->aux) != cudaSuccess ||
-      cudaStreamWaitEvent(st, set->ev_join, 0) != cudaSuccess)
+    if (cudaEventRecord(set->ev_fork, st) != cudaSuccess ||
+        cudaStreamWaitEvent(set->aux, set->ev_fork, 0) != cudaSuccess)
+      return MFSDP_ECUDA;
+    const cudaStream_t gst[2] = {st, set->aux};
+    const int goff[2] = {0, set->split}, gn[2] = {set->split, (int)ns - set->split};
+    const int nb_max = std::max(set->nb_max_group[0], set->nb_max_group[1]);
+    for (int sw = 0; sw < h->max_sweeps; ++sw) {
+      for (int r = 0; r < nb_max - 1; ++r)
+        for (int g = 0; g < 2; ++g) {
+          if (gn[g] == 0 || r >= set->nb_max_group[g] - 1) continue;
+          jacobi_solve_kernel<<<(unsigned)tb.solve_begin[g].back(), kSolveThreads, 0, gst[g]>>>(
+              d_sides + goff[g], d_solve_begin[g], gn[g], ctl + goff[g], r);
+          jacobi_apply_kernel<<<(unsigned)tb.apply_begin[g].back(), kJThreads, kApplySmem,
+                                gst[g]>>>(d_sides + goff[g], d_apply_begin[g], gn[g],
+                                          ctl + goff[g], r);
+        }
+      for (int g = 0; g < 2; ++g) {
+        if (gn[g] == 0) continue;
+        jacobi_sweep_end_kernel<<<(gn[g] + 255) / 256, 256, 0, gst[g]>>>(ctl + goff[g], gn[g]);
+        diag_max_kernel<<<(unsigned)gn[g], 1024, 0, gst[g]>>>(d_sides + goff[g], ctl + goff[g]);
+      }
+    }
+    if (cudaEventRecord(set->ev_join, set->aux) != cudaSuccess ||
+        cudaStreamWaitEvent(st, set->ev_join, 0) != cudaSuccess)
+      return MFSDP_ECUDA;
+    if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
+    // eigenvalues (Rayleigh quotients) in descending order, the basis columns with them
+    if ((e = run_gemms(tb.ray, d_ray, 0, 0, st)) != MFSDP_OK) return e;
+    rayleigh_kernel<<<dim3(64, ns), 256, 0, st>>>(d_sides);
+    eig_rank_kernel<<<dim3((unsigned)((set->d_max + 255) / 256), ns), 256, 0, st>>>(d_sides);
+    {
+      const unsigned tiles = (unsigned)((set->d_max + 31) / 32);
+      eig_scatter_kernel<<<dim3(tiles, tiles, ns), 256, 0, st>>>(d_sides);
+    }
+    if (info) jacobi_info_kernel<<<sweep_blocks, 256, 0, st>>>(d_sides, ctl, (int)ns, info);
+  } else if (info && cudaMemsetAsync(info, 0, sizeof(int32_t) * ns, st) != cudaSuccess) {
     return MFSDP_ECUDA;
-  if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
-  // eigenvalues (Rayleigh quotients) in descending order, the basis columns with them
-  if ((e = run_gemms(tb.ray, d_ray, 0, 0, st)) != MFSDP_OK) return e;
-  rayleigh_kernel<<<dim3(64, ns), 256, 0, st>>>(d_sides);
-  eig_rank_kernel<<<dim3((unsigned)((set->d_max + 255) / 256), ns), 256, 0, st>>>(d_sides);
-  {
-    const unsigned tiles = (unsigned)((set->d_max + 31) / 32);
-    eig_scatter_kernel<<<dim3(tiles, tiles, ns), 256, 0, st>>>(d_sides);
   }
-  if (info) jacobi_info_kernel<<<sweep_blocks, 256, 0, st>>>(d_sides, ctl, (int)ns, info);
   // Adam in the eigenbasis
   soap_moment_kernel<<<dim3(128, (unsigned)n), 256, 0, st>>>(d_mats, state->exp_avg, grad,
                                                              h->beta1);

@@ -302,10 +302,12 @@ class SoapSet:
 
     def step(self, grad, weights, state, t: int, *, lr: float, beta1: float, beta2: float,
              beta_stats: float, eps: float, weight_decay: float, max_sweeps: int, workspace,
-             info=None, stream=None, jacobi_tol: float = 0.0) -> None:
+             info=None, stream=None, jacobi_tol: float = 0.0, refresh: bool = True) -> None:
+        """``refresh`` false keeps the state's eigenbases for this step (SOAP refreshes them
+        every f steps)."""
         st = self._state(state)
         hy = _lib.SoapHyper(lr, beta1, beta2, beta_stats, eps, weight_decay, max_sweeps,
-                            jacobi_tol)
+                            jacobi_tol, 1 if refresh else 0)
         _check("mfsdp_soap_step",
                _lib.load().mfsdp_soap_step(self._h, _ptr(grad), _ptr(weights), C.byref(st), t,
                                            C.byref(hy), _ptr(info) if info is not None else None,

@@ -17,7 +17,9 @@ exactly at every step:
     W <- W (1 - lr wd) - lr N
 
 G is the owner's deposited gradient (grad_scale times the sum of the contributions); t >= 1
-counts steps.  The eigenvectors are only fixed up to sign, and N does not depend on the
+counts steps.  SOAP itself refreshes the eigenbasis only every f steps (its preconditioning
+frequency); ``refresh=False`` keeps the previous basis for a step, as it does in between.
+The eigenvectors are only fixed up to sign, and N does not depend on the
 signs: flipping column j of Q_L flips row j of G' and M' and so of N', which Q_L flips back.
 Within an eigenspace of a repeated eigenvalue the basis is free; where that eigenspace lies
 in the null space of every gradient seen (a rank-deficient L or R), G' and M' vanish there
@@ -52,14 +54,22 @@ def soap_direction(g, m, v, q_l, q_r, *, t: int, beta1: float, beta2: float, eps
 
 def soap_matrix_step(w, l, r, m, v, contributions: Sequence[np.ndarray], *, t: int,
                      grad_scale: float, lr: float, weight_decay: float, beta1: float,
-                     beta2: float, eps: float, beta_stats: float) -> Dict[str, np.ndarray]:
+                     beta2: float, eps: float, beta_stats: float, refresh: bool = True,
+                     basis=None) -> Dict[str, np.ndarray]:
     """One owner SOAP step of one matrix; returns the new W, L, R, M, V, the eigenbases and
-    eigenvalues, and the direction N."""
+    eigenvalues, and the direction N.
+
+    With ``refresh`` false the eigenbases are not recomputed: ``basis`` = (lam_l, Q_L, lam_r,
+    Q_R) from the last refreshing step is used as it stands (SOAP's preconditioning
+    frequency: the statistics still accumulate every step)."""
     g = sum(np.asarray(c, dtype=np.float64) for c in contributions) * grad_scale
     l = beta_stats * np.asarray(l, dtype=np.float64) + (1.0 - beta_stats) * (g @ g.T)
     r = beta_stats * np.asarray(r, dtype=np.float64) + (1.0 - beta_stats) * (g.T @ g)
-    lam_l, q_l = eigenbasis(l)
-    lam_r, q_r = eigenbasis(r)
+    if refresh:
+        lam_l, q_l = eigenbasis(l)
+        lam_r, q_r = eigenbasis(r)
+    else:
+        lam_l, q_l, lam_r, q_r = basis
     m = beta1 * np.asarray(m, dtype=np.float64) + (1.0 - beta1) * g
     n, _, v = soap_direction(g, m, v, q_l, q_r, t=t, beta1=beta1, beta2=beta2, eps=eps)
     w = np.asarray(w, dtype=np.float64) * (1.0 - lr * weight_decay) - lr * n

@@ -73,7 +73,7 @@ def _sign_match(q_gpu, q_ref):
     return np.abs(q_gpu * s - q_ref).max()
 
 
-def _parity(shapes, steps, seed):
+def _parity(shapes, steps, seed, refresh=None):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     from matrix_optimizer_owner_gb300 import mfsdp
@@ -91,22 +91,28 @@ def _parity(shapes, steps, seed):
                 R=r0[i].astype(np.float32).astype(np.float64),
                 M=np.zeros(shapes[i]), V=np.zeros(shapes[i])) for i in range(len(shapes))]
     for t in range(1, steps + 1):
+        fresh = refresh is None or refresh[t - 1]
         g = (rng.standard_normal(numel) * 1e-3).astype(np.float32)
         w_old = w.double().cpu().numpy()
         sset.step(torch.from_numpy(g).to(dev), w, state, t, max_sweeps=SWEEPS, workspace=ws,
-                  info=info, **H)
+                  info=info, refresh=fresh, **H)
         torch.cuda.synchronize()
         assert mfsdp.mfsdp_query_status() == 0
         w_new = w.double().cpu().numpy()
-        assert (info.cpu().numpy() > 0).all(), info.cpu().numpy()
+        if fresh:
+            assert (info.cpu().numpy() > 0).all(), info.cpu().numpy()
+        else:
+            assert (info.cpu().numpy() == 0).all(), info.cpu().numpy()
         st = {k: v.double().cpu().numpy() for k, v in state.items()}
         for i, ((rows, cols), off, v) in enumerate(zip(shapes, offs, views)):
             n = rows * cols
             gi = g[off:off + n].astype(np.float64).reshape(rows, cols)
             wo = w_old[off:off + n].reshape(rows, cols)
             o = osoap.soap_matrix_step(wo, ref[i]["L"], ref[i]["R"], ref[i]["M"], ref[i]["V"],
-                                       [gi], t=t, grad_scale=1.0, **H)
-            ref[i].update(L=o["L"], R=o["R"], M=o["M"], V=o["V"])
+                                       [gi], t=t, grad_scale=1.0, refresh=fresh,
+                                       basis=ref[i].get("basis"), **H)
+            ref[i].update(L=o["L"], R=o["R"], M=o["M"], V=o["V"],
+                          basis=(o["lamL"], o["QL"], o["lamR"], o["QR"]))
             n_gpu = (wo * (1 - H["lr"] * H["weight_decay"]) -
                      w_new[off:off + n].reshape(rows, cols)) / H["lr"]
             tag = ((rows, cols), t)
@@ -128,6 +134,12 @@ def test_small_set_three_steps():
 
 def test_ragged_shapes():
     _parity([(100, 37), (37, 100), (129, 130), (1, 50), (50, 1)], 2, 2)
+
+
+def test_basis_refreshed_every_other_step():
+    """SOAP's preconditioning frequency: the eigenbases are recomputed on steps 1 and 3 only;
+    steps 2 and 4 keep them (and the eigenvalues) while the statistics and moments advance."""
+    _parity([(64, 64), (128, 96), (37, 100)], 4, 5, refresh=[True, False, True, False])
 
 
 def test_gpt2_layer_properties():

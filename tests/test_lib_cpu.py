@@ -287,15 +287,15 @@ def test_soap_validation_before_any_launch(lib):
     assert ws.value >= 4 * 2 * (3 * 64 * 64 + 128 * 128)
     p = C.c_void_p(1 << 20)  # never dereferenced: every case fails first
     st = L.SoapState(*([p.value] * 8))
-    good = L.SoapHyper(1e-3, 0.9, 0.95, 0.95, 1e-8, 0.01, 10, 0.0)
+    good = L.SoapHyper(1e-3, 0.9, 0.95, 0.95, 1e-8, 0.01, 10, 0.0, 1)
     step = lib.mfsdp_soap_step
     assert step(h, None, p, C.byref(st), 1, C.byref(good), None, p, ws.value, None) == -1
     assert step(h, p, p, None, 1, C.byref(good), None, p, ws.value, None) == -1
     assert step(h, p, p, C.byref(st), 0, C.byref(good), None, p, ws.value, None) == -1  # t
     for field, bad in (("max_sweeps", 0), ("max_sweeps", 101), ("beta1", 1.0),
                        ("beta2", -0.1), ("beta_stats", 1.0), ("eps", -1.0),
-                       ("jacobi_tol", -1e-6), ("jacobi_tol", 0.5)):
-        hb = L.SoapHyper(1e-3, 0.9, 0.95, 0.95, 1e-8, 0.01, 10, 0.0)
+                       ("jacobi_tol", -1e-6), ("jacobi_tol", 0.5), ("refresh", 2)):
+        hb = L.SoapHyper(1e-3, 0.9, 0.95, 0.95, 1e-8, 0.01, 10, 0.0, 1)
         setattr(hb, field, bad)
         assert step(h, p, p, C.byref(st), 1, C.byref(hb), None, p, ws.value, None) == -1, field
     assert step(h, p, p, C.byref(st), 1, C.byref(good), None, None, ws.value, None) == -5

@@ -643,3 +643,30 @@ def test_planted_soap_mistakes_are_caught():
     assert np.abs(ql @ n_rot @ qr.T - want).max() < 1e-12
     n_param = g / (np.abs(g) + eps)                                       # Adam in W coordinates
     assert np.abs(n_param - want).max() > 1e-2
+
+
+def test_soap_without_refresh_keeps_the_basis():
+    # refresh=False with the basis of the previous step is the same step as refresh=True when
+    # the statistics' eigenvectors do not move (diagonal statistics in a fixed order), and
+    # otherwise uses exactly the given basis
+    from oracle import soap
+    rng = np.random.default_rng(26)
+    gs = [np.diag(np.array([3.0, 2.0, 1.0]) * rng.uniform(0.5, 0.6, 3)) for _ in range(2)]
+    h = dict(SOAP_HYPER)
+    o1 = soap.soap_matrix_step(np.eye(3), np.zeros((3, 3)), np.zeros((3, 3)), np.zeros((3, 3)),
+                               np.zeros((3, 3)), [gs[0]], t=1, **h)
+    basis = (o1["lamL"], o1["QL"], o1["lamR"], o1["QR"])
+    a = soap.soap_matrix_step(o1["W"], o1["L"], o1["R"], o1["M"], o1["V"], [gs[1]], t=2, **h)
+    b = soap.soap_matrix_step(o1["W"], o1["L"], o1["R"], o1["M"], o1["V"], [gs[1]], t=2,
+                              refresh=False, basis=basis, **h)
+    np.testing.assert_allclose(b["W"], a["W"], rtol=1e-13)
+    g = rng.normal(size=(4, 5))
+    ql, _ = np.linalg.qr(rng.normal(size=(4, 4)))
+    qr, _ = np.linalg.qr(rng.normal(size=(5, 5)))
+    c = soap.soap_matrix_step(np.zeros((4, 5)), np.zeros((4, 4)), np.zeros((5, 5)),
+                              np.zeros((4, 5)), np.zeros((4, 5)), [g], t=1, refresh=False,
+                              basis=(np.zeros(4), ql, np.zeros(5), qr), **dict(h, eps=1e-6))
+    n_ref, _, _ = soap.soap_direction(g, 0.1 * g, np.zeros((4, 5)), ql, qr, t=1, beta1=0.9,
+                                      beta2=0.95, eps=1e-6)
+    np.testing.assert_allclose(c["N"], n_ref, atol=1e-14)
+    assert c["QL"] is ql
