@@ -1,5 +1,5 @@
 // Owner Shampoo: full left / right preconditioners with an inverse fourth root, on the owner's
-// whole matrices (fp32).
+// whole matrices.
 //
 // "MatrixFSDP: communication-free matrix optimizers under ZeRO-3 parameter sharding", §5.7:
 // with every 2D matrix whole on its owner, the owner can run Shampoo, with full left and
@@ -14,10 +14,13 @@
 //     T_k = (5 I - M_k) / 4,  X_{k+1} = X_k T_k,  M_{k+1} = T_k^4 M_k,
 // so M_k -> I and X_k -> A^{-1/4}; an eigenvalue ratio of 1e-8 converges in 26 iterations.
 //
-// Everything is a dense fp32 product, run by one batched SGEMM kernel on the CUDA cores
-// (fp32 FFMA, 128 x 128 output tiles, 8 x 8 outputs per thread, double-buffered shared
-// memory): a launch runs the same product for every owned matrix (blockIdx.z = matrix).
-// The iteration's T = (5I - M) / 4 is written by the epilogue of the product that forms M.
+// Two precisions.  fp32: every product is one batched SGEMM kernel on the CUDA cores (fp32
+// FFMA, 128 x 128 output tiles, 8 x 8 outputs per thread, double-buffered shared memory; a
+// launch runs the same product for every owned matrix, blockIdx.z = matrix), the iteration's
+// T = (5I - M) / 4 written by the epilogue of the product that forms M.  Split-bf16: the
+// statistics as above, the root iteration and P on the tensor cores through the
+// Newton-Schulz path's single-CTA split kernel (values held as bf16 pairs hi + lo, three MMAs
+// per product, fp32 accumulation), symmetric side products as upper-triangle tiles.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -239,7 +242,7 @@ __device__ __forceinline__ float join_bf16(uint16_t hi, uint16_t lo) {
 }
 
 struct SplitDesc {   // a rows x cols fp32 matrix (pitch lds) to / from a split pair (pitch ldd)
-  const float* src;  // nullable (prep, T-update): see the kernels
+  const float* src;
   uint16_t* hi;
   uint16_t* lo;
   int32_t rows, cols, lds, ldd;
@@ -290,7 +293,7 @@ __global__ void root_prep_split_kernel(const RootPrepDesc* descs) {
   }
 }
 
-// T = (5I - M) / 4 from the split M (hi, lo in `src` slots reinterpreted: see the host).
+// T = (5I - M) / 4 from the split M, as a split pair.
 struct TDesc {
   const uint16_t *m_hi, *m_lo;
   uint16_t *t_hi, *t_lo;
