@@ -239,7 +239,12 @@ typedef struct {
  *                             the tcgen05 tensor cores with split-bf16 operands (value = hi +
  *                             lo, three products per multiply, fp32 accumulation: about 16
  *                             significant bits per stored value, so the roots carry a relative
- *                             error near 1e-4 where the fp32 path reaches 1e-6).
+ *                             error near 1e-4 where the fp32 path reaches 1e-6).  It resolves
+ *                             statistics whose eigenvalues span about four decades: below
+ *                             ~1e-5 of the largest, bf16 pairs hold only rounding noise, which
+ *                             can be negative and make the iteration diverge (then the
+ *                             non-finite status below is set); use the fp32 precision, or a
+ *                             larger eps, for statistics spread wider than that.
  *
  * Buffers (DEVICE, fp32, caller-owned): `grad` and `weights` are the flat owner buffers the
  * matrix table's offsets index (grad = the deposited gradient, e.g. the reduced_grad_out of

@@ -136,3 +136,76 @@ class OwnerStep:
 
     def close(self):
         self.oset.close()
+
+
+class OwnerSecondOrderStep:
+    """The same owner placement with Shampoo or SOAP in place of Muon (§5.7: the optimizer is
+    swapped while placement and the gradient deposit stay).  One step: the W-way deposit (the
+    deposit kernel, whose fp32 reduced-gradient output is the gradient the optimizer reads;
+    its momentum and Newton-Schulz outputs go unused), the Shampoo or SOAP step of every owned
+    matrix, AdamW on the tail.
+
+    optimizer "shampoo": ``root_iters`` coupled-Newton steps per inverse fourth root,
+    ``precision`` mfsdp.SHAMPOO_FP32 or SHAMPOO_SPLIT_BF16, statistics from ``shampoo_eps`` I.
+    optimizer "soap": Adam moments with ``soap_betas`` and ``soap_eps``, statistics EMA with
+    ``beta_stats``, eigenbases refreshed every ``refresh_every`` steps (1: every step).
+    """
+
+    def __init__(self, shapes: Sequence[Tuple[int, int]], offsets: Sequence[int], n_tail: int,
+                 optimizer: str = "shampoo", device=None, root_iters: int = 30,
+                 precision: int = mfsdp.SHAMPOO_SPLIT_BF16, shampoo_eps: float = 1e-6,
+                 soap_betas=(0.9, 0.95), beta_stats: float = 0.95, soap_eps: float = 1e-8,
+                 refresh_every: int = 1, max_sweeps: int = 20):
+        if optimizer not in ("shampoo", "soap"):
+            raise ValueError("optimizer must be 'shampoo' or 'soap'")
+        self.optimizer = optimizer
+        self.base = OwnerStep(shapes, offsets, n_tail, split_max_numel=0, device=device)
+        dev = self.base.device
+        self.grad = torch.zeros(self.base.n, dtype=torch.float32, device=dev)
+        mats = [(r, c, o) for (r, c), o in zip(self.base.shapes, self.base.offsets)]
+        self.root_iters, self.precision = root_iters, precision
+        self.soap_betas, self.beta_stats, self.soap_eps = soap_betas, beta_stats, soap_eps
+        self.refresh_every, self.max_sweeps = max(1, refresh_every), max_sweeps
+        if optimizer == "shampoo":
+            self.opt = mfsdp.ShampooSet(mats)
+            self.ws = torch.empty(max(self.opt.workspace_bytes, 1), dtype=torch.uint8, device=dev)
+            self.l = torch.empty(max(self.opt.l_numel, 1), dtype=torch.float32, device=dev)
+            self.r = torch.empty(max(self.opt.r_numel, 1), dtype=torch.float32, device=dev)
+            self.opt.init_state(shampoo_eps, self.l, self.r, self.ws)
+        else:
+            self.opt = mfsdp.SoapSet(mats)
+            self.ws = torch.empty(max(self.opt.workspace_bytes, 1), dtype=torch.uint8, device=dev)
+            self.state = {k: torch.empty(max(n, 1), dtype=torch.float32, device=dev)
+                          for k, n in self.opt.state_sizes(self.base.n).items()}
+            self.opt.init_state(self.state, self.ws)
+        self.t = 0
+
+    @property
+    def weights(self):
+        return self.base.weights
+
+    @property
+    def tail_p(self):
+        return self.base.tail_p
+
+    def step(self, contribs, tail_contribs, hyper, stream=None):
+        """One owner step: deposit, Shampoo or SOAP on the owned matrices, AdamW on the tail.
+        Uses hyper.grad_scale, lr, weight_decay and the AdamW tail settings."""
+        self.t += 1
+        b = self.base
+        b.reduce_momentum(contribs, hyper, self.grad, stream)
+        if self.optimizer == "shampoo":
+            self.opt.step(self.grad, self.l, self.r, b.weights, hyper.lr, hyper.weight_decay,
+                          self.root_iters, self.ws, stream=stream, precision=self.precision)
+        else:
+            b1, b2 = self.soap_betas
+            self.opt.step(self.grad, b.weights, self.state, self.t, lr=hyper.lr, beta1=b1,
+                          beta2=b2, beta_stats=self.beta_stats, eps=self.soap_eps,
+                          weight_decay=hyper.weight_decay, max_sweeps=self.max_sweeps,
+                          workspace=self.ws, stream=stream,
+                          refresh=(self.t - 1) % self.refresh_every == 0)
+        b.adamw_tail(tail_contribs, hyper, self.t, stream)
+
+    def close(self):
+        self.opt.close()
+        self.base.close()
