@@ -414,6 +414,12 @@ def time_repack(wb, reps, stream, world=8):
 FFMA_PEAK_NOTE = "152 SMs x 128 fp32 lanes x 2 FLOP x the sampled SM clock"
 
 
+def _upper_tiles(d, tile=256):
+    """Output tiles of a d x d symmetric product that reach the upper triangle."""
+    nt = -(-d // tile)
+    return nt * (nt + 1) // 2
+
+
 def time_shampoo(device, reps=2, root_iters=30, precision=0):
     """Owner Shampoo step on one GPT-2-small layer's matrices (2304x768, 768x768, 3072x768,
     768x3072): statistics, 30 coupled-Newton steps for every inverse fourth root, the
@@ -447,9 +453,9 @@ def time_shampoo(device, reps=2, root_iters=30, precision=0):
         flops += 2 * r * r * c + 2 * r * c * c          # statistics
         flops += root_iters * 4 * 2 * (r ** 3 + c ** 3)  # roots
         flops += 2 * r * r * c + 2 * r * c * c          # P
-        # tensor path: symmetric side products keep the upper triangle, the last iteration
-        # forms X only, three MMAs per split product
-        sym = sum(d * (d + 1) * d for d in (r, c))
+        # tensor path: a symmetric side product runs the 256x256 output tiles that reach the
+        # upper triangle, the last iteration forms X only, three MMAs per split product
+        sym = sum(_upper_tiles(d) * 256 * 256 * 2 * (64 * -(-d // 64)) for d in (r, c))
         tensor += 3 * ((4 * (root_iters - 1) + 1) * sym + 2 * r * r * c + 2 * r * c * c)
     sset.close()
     return s.elapsed_time(e) / reps, flops, tensor
@@ -621,8 +627,8 @@ def run_ours(args, rank, world, local_rank):
             "frac": round(sflops / (sms_ * 1e-3) / 1e12 / ffma_peak, 4)}
         tms, tflops, texec = time_shampoo(dev, precision=1)
         line["shampoo_tc"] = {
-            "kernel": "ns_gemm_kernel<split> (tcgen05, split-bf16) for the roots and P; "
-                      "sgemm_batched_kernel for the statistics",
+            "kernel": "ns_gemm_pair_kernel<split> (tcgen05 CTA pairs, split-bf16) for the "
+                      "roots and P; sgemm_batched_kernel for the statistics",
             "what": what, "precision": "split_bf16",
             "ms": round(tms, 3), "flops": tflops, "bound": "tensor",
             "tensor_flops_executed": texec,

@@ -180,9 +180,13 @@ struct NsLaunchParams {
 };
 
 cudaError_t ns_prepare_kernels();  // set the dynamic shared memory attribute once per device
-int ns_pair_max_clusters(int num_sms);  // co-resident CTA pairs of the pair kernel (-1: error)
+// co-resident CTA pairs of the pair kernel, bf16 or split operands (-1: error)
+int ns_pair_max_clusters(int num_sms, bool split = false);
 // split: single-CTA kernel, `grid` CTAs; else the CTA-pair kernel, `grid` pairs.
 cudaError_t launch_ns_phase(const NsLaunchParams& p, bool split, int grid, cudaStream_t s);
+// The CTA-pair kernel with split (hi + lo) operands and outputs: 256 x 256 tiles (tiles built
+// with 256-row blocks), `pairs` pairs.
+cudaError_t launch_ns_pair_split(const NsLaunchParams& p, int pairs, cudaStream_t s);
 
 // 2D bf16 tensor map over a rows x cols row-major buffer of pitch ld elements (box_rows x
 // box_cols boxes; 128-byte swizzle, or 64-byte for the epilogue's store boxes) and the 3D

@@ -560,18 +560,24 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
 // Tensor memory is allocated by one warp of each CTA (cta_group::2) and both CTAs check that
 // they received the same base column before any work; on a mismatch the kernel records an
 // error and does nothing.
-struct PairCfg {
-  static constexpr int kStages = 6;
+// SPLIT: split-precision operands (hi and lo bf16 copies of both tiles in every stage, three
+// MMAs per k-step) and an epilogue that writes hi and lo rows directly, no staging.
+template <bool SPLIT>
+struct PairCfgT {
+  static constexpr int kOps = SPLIT ? 2 : 1;              // hi (+ lo) operand copies
+  static constexpr int kStages = SPLIT ? 3 : 6;
   static constexpr uint32_t kHalfA = 128 * kBK * 2;       // 16 KB: this CTA's A rows
   static constexpr uint32_t kHalfB = 128 * kBK * 2;       // 16 KB: this CTA's B rows
-  static constexpr uint32_t kStageBytes = kHalfA + kHalfB;
+  static constexpr uint32_t kLoOffset = kHalfA + kHalfB;  // the lo copies follow the hi ones
+  static constexpr uint32_t kStageBytes = kOps * (kHalfA + kHalfB);
   static constexpr uint32_t kStagingOffset = kStages * kStageBytes;
-  static constexpr uint32_t kStagingPerWarp = 2 * 32 * 32 * 2;  // a 32x32 block + its transpose
+  static constexpr uint32_t kStagingPerWarp = SPLIT ? 0 : 2 * 32 * 32 * 2;  // block + transpose
   static constexpr uint32_t kBarOffset = kStagingOffset + kEpiWarps * kStagingPerWarp;
   static constexpr uint32_t kSmem = 1024 + kBarOffset + 256;
   static constexpr uint32_t kTmemCols = 512;              // two 128 x 256 fp32 accumulators
   static constexpr int kAccs = kTmemCols / kBN;
 };
+using PairCfg = PairCfgT<false>;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -742,8 +748,9 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t cta_mask) 
       : "memory");
 }
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __grid_constant__ NsLaunchParams P) {
-  using C = PairCfg;
+  using C = PairCfgT<SPLIT>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // as in ns_gemm_kernel
@@ -810,6 +817,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
       cur.norm(P, npairs);
       uint32_t q = (uint32_t)par;  // position in the k-block sequence
       uint32_t armed = 0, last_par = 0;
+      int last_q = -1;             // the last k-block this lane issued
       for (;;) {
         bool act = cur.t < P.ntiles && !*abort_flag;
         if (!__any_sync(0xFu, act)) break;
@@ -823,7 +831,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
           const NsProblem& pr = P.probs[tile.prob];
           mp = P.maps + (opnd ? pr.map_b : pr.map_a);
           mn = opnd ? pr.b_mn : pr.a_mn;
-          view3 = (pr.mn3d >> opnd) & 1;
+          view3 = SPLIT ? 0 : (pr.mn3d >> opnd) & 1;
           r0 = opnd ? tile.tn * kBN + 128 * (int)rank : tile.tm * 256 + 128 * (int)rank;
           k0 = cur.kb * kBK;
           if (cur.kb == 0) prefetch_map(mp + (mn ? (view3 ? 2 : 0) : 1));
@@ -836,18 +844,40 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
         tma_load_pair_p(act && mn && !view3, dst, mp, r0, k0, fb);
         tma_load_pair_p(act && mn && !view3, dst + kBoxBytes, mp, r0 + 64, k0, fb);
         tma_load_pair_p(act && !mn, dst, mp + 1, k0, r0, fb);
+        if constexpr (SPLIT) {  // the lo copy of the same box, from the lo half's maps
+          const CUtensorMap* ml = mp + kMapsPerHalf;
+          const uint32_t dl = dst + C::kLoOffset;
+          tma_load_pair_p(act && mn, dl, ml, r0, k0, fb);
+          tma_load_pair_p(act && mn, dl + kBoxBytes, ml, r0 + 64, k0, fb);
+          tma_load_pair_p(act && !mn, dl, ml + 1, k0, r0, fb);
+        }
         if (act && opnd == 0) {
           armed |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (ph << stage);
+          last_q = (int)q;
         }
         q += 2;
         cur.kb += 2;
         cur.norm(P, npairs);
       }
       // teardown: the leader's full barriers count both CTAs' bytes
-      if (leader)
-        for (int st = 0; st < S; ++st)
-          if (armed & (1u << st)) mbar_wait(bar(full0 + st), (last_par >> st) & 1u, g, false);
+      if constexpr (S % 2 == 0) {
+        // an even stage count gives each parity lane its own stages
+        if (leader)
+          for (int st = 0; st < S; ++st)
+            if (armed & (1u << st)) mbar_wait(bar(full0 + st), (last_par >> st) & 1u, g, false);
+      } else {
+        // an odd stage count makes the two parity lanes share stages, so a lane's own record
+        // can be a phase behind: every k-block q < n was issued (even ones by lane 0, odd
+        // ones by lane 2), and stage st last held k-block st + S floor((n - 1 - st) / S)
+        const int l0 = __shfl_sync(0xFu, last_q, 0), l2 = __shfl_sync(0xFu, last_q, 2);
+        const int n = max(l0, l2) + 1;
+        if (leader && lane == 0)
+          for (int st = 0; st < S && st < n; ++st) {
+            const int ql = st + S * ((n - 1 - st) / S);
+            mbar_wait(bar(full0 + st), (uint32_t)((ql / S) & 1), g, false);
+          }
+      }
     }
   } else if (warp == 1 && lane == 0 && leader) {
     // ------------------------------------------------------------ MMA issuer (leader only)
@@ -871,9 +901,14 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
         const uint32_t sa = sbase + (uint32_t)stage * C::kStageBytes;
         const uint32_t sbb = sa + C::kHalfA;
 #pragma unroll
-        for (int j = 0; j < kBK / 16; ++j)
-          tc_mma_pair(d_tmem, operand_desc(sa, a_mn, j), operand_desc(sbb, b_mn, j), idesc,
-                      (kb | j) != 0);
+        for (int j = 0; j < kBK / 16; ++j) {
+          const uint64_t ad = operand_desc(sa, a_mn, j), bd = operand_desc(sbb, b_mn, j);
+          tc_mma_pair(d_tmem, ad, bd, idesc, (kb | j) != 0);
+          if constexpr (SPLIT) {
+            tc_mma_pair(d_tmem, ad, operand_desc(sbb + C::kLoOffset, b_mn, j), idesc, 1u);
+            tc_mma_pair(d_tmem, operand_desc(sa + C::kLoOffset, a_mn, j), bd, idesc, 1u);
+          }
+        }
         tc_commit_pair(bar(empty0 + stage), 0x3);
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
@@ -883,6 +918,83 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
     }
     tc_commit_pair(bar(drain), 0x1);
     mbar_wait(bar(drain), 0u, g, false);
+  } else if (warp >= 2 && SPLIT) {
+    // ------------------------------------------------------------ epilogue, split outputs
+    // One row per lane: the fp32 accumulator, combined with the addend (its hi + lo rows),
+    // is rounded to a hi and a lo bf16 part and both are stored directly; a symmetric output
+    // stores the columns >= r of row r and mirrors the columns > r.
+    const int quarter = warp & 3;
+    const int c_first = ((warp - 2) >> 2) * kEpiChunks;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = pair; t < P.ntiles; t += npairs) {
+      const NsTile tile = P.tiles[t];
+      const NsProblem& pr = P.probs[tile.prob];
+      const int M = pr.M, N = pr.N, kind = pr.kind, sym = pr.sym;
+      const int m0 = tile.tm * 256 + 128 * (int)rank, n0 = tile.tn * kBN;
+      const int rw = m0 + quarter * 32, r = rw + lane;
+      const bool rvalid = r < M;
+      const float s = 1.f / (P.norm[pr.mat] + P.eps);
+      if (!mbar_wait(bar(tfull0 + acc), acc_phase, g)) break;
+      tc_fence_after();
+      float alpha = 1.f, beta = 0.f;
+      if (kind == kGram) {
+        alpha = pr.first ? s * s : 1.f;
+      } else if (kind == kPoly) {
+        alpha = P.c;
+        beta = P.b;
+      } else {
+        alpha = pr.first ? s : 1.f;
+        beta = P.a * alpha;
+      }
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
+#pragma unroll 1
+      for (int q = 0; q < kEpiChunks; ++q) {
+        const int cc = c_first + q, c0 = n0 + cc * 32;
+        if (c0 >= N || rw >= M) break;                 // warp-uniform
+        if (sym && c0 + 31 < rw) continue;             // chunk entirely below the diagonal
+        uint32_t a32[32];
+        tc_ld32_issue(taddr + (uint32_t)(cc * 32), a32);
+        tc_ld_wait(a32);
+        if (!rvalid) continue;
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(a32[j]);
+        if (beta != 0.f) {
+          float d[32], dl[32];
+          load_row32(pr.d_hi, pr.ldd, r, c0, N, d);
+          load_row32(pr.d_lo, pr.ldd, r, c0, N, dl);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = fmaf(alpha, v[j], beta * (d[j] + dl[j]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= alpha;
+        }
+        uint16_t h[32], l[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          h[j] = f2bf(v[j]);
+          l[j] = f2bf(v[j] - bf2f(h[j]));
+        }
+        const int cmin = sym ? r : 0;
+        store_row32(pr.o_hi, pr.ldo, r, c0, cmin, N, h);
+        store_row32(pr.o_lo, pr.ldo, r, c0, cmin, N, l);
+        if (sym && c0 + 31 > r) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c = c0 + j;
+            if (c > r && c < N) {
+              pr.o_hi[(int64_t)c * pr.ldo + r] = h[j];
+              pr.o_lo[(int64_t)c * pr.ldo + r] = l[j];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_rank(bar(tempty0 + acc), 0));
+      if (++acc == C::kAccs) { acc = 0; acc_phase ^= 1u; }
+    }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     // Warp w covers TMEM lane quarter (w & 3), i.e. 32 rows of the CTA's 128, and four
@@ -1094,19 +1206,22 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
 
 
 cudaError_t ns_prepare_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel,
+  cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)PairCfg::kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ns_gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)PairCfgT<true>::kSmem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(ns_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)Cfg<true>::kSmem);
 }
 
-int ns_pair_max_clusters(int num_sms) {
+int ns_pair_max_clusters(int num_sms, bool split) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
   cfg.blockDim = dim3(kNsThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg::kSmem;
+  cfg.dynamicSmemBytes = split ? PairCfgT<true>::kSmem : PairCfg::kSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -1115,8 +1230,10 @@ int ns_pair_max_clusters(int num_sms) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, ns_gemm_pair_kernel, &cfg) != cudaSuccess) return -1;
-  return n;
+  const cudaError_t e = split
+      ? cudaOccupancyMaxActiveClusters(&n, ns_gemm_pair_kernel<true>, &cfg)
+      : cudaOccupancyMaxActiveClusters(&n, ns_gemm_pair_kernel<false>, &cfg);
+  return e == cudaSuccess ? n : -1;
 }
 
 cudaError_t launch_ns_phase(const NsLaunchParams& p, bool split, int grid, cudaStream_t s) {
@@ -1145,7 +1262,27 @@ cudaError_t launch_ns_phase(const NsLaunchParams& p, bool split, int grid, cudaS
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel, p);
+  return cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel<false>, p);
+}
+
+cudaError_t launch_ns_pair_split(const NsLaunchParams& p, int pairs, cudaStream_t s) {
+  if (p.ntiles <= 0) return cudaSuccess;
+  pairs = std::max(1, std::min(p.ntiles, pairs));
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(kNsThreads, 1, 1);
+  cfg.dynamicSmemBytes = PairCfgT<true>::kSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel<true>, p);
 }
 
 }  // namespace mfsdp

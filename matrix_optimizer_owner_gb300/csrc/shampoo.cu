@@ -19,8 +19,9 @@
 // launch runs the same product for every owned matrix, blockIdx.z = matrix), the iteration's
 // T = (5I - M) / 4 written by the epilogue of the product that forms M.  Split-bf16: the
 // statistics as above, the root iteration and P on the tensor cores through the
-// Newton-Schulz path's single-CTA split kernel (values held as bf16 pairs hi + lo, three MMAs
-// per product, fp32 accumulation), symmetric side products as upper-triangle tiles.
+// Newton-Schulz path's CTA-pair kernel in its split mode (values held as bf16 pairs hi + lo,
+// three MMAs per product, fp32 accumulation, 256 x 256 tiles), symmetric side products as
+// upper-triangle tiles.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -370,6 +371,7 @@ struct mfsdp_shampoo_set {
   std::vector<int32_t> side_ld, mat_ld;
   size_t tc_off_norms = 0, tc_off_fnorm = 0, tc_off_tables = 0, tc_table_bytes = 0;
   size_t tc_ws_bytes = 0;
+  mutable int tc_pairs = 0, tc_pairs_dev = -1;  // co-resident pairs of the split pair kernel
   int max_rows() const {
     int64_t v = 0;
     for (const auto& m : mats) v = std::max(v, m.rows);
@@ -467,7 +469,7 @@ void tc_tables(const mfsdp_shampoo_set* s, uint8_t* base, int root_iters, TcTabl
   for (int l = 0; l < kTcLaunches; ++l)
     for (size_t q = 0; q < tt.probs[l].size(); ++q) {
       const NsProblem& p = tt.probs[l][q];
-      add_tiles(tt.tiles[l], (int32_t)q, p.M, p.N, p.sym != 0, kBM);
+      add_tiles(tt.tiles[l], (int32_t)q, p.M, p.N, p.sym != 0, kPairBM);
       if ((l == kXT0 || l == kXT1) && q + 1 == (size_t)(2 * n))
         tt.x_tiles[l == kXT1] = (int32_t)tt.tiles[l].size();
     }
@@ -701,6 +703,12 @@ int shampoo_step_split(const mfsdp_shampoo_set* set, const float* grad, float* l
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return MFSDP_ECUDA;
+  if (set->tc_pairs <= 0 || set->tc_pairs_dev != dev) {
+    set->tc_pairs = ns_pair_max_clusters(sms, true);
+    set->tc_pairs_dev = dev;
+    if (set->tc_pairs <= 0) return MFSDP_ECUDA;
+  }
+  const int pairs = set->tc_pairs;
   int* status = status_word_address();
   if (status == nullptr) return MFSDP_ECUDA;
 
@@ -717,7 +725,7 @@ int shampoo_step_split(const mfsdp_shampoo_set* set, const float* grad, float* l
     lp.c = 1.f;
     lp.wait_limit_ns = wait_limit_ns();
     lp.status = status;
-    return launch_ns_phase(lp, true, std::min(ntiles, sms), st) == cudaSuccess;
+    return launch_ns_pair_split(lp, pairs, st) == cudaSuccess;
   };
   auto all = [&](int q) { return (int32_t)tt.tiles[q].size(); };
   const unsigned nb = (unsigned)n;
