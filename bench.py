@@ -58,7 +58,7 @@ NS_TRAFFIC_SOURCES = ("matrix_optimizer_owner_gb300/csrc/ns_gemm.cu",
                       "matrix_optimizer_owner_gb300/csrc/mfsdp_internal.h")
 NS_TRAFFIC = {
     # config index: (sources sha256, bytes per launch, profile summary)
-    1: ("6a63a09e508998d8c4f12dd71c25f05a2484edfe6fde69933d067fec2418e4a1", 208883128,
+    1: ("8315436d1345252bd2113557d77646727f05dfcc13ac7795d921205e395e9ddd", 208986341,
         "profiles/owner_step_gpt2_small_launch_list.md"),
 }
 

@@ -415,9 +415,39 @@ struct TcTables {
   int32_t x_tiles[2] = {0, 0};  // leading X' tiles of kXT0 / kXT1
 };
 
+// Orders tiles [from, end) of a launch for the pair kernel's static schedule, in which pair p
+// runs table entries p, p + P, p + 2P, ...  The sides' contraction lengths differ (768 … 3072
+// on a transformer layer), so the plain order can leave one pair with well over the average
+// work.  Wave by wave (P consecutive entries, one per pair), the longest remaining tiles go to
+// the pairs with the least work so far; `load` carries each pair's work in k-blocks (plus a
+// fixed cost for the epilogue) from the entries before `from`.
+void balance_tiles(std::vector<NsTile>& tiles, size_t from, const std::vector<NsProblem>& probs,
+                   int P, std::vector<int64_t>& load) {
+  constexpr int64_t kTileFixed = 2;  // the epilogue's share of a tile, in k-block units
+  auto cost = [&](const NsTile& t) { return (probs[(size_t)t.prob].K + 63) / 64 + kTileFixed; };
+  std::stable_sort(tiles.begin() + (std::ptrdiff_t)from, tiles.end(),
+                   [&](const NsTile& x, const NsTile& y) { return cost(x) > cost(y); });
+  std::vector<size_t> pos;
+  for (size_t i0 = from; i0 < tiles.size(); i0 += (size_t)P) {
+    const size_t w = std::min((size_t)P, tiles.size() - i0);
+    const std::vector<NsTile> wave(tiles.begin() + (std::ptrdiff_t)i0,
+                                   tiles.begin() + (std::ptrdiff_t)(i0 + w));
+    pos.resize(w);
+    for (size_t j = 0; j < w; ++j) pos[j] = i0 + j;
+    std::stable_sort(pos.begin(), pos.end(),
+                     [&](size_t a, size_t b) { return load[a % P] < load[b % P]; });
+    for (size_t j = 0; j < w; ++j) {
+      tiles[pos[j]] = wave[j];
+      load[pos[j] % P] += cost(wave[j]);
+    }
+  }
+}
+
 // Problems and tiles of every split-kernel launch; buffer addresses from the workspace `base`,
-// or null when only the counts are wanted.
-void tc_tables(const mfsdp_shampoo_set* s, uint8_t* base, int root_iters, TcTables& tt) {
+// or null when only the counts are wanted.  With `pairs` > 0 each launch's tiles are ordered
+// for that many co-resident CTA pairs (any order gives the same result).
+void tc_tables(const mfsdp_shampoo_set* s, uint8_t* base, int root_iters, int pairs,
+               TcTables& tt) {
   const int n = (int)s->mats.size();
   auto sbuf = [&](int k, int b, int h) -> uint16_t* {
     if (!base) return nullptr;
@@ -473,6 +503,23 @@ void tc_tables(const mfsdp_shampoo_set* s, uint8_t* base, int root_iters, TcTabl
       if ((l == kXT0 || l == kXT1) && q + 1 == (size_t)(2 * n))
         tt.x_tiles[l == kXT1] = (int32_t)tt.tiles[l].size();
     }
+  if (pairs <= 0) return;
+  for (int l = 0; l < kTcLaunches; ++l) {
+    std::vector<int64_t> load((size_t)pairs, 0);
+    auto& t = tt.tiles[l];
+    if (l == kXT0 || l == kXT1) {
+      // the X' tiles stay a prefix (the last iteration runs them alone), balanced on their
+      // own; the T^2 tiles continue from the loads they leave
+      const size_t x = (size_t)tt.x_tiles[l == kXT1];
+      std::vector<NsTile> rest(t.begin() + (std::ptrdiff_t)x, t.end());
+      t.resize(x);
+      balance_tiles(t, 0, tt.probs[l], pairs, load);
+      t.insert(t.end(), rest.begin(), rest.end());
+      balance_tiles(t, x, tt.probs[l], pairs, load);
+    } else {
+      balance_tiles(t, 0, tt.probs[l], pairs, load);
+    }
+  }
 }
 
 size_t tc_table_bytes(const TcTables& tt, int n) {
@@ -506,7 +553,7 @@ void tc_layout(mfsdp_shampoo_set* s) {
   s->tc_off_tables = align256(s->tc_off_fnorm + sizeof(float) * 2 * (size_t)std::max(n, 1));
   s->tc_off_tables = (s->tc_off_tables + 1023) & ~size_t(1023);  // tensor maps: 64-byte aligned
   TcTables tt;
-  tc_tables(s, nullptr, 1, tt);
+  tc_tables(s, nullptr, 1, 0, tt);
   s->tc_table_bytes = tc_table_bytes(tt, std::max(n, 1));
   s->tc_ws_bytes = align256(s->tc_off_tables + s->tc_table_bytes);
 }
@@ -609,8 +656,19 @@ int shampoo_step_split(const mfsdp_shampoo_set* set, const float* grad, float* l
                        float* weights, float lr, float weight_decay, int32_t root_iters,
                        uint8_t* ws, cudaStream_t st) {
   const int n = (int)set->mats.size();
+  if (ns_prepare_kernels() != cudaSuccess) return MFSDP_ECUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MFSDP_ECUDA;
+  if (set->tc_pairs <= 0 || set->tc_pairs_dev != dev) {
+    set->tc_pairs = ns_pair_max_clusters(sms, true);
+    set->tc_pairs_dev = dev;
+    if (set->tc_pairs <= 0) return MFSDP_ECUDA;
+  }
+  const int pairs = set->tc_pairs;
   TcTables tt;
-  tc_tables(set, ws, root_iters, tt);
+  tc_tables(set, ws, root_iters, pairs, tt);
   double* norms = reinterpret_cast<double*>(ws + set->tc_off_norms);
   float* fnorm = reinterpret_cast<float*>(ws + set->tc_off_fnorm);
   auto sbuf = [&](int k, int b, int h) {
@@ -698,17 +756,6 @@ int shampoo_step_split(const mfsdp_shampoo_set* set, const float* grad, float* l
   if (cudaMemcpyAsync(tab, host.data(), at, cudaMemcpyHostToDevice, st) != cudaSuccess ||
       cudaMemsetAsync(fnorm, 0, sizeof(float) * 2 * (size_t)n, st) != cudaSuccess)
     return MFSDP_ECUDA;
-  if (ns_prepare_kernels() != cudaSuccess) return MFSDP_ECUDA;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return MFSDP_ECUDA;
-  if (set->tc_pairs <= 0 || set->tc_pairs_dev != dev) {
-    set->tc_pairs = ns_pair_max_clusters(sms, true);
-    set->tc_pairs_dev = dev;
-    if (set->tc_pairs <= 0) return MFSDP_ECUDA;
-  }
-  const int pairs = set->tc_pairs;
   int* status = status_word_address();
   if (status == nullptr) return MFSDP_ECUDA;
 

@@ -363,23 +363,40 @@ __device__ __forceinline__ void mm64_tn(const float (*P)[kALd], const float (*Q)
   }
 }
 
+constexpr int kZTiles = 4;  // 64-column tiles of Z^T one apply CTA updates with the same J_p
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // 64 x 64 block of a row-major global matrix (pitch ld) into shared memory: rows rowi(r),
-// columns coli(c), 4 consecutive columns at a time (they never straddle a 32-block).
+// columns coli(c), 4 consecutive columns at a time (they never straddle a 32-block).  The
+// copies are asynchronous (16-byte cp.async): the caller commits and waits for them.
 template <typename RowF, typename ColF>
 __device__ __forceinline__ void load_block(float (*dst)[kALd], const float* src, int64_t ld,
                                            RowF rowi, ColF coli) {
   for (int e = threadIdx.x; e < kJP * kJP / 4; e += kJThreads) {
     const int r = e / (kJP / 4), c = (e % (kJP / 4)) * 4;
-    *reinterpret_cast<float4*>(&dst[r][c]) =
-        *reinterpret_cast<const float4*>(src + (int64_t)rowi(r) * ld + coli(c));
+    cp_async16(&dst[r][c], src + (int64_t)rowi(r) * ld + coli(c));
   }
 }
 
 // The round's rotations applied; compact grid, blocks [begin[k], begin[k + 1]) for side k.
 // Its blocks [0, P(P+1)/2) update A's block pair (p, q), p <= q: Y = Jp^T (A_pq Jq), with
 // A_pq Jq formed from the mirrored block (A is symmetric), Y written to (p, q) and Y^T to
-// (q, p).  Blocks [P(P+1)/2, P(P+1)/2 + P^2) update the rows I_p of Z^T over one 64-column
-// tile: Z^T <- Jp^T Z^T.
+// (q, p).  The next P ceil(P / kZTiles) blocks update the rows I_p of Z^T, Z^T <- Jp^T Z^T,
+// over kZTiles 64-column tiles each: J_p stays in shared memory and the tiles stream through
+// two buffers, the next one loading while the current one is multiplied.
 __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* sides,
                                                                  const int32_t* begin,
                                                                  int nsides,
@@ -413,6 +430,8 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
     load_block(B0, s.a, s.dp, [&](int r) { return idx(q, r); }, [&](int c) { return idx(p, c); });
     load_block(B1, jp, kJP, [](int r) { return r; }, [](int c) { return c; });
     load_block(B2, jq, kJP, [](int r) { return r; }, [](int c) { return c; });
+    cp_async_commit();
+    cp_async_wait<0>();
     __syncthreads();
     mm64_tn(B0, B2, ty, tx, acc);  // W = A_pq Jq
     __syncthreads();               // B0 is free: W goes there
@@ -437,23 +456,32 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
       }
     }
   } else {
-    const int e0 = bid - na, t = e0 / P, p = e0 % P;
+    const int e0 = bid - na, c = e0 / P, p = e0 % P;
     if (!s.rot[p]) return;
     if (tid < kJP) ip[tid] = pair_index(nb, round, p, tid);
     __syncthreads();
-    auto idx = [&](int, int c) { return ip[c]; };
+    const int t0 = c * kZTiles, t1 = min(P, t0 + kZTiles);
+    auto rows = [&](int r) { return ip[r]; };
     const float* jp = s.j + (int64_t)p * kJP * kJP;
-    // B0[k][j] = Z^T[I_p(k)][64 t + j]
-    load_block(B0, s.zt, s.dp, [&](int r) { return idx(p, r); },
-               [&](int c) { return t * kJP + c; });
+    // B1 = J_p; B0 and B2 take turns holding a tile, B[k][j] = Z^T[I_p(k)][64 t + j]
     load_block(B1, jp, kJP, [](int r) { return r; }, [](int c) { return c; });
-    __syncthreads();
-    mm64_tn(B1, B0, ty, tx, acc);  // Jp^T Z^T_p
+    load_block(B0, s.zt, s.dp, rows, [&](int c) { return t0 * kJP + c; });
+    cp_async_commit();
+    for (int t = t0; t < t1; ++t) {
+      float (*cur)[kALd] = ((t - t0) & 1) ? B2 : B0;
+      float (*nxt)[kALd] = ((t - t0) & 1) ? B0 : B2;
+      if (t + 1 < t1) load_block(nxt, s.zt, s.dp, rows, [&](int c) { return (t + 1) * kJP + c; });
+      cp_async_commit();
+      cp_async_wait<1>();  // everything but the next tile has landed
+      __syncthreads();
+      mm64_tn(B1, cur, ty, tx, acc);  // Jp^T Z^T_p over tile t
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int gr = idx(p, 4 * ty + i);
-      *reinterpret_cast<float4*>(s.zt + (int64_t)gr * s.dp + t * kJP + 4 * tx) =
-          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      for (int i = 0; i < 4; ++i) {
+        const int gr = ip[4 * ty + i];
+        *reinterpret_cast<float4*>(s.zt + (int64_t)gr * s.dp + t * kJP + 4 * tx) =
+            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      }
+      __syncthreads();  // cur is free: the next iteration loads into it
     }
   }
 }
@@ -806,7 +834,7 @@ void soap_fill(const mfsdp_soap_set* set, const mfsdp_soap_state* st, uint8_t* w
       tb.solve_begin[g].push_back(sb);
       tb.apply_begin[g].push_back(ab);
       sb += P;
-      ab += P * (P + 1) / 2 + P * P;
+      ab += P * (P + 1) / 2 + P * ((P + kZTiles - 1) / kZTiles);
     }
     tb.solve_begin[g].push_back(sb);
     tb.apply_begin[g].push_back(ab);
