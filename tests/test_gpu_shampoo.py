@@ -95,6 +95,13 @@ def test_ragged_shapes(precision):
 
 
 @PRECISIONS
+def test_ragged_sides_over_several_tiles(precision):
+    """Sides of 300 and 520: two and three 256-row tiles of the CTA-pair products, each with
+    a ragged last tile (and 64-wide k-blocks with a ragged last one)."""
+    _check([(300, 520), (520, 300)], 2, 4, precision)
+
+
+@PRECISIONS
 def test_gpt2_small_shapes_one_step(precision):
     _check([(2304, 768), (768, 768), (3072, 768), (768, 3072)], 1, 3, precision)
 
