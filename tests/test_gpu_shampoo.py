@@ -97,8 +97,9 @@ def test_ragged_shapes(precision):
 @PRECISIONS
 def test_ragged_sides_over_several_tiles(precision):
     """Sides of 300 and 520: two and three 256-row tiles of the CTA-pair products, each with
-    a ragged last tile (and 64-wide k-blocks with a ragged last one)."""
-    _check([(300, 520), (520, 300)], 2, 4, precision)
+    a ragged last tile (and 64-wide k-blocks with a ragged last one); a side of 257, whose
+    second tile has one row, so that the second CTA of its pair lies wholly outside it."""
+    _check([(300, 520), (520, 300), (257, 130)], 2, 4, precision)
 
 
 @PRECISIONS
