@@ -4,16 +4,15 @@ the same input values (copied back from the device)."""
 
 from __future__ import annotations
 
-from dataclasses import dataclass, field
-from typing import Dict, List, Optional, Sequence, Tuple
+from dataclasses import dataclass
+from typing import Dict, List, Optional, Tuple
 
 import numpy as np
 import torch
 
-from oracle import adamw as oadamw
 from oracle import step as ostep
 from workloads import synth
-from workloads.configs import Hyper, ParamSpec, Workload
+from workloads.configs import Hyper, Workload
 
 from matrix_optimizer_owner_gb300 import owner_step
 

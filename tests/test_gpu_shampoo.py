@@ -18,7 +18,6 @@ import pytest
 import torch
 
 from oracle import shampoo as oshampoo
-from workloads import get_config, synth
 
 pytestmark = pytest.mark.gpu
 

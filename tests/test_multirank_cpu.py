@@ -11,7 +11,6 @@ rank-dependent time is checked.
 import os
 import socket
 
-import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
