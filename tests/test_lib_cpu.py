@@ -26,7 +26,8 @@ def lib():
 
 
 def header_functions():
-    src = open(os.path.join(ROOT, "include", "mfsdp.h")).read()
+    with open(os.path.join(ROOT, "include", "mfsdp.h"), encoding="utf-8") as f:
+        src = f.read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(mfsdp_\w+)\s*\(", src)))
 
