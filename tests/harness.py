@@ -75,7 +75,7 @@ def case_from_workload(wl: Workload) -> Case:
                 wl.weight_std, wl.index, wl, lay.matrices, lay.tails, lay.tail_offsets)
 
 
-class GpuRun:
+class DeviceRun:
     """Runs owner steps on the device and keeps host copies of every intermediate."""
 
     def __init__(self, case: Case, split_max_numel=owner_step.DEFAULT_SPLIT_MAX_NUMEL,
@@ -140,7 +140,7 @@ class GpuRun:
         return arr[off:off + rr * cc].reshape(rr, cc)
 
 
-def oracle_matrix(run: GpuRun, init, k: int, steps: int):
+def oracle_matrix(run: DeviceRun, init, k: int, steps: int):
     """The oracle's trajectory of matrix k on the same (device-drawn) inputs."""
     c = run.case
     W0 = run.mat(init["W"], k)
@@ -148,7 +148,7 @@ def oracle_matrix(run: GpuRun, init, k: int, steps: int):
     return ostep.muon_trajectory(W0, contribs_at, steps, c.hyper)
 
 
-def oracle_tail(run: GpuRun, init, steps: int):
+def oracle_tail(run: DeviceRun, init, steps: int):
     c = run.case
     return ostep.adamw_trajectory(init["p"], lambda t: run.history[t]["tail_contrib"], steps,
                                   c.hyper)

@@ -17,7 +17,7 @@ from oracle import muon as omuon
 from workloads import get_config
 from workloads.configs import Hyper
 
-from harness import GpuRun, case_from_shapes, case_from_workload, max_rel, oracle_matrix, \
+from harness import DeviceRun, case_from_shapes, case_from_workload, max_rel, oracle_matrix, \
     oracle_tail, rel
 
 pytestmark = pytest.mark.gpu
@@ -48,7 +48,7 @@ def derived_w_tol(ref, t, hp, shape):
     return max(TOL_W, 1.25 * TOL_NS_BF16 * step / np.linalg.norm(ref[t]["W"]))
 
 
-def check_run(run: GpuRun, init, steps, ns_tol_bf16=TOL_NS_BF16, check_stream=True, mats=None,
+def check_run(run: DeviceRun, init, steps, ns_tol_bf16=TOL_NS_BF16, check_stream=True, mats=None,
               derive_w_tol=False):
     """derive_w_tol: for matrices forced onto bf16 operands whose update is a large fraction of
     the weight (small matrices), bound the weight error by the NS bound instead of 1e-3."""
@@ -101,7 +101,7 @@ def check_run(run: GpuRun, init, steps, ns_tol_bf16=TOL_NS_BF16, check_stream=Tr
 def test_tiny_workload_three_steps():
     wl = get_config(0)
     case = case_from_workload(wl)
-    run = GpuRun(case)
+    run = DeviceRun(case)
     assert run.runner.oset.split_count() == 4
     init = run.run(wl.steps)
     check_run(run, init, wl.steps)
@@ -110,7 +110,7 @@ def test_tiny_workload_three_steps():
 def test_gpt2_small_workload_three_steps():
     wl = get_config(1)
     case = case_from_workload(wl)
-    run = GpuRun(case)
+    run = DeviceRun(case)
     assert run.runner.oset.split_count() == 0
     init = run.run(wl.steps)
     check_run(run, init, wl.steps)
@@ -122,7 +122,7 @@ def test_multi_tile_and_ragged_shapes(dtype):
     # multiple of 64; a matrix with m spanning 3 row tiles.
     shapes = [(384, 640), (640, 384), (300, 700), (700, 300), (200, 136), (136, 200),
               (257, 520), (520, 257), (512, 512)]
-    run = GpuRun(case_from_shapes(shapes, W=3, dtype=dtype, grad_std=1e-3, n_tail=1000, seed=3),
+    run = DeviceRun(case_from_shapes(shapes, W=3, dtype=dtype, grad_std=1e-3, n_tail=1000, seed=3),
                  split_max_numel=0)
     init = run.run(2)
     check_run(run, init, 2, derive_w_tol=True)
@@ -133,7 +133,7 @@ def test_unaligned_tiny_and_empty_matrices():
     # an empty matrix, and both precisions in one set.
     shapes = [(1, 64), (64, 1), (3, 5), (100, 100), (0, 7), (33, 70), (70, 33), (96, 200),
               (130, 129)]
-    run = GpuRun(case_from_shapes(shapes, W=2, dtype=torch.bfloat16, grad_std=1e-2, n_tail=37,
+    run = DeviceRun(case_from_shapes(shapes, W=2, dtype=torch.bfloat16, grad_std=1e-2, n_tail=37,
                                   seed=5, gaps=True), split_max_numel=4000)
     assert 0 < run.runner.oset.split_count() < len(shapes) - 1
     init = run.run(2)
@@ -146,14 +146,14 @@ def test_heavy_tailed_gradient_scales():
     stds = [1e-5, 1e-4, 1e-3, 1e-2, 1e-1, 3e-5]
     case = case_from_shapes(shapes, W=4, dtype=torch.bfloat16, seed=7)
     case.grad_std = stds
-    run = GpuRun(case, split_max_numel=0)
+    run = DeviceRun(case, split_max_numel=0)
     init = run.run(2)
     check_run(run, init, 2, derive_w_tol=True)
 
 
 def test_non_nesterov_and_match_rms():
     hp = Hyper(nesterov=False, lr_adjust="match_rms_adamw", lr=1e-3, momentum=0.5, ns_steps=2)
-    run = GpuRun(case_from_shapes([(256, 128), (128, 384)], W=2, dtype=torch.bfloat16,
+    run = DeviceRun(case_from_shapes([(256, 128), (128, 384)], W=2, dtype=torch.bfloat16,
                                   grad_std=1e-3, n_tail=64, seed=9, hyper=hp), split_max_numel=0)
     init = run.run(2)
     check_run(run, init, 2, derive_w_tol=True)
@@ -163,7 +163,7 @@ def test_bitwise_deterministic():
     shapes = [(384, 640), (640, 384), (64, 64)]
     outs = []
     for _ in range(2):
-        run = GpuRun(case_from_shapes(shapes, W=4, dtype=torch.bfloat16, grad_std=1e-3,
+        run = DeviceRun(case_from_shapes(shapes, W=4, dtype=torch.bfloat16, grad_std=1e-3,
                                       n_tail=100, seed=11))
         run.run(2)
         h = run.history[-1]
@@ -179,7 +179,7 @@ def test_status_timeout_and_nonfinite():
     assert mfsdp.mfsdp_query_status() == -7
     assert mfsdp.mfsdp_query_status() == 0        # read clears it
     # the context is still usable, and a non-finite gradient is reported
-    run = GpuRun(case_from_shapes([(64, 64)], W=1, dtype=torch.float32))
+    run = DeviceRun(case_from_shapes([(64, 64)], W=1, dtype=torch.float32))
     contribs, _ = run.contributions(0)
     contribs[0][5] = float("inf")
     run.runner.reduce_momentum(contribs, run.case.hyper)
