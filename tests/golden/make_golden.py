@@ -17,7 +17,7 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, os.path.dirname(os.path.dirname(HERE)))
 
-from oracle import muon, plan, soap  # noqa: E402
+from oracle import muon, plan, shampoo, soap  # noqa: E402
 from workloads import get_config  # noqa: E402
 
 SOURCE = ('"MatrixFSDP: communication-free matrix optimizers under ZeRO-3 parameter '
@@ -31,6 +31,24 @@ def ns_input():
 def soap_inputs():
     rng = np.random.default_rng(5)
     return [rng.normal(size=(5, 7)) * 1e-2 for _ in range(3)], rng.normal(size=(5, 7)) * 0.02
+
+
+def shampoo_inputs():
+    rng = np.random.default_rng(7)
+    return [rng.normal(size=(6, 4)) * 1e-2 for _ in range(3)], rng.normal(size=(6, 4)) * 0.02
+
+
+SHAMPOO_EPS = 1e-6
+SHAMPOO_HYPER = dict(grad_scale=1.0, lr=0.02, weight_decay=1e-2)
+
+
+def shampoo_run():
+    gs, w = shampoo_inputs()
+    l, r = SHAMPOO_EPS * np.eye(6), SHAMPOO_EPS * np.eye(4)
+    for g in gs:
+        o = shampoo.shampoo_matrix_step(w, l, r, [g], **SHAMPOO_HYPER)
+        w, l, r = o["W"], o["L"], o["R"]
+    return w
 
 
 SOAP_HYPER = dict(grad_scale=1.0, lr=1e-3, weight_decay=1e-2, beta1=0.9, beta2=0.95, eps=1e-6,
@@ -75,6 +93,13 @@ def main():
                   "(3.4445, -4.7750, 2.0315), X0 = U / (||U||_F + 1e-7)",
                   "input: numpy default_rng(3).normal(size=(8, 12)) * 0.1"],
                  muon.newton_schulz(ns_input()))
+    write_matrix(os.path.join(HERE, "shampoo_6x4_3steps_seed7.txt"),
+                 [f"{SOURCE}, §5.7: Shampoo (full left and right preconditioners, inverse "
+                  "fourth roots), W after 3 steps",
+                  "inputs: numpy default_rng(7): three normal(size=(6, 4)) * 1e-2 gradients, "
+                  "then W0 = normal(size=(6, 4)) * 0.02; L = 1e-6 I, R = 1e-6 I",
+                  "lr 0.02, wd 1e-2, grad_scale 1"],
+                 shampoo_run())
     gs, w0 = soap_inputs()
     st = {"W": w0, "L": np.zeros((5, 5)), "R": np.zeros((7, 7)), "M": np.zeros((5, 7)),
           "V": np.zeros((5, 7))}

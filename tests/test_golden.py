@@ -84,3 +84,9 @@ def test_soap_fixture():
                                    **mg.SOAP_HYPER)
     np.testing.assert_allclose(st["W"], _read_matrix("soap_5x7_3steps_seed5.txt"), rtol=0,
                                atol=1e-12)
+
+
+def test_shampoo_fixture():
+    mg = _load_golden()
+    np.testing.assert_allclose(mg.shampoo_run(), _read_matrix("shampoo_6x4_3steps_seed7.txt"),
+                               rtol=0, atol=1e-12)
