@@ -131,7 +131,49 @@ def test_update_closed_forms():
         ones = np.ones((r, c))
         np.testing.assert_allclose(muon.apply_update(W0, ones, lr, wd),
                                    W0 * (1 - lr * wd) - lr * s, rtol=1e-14)
-        assert muon.update_scale(r, c, "match_rms_adamw") == pytest.approx(0.2 * math.sqrt(max(r, c)))
+
+
+def test_update_scale_match_rms_adamw_hand_values():
+    # MatrixFSDP §5.1 runs Muon with the match-RMS-to-AdamW learning-rate adjustment: the step
+    # is scaled by 0.2 * sqrt(max(rows, cols)), independent of which side is longer.  Worked by
+    # hand: sqrt(256) = 16, sqrt(9) = 3, sqrt(64) = 8, sqrt(2500) = 50, sqrt(1) = 1.
+    for (r, c), s in [((256, 64), 3.2), ((64, 256), 3.2), ((9, 4), 0.6), ((4, 9), 0.6),
+                      ((64, 64), 1.6), ((100, 2500), 10.0), ((1, 1), 0.2)]:
+        assert abs(muon.update_scale(r, c, "match_rms_adamw") - s) <= 1e-15 * s, (r, c)
+    # ...and the original scale sqrt(max(1, rows / cols)) on the same shapes
+    for (r, c), s in [((256, 64), 2.0), ((64, 256), 1.0), ((9, 4), 1.5), ((4, 9), 1.0),
+                      ((64, 64), 1.0), ((100, 2500), 1.0), ((2500, 100), 5.0)]:
+        assert abs(muon.update_scale(r, c, "original") - s) <= 1e-15 * s, (r, c)
+    # The whole update in that mode, by hand: W0 = 2, O = 1, lr 0.02, wd 0.01, (9, 4):
+    # 2 * (1 - 0.0002) - 0.02 * 0.6 = 1.9996 - 0.012 = 1.9876; O = -0.5 on (256, 64):
+    # 2 * 0.9998 + 0.02 * 3.2 * 0.5 = 1.9996 + 0.032 = 2.0316.
+    W = muon.apply_update(np.full((9, 4), 2.0), np.ones((9, 4)), 0.02, 0.01, "match_rms_adamw")
+    np.testing.assert_allclose(W, np.full((9, 4), 1.9876), rtol=1e-14)
+    W = muon.apply_update(np.full((256, 64), 2.0), np.full((256, 64), -0.5), 0.02, 0.01,
+                          "match_rms_adamw")
+    np.testing.assert_allclose(W, np.full((256, 64), 2.0316), rtol=1e-14)
+
+
+def test_update_scale_ratio_matches_torch_muon():
+    """Third-party cross-check of both scales: torch.optim.Muon with weight decay 0 takes the
+    same orthogonalised step under either adjustment, so the ratio of its two updates is
+    s_match / s_original, whatever its own Newton–Schulz precision."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch.optim, "Muon"):
+        pytest.skip("torch.optim.Muon not available")
+    rng = np.random.default_rng(9)
+    for r, c in [(256, 64), (64, 256), (96, 96)]:
+        G = torch.tensor(rng.normal(size=(r, c)), dtype=torch.float32)
+        steps = {}
+        for mode in ("original", "match_rms_adamw"):
+            t = torch.zeros(r, c, requires_grad=True)
+            opt = torch.optim.Muon([t], lr=0.01, weight_decay=0.0, adjust_lr_fn=mode)
+            t.grad = G.clone()
+            opt.step()
+            steps[mode] = t.detach().double().numpy()
+        ratio = np.linalg.norm(steps["match_rms_adamw"]) / np.linalg.norm(steps["original"])
+        want = muon.update_scale(r, c, "match_rms_adamw") / muon.update_scale(r, c, "original")
+        assert abs(ratio - want) <= 1e-6 * want, (r, c, ratio, want)
 
 
 # ----------------------------------------------------------------------------- AdamW
