@@ -48,6 +48,21 @@ int scratch_address(void** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Up to 64 table entries travel as one kernel's parameters (3 KB) and one thread per entry
+// stores them into the scratch table.  The runtime copies a launch's parameters when the launch
+// is issued, so the table never depends on host memory after this call returns.
+constexpr int kTableBatch = 64;
+struct TableBatch {
+  DevMat m[kTableBatch];
+  int32_t first, count;
+};
+static_assert(sizeof(TableBatch) <= 4000, "table batch must fit the kernel parameter space");
+
+__global__ void write_table_kernel(const TableBatch b, DevMat* table) {
+  const int k = threadIdx.x;
+  if (k < b.count) table[b.first + k] = b.m[k];
+}
+
 }  // namespace
 }  // namespace mfsdp
 
@@ -99,16 +114,19 @@ extern "C" int mfsdp_owner_reduce_momentum_noalloc(
   DevMat* table = static_cast<DevMat*>(scratch);
   float* partials = reinterpret_cast<float*>(static_cast<char*>(scratch) + kTableBytes);
 
-  // The matrix table, written in small batches from a stack buffer (no host allocation either;
-  // a copy from pageable memory is staged before cudaMemcpyAsync returns).
-  DevMat batch[64];
+  // The matrix table, written in batches of 64 entries by a one-CTA kernel that receives them
+  // as its parameters (no host allocation, and no copy from host memory that must outlive the
+  // call).
+  TableBatch batch;
   int32_t cta = 0;
-  for (int32_t i0 = 0; i0 < n_mats; i0 += 64) {
-    const int32_t cnt = n_mats - i0 < 64 ? n_mats - i0 : 64;
+  for (int32_t i0 = 0; i0 < n_mats; i0 += kTableBatch) {
+    const int32_t cnt = n_mats - i0 < kTableBatch ? n_mats - i0 : kTableBatch;
+    std::memset(&batch, 0, sizeof(batch));
+    batch.first = i0;
+    batch.count = cnt;
     for (int32_t k = 0; k < cnt; ++k) {
       const mfsdp_matrix& q = mats[i0 + k];
-      DevMat& d = batch[k];
-      std::memset(&d, 0, sizeof(d));
+      DevMat& d = batch.m[k];
       d.offset = q.offset;
       d.numel = q.rows * q.cols;
       d.rows = q.rows;
@@ -117,9 +135,8 @@ extern "C" int mfsdp_owner_reduce_momentum_noalloc(
       d.split = d.numel > 0 && d.numel <= split_max_numel;
       cta += (int32_t)((d.numel + kChunk - 1) / kChunk);
     }
-    if (cudaMemcpyAsync(table + i0, batch, sizeof(DevMat) * cnt, cudaMemcpyHostToDevice, s) !=
-        cudaSuccess)
-      return MFSDP_ECUDA;
+    write_table_kernel<<<1, kTableBatch, 0, s>>>(batch, table);
+    if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
   }
 
   // Every partial is written by its CTA before the norm kernel reads it, so nothing in the
