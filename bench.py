@@ -1,13 +1,17 @@
 """Benchmark of the owner-local Muon optimizer step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+    python bench.py --case soap|shampoo [--steps K] ...     (one second-order case, one line)
 
 A step is one pass of the whole hot path over one batch of synthetic input resident in HBM:
 W-way gradient deposit + Nesterov momentum + Frobenius norm, Newton–Schulz (5 quintic
 iterations) of every owned matrix, the scaled update with decoupled weight decay, and AdamW on
-the packed tail.  The default workload is the GPT-2-small owner set (48 matrices of hidden 768,
-W = 8 bf16 contributions).  The same contribution batch is reused every step; momentum, weights
-and AdamW state evolve.  Inputs (about 2 GB) exceed the 129 MB L2, so no flush is inserted.
+the packed tail.  The default workload is the Llama-3-70B owner share (24 MLP matrices of
+28672x8192 / 8192x28672 and 16 of 8192x8192, W = 2 bf16 contributions, about 131 GB resident),
+the largest of the five workloads on one GPU; the GPT-2-small owner set (48 matrices of hidden
+768, W = 8) is measured beside it under ``gpt2_small``.  The same contribution batch is reused
+every step; momentum, weights and AdamW state evolve.  Inputs exceed the 129 MB L2, so no
+flush is inserted.
 
 Prints ONE JSON line (rank 0).  ``value`` is owner-step milliseconds (lower is better); the
 Newton–Schulz TFLOP/s count 4 m^2 n + 2 m^3 FLOPs per iteration (m <= n).  ``--impl reference``
@@ -232,35 +236,55 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def oracle_sample(wb: "Workload", budget_s: float, max_mats=None):
-    """Time the oracle's owner step on a bounded sample of the owned set (host cores).
+# The fp64 oracle runs one owned matrix's whole Muon step when it costs at most this many
+# nominal Newton–Schulz FLOPs (a few seconds on the host cores); above it a sample runs the
+# step with one Newton–Schulz iteration in place of five (every iteration costs the same).
+ORACLE_SAMPLE_MAX_FLOPS = 4e12
 
-    Returns (seconds spent, nominal NS FLOPs covered, elements covered, sample text)."""
+
+def _ns_nominal(rows, cols, steps):
+    m, n = min(rows, cols), max(rows, cols)
+    return steps * (4 * m * m * n + 2 * m ** 3)
+
+
+def oracle_muon_sample(wl, shapes, inputs_of, budget_s, max_mats=None):
+    """Time the oracle's owner Muon step on a bounded sample of an owned set (host cores).
+
+    shapes: the owned (rows, cols) in set order; inputs_of(k) -> (W0, contributions) of owned
+    matrix k as fp64 arrays.  Matrices are taken smallest first (nominal Newton–Schulz FLOPs)
+    until ``budget_s`` is spent or ``max_mats`` are done.  A matrix whose full step exceeds
+    ORACLE_SAMPLE_MAX_FLOPS runs with one Newton–Schulz iteration (and only that one matrix).
+    Returns (seconds, nominal NS FLOPs covered, description)."""
     from oracle import step as ostep
-    wl, lay, r = wb.wl, wb.lay, wb.runner
     hp = wl.hyper
-    spent = flops = elems = 0.0
-    taken = 0
-    order = list(range(len(wb.shapes)))
+    order = sorted(range(len(shapes)), key=lambda k: (_ns_nominal(*shapes[k], 1), k))
+    spent = flops = 0.0
+    taken, iters = 0, hp.ns_steps
     for k in order:
         if spent >= budget_s or (max_mats is not None and taken >= max_mats):
             break
-        rr, cc = wb.shapes[k]
-        off = lay.matrix_offsets[k]
-        W0 = r.weights[off:off + rr * cc].double().cpu().numpy().reshape(rr, cc)
-        cs = [c[off:off + rr * cc].double().cpu().numpy().reshape(rr, cc) for c in wb.contrib]
+        rr, cc = shapes[k]
+        if taken == 0 and _ns_nominal(rr, cc, hp.ns_steps) > ORACLE_SAMPLE_MAX_FLOPS:
+            iters = 1
+        W0, cs = inputs_of(k)
         t0 = time.perf_counter()
         ostep.muon_matrix_step(W0, np.zeros_like(W0), cs, momentum=hp.momentum,
                                nesterov=hp.nesterov, grad_scale=hp.grad_scale,
-                               ns_steps=hp.ns_steps, a=hp.ns_a, b=hp.ns_b, c=hp.ns_c,
+                               ns_steps=iters, a=hp.ns_a, b=hp.ns_b, c=hp.ns_c,
                                eps=hp.ns_eps, lr=hp.lr, weight_decay=hp.weight_decay,
                                lr_adjust=hp.lr_adjust)
         spent += time.perf_counter() - t0
-        m, n = min(rr, cc), max(rr, cc)
-        flops += hp.ns_steps * (4 * m * m * n + 2 * m ** 3)
-        elems += rr * cc
+        flops += _ns_nominal(rr, cc, iters)
         taken += 1
-    return spent, flops, elems, f"{taken} of {len(wb.shapes)} owned matrices, one step"
+        if iters != hp.ns_steps:
+            break
+    if iters != hp.ns_steps:
+        r, c = shapes[order[0]]
+        what = (f"one {r}x{c} owned matrix: deposit, momentum, norm, 1 of the "
+                f"{hp.ns_steps} Newton–Schulz iterations, update")
+    else:
+        what = f"{taken} of {len(shapes)} owned matrices, one whole step each"
+    return spent, flops, what
 
 
 def blas_threads():
@@ -274,9 +298,8 @@ def blas_threads():
     return os.cpu_count()
 
 
-def extrapolated_ms(wb, spent, flops):
-    nominal, _ = wb.ns_flops()
-    return 1e3 * spent * nominal / flops if flops else None
+def set_nominal_ns_flops(wl, shapes):
+    return sum(_ns_nominal(r, c, wl.hyper.ns_steps) for r, c in shapes)
 
 
 # ----------------------------------------------------------------------------- runs
@@ -345,7 +368,11 @@ def time_e2e(wb, steps, stream, n_copy_streams=2):
     computes (each waits until the step that last used its buffers has finished)."""
     hp = wb.wl.hyper
     r = wb.runner
-    host = [c.cpu().pin_memory() for c in wb.contrib + wb.tail_contrib]
+    host = []
+    for c in wb.contrib + wb.tail_contrib:   # pinned host copies, written straight from HBM
+        h = torch.empty(c.shape, dtype=c.dtype, pin_memory=True)
+        h.copy_(c)
+        host.append(h)
     n_c = len(wb.contrib)
     sets = [wb.contrib + wb.tail_contrib,
             [torch.empty_like(c) for c in wb.contrib + wb.tail_contrib]]
@@ -520,23 +547,22 @@ def time_soap(device, warm=3, reps=2, max_sweeps=20):
     return s.elapsed_time(e) / reps, sweeps, gemm, jac, keep_ms
 
 
-def config_block(wb, cfg):
-    wl = wb.wl
-    return {"workload": wl.name, "config_index": cfg, "owner_rank": wb.rank,
-            "matrices": len(wb.shapes), "owned_elements": int(sum(r * c for r, c in wb.shapes)),
-            "tail_elements": wb.lay.n_tail, "W": wl.W, "contrib_dtype": wl.contrib_dtype,
+def config_of(wl, cfg, rank, shapes, n_tail):
+    """The workload block of the JSON line (the same for both arms)."""
+    return {"workload": wl.name, "config_index": cfg, "owner_rank": rank,
+            "matrices": len(shapes), "owned_elements": int(sum(r * c for r, c in shapes)),
+            "tail_elements": int(n_tail), "W": wl.W, "contrib_dtype": wl.contrib_dtype,
             "ns_steps": wl.hyper.ns_steps, "l2": "inputs > 129 MB L2, no flush",
             "parallelism": "owner replicas, no collective"}
 
 
-def run_ours(args, rank, world, local_rank):
-    from matrix_optimizer_owner_gb300 import mfsdp
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    wb = Workload(args.config, rank, dev, args.shapes)
-    stream = torch.cuda.current_stream()
-    peaks, peak_src = load_peaks()
+def config_block(wb, cfg):
+    return config_of(wb.wl, cfg, wb.rank, wb.shapes, wb.lay.n_tail)
 
+
+def measure_step(wb, args, stream, peaks, peak_src, world, dev, local_rank):
+    """Owner-step time of one resident workload (call by call with per-phase events, then as a
+    CUDA graph), with the clock record of both timed regions and the Newton–Schulz roofline."""
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -551,22 +577,12 @@ def run_ours(args, rank, world, local_rank):
     if clocks is not None:
         clocks["window"] = (f"{args.clock_window_s:.1f} s of untimed steps + the timed "
                             "regions (call by call, then graph replay)")
-    status = mfsdp.mfsdp_query_status()
     eager_ms = total_ms / args.steps
     step_ms = graph_ms if graph_ms is not None else eager_ms
     if world > 1:
         t = torch.tensor([step_ms, eager_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         step_ms, eager_ms = float(t[0].item()), float(t[1].item())
-    ms = step_ms
-
-    e2e_ms, h2d, d2h = time_e2e(wb, max(3, min(args.steps, 10)), stream) if not args.no_e2e \
-        else (None, 0, 0)
-    if world > 1 and e2e_ms is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-
     nominal, executed = wb.ns_flops()
     ns_ms = phases["newton_schulz"] / args.steps
     ns_tf_nominal = nominal / (ns_ms * 1e-3) / 1e12
@@ -576,29 +592,26 @@ def run_ours(args, rank, world, local_rank):
     sustained = total_ms > 1000.0 and "bf16_tflops_sustained" in peaks
     peak_tf = float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"])
     ns_launches = wb.ns_launches_per_step()
-    kernel = wb.ns_kernel_name()
-    traffic = ns_traffic_per_launch(wb, args)
     sb = wb.stream_bytes()
     gbs = {k: (sb[k] / (phases[k] / args.steps * 1e-3) / 1e9 if phases[k] > 0 else None)
            for k in sb}
-    line = {
-        "metric": METRIC, "value": round(ms, 4), "unit": "ms", "n_gpus": world,
-        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4),
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded, device-drawn)",
-        "config": dict(config_block(wb, args.config),
-                       launch=("CUDA graph (deposit, Newton–Schulz, update) + AdamW tail"
-                               if graph_ms is not None else "call by call")),
-        "eager_ms_per_step": round(eager_ms, 4),
+    hbm = float(peaks["hbm_gbs"])
+    return {
+        "ms_per_step": step_ms, "eager_ms_per_step": round(eager_ms, 4),
+        "launch": ("CUDA graph (deposit, Newton–Schulz, update) + AdamW tail"
+                   if graph_ms is not None else "call by call"),
         "step_ms_median": round(statistics.median(graph_steps), 4) if graph_steps else None,
         "step_ms_max": round(max(graph_steps), 4) if graph_steps else None,
+        "ns_ms_per_step": round(ns_ms, 4),
         "ns_tflops": round(ns_tf_nominal, 1), "ns_tflops_executed": round(ns_tf_exec, 1),
         "ns_frac_of_peak": round(ns_tf_exec / peak_tf, 4),
         "phases_ms_per_step": {k: round(v / args.steps, 4) for k, v in phases.items()},
         "streaming_gbs": {k: (round(v, 1) if v else None) for k, v in gbs.items()},
-        "roofline": {"kernel": kernel, "bound": "tensor", "achieved": round(ns_tf_exec, 1),
-                     "peak": peak_tf, "unit": "TFLOP/s", "frac": round(ns_tf_exec / peak_tf, 4),
-                     "traffic": traffic,
+        "streaming_frac_of_hbm": {k: (round(v / hbm, 4) if v else None) for k, v in gbs.items()},
+        "roofline": {"kernel": wb.ns_kernel_name(), "bound": "tensor",
+                     "achieved": round(ns_tf_exec, 1), "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(ns_tf_exec / peak_tf, 4),
+                     "traffic": ns_traffic_per_launch(wb, args),
                      "peak_source": f"{peak_src} bf16 {'sustained' if sustained else 'burst'}",
                      "launches_per_step": ns_launches,
                      "avg_launch_us": round(1e3 * ns_ms / ns_launches, 2),
@@ -606,12 +619,106 @@ def run_ours(args, rank, world, local_rank):
                      "flops_counted": "executed: upper 256-tiles of the symmetric Gram and "
                                       "polynomial products, m(m+1)n + m^2(m+1) + 2m^2n per "
                                       "iteration"},
+        "gpu_launches": wb.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+
+
+def cpu_baseline_of(wb, budget_s):
+    """The oracle on the host cores, on a bounded sample of the resident workload's own
+    (device-drawn) inputs, extrapolated to the whole owned set by nominal Newton–Schulz FLOP
+    share."""
+    r, lay = wb.runner, wb.lay
+
+    def inputs_of(k):
+        rr, cc = wb.shapes[k]
+        off = lay.matrix_offsets[k]
+        W0 = r.weights[off:off + rr * cc].double().cpu().numpy().reshape(rr, cc)
+        cs = [c[off:off + rr * cc].double().cpu().numpy().reshape(rr, cc) for c in wb.contrib]
+        return W0, cs
+
+    spent, flops, what = oracle_muon_sample(wb.wl, wb.shapes, inputs_of, budget_s)
+    total = set_nominal_ns_flops(wb.wl, wb.shapes)
+    return {"value": round(1e3 * spent * total / flops, 1), "unit": "ms",
+            "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{what} ({spent:.1f} s), extrapolated to the whole owned set by "
+                      "nominal Newton–Schulz FLOP share",
+            "timed_s": round(spent, 2), "extrapolated": flops < total,
+            "sampled_flop_fraction": round(flops / total, 6)}
+
+
+def free_workload(wb):
+    wb.runner.close()
+    wb.contrib.clear()
+    wb.tail_contrib.clear()
+    del wb.runner
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def run_ours(args, rank, world, local_rank):
+    from matrix_optimizer_owner_gb300 import mfsdp
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wb = Workload(args.config, rank, dev, args.shapes)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+
+    m = measure_step(wb, args, stream, peaks, peak_src, world, dev, local_rank)
+    status = mfsdp.mfsdp_query_status()
+    ms = m.pop("ms_per_step")
+    clocks = m.pop("clocks")
+    launches = m.pop("gpu_launches")
+    roofline = m.pop("roofline")
+
+    e2e_ms, h2d, d2h = time_e2e(wb, max(3, min(args.steps, 10)), stream) if not args.no_e2e \
+        else (None, 0, 0)
+    if world > 1 and e2e_ms is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    line = {
+        "metric": METRIC, "value": round(ms, 4), "unit": "ms", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded, device-drawn)",
+        "config": config_block(wb, args.config if not args.shapes else None),
+        **m,
+        "roofline": roofline,
         "e2e": {"value": round(e2e_ms, 4) if e2e_ms is not None else None, "unit": "ms",
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": wb.launches_per_step() * args.steps,
+        "gpu_launches": launches,
         "clocks": clocks, "device_status": status,
     }
+    if not args.no_repack:
+        rms, rbytes, nparams = time_repack(wb, 10, stream)
+        line["repack"] = {
+            "kernel": "segment_copy_kernel", "what": f"pack {nparams} parameters (2-byte "
+            f"elements) of the {wb.wl.name.split(':')[0]} list from the canonical axis into "
+            "8-rank RoleGreedy owner shards",
+            "ms": round(rms, 4), "bytes": rbytes, "bound": "hbm",
+            "achieved_gbs": round(rbytes / (rms * 1e-3) / 1e9, 1), "peak_gbs": peaks["hbm_gbs"],
+            "frac": round(rbytes / (rms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 4)}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_of(wb, args.cpu_seconds)
+    free_workload(wb)
+    del wb
+
+    # The GPT-2-small owner set (48 matrices of hidden 768): the small-matrix regime of the
+    # same step, reported beside the headline workload.
+    if not args.shapes and args.config != 1 and not args.no_gpt2_small:
+        wb1 = Workload(1, rank, dev)
+        m1 = measure_step(wb1, args, stream, peaks, peak_src, world, dev, local_rank)
+        m1["ms_per_step"] = round(m1["ms_per_step"], 4)
+        line["gpt2_small"] = {"config": config_block(wb1, 1), **m1,
+                              "device_status": mfsdp.mfsdp_query_status()}
+        if rank == 0 and not args.no_cpu_baseline:
+            line["gpt2_small"]["cpu_baseline"] = cpu_baseline_of(wb1, args.cpu_seconds)
+        free_workload(wb1)
+        del wb1
+
     if not args.no_shampoo and rank == 0:
         what = ("one owner Shampoo step of one GPT-2-small layer (2304x768, 768x768, "
                 "3072x768, 768x3072), 30 coupled-Newton steps per inverse fourth root")
@@ -657,91 +764,130 @@ def run_ours(args, rank, world, local_rank):
             "flops_counted": "SGEMMs + 8 dp^3 per side per rotating sweep (every 64x64 block "
                              "product of the rotations): an upper bound, since pairs whose "
                              "rotation is the identity skip their blocks"}
-    if not args.no_repack:
-        rms, rbytes, nparams = time_repack(wb, 10, stream)
-        line["repack"] = {
-            "kernel": "segment_copy_kernel", "what": f"pack {nparams} parameters (2-byte "
-            "elements) from the canonical axis into 8-rank RoleGreedy owner shards",
-            "ms": round(rms, 4), "bytes": rbytes, "bound": "hbm",
-            "achieved_gbs": round(rbytes / (rms * 1e-3) / 1e9, 1), "peak_gbs": peaks["hbm_gbs"],
-            "frac": round(rbytes / (rms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 4)}
-    if rank == 0 and not args.no_cpu_baseline:
-        spent, flops, elems, sample = oracle_sample(wb, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(extrapolated_ms(wb, spent, flops), 1), "unit": "ms",
-                                "cores": blas_threads(), "kind": "oracle",
-                                "sample": sample + f" ({spent:.1f} s), extrapolated by "
-                                          "nominal Newton–Schulz FLOP share"}
     return line
 
 
 def run_reference(args, rank, world):
-    """The CPU oracle as the reference arm: ownership from the oracle's planner, inputs drawn on
-    the host, and each step times the oracle's Muon step on ``--ref-mats`` owned matrices
-    (cycling through the set) plus the AdamW tail, extrapolated to the whole owned set by
-    nominal Newton–Schulz FLOP share.  No library code and no GPU work on this path."""
+    """The CPU oracle as the reference arm: ownership from the oracle's planner, the workload's
+    seeded inputs drawn on the host (torch's CPU generator: the same distributions as the
+    device draws, other values), and each step times the oracle's Muon step on a bounded
+    sample of the owned set (the same sample rule as our arm's cpu_baseline), extrapolated to
+    the whole owned set by nominal Newton–Schulz FLOP share, plus the whole AdamW tail.  No
+    library code and no GPU work on this path."""
     if rank != 0:
         return None
     from oracle import adamw as oadamw
     from oracle import plan as oplan
-    from oracle import step as ostep
     wl = get_config(args.config)
     hp = wl.hyper
     ps = [oplan.Param(p.rows, p.cols, p.block, p.is_matrix) for p in wl.params]
     mats, tails = oplan.owned(ps, oplan.plan(ps, wl.world_size), wl.rank)
-    flops_of = lambda i: hp.ns_steps * (4 * min(ps[i].rows, ps[i].cols) ** 2 *
-                                        max(ps[i].rows, ps[i].cols) +
-                                        2 * min(ps[i].rows, ps[i].cols) ** 3)
-    total_flops = sum(flops_of(i) for i in mats)
-    per_step, cursor = [], 0
+    shapes = [(ps[i].rows, ps[i].cols) for i in mats]
+    total_flops = set_nominal_ns_flops(wl, shapes)
+    cache = {}
+
+    def inputs_of(k):          # drawn once (outside the timed region), reused every step
+        if k not in cache:
+            i = mats[k]
+            r, c = shapes[k]
+            cache[k] = (synth.weight(wl, i).double().numpy().reshape(r, c),
+                        [synth.contribution(wl, 0, i, w).double().numpy().reshape(r, c)
+                         for w in range(wl.W)])
+        return cache[k]
+
+    tail_in = None
+    if tails:
+        p0 = np.concatenate([synth.weight(wl, i).double().numpy() for i in tails])
+        g = sum(np.concatenate([synth.contribution(wl, 0, i, w).double().numpy()
+                                for i in tails]) for w in range(wl.W)) * hp.grad_scale
+        tail_in = (p0, g)
+    per_step, timed, what, frac = [], 0.0, "", 1.0
     for k in range(max(args.warmup, 0) + args.steps):
-        spent = flops = 0.0
-        for _ in range(min(args.ref_mats, len(mats))):
-            i = mats[cursor % len(mats)]
-            cursor += 1
-            p = wl.params[i]
-            W0 = synth.weight(wl, i).double().numpy().reshape(p.rows, p.cols)
-            cs = [synth.contribution(wl, 0, i, w).double().numpy().reshape(p.rows, p.cols)
-                  for w in range(wl.W)]
-            t0 = time.perf_counter()
-            ostep.muon_matrix_step(W0, np.zeros_like(W0), cs, momentum=hp.momentum,
-                                   nesterov=hp.nesterov, grad_scale=hp.grad_scale,
-                                   ns_steps=hp.ns_steps, a=hp.ns_a, b=hp.ns_b, c=hp.ns_c,
-                                   eps=hp.ns_eps, lr=hp.lr, weight_decay=hp.weight_decay,
-                                   lr_adjust=hp.lr_adjust)
-            spent += time.perf_counter() - t0
-            flops += flops_of(i)
-        step_ms = 1e3 * spent * total_flops / flops if flops else 0.0
-        if tails:  # the AdamW tail, whole
-            p0 = np.concatenate([synth.weight(wl, i).double().numpy() for i in tails])
-            g = sum(np.concatenate([synth.contribution(wl, 0, i, w).double().numpy()
-                                    for i in tails]) for w in range(wl.W)) * hp.grad_scale
+        spent, flops, what = oracle_muon_sample(wl, shapes, inputs_of, args.ref_seconds,
+                                                max_mats=args.ref_mats)
+        frac = flops / total_flops if total_flops else 1.0
+        step_s = spent / frac if flops else 0.0
+        if tail_in is not None:  # the AdamW tail, whole
             b1, b2 = hp.adam_betas
             t0 = time.perf_counter()
-            oadamw.adamw_step(p0, np.zeros_like(p0), np.zeros_like(p0), g, 1, hp.adam_lr, b1, b2,
-                              hp.adam_eps, hp.adam_wd)
-            step_ms += 1e3 * (time.perf_counter() - t0)
+            oadamw.adamw_step(tail_in[0], np.zeros_like(tail_in[0]), np.zeros_like(tail_in[0]),
+                              tail_in[1], 1, hp.adam_lr, b1, b2, hp.adam_eps, hp.adam_wd)
+            dt = time.perf_counter() - t0
+            step_s += dt
+            spent += dt
         if k >= args.warmup:
-            per_step.append(step_ms)
+            per_step.append(1e3 * step_s)
+            timed += spent
     v = statistics.mean(per_step)
-    config = {"workload": wl.name, "config_index": args.config, "owner_rank": wl.rank,
-              "matrices": len(mats),
-              "owned_elements": int(sum(ps[i].numel for i in mats)),
-              "tail_elements": int(sum(ps[i].numel for i in tails)), "W": wl.W,
-              "contrib_dtype": wl.contrib_dtype, "ns_steps": hp.ns_steps,
-              "l2": "host oracle", "parallelism": "rank 0 only"}
+    n_tail = sum(ps[i].numel for i in tails)
     return {
         "metric": METRIC, "value": round(v, 1), "unit": "ms", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v, 1),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded, host-drawn)", "config": config, "impl": "reference",
+        "data": "synthetic (seeded, host-drawn)",
+        "config": config_of(wl, args.config, wl.rank, shapes, n_tail), "impl": "reference",
         "cpu_baseline": {"value": round(v, 1), "unit": "ms", "cores": blas_threads(),
                          "kind": "oracle",
-                         "sample": f"{args.ref_mats} owned matrices per step (cycling), "
-                                   "extrapolated by nominal Newton–Schulz FLOP share, plus "
-                                   "the whole AdamW tail"},
+                         "sample": f"each step: {what}, extrapolated to the whole owned set by "
+                                   "nominal Newton–Schulz FLOP share"
+                                   + (", plus the whole AdamW tail" if tails else ""),
+                         "timed_s": round(timed, 2), "extrapolated": frac < 1.0,
+                         "sampled_flop_fraction": round(frac, 6)},
         "e2e": {"value": round(v, 1), "unit": "ms", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+
+
+# ----------------------------------------------------------------------------- cases
+GPT2_LAYER = [(2304, 768), (768, 768), (3072, 768), (768, 3072)]
+
+
+def run_case(args):
+    """One second-order case for timing and profiling: ``args.steps`` owner steps of one
+    GPT-2-small layer's matrices on cuda:0 from seeded synthetic gradients; prints the time of
+    the last step and, for SOAP, the Jacobi sweeps each side took."""
+    from matrix_optimizer_owner_gb300 import mfsdp
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    offs, numel = [], 0
+    for r, c in GPT2_LAYER:
+        offs.append(numel)
+        numel += r * c
+    mats = [(r, c, off) for (r, c), off in zip(GPT2_LAYER, offs)]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    w = torch.randn(numel, generator=gen, device=dev) * 0.02
+    if args.case == "soap":
+        sset = mfsdp.SoapSet(mats)
+        ws = torch.empty(sset.workspace_bytes, dtype=torch.uint8, device=dev)
+        st = {k: torch.empty(n, dtype=torch.float32, device=dev)
+              for k, n in sset.state_sizes(numel).items()}
+        sset.init_state(st, ws)
+        info = torch.zeros(2 * len(GPT2_LAYER), dtype=torch.int32, device=dev)
+    else:
+        sset = mfsdp.ShampooSet(mats)
+        ws = torch.empty(sset.workspace_bytes, dtype=torch.uint8, device=dev)
+        lst = torch.empty(sset.l_numel, dtype=torch.float32, device=dev)
+        rst = torch.empty(sset.r_numel, dtype=torch.float32, device=dev)
+        sset.init_state(1e-6, lst, rst, ws)
+    ms = 0.0
+    for t in range(1, args.steps + 1):
+        g = torch.randn(numel, generator=gen, device=dev) * 1e-3
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        if args.case == "soap":
+            sset.step(g, w, st, t, lr=1e-3, beta1=0.9, beta2=0.95, beta_stats=0.95, eps=1e-8,
+                      weight_decay=1e-2, max_sweeps=args.max_sweeps, workspace=ws, info=info)
+        else:
+            sset.step(g, lst, rst, w, 0.02, 0.01, args.root_iters, ws, precision=args.precision)
+        e.record()
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e)
+    extra = f" sweeps={info.cpu().tolist()}" if args.case == "soap" else \
+        f" precision={args.precision}"
+    print(f"{args.case} steps={args.steps} last_ms={ms:.2f}{extra} "
+          f"status={mfsdp.mfsdp_query_status()}", flush=True)
+    sset.close()
 
 
 def main():
@@ -749,12 +895,16 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--shapes", default=None,
                     help='custom owned set for profiling, e.g. "4096x14336,1024x4096"')
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--ref-mats", type=int, default=2)
+    ap.add_argument("--ref-seconds", type=float, default=5.0,
+                    help="reference arm: oracle seconds per step (at least one sample unit)")
+    ap.add_argument("--ref-mats", type=int, default=None,
+                    help="reference arm: owned matrices per step (default: as many as the "
+                         "--cpu-seconds budget allows)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-repack", action="store_true",
@@ -763,10 +913,21 @@ def main():
                     help="skip the owner SOAP measurement (one GPT-2-small layer)")
     ap.add_argument("--no-shampoo", action="store_true",
                     help="skip the owner Shampoo measurement")
+    ap.add_argument("--no-gpt2-small", action="store_true",
+                    help="skip the GPT-2-small owner set measured beside another workload")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step call by call only (no CUDA-graph replay)")
     ap.add_argument("--clock-window-s", type=float, default=1.0)
+    ap.add_argument("--case", choices=["soap", "shampoo"], default=None,
+                    help="run one second-order case of a GPT-2-small layer and print one line")
+    ap.add_argument("--max-sweeps", type=int, default=20, help="--case soap: Jacobi sweep limit")
+    ap.add_argument("--precision", type=int, default=0,
+                    help="--case shampoo: 0 fp32, 1 split-bf16 tensor cores")
+    ap.add_argument("--root-iters", type=int, default=30, help="--case shampoo: Newton steps")
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -40,12 +40,47 @@ def test_reference_arm_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    cb = d["cpu_baseline"]
+    assert cb["timed_s"] > 0 and cb["extrapolated"] is False and cb["sampled_flop_fraction"] == 1
+    assert d["config"]["config_index"] == 0 and d["config"]["matrices"] == 4
+
+
+def test_reference_arm_samples_one_iteration_of_the_largest_workload():
+    """On the Llama-3-70B share a whole oracle step is about an hour of host time, so each
+    reference step runs one 8192x8192 matrix with one Newton–Schulz iteration and says so."""
+    import bench
+    from workloads import get_config
+    wl = get_config(4)
+    shapes = [(p.rows, p.cols) for p in wl.params]
+    calls = []
+
+    def inputs_of(k):
+        calls.append(k)
+        r, c = shapes[k]
+        return None, None
+
+    import oracle.step as ostep
+    orig = ostep.muon_matrix_step
+    seen = {}
+
+    def fake(W0, B, cs, **kw):
+        seen.update(kw)
+        return {}
+    ostep.muon_matrix_step = fake
+    try:
+        spent, flops, what = bench.oracle_muon_sample(wl, shapes, inputs_of, 5.0)
+    finally:
+        ostep.muon_matrix_step = orig
+    assert len(calls) == 1 and shapes[calls[0]] == (8192, 8192)
+    assert seen["ns_steps"] == 1
+    assert flops == 4 * 8192 ** 3 + 2 * 8192 ** 3
+    assert "1 of the 5 Newton–Schulz iterations" in what
 
 
 @pytest.mark.gpu
 def test_our_arm_line():
-    d = _run(["--steps", "3", "--warmup", "3", "--cpu-seconds", "2", "--clock-window-s", "0.2"],
-             900)
+    d = _run(["--config", "1", "--steps", "3", "--warmup", "3", "--cpu-seconds", "2",
+              "--clock-window-s", "0.2"], 900)
     _check_base(d)
     r = d["roofline"]
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
