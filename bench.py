@@ -439,6 +439,7 @@ def time_repack(wb, reps, stream, world=8):
 
 
 FFMA_PEAK_NOTE = "152 SMs x 128 fp32 lanes x 2 FLOP x the sampled SM clock"
+TF32_PER_BF16 = 1.1 / 2.25   # nominal dense tensor rates of GB300, PFLOP/s
 
 
 def _upper_tiles(d, tile=256):
@@ -450,7 +451,7 @@ def _upper_tiles(d, tile=256):
 def time_shampoo(device, reps=2, root_iters=30, precision=0):
     """Owner Shampoo step on one GPT-2-small layer's matrices (2304x768, 768x768, 3072x768,
     768x3072): statistics, 30 coupled-Newton steps for every inverse fourth root, the
-    preconditioned update; precision 0 = fp32 products on the CUDA cores, 1 = the root
+    preconditioned update; precision 0 = fp32 products (3xTF32 tensor cores), 1 = the root
     iteration and P on the tensor cores with split-bf16 operands.  Returns (ms per step,
     nominal FLOPs per step, tensor-core FLOPs executed per step)."""
     from matrix_optimizer_owner_gb300 import mfsdp
@@ -723,19 +724,24 @@ def run_ours(args, rank, world, local_rank):
         what = ("one owner Shampoo step of one GPT-2-small layer (2304x768, 768x768, "
                 "3072x768, 768x3072), 30 coupled-Newton steps per inverse fourth root")
         sms_, sflops, _ = time_shampoo(dev)
-        sm_mhz = (clocks or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
-        ffma_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+        tf32_peak = float(peaks["bf16_tflops"]) * TF32_PER_BF16
         line["shampoo"] = {
-            "kernel": "sgemm_batched_kernel (fp32 FFMA) + root and update kernels",
-            "what": what, "precision": "fp32",
-            "ms": round(sms_, 3), "flops": sflops, "bound": "alu",
-            "achieved_tflops": round(sflops / (sms_ * 1e-3) / 1e12, 2),
-            "peak_tflops": round(ffma_peak, 1), "peak_source": FFMA_PEAK_NOTE,
-            "frac": round(sflops / (sms_ * 1e-3) / 1e12 / ffma_peak, 4)}
+            "kernel": "tf32x3_gemm_kernel (tcgen05 kind::tf32, three split products per "
+                      "multiply) + root and update kernels",
+            "what": what, "precision": "fp32 (3xTF32)",
+            "ms": round(sms_, 3), "flops": sflops, "bound": "tensor",
+            "tensor_flops_executed": 3 * sflops,
+            "achieved_tflops": round(3 * sflops / (sms_ * 1e-3) / 1e12, 1),
+            "peak_tflops": round(tf32_peak, 1),
+            "peak_source": f"{peak_src} bf16 burst x {TF32_PER_BF16:.4f} (nominal dense TF32 / "
+                           "bf16 rate, 1.1 / 2.25 PFLOP/s)",
+            "frac": round(3 * sflops / (sms_ * 1e-3) / 1e12 / tf32_peak, 4),
+            "frac_note": "three TF32 products per fp32 multiply over the whole step time "
+                         "(norms and elementwise kernels included)"}
         tms, tflops, texec = time_shampoo(dev, precision=1)
         line["shampoo_tc"] = {
             "kernel": "ns_gemm_pair_kernel<split> (tcgen05 CTA pairs, split-bf16) for the "
-                      "roots and P; sgemm_batched_kernel for the statistics",
+                      "roots and P; tf32x3_gemm_kernel (tcgen05 3xTF32) for the statistics",
             "what": what, "precision": "split_bf16",
             "ms": round(tms, 3), "flops": tflops, "bound": "tensor",
             "tensor_flops_executed": texec,
@@ -751,8 +757,9 @@ def run_ours(args, rank, world, local_rank):
         ffma_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
         ach = (gemm + jac) / (sms_ * 1e-3) / 1e12
         line["soap"] = {
-            "kernel": "jacobi_apply_kernel + jacobi_solve_kernel (block Jacobi eigenbases, fp32) "
-                      "+ sgemm_batched_kernel",
+            "kernel": "jacobi_apply_kernel + jacobi_solve_kernel (block Jacobi eigenbases, fp32 "
+                      "CUDA cores) + tf32x3_gemm_kernel (statistics, Q^T L Q, Rayleigh "
+                      "quotients, rotations: tcgen05 3xTF32)",
             "what": "one owner SOAP step of one GPT-2-small layer (2304x768, 768x768, 3072x768, "
                     "768x3072), exact eigenbases every step, warm-started",
             "ms": round(sms_, 3), "sweeps_per_side": sweeps, "bound": "alu",

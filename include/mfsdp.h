@@ -234,7 +234,9 @@ typedef struct {
  * eigenvalue ratio of 1e-8 converges within 26 steps.
  *
  * `precision` selects where the products run:
- *   MFSDP_SHAMPOO_FP32        every product an fp32 GEMM on the CUDA cores;
+ *   MFSDP_SHAMPOO_FP32        every product an fp32 GEMM on the tcgen05 tensor cores in
+ *                             3xTF32 (mfsdp_gemm_f32_batched below: about 21 significant
+ *                             bits per product, the accuracy of an fp32 FFMA GEMM);
  *   MFSDP_SHAMPOO_SPLIT_BF16  the statistics as above; the root iteration and P = X_L G X_R on
  *                             the tcgen05 tensor cores with split-bf16 operands (value = hi +
  *                             lo, three products per multiply, fp32 accumulation: about 16
@@ -279,6 +281,38 @@ int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* grad, float* l
 
 
 /* ------------------------------------------------------------------------------------------
+ * Batched fp32 GEMM on the tensor cores (§5.7: the contractions of the second-order owner
+ * optimizers, G G^T and G^T G for the statistics, the products of the root iteration and of
+ * the preconditioning, the rotations into and out of an eigenbasis).  For every problem i:
+ *     C_i = alpha_i op(A_i) op(B_i) + beta_i C_i,    op(A_i): m x k,  op(B_i): k x n
+ * op(A) = A (stored m x k, pitch lda >= k) or A^T when trans_a (A stored k x m, lda >= m);
+ * op(B) = B (stored k x n, ldb >= n) or B^T when trans_b (B stored n x k, ldb >= k); C is
+ * m x n with pitch ldc >= n.  All row-major fp32 in DEVICE memory; C may not overlap A or B
+ * (beta = 0: C is not read).  Every problem runs in one persistent tcgen05 launch:
+ * values are cut into a TF32 high part and an fp32 remainder and each multiply is three
+ * TF32 products (hi hi + hi lo + lo hi) accumulated in fp32, about 21 significant bits per
+ * product.  `workspace` (DEVICE, >= mfsdp_gemm_f32_workspace_bytes(n_probs) bytes, 256-byte
+ * aligned) receives the problem table.  n_probs == 0 or an empty problem is no work.
+ * Errors: MFSDP_EINVAL (null table or pointers, negative sizes, a pitch below its minimum),
+ * MFSDP_EWORKSPACE, MFSDP_ECUDA; a wait that runs out on the device sets MFSDP_ETIMEOUT in the
+ * status word.
+ * ------------------------------------------------------------------------------------------ */
+
+typedef struct {
+  const float* a;
+  const float* b;
+  float* c;
+  int32_t m, n, k;
+  int32_t lda, ldb, ldc;
+  float alpha, beta;
+} mfsdp_gemm_problem;
+
+size_t mfsdp_gemm_f32_workspace_bytes(int32_t n_probs);
+int mfsdp_gemm_f32_batched(const mfsdp_gemm_problem* probs, int32_t n_probs, int32_t trans_a,
+                           int32_t trans_b, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * Owner SOAP (§5.7): Adam run in the eigenbasis of the Shampoo statistics, on the owner's
  * whole matrices, in place of Muon.  For every matrix G (rows x cols) of the set and step
  * t >= 1 (the pages name the method only; this is the SOAP update with the eigenbasis taken
@@ -292,7 +326,9 @@ int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* grad, float* l
  *     W = W (1 - lr weight_decay) - lr N
  * The eigenbases come from cyclic block Jacobi on Q^T L Q, started from the basis the state
  * holds (the previous step's), until a sweep rotates nothing or `max_sweeps` sweeps ran;
- * every product is fp32 on the CUDA cores.  Eigenvectors are fixed up to sign, and N does not
+ * the statistics, Q^T L Q, the Rayleigh quotients and the rotations into and out of the
+ * eigenbasis are fp32 GEMMs on the tensor cores (3xTF32, as mfsdp_gemm_f32_batched), the
+ * Jacobi rotations fp32 on the CUDA cores.  Eigenvectors are fixed up to sign, and N does not
  * depend on the signs.  The solves run on `stream` and on one internal stream of the set,
  * forked from and joined back into `stream` with events (created at the first step, on the
  * device current then), so a capture of `stream` takes both; a set serves one host thread at

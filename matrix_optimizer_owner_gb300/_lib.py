@@ -44,6 +44,12 @@ class SoapHyper(C.Structure):
                 ("max_sweeps", C.c_int32), ("jacobi_tol", C.c_float), ("refresh", C.c_int32)]
 
 
+class GemmProblem(C.Structure):
+    _fields_ = [("a", C.c_void_p), ("b", C.c_void_p), ("c", C.c_void_p), ("m", C.c_int32),
+                ("n", C.c_int32), ("k", C.c_int32), ("lda", C.c_int32), ("ldb", C.c_int32),
+                ("ldc", C.c_int32), ("alpha", C.c_float), ("beta", C.c_float)]
+
+
 class CostModel(C.Structure):
     _fields_ = [("param_bytes", C.c_int32), ("grad_bytes", C.c_int32),
                 ("state_bytes", C.c_int32), ("ns_steps", C.c_int32)]
@@ -79,6 +85,9 @@ SIGNATURES = {
     "mfsdp_shampoo_init_state": (C.c_int, [_vp, _f32, _vp, _vp, _vp, C.c_size_t, _vp]),
     "mfsdp_shampoo_step": (C.c_int, [_vp, _vp, _vp, _vp, _vp, _f32, _f32, _i32, _i32, _vp,
                                      C.c_size_t, _vp]),
+    "mfsdp_gemm_f32_workspace_bytes": (C.c_size_t, [_i32]),
+    "mfsdp_gemm_f32_batched": (C.c_int, [C.POINTER(GemmProblem), _i32, _i32, _i32, _vp,
+                                         C.c_size_t, _vp]),
     "mfsdp_soap_set_create": (C.c_int, [C.POINTER(Matrix), _i32, C.POINTER(_vp)]),
     "mfsdp_soap_set_destroy": (C.c_int, [_vp]),
     "mfsdp_soap_set_sizes": (C.c_int, [_vp, C.POINTER(C.c_size_t), C.POINTER(_i64),

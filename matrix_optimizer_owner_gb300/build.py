@@ -24,7 +24,7 @@ OBJ_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(OUT_DIR, "libmfsdp.so")
 
 SOURCES = ["api.cpp", "plan.cpp", "stream_kernels.cu", "ns_gemm.cu", "noalloc.cu", "repack.cu",
-           "shampoo.cu", "soap.cu"]
+           "shampoo.cu", "soap.cu", "tf32_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3", "-I", INCLUDE, "-I", CSRC]
 

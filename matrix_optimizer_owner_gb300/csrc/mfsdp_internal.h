@@ -117,7 +117,7 @@ cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int* status, cudaStr
 int* status_word_address();  // device address of this device's status word (nullptr on error)
 uint64_t wait_limit_ns();    // limit of every bounded device-side wait (mfsdp_set_wait_limit_ns)
 
-// ---- batched fp32 GEMM on the CUDA cores (second-order optimizers) ------------------------
+// ---- batched fp32 GEMM on the tensor cores, 3xTF32 (second-order optimizers) --------------
 struct GemmDesc {          // C = alpha op(A) op(B) + beta C, row-major, one problem
   const float* a;
   const float* b;
@@ -127,10 +127,11 @@ struct GemmDesc {          // C = alpha op(A) op(B) + beta C, row-major, one pro
   int32_t lda, ldb, ldc;
   float alpha, beta;
 };
-// Every problem of the table in one launch (blockIdx.z = problem); ta / tb: op = transpose.
-// Returns an MFSDP status.
-int launch_gemm(const GemmDesc* dev_descs, int nprob, int max_m, int max_n, int ta, int tb,
-                cudaStream_t st);
+// Every problem of the table in one persistent launch (one per 480 problems); ta / tb: op =
+// transpose.  host_descs is the host copy of the device table dev_descs (the host orders the
+// tiles from it).  Returns an MFSDP status.
+int launch_gemm(const GemmDesc* dev_descs, const GemmDesc* host_descs, int nprob, int ta,
+                int tb, cudaStream_t st);
 
 // ---- Newton–Schulz grouped GEMM (tcgen05 / TMEM / TMA) ------------------------------------
 constexpr int kBM = 128;   // tile rows    = UMMA M (one CTA, TMEM lanes 0..127)
@@ -161,6 +162,8 @@ struct NsProblem {         // one output matrix of one Newton–Schulz phase
   uint16_t* o_hi;          // output, row pitch ldo
   uint16_t* o_lo;
   int64_t ldo;
+  uint16_t* t_hi;          // split epilogue only, nullable: also T = (5 I - out) / 4 (pitch ldo)
+  uint16_t* t_lo;
 };
 
 struct NsTile {

@@ -683,6 +683,14 @@ __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
 __device__ __forceinline__ void sts16(uint32_t a, uint16_t v) {
   asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(v) : "memory");
 }
+__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -989,6 +997,27 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
             }
           }
         }
+        if (pr.t_hi) {
+          // T = (5 I - out) / 4 of the stored output (hi + lo), as a split pair
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float tv = ((r == c0 + j ? 5.f : 0.f) - (bf2f(h[j]) + bf2f(l[j]))) * 0.25f;
+            h[j] = f2bf(tv);
+            l[j] = f2bf(tv - bf2f(h[j]));
+          }
+          store_row32(pr.t_hi, pr.ldo, r, c0, cmin, N, h);
+          store_row32(pr.t_lo, pr.ldo, r, c0, cmin, N, l);
+          if (sym && c0 + 31 > r) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int c = c0 + j;
+              if (c > r && c < N) {
+                pr.t_hi[(int64_t)c * pr.ldo + r] = h[j];
+                pr.t_lo[(int64_t)c * pr.ldo + r] = l[j];
+              }
+            }
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -1144,20 +1173,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
           }
           hw[k] = pack_bf16x2(v0, v1);
         }
-        if (sym && c0 == rw) {
-          // block on the diagonal: row r stores columns >= r and mirrors columns > r
-          if (r < M) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int c = c0 + j;
-              const uint16_t hj = (uint16_t)(hw[j >> 1] >> (16 * (j & 1)));
-              if (c >= r && c < N) pr.o_hi[(int64_t)r * pr.ldo + c] = hj;
-              if (c > r && c < N) pr.o_hi[(int64_t)c * pr.ldo + r] = hj;
-            }
-          }
-          continue;
-        }
-        // off-diagonal block (and its transpose for a symmetric output): stage, then TMA store
+        // stage the block (and its transpose for a symmetric output), then TMA store
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           sts128(stg + stg_off(lane, k), make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2],
@@ -1168,12 +1184,31 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
             sts16(stg_t + stg_off(j, lane >> 3) + (uint32_t)((lane & 7) * 2),
                   (uint16_t)(hw[j >> 1] >> (16 * (j & 1))));
         }
+        const bool diag = sym && c0 == rw;
+        if (diag) {
+          // block on the diagonal: the stored block is symmetric, row r keeping its own
+          // columns >= r and taking, below the diagonal, column r of row c from the staged
+          // transpose; it leaves in one store (rows and columns past M clipped by the map).
+          // Word w of a staged row holds columns 2w (low half) and 2w + 1 (high half).
+          __syncwarp();
+#pragma unroll 1
+          for (int w = 0; w < 16; ++w) {
+            if (2 * w < lane) {
+              const uint32_t off = stg_off(lane, w >> 2) + (uint32_t)((w & 3) * 4);
+              const uint32_t tv = lds32(stg_t + off);
+              if (2 * w + 1 < lane)
+                sts32(stg + off, tv);
+              else
+                sts16(stg + off, (uint16_t)tv);
+            }
+          }
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
           const CUtensorMap* map_o = P.maps + pr.map_o;
           tma_store_block(map_o, stg, c0, rw);
-          if (sym) tma_store_block(map_o, stg_t, rw, c0);
+          if (sym && !diag) tma_store_block(map_o, stg_t, rw, c0);
           asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
         ++nstore;

@@ -14,14 +14,13 @@
 //     T_k = (5 I - M_k) / 4,  X_{k+1} = X_k T_k,  M_{k+1} = T_k^4 M_k,
 // so M_k -> I and X_k -> A^{-1/4}; an eigenvalue ratio of 1e-8 converges in 26 iterations.
 //
-// Two precisions.  fp32: every product is one batched SGEMM kernel on the CUDA cores (fp32
-// FFMA, 128 x 128 output tiles, 8 x 8 outputs per thread, double-buffered shared memory; a
-// launch runs the same product for every owned matrix, blockIdx.z = matrix), the iteration's
-// T = (5I - M) / 4 written by the epilogue of the product that forms M.  Split-bf16: the
-// statistics as above, the root iteration and P on the tensor cores through the
-// Newton-Schulz path's CTA-pair kernel in its split mode (values held as bf16 pairs hi + lo,
-// three MMAs per product, fp32 accumulation, 256 x 256 tiles), symmetric side products as
-// upper-triangle tiles.
+// Two precisions.  fp32: every product is one launch of the batched fp32 GEMM (tcgen05
+// kind::tf32 with three split products per multiply, "3xTF32", fp32 accumulation; a launch
+// runs the same product for every owned matrix), the iteration's T = (5I - M) / 4 written by
+// the epilogue of the product that forms M.  Split-bf16: the statistics as above, the root
+// iteration and P on the tensor cores through the Newton-Schulz path's CTA-pair kernel in its
+// split mode (values held as bf16 pairs hi + lo, three MMAs per product, fp32 accumulation,
+// 256 x 256 tiles), symmetric side products as upper-triangle tiles.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -36,120 +35,6 @@
 
 namespace mfsdp {
 namespace {
-
-constexpr int kGemmThreads = 256;
-constexpr int kTM = 128, kTN = 128, kTK = 16;
-constexpr int kPad = 4;  // shared-memory row padding (keeps 16-byte alignment)
-
-
-// 8 consecutive floats of a row at (r, c0) of a row-major buffer, zero outside rows x cols;
-// 16-byte loads when the 8 are inside and aligned.
-__device__ __forceinline__ void load8(const float* p, int64_t ld, int r, int c0, int rows,
-                                      int cols, float (&v)[8]) {
-  if (r < rows && c0 + 8 <= cols && ((reinterpret_cast<uintptr_t>(p + (int64_t)r * ld + c0) &
-                                      15u) == 0)) {
-    const float4* q = reinterpret_cast<const float4*>(p + (int64_t)r * ld + c0);
-    const float4 x = __ldg(q), y = __ldg(q + 1);
-    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-    v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
-    return;
-  }
-#pragma unroll
-  for (int u = 0; u < 8; ++u)
-    v[u] = (r < rows && c0 + u < cols) ? p[(int64_t)r * ld + c0 + u] : 0.f;
-}
-
-// C = alpha op(A) op(B) + beta C for every descriptor (blockIdx.z).  op(A) is m x k: A stored
-// m x k row-major (ta = 0) or k x m (ta = 1); op(B) is k x n: B stored k x n (tb = 0) or
-// n x k (tb = 1).  Tiles of op(A) and op(B) are kept k-major in shared memory; thread
-// (ty, tx) of the 16 x 16 grid computes rows {4ty + i, 64 + 4ty + i} and columns
-// {4tx + j, 64 + 4tx + j}, i, j < 4.  A k-tile is 16 deep; each thread moves 8 floats of each
-// operand per k-tile, mapped so that consecutive lanes write consecutive shared-memory words.
-template <int TA, int TB>
-__global__ void __launch_bounds__(kGemmThreads, 2) sgemm_batched_kernel(const GemmDesc* descs) {
-  __shared__ __align__(16) float As[2][kTK][kTM + kPad];
-  __shared__ __align__(16) float Bs[2][kTK][kTN + kPad];
-  const GemmDesc d = descs[blockIdx.z];
-  const int m0 = blockIdx.y * kTM, n0 = blockIdx.x * kTN;
-  if (m0 >= d.m || n0 >= d.n) return;
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  // k-major operand (A with ta = 0, B with tb = 1): lane -> row tid & 127, k half tid >> 7;
-  // mn-major operand (A with ta = 1, B with tb = 0): k tid >> 4, 8 columns from (tid & 15) * 8
-  const int kr_row = tid & 127, kr_k = (tid >> 7) * 8;
-  const int mr_k = tid >> 4, mr_c = (tid & 15) * 8;
-
-  float ra[8], rb[8];
-  auto load_tile = [&](int k0) {
-    if (TA == 0) load8(d.a, d.lda, m0 + kr_row, k0 + kr_k, d.m, d.k, ra);
-    else load8(d.a, d.lda, k0 + mr_k, m0 + mr_c, d.k, d.m, ra);
-    if (TB == 0) load8(d.b, d.ldb, k0 + mr_k, n0 + mr_c, d.k, d.n, rb);
-    else load8(d.b, d.ldb, n0 + kr_row, k0 + kr_k, d.n, d.k, rb);
-  };
-  auto store_tile = [&](int buf) {
-    if (TA == 0) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) As[buf][kr_k + u][kr_row] = ra[u];
-    } else {
-      *reinterpret_cast<float4*>(&As[buf][mr_k][mr_c]) = make_float4(ra[0], ra[1], ra[2], ra[3]);
-      *reinterpret_cast<float4*>(&As[buf][mr_k][mr_c + 4]) =
-          make_float4(ra[4], ra[5], ra[6], ra[7]);
-    }
-    if (TB == 0) {
-      *reinterpret_cast<float4*>(&Bs[buf][mr_k][mr_c]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
-      *reinterpret_cast<float4*>(&Bs[buf][mr_k][mr_c + 4]) =
-          make_float4(rb[4], rb[5], rb[6], rb[7]);
-    } else {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) Bs[buf][kr_k + u][kr_row] = rb[u];
-    }
-  };
-
-  float acc[8][8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-
-  const int ntiles = (d.k + kTK - 1) / kTK;
-  load_tile(0);
-  store_tile(0);
-  __syncthreads();
-  for (int kt = 0; kt < ntiles; ++kt) {
-    const int buf = kt & 1;
-    if (kt + 1 < ntiles) load_tile((kt + 1) * kTK);
-#pragma unroll
-    for (int kk = 0; kk < kTK; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][4 * ty]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + 4 * ty]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][4 * tx]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + 4 * tx]);
-      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-    if (kt + 1 < ntiles) store_tile(buf ^ 1);
-    __syncthreads();
-  }
-
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int mm = m0 + (i < 4 ? 4 * ty + i : 64 + 4 * ty + i - 4);
-    if (mm >= d.m) continue;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int nn = n0 + (j < 4 ? 4 * tx + j : 64 + 4 * tx + j - 4);
-      if (nn >= d.n) continue;
-      float* cp = d.c + (int64_t)mm * d.ldc + nn;
-      float v = d.alpha * acc[i][j];
-      if (d.beta != 0.f) v = fmaf(d.beta, *cp, v);
-      *cp = v;
-      if (d.t_out) d.t_out[(int64_t)mm * d.ldc + nn] = ((mm == nn ? 5.f : 0.f) - v) * 0.25f;
-    }
-  }
-}
 
 // ||A||_F of each matrix (fp64, fixed order: per-thread strided sums, then a tree).
 struct NormDesc {
@@ -294,26 +179,6 @@ __global__ void root_prep_split_kernel(const RootPrepDesc* descs) {
   }
 }
 
-// T = (5I - M) / 4 from the split M, as a split pair.
-struct TDesc {
-  const uint16_t *m_hi, *m_lo;
-  uint16_t *t_hi, *t_lo;
-  int32_t dim, ld;
-};
-
-__global__ void t_from_m_kernel(const TDesc* descs) {
-  const TDesc d = descs[blockIdx.y];
-  const int64_t n = (int64_t)d.dim * d.dim;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = e / d.dim, col = e % d.dim, o = r * d.ld + col;
-    uint16_t h, l;
-    split_bf16(((r == col ? 5.f : 0.f) - join_bf16(d.m_hi[o], d.m_lo[o])) * 0.25f, h, l);
-    d.t_hi[o] = h;
-    d.t_lo[o] = l;
-  }
-}
-
 // W = W (1 - lr wd) - lr (P_hi + P_lo) for one matrix (P pitch ldp).
 __global__ void update_split_kernel(float* w, const uint16_t* p_hi, const uint16_t* p_lo,
                                     int32_t rows, int32_t cols, int32_t ldp, float decay,
@@ -331,18 +196,6 @@ __global__ void update_split_kernel(float* w, const uint16_t* p_hi, const uint16
 }
 
 }  // namespace
-
-int launch_gemm(const GemmDesc* dev_descs, int nprob, int max_m, int max_n, int ta, int tb,
-                cudaStream_t st) {
-  if (nprob <= 0) return MFSDP_OK;
-  const dim3 grid((unsigned)((max_n + kTN - 1) / kTN), (unsigned)((max_m + kTM - 1) / kTM),
-                  (unsigned)nprob);
-  if (ta == 0 && tb == 0) sgemm_batched_kernel<0, 0><<<grid, kGemmThreads, 0, st>>>(dev_descs);
-  else if (ta == 0 && tb == 1) sgemm_batched_kernel<0, 1><<<grid, kGemmThreads, 0, st>>>(dev_descs);
-  else if (ta == 1 && tb == 0) sgemm_batched_kernel<1, 0><<<grid, kGemmThreads, 0, st>>>(dev_descs);
-  else sgemm_batched_kernel<1, 1><<<grid, kGemmThreads, 0, st>>>(dev_descs);
-  return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
-}
 
 }  // namespace mfsdp
 
@@ -372,16 +225,6 @@ struct mfsdp_shampoo_set {
   size_t tc_off_norms = 0, tc_off_fnorm = 0, tc_off_tables = 0, tc_table_bytes = 0;
   size_t tc_ws_bytes = 0;
   mutable int tc_pairs = 0, tc_pairs_dev = -1;  // co-resident pairs of the split pair kernel
-  int max_rows() const {
-    int64_t v = 0;
-    for (const auto& m : mats) v = std::max(v, m.rows);
-    return (int)v;
-  }
-  int max_cols() const {
-    int64_t v = 0;
-    for (const auto& m : mats) v = std::max(v, m.cols);
-    return (int)v;
-  }
 };
 
 namespace {
@@ -395,8 +238,9 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 namespace {
 
 // Split-kernel launches of a step.  One root iteration is three launches over every side:
-// kXT (X' = T X and T2 = T T, both from the current T), kT4 (T4 = T2 T2) and kTM (M' = T4 M),
-// then T = (5I - M') / 4 elementwise; the last iteration runs only the X' tiles of kXT.
+// kXT (X' = T X and T2 = T T, both from the current T), kT4 (T4 = T2 T2) and kTM (M' = T4 M,
+// whose epilogue also writes the next T = (5I - M') / 4); the last iteration runs only the X'
+// tiles of kXT.
 // Every side product is a polynomial in the statistics matrix, so symmetric: only the tiles
 // touching the upper triangle run and the epilogue mirrors them.
 constexpr int kTcLaunches = 7;
@@ -483,7 +327,12 @@ void tc_tables(const mfsdp_shampoo_set* s, uint8_t* base, int root_iters, int pa
     auto& xt = tt.probs[par ? kXT1 : kXT0];
     for (int k = 0; k < 2 * n; ++k) xt.push_back(side(k, T, xi, xo));
     for (int k = 0; k < 2 * n; ++k) xt.push_back(side(k, T, T, T2));
-    for (int k = 0; k < 2 * n; ++k) tt.probs[par ? kTM1 : kTM0].push_back(side(k, T4, mi, mo));
+    for (int k = 0; k < 2 * n; ++k) {  // M' = T4 M, and from its epilogue T = (5I - M') / 4
+      NsProblem p = side(k, T4, mi, mo);
+      p.t_hi = sbuf(k, T, 0);
+      p.t_lo = sbuf(k, T, 1);
+      tt.probs[par ? kTM1 : kTM0].push_back(p);
+    }
   }
   for (int k = 0; k < 2 * n; ++k) tt.probs[kT4].push_back(side(k, T2, T2, T4));
   // P = X_L G X_R with the roots in X[root_iters & 1]: Y = X_L G, P = Y X_R
@@ -528,8 +377,7 @@ size_t tc_table_bytes(const TcTables& tt, int n) {
     b += align256(sizeof(NsProblem) * std::max<size_t>(tt.probs[l].size(), 1)) +
          align256(sizeof(NsTile) * std::max<size_t>(tt.tiles[l].size(), 1));
   b += align256(sizeof(GemmDesc) * 2 * (size_t)n) + align256(sizeof(NormDesc) * 2 * (size_t)n) +
-       align256(sizeof(RootPrepDesc) * 2 * (size_t)n) + align256(sizeof(TDesc) * 4 * (size_t)n) +
-       align256(sizeof(SplitDesc) * (size_t)n);
+       align256(sizeof(RootPrepDesc) * 2 * (size_t)n) + align256(sizeof(SplitDesc) * (size_t)n);
   return b;
 }
 
@@ -709,7 +557,6 @@ int shampoo_step_split(const mfsdp_shampoo_set* set, const float* grad, float* l
   std::vector<GemmDesc> stats(2 * (size_t)n);
   std::vector<NormDesc> nd(2 * (size_t)n);
   std::vector<RootPrepDesc> pd(2 * (size_t)n);
-  std::vector<TDesc> td(4 * (size_t)n);
   std::vector<SplitDesc> sp((size_t)n);
   for (int i = 0; i < n; ++i) {
     const auto& m = set->mats[(size_t)i];
@@ -726,9 +573,6 @@ int shampoo_step_split(const mfsdp_shampoo_set* set, const float* grad, float* l
     nd[k] = {a, (int64_t)d * d, norms + k};
     pd[k] = {a, norms + k, sbuf(k, X0, 0), sbuf(k, X0, 1), sbuf(k, M0, 0), sbuf(k, M0, 1),
              sbuf(k, T, 0), sbuf(k, T, 1), d, ld};
-    // after an even iteration M is in M1, after an odd one in M0
-    td[k] = {sbuf(k, M1, 0), sbuf(k, M1, 1), sbuf(k, T, 0), sbuf(k, T, 1), d, ld};
-    td[2 * n + k] = {sbuf(k, M0, 0), sbuf(k, M0, 1), sbuf(k, T, 0), sbuf(k, T, 1), d, ld};
   }
 
   // one upload, in the layout the table area is sized for
@@ -749,7 +593,6 @@ int shampoo_step_split(const mfsdp_shampoo_set* set, const float* grad, float* l
   const size_t o_stats = put(stats.data(), stats.size() * sizeof(GemmDesc));
   const size_t o_norm = put(nd.data(), nd.size() * sizeof(NormDesc));
   const size_t o_prep = put(pd.data(), pd.size() * sizeof(RootPrepDesc));
-  const size_t o_t = put(td.data(), td.size() * sizeof(TDesc));
   const size_t o_split = put(sp.data(), sp.size() * sizeof(SplitDesc));
   if (at > set->tc_table_bytes) return MFSDP_EWORKSPACE;
   uint8_t* tab = ws + set->tc_off_tables;
@@ -779,23 +622,19 @@ int shampoo_step_split(const mfsdp_shampoo_set* set, const float* grad, float* l
   int e;
   // statistics: L += G G^T, R += G^T G (fp32), and G as a split pair
   const GemmDesc* d_stats = reinterpret_cast<const GemmDesc*>(tab + o_stats);
-  if ((e = launch_gemm(d_stats, n, set->max_rows(), set->max_rows(), 0, 1, st)) != MFSDP_OK)
-    return e;
-  if ((e = launch_gemm(d_stats + n, n, set->max_cols(), set->max_cols(), 1, 0, st)) != MFSDP_OK)
-    return e;
+  if ((e = launch_gemm(d_stats, stats.data(), n, 0, 1, st)) != MFSDP_OK) return e;
+  if ((e = launch_gemm(d_stats + n, stats.data() + n, n, 1, 0, st)) != MFSDP_OK) return e;
   to_split_kernel<<<dim3(128, nb), 256, 0, st>>>(reinterpret_cast<const SplitDesc*>(tab + o_split));
   frob_kernel<<<2 * n, 1024, 0, st>>>(reinterpret_cast<const NormDesc*>(tab + o_norm));
   root_prep_split_kernel<<<dim3(256, 2 * nb), 256, 0, st>>>(
       reinterpret_cast<const RootPrepDesc*>(tab + o_prep));
   if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
-  const TDesc* d_t = reinterpret_cast<const TDesc*>(tab + o_t);
   for (int it = 0; it < root_iters; ++it) {
     const int par = it & 1;
     const bool last = it + 1 == root_iters;
     if (!ns(par ? kXT1 : kXT0, last ? tt.x_tiles[par] : all(par ? kXT1 : kXT0))) return MFSDP_ECUDA;
     if (last) break;
     if (!ns(kT4, all(kT4)) || !ns(par ? kTM1 : kTM0, all(par ? kTM1 : kTM0))) return MFSDP_ECUDA;
-    t_from_m_kernel<<<dim3(256, 2 * nb), 256, 0, st>>>(d_t + par * 2 * n);
   }
   // P = X_L G X_R
   if (!ns(kY, all(kY)) || !ns(kP, all(kP))) return MFSDP_ECUDA;
@@ -837,12 +676,6 @@ extern "C" int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* gra
            (int64_t)b * set->side_dim[(size_t)(sd * n + i)] * set->side_dim[(size_t)(sd * n + i)];
   };
   enum { X0 = 0, X1 = 1, M0 = 2, M1 = 3, T = 4, T2 = 5, T4 = 6 };
-  int max_rows = 0, max_cols = 0;
-  for (const auto& m : set->mats) {
-    max_rows = std::max(max_rows, (int)m.rows);
-    max_cols = std::max(max_cols, (int)m.cols);
-  }
-  const int max_dim = std::max(max_rows, max_cols);
 
   // Host tables, uploaded once per step.
   std::vector<GemmDesc> stats(2 * (size_t)n), iter(4 * 2 * (size_t)n), pre(2 * (size_t)n);
@@ -926,21 +759,23 @@ extern "C" int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* gra
 
   int e;
   // statistics: L += G G^T, R += G^T G
-  if ((e = launch_gemm(d_stats, n, max_rows, max_rows, 0, 1, st)) != MFSDP_OK) return e;
-  if ((e = launch_gemm(d_stats + n, n, max_cols, max_cols, 1, 0, st)) != MFSDP_OK) return e;
+  if ((e = launch_gemm(d_stats, stats.data(), n, 0, 1, st)) != MFSDP_OK) return e;
+  if ((e = launch_gemm(d_stats + n, stats.data() + n, n, 1, 0, st)) != MFSDP_OK) return e;
   // inverse fourth roots of every L and R
   frob_kernel<<<2 * n, 1024, 0, st>>>(d_norm);
   root_prep_kernel<<<dim3(256, (unsigned)(2 * n)), 256, 0, st>>>(d_prep);
   if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
   for (int it = 0; it < root_iters; ++it) {
     const GemmDesc* tbl = (it & 1) ? d_odd : d_even;
+    const GemmDesc* htbl = (it & 1) ? iter_odd.data() : iter.data();
     for (int prod = 0; prod < 4; ++prod)
-      if ((e = launch_gemm(tbl + prod * 2 * n, 2 * n, max_dim, max_dim, 0, 0, st)) != MFSDP_OK)
+      if ((e = launch_gemm(tbl + prod * 2 * n, htbl + prod * 2 * n, 2 * n, 0, 0, st)) !=
+          MFSDP_OK)
         return e;
   }
   // P = L^{-1/4} G R^{-1/4}
-  if ((e = launch_gemm(d_pre, n, max_rows, max_cols, 0, 0, st)) != MFSDP_OK) return e;
-  if ((e = launch_gemm(d_pre + n, n, max_rows, max_cols, 0, 0, st)) != MFSDP_OK) return e;
+  if ((e = launch_gemm(d_pre, pre.data(), n, 0, 0, st)) != MFSDP_OK) return e;
+  if ((e = launch_gemm(d_pre + n, pre.data() + n, n, 0, 0, st)) != MFSDP_OK) return e;
   // W = W (1 - lr wd) - lr P, matrix by matrix
   int* status = status_word_address();
   if (status == nullptr) return MFSDP_ECUDA;

@@ -851,20 +851,9 @@ const T* put(std::vector<uint8_t>& host, size_t& at, uint8_t* dev, const std::ve
   return p;
 }
 
-int gemm_max(const std::vector<GemmDesc>& v, int& mm, int& mn) {
-  mm = mn = 0;
-  for (const auto& g : v) {
-    mm = std::max(mm, g.m);
-    mn = std::max(mn, g.n);
-  }
-  return (int)v.size();
-}
-
 int run_gemms(const std::vector<GemmDesc>& v, const GemmDesc* dev, int ta, int tb,
               cudaStream_t st) {
-  int mm, mn;
-  const int cnt = gemm_max(v, mm, mn);
-  return launch_gemm(dev, cnt, mm, mn, ta, tb, st);
+  return launch_gemm(dev, v.data(), (int)v.size(), ta, tb, st);
 }
 
 }  // namespace

@@ -12,7 +12,7 @@ import ctypes as C
 from typing import Optional, Sequence, Tuple
 
 from . import _lib
-from ._lib import CostModel, Matrix, ParamDesc, RankResources, Segment
+from ._lib import CostModel, GemmProblem, Matrix, ParamDesc, RankResources, Segment
 
 POLICY_ROLE_GREEDY = 0
 POLICY_SCOPE_GREEDY = 1
@@ -410,3 +410,31 @@ def mfsdp_set_wait_limit_ns(limit_ns: int) -> None:
 def mfsdp_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     _check("mfsdp_selftest_wait_timeout",
            _lib.load().mfsdp_selftest_wait_timeout(limit_ns, _stream(stream)))
+
+
+# ------------------------------------------------------------------------------- fp32 GEMM
+def mfsdp_gemm_f32_batched(problems, trans_a: bool = False, trans_b: bool = False,
+                           workspace=None, stream=None) -> None:
+    """C_i = alpha_i op(A_i) op(B_i) + beta_i C_i for every (A, B, C, alpha, beta) in
+    ``problems`` (fp32 2D tensors on the current device, row-major with unit column stride);
+    op = transpose where ``trans_a`` / ``trans_b``.  ``workspace`` (uint8 tensor) defaults
+    to a fresh one of mfsdp_gemm_f32_workspace_bytes(len(problems)) bytes."""
+    import torch
+    lib = _lib.load()
+    n = len(problems)
+    tab = (GemmProblem * max(n, 1))()
+    for i, (a, b, c, alpha, beta) in enumerate(problems):
+        for t in (a, b, c):
+            if t.dtype != torch.float32 or t.dim() != 2 or t.stride(1) != 1:
+                raise TypeError("fp32 2D row-major tensors expected")
+        m, k = (a.shape[1], a.shape[0]) if trans_a else (a.shape[0], a.shape[1])
+        nn = b.shape[0] if trans_b else b.shape[1]
+        tab[i] = GemmProblem(a.data_ptr(), b.data_ptr(), c.data_ptr(), m, nn, k, a.stride(0),
+                             b.stride(0), c.stride(0), alpha, beta)
+    if workspace is None:
+        workspace = torch.empty(max(lib.mfsdp_gemm_f32_workspace_bytes(n), 1), dtype=torch.uint8,
+                                device=problems[0][2].device if n else None)
+    _check("mfsdp_gemm_f32_batched",
+           lib.mfsdp_gemm_f32_batched(tab, n, 1 if trans_a else 0, 1 if trans_b else 0,
+                                      _ptr(workspace), workspace.numel(), _stream(stream)))
+

@@ -92,7 +92,7 @@ def test_our_arm_line():
     assert d["gpu_launches"] == 19 * 3
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     assert d["device_status"] == 0
-    assert d["repack"]["bound"] == "hbm" and d["shampoo"]["bound"] == "alu"
+    assert d["repack"]["bound"] == "hbm" and d["shampoo"]["bound"] == "tensor"
     assert d["shampoo_tc"]["bound"] == "tensor" and d["shampoo_tc"]["ms"] > 0
     assert d["soap"]["bound"] == "alu" and d["soap"]["ms"] > 0
     assert all(x > 0 for x in d["soap"]["sweeps_per_side"])
