@@ -62,8 +62,10 @@ NS_TRAFFIC_SOURCES = ("matrix_optimizer_owner_gb300/csrc/ns_gemm.cu",
                       "matrix_optimizer_owner_gb300/csrc/mfsdp_internal.h")
 NS_TRAFFIC = {
     # config index: (sources sha256, bytes per launch, profile summary)
-    1: ("8315436d1345252bd2113557d77646727f05dfcc13ac7795d921205e395e9ddd", 208986341,
+    1: ("675dbfcdc57e3188bf1d042db694a7176e23005c54fd9b5e3c26ef2812d82eae", 209326353,
         "profiles/owner_step_gpt2_small_launch_list.md"),
+    4: ("675dbfcdc57e3188bf1d042db694a7176e23005c54fd9b5e3c26ef2812d82eae", 71367272721,
+        "profiles/owner_step_llama3_70b_launch_list.md"),
 }
 
 
@@ -83,10 +85,10 @@ def ns_sources_sha():
     return h.hexdigest()
 
 
-def ns_traffic_per_launch(wb, args):
-    if args.shapes or args.config not in NS_TRAFFIC:
+def ns_traffic_per_launch(cfg):
+    if cfg is None or cfg not in NS_TRAFFIC:
         return None
-    sha, nbytes, _ = NS_TRAFFIC[args.config]
+    sha, nbytes, _ = NS_TRAFFIC[cfg]
     return nbytes if sha == ns_sources_sha() else None
 
 
@@ -561,7 +563,7 @@ def config_block(wb, cfg):
     return config_of(wb.wl, cfg, wb.rank, wb.shapes, wb.lay.n_tail)
 
 
-def measure_step(wb, args, stream, peaks, peak_src, world, dev, local_rank):
+def measure_step(wb, cfg, args, stream, peaks, peak_src, world, dev, local_rank):
     """Owner-step time of one resident workload (call by call with per-phase events, then as a
     CUDA graph), with the clock record of both timed regions and the Newton–Schulz roofline."""
     if world > 1:
@@ -612,7 +614,7 @@ def measure_step(wb, args, stream, peaks, peak_src, world, dev, local_rank):
         "roofline": {"kernel": wb.ns_kernel_name(), "bound": "tensor",
                      "achieved": round(ns_tf_exec, 1), "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": round(ns_tf_exec / peak_tf, 4),
-                     "traffic": ns_traffic_per_launch(wb, args),
+                     "traffic": ns_traffic_per_launch(cfg),
                      "peak_source": f"{peak_src} bf16 {'sustained' if sustained else 'burst'}",
                      "launches_per_step": ns_launches,
                      "avg_launch_us": round(1e3 * ns_ms / ns_launches, 2),
@@ -665,7 +667,8 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     peaks, peak_src = load_peaks()
 
-    m = measure_step(wb, args, stream, peaks, peak_src, world, dev, local_rank)
+    m = measure_step(wb, None if args.shapes else args.config, args, stream, peaks, peak_src,
+                     world, dev, local_rank)
     status = mfsdp.mfsdp_query_status()
     ms = m.pop("ms_per_step")
     clocks = m.pop("clocks")
@@ -711,7 +714,7 @@ def run_ours(args, rank, world, local_rank):
     # same step, reported beside the headline workload.
     if not args.shapes and args.config != 1 and not args.no_gpt2_small:
         wb1 = Workload(1, rank, dev)
-        m1 = measure_step(wb1, args, stream, peaks, peak_src, world, dev, local_rank)
+        m1 = measure_step(wb1, 1, args, stream, peaks, peak_src, world, dev, local_rank)
         m1["ms_per_step"] = round(m1["ms_per_step"], 4)
         line["gpt2_small"] = {"config": config_block(wb1, 1), **m1,
                               "device_status": mfsdp.mfsdp_query_status()}
