@@ -1179,10 +1179,23 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
           sts128(stg + stg_off(lane, k), make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2],
                                                     hw[4 * k + 3]));
         if (sym) {
+          // the transpose, 8 x 8 sub-blocks at a time: ldmatrix.trans reads sub-blocks
+          // (n, 0..3) of the staged block transposed into registers and stmatrix writes them as
+          // sub-blocks (0..3, n) of the transposed block (both conflict-free in this layout)
+          __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            sts16(stg_t + stg_off(j, lane >> 3) + (uint32_t)((lane & 7) * 2),
-                  (uint16_t)(hw[j >> 1] >> (16 * (j & 1))));
+          for (int n = 0; n < 4; ++n) {
+            uint32_t t0, t1, t2, t3;
+            asm volatile(
+                "ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                : "=r"(t0), "=r"(t1), "=r"(t2), "=r"(t3)
+                : "r"(stg + stg_off(8 * n + (lane & 7), lane >> 3))
+                : "memory");
+            asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(
+                             stg_t + stg_off(lane, n)),
+                         "r"(t0), "r"(t1), "r"(t2), "r"(t3)
+                         : "memory");
+          }
         }
         const bool diag = sym && c0 == rw;
         if (diag) {

@@ -14,16 +14,18 @@
 // GEMM's accuracy.
 //
 // Structure (one CTA per SM, 512 threads in four warpgroups, registers split by setmaxnreg):
-//   warps 0-3    producers (136 registers): load a 128 x 32 tile of op(A) and a 256 x 32
-//                tile of op(B) from global memory with 16-byte loads (zero outside the
-//                problem), split every value into hi and lo, and store both into the
+//   warps 0-3    producers (104 registers): copy a 128 x 32 tile of op(A) and a 256 x 32
+//                tile of op(B) from global memory with cp.async straight into the
 //                128-byte-swizzled K-major layout the MMA reads (an MN-major operand, stored
-//                transposed, is transposed in registers on the way); two stages of 96 KB
-//                (A hi, B hi, A lo, B lo), full / empty mbarriers;
+//                transposed, value by value to its transposed place; zero outside the
+//                problem), then split each value in place into hi and lo; two stages of
+//                96 KB (A hi, B hi, A lo, B lo), full / empty mbarriers.  A k-block is split
+//                as soon as its copies land and the next one's copies go out as soon as its
+//                stage is free, so they fly while the MMA works on the other stage;
 //   warp 4       lane 0 issues the MMAs (M = 128, N = 256, K = 8; 12 per k-block) into one of
 //                two TMEM accumulators (2 x 256 columns), one k-block each, alternating;
 //                warps 5-7 idle (24 registers);
-//   warps 8-15   epilogue (168 registers): warp w reads TMEM lanes 32 (w % 4) .. + 31 and
+//   warps 8-15   epilogue (176 registers): warp w reads TMEM lanes 32 (w % 4) .. + 31 and
 //                columns 128 ((w - 8) / 4) .. + 127 of each k-block partial (tcgen05.ld),
 //                adds them into a 128-value running sum per thread, releases the
 //                accumulator, and at the end of the tile writes alpha * sum + beta * C (and
@@ -62,7 +64,7 @@ constexpr uint32_t kGSmem = 1024 + kGBarOffset + 256;
 constexpr uint32_t kGTmemCols = 2 * kGN;
 // Registers per thread after setmaxnreg: the four warpgroups together must stay within the
 // 512 x 128 the block is launched with (launch_gemm checks the kernel's register count).
-constexpr int kGRegsProd = 136, kGRegsMma = 24, kGRegsEpi = 168;
+constexpr int kGRegsProd = 104, kGRegsMma = 24, kGRegsEpi = 176;
 static_assert(128 * kGRegsProd + 128 * kGRegsMma + 256 * kGRegsEpi <= kGThreads * 128,
               "register split");
 static_assert(kGRegsMma <= 128 && kGRegsEpi >= 128, "the MMA warpgroup frees, the epilogue takes");
@@ -178,9 +180,6 @@ __device__ __forceinline__ void sts128f(uint32_t a, float4 v) {
                "f"(v.z), "f"(v.w)
                : "memory");
 }
-__device__ __forceinline__ void sts32f(uint32_t a, float v) {
-  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
-}
 
 __device__ __forceinline__ bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
@@ -202,16 +201,6 @@ __device__ __forceinline__ uint32_t tile_off(int r, int k) {
                     (k & 3) * 4);
 }
 
-// Four consecutive fp32 of `p` (zero past `avail`), one 16-byte load when possible.
-__device__ __forceinline__ float4 load4(const float* p, int avail) {
-  if (avail >= 4 && aligned16(p)) return __ldg(reinterpret_cast<const float4*>(p));
-  float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (avail > 0) x.x = p[0];
-  if (avail > 1) x.y = p[1];
-  if (avail > 2) x.z = p[2];
-  if (avail > 3) x.w = p[3];
-  return x;
-}
 
 // Split four values and store them as one 16-byte chunk (hi and lo halves) at byte `off`.
 __device__ __forceinline__ void store_split4(uint32_t s_hi, uint32_t off, float4 x) {
@@ -224,69 +213,123 @@ __device__ __forceinline__ void store_split4(uint32_t s_hi, uint32_t off, float4
   sts128f(s_hi + kGLoOffset + off, lo);
 }
 
+// ---------------------------------------------------------------- asynchronous operand copies
+__device__ __forceinline__ void cp_async16(uint32_t dst, const float* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const float* src, int bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128u(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 lds128f(uint32_t a) {
+  const uint4 v = lds128u(a);
+  return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                     __uint_as_float(v.w));
+}
+// Copy four consecutive fp32 (`avail` of them inside the operand, the rest zero-filled) from
+// global to shared memory with cp.async: one 16-byte copy when the source is 16-byte aligned,
+// else four 4-byte copies.
+__device__ __forceinline__ void copy4(uint32_t dst, const float* src, int avail,
+                                      const float* base) {
+  const int bytes = avail >= 4 ? 16 : (avail > 0 ? 4 * avail : 0);
+  if (bytes == 0) {
+    cp_async16(dst, base, 0);  // nothing read: zero fill
+  } else if (aligned16(src)) {
+    cp_async16(dst, src, bytes);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cp_async4(dst + 4 * e, e < avail ? src + e : base, e < avail ? 4 : 0);
+  }
+}
+
 // One operand tile (R rows x 32 k) of a k-block, moved by the 128 producer threads (p = thread
-// index) in two steps: load_operand() reads it from global memory into registers (R / 16
-// 16-byte loads per thread, zero outside the problem), store_operand() splits the values and
-// writes hi and lo into shared memory.  The loads of a k-block are issued before the
-// producers wait for its stage to be free, so their latency overlaps the MMAs of the two
-// k-blocks in flight.
-// K-major source (element (r, k) at src[(row0 + r) * ld + k0 + k]): 16-byte chunk idx holds row
-// idx / 8, k 4 (idx % 8) .. + 3; a warp reads and stores 4 whole rows, each quarter warp one
-// row (conflict-free).
-// MN-major source (element (r, k) at src[(k0 + k) * ld + row0 + r]): a thread reads a 4 x 4
-// block (rows 4 rq .. + 3 at k 4 kq .. + 3, four 16-byte loads), which transposes in registers
-// into the four rows' chunks.  Lane l takes k quad l % 8 and row quad 4 g + l / 8: each load
-// instruction reads 64 contiguous bytes of 8 k-rows, and each quarter warp stores to 8
-// distinct 16-byte bank groups (conflict-free).
+// index) in two steps.  issue() starts asynchronous copies of the fp32 values straight to their
+// places in the stage's lo half (K-major, 128-byte-swizzled; zero outside the problem), so that
+// a k-block's loads are in flight while the previous one is converted; convert(), once this
+// thread's copies have landed, splits every 16-byte chunk it copied into hi (written to the hi
+// half) and lo (written over the raw chunk).  A thread converts exactly the chunks it copied,
+// so no other thread's copies are involved.
+// K-major source (element (r, k) at src[(row0 + r) * ld + k0 + k]): chunk idx holds row idx / 8,
+// k 4 (idx % 8) .. + 3, one 16-byte copy; a quarter warp covers one row (conflict-free).
+// MN-major source (element (r, k) at src[(k0 + k) * ld + row0 + r]): a thread takes the 4 x 4
+// block of rows 4 rq .. + 3 at k 4 kq .. + 3 (lane l: kq = l % 8, row quad 4 g + l / 8): four
+// 16-byte copies, one per k, each landing in one of the block's four final chunk places (k
+// 4 kq + i in the place of row 4 rq + i), so that the block occupies exactly the places its
+// four rows' chunks end up in; convert() transposes it in registers.  Each quarter warp
+// touches 8 distinct bank groups.
 template <int R, bool MN>
 struct Operand {
-  static constexpr int kLoads = R / 16;  // 16-byte loads per thread per k-block
-  static_assert(R * 8 == kLoads * kGProducers, "chunks per thread");
-  float4 x[kLoads];
+  static constexpr int kChunks = R / 16;  // 16-byte chunks per thread per k-block
+  static_assert(R * 8 == kChunks * kGProducers, "chunks per thread");
 
-  __device__ __forceinline__ void load(const float* src, int64_t ld, int row0, int rows, int k0,
-                                       int K, int p) {
+  __device__ __forceinline__ static void issue(const float* src, int64_t ld, int row0, int rows,
+                                               int k0, int K, uint32_t s_lo, int p) {
     if (!MN) {
 #pragma unroll
-      for (int j = 0; j < kLoads; ++j) {
+      for (int j = 0; j < kChunks; ++j) {
         const int idx = j * kGProducers + p;
         const int row = row0 + (idx >> 3), kk = k0 + 4 * (idx & 7);
-        x[j] = row < rows ? load4(src + (int64_t)row * ld + kk, K - kk)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint32_t dst = s_lo + tile_off(idx >> 3, 4 * (idx & 7));
+        if (row < rows)
+          copy4(dst, src + (int64_t)row * ld + kk, K - kk, src);
+        else
+          copy4(dst, src, 0, src);
       }
     } else {
 #pragma unroll
-      for (int b = 0; b < kLoads / 4; ++b) {
+      for (int b = 0; b < kChunks / 4; ++b) {
         const int bi = b * kGProducers + p, l = bi & 31;
         const int kq = l & 7, rq = 4 * (bi >> 5) + (l >> 3);
         const int row = row0 + 4 * rq;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int kk = k0 + 4 * kq + i;
-          x[4 * b + i] = kk < K ? load4(src + (int64_t)kk * ld + row, rows - row)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+          const uint32_t dst = s_lo + tile_off(4 * rq + i, 4 * kq);
+          if (kk < K)
+            copy4(dst, src + (int64_t)kk * ld + row, rows - row, src);
+          else
+            copy4(dst, src, 0, src);
         }
       }
     }
   }
 
-  __device__ __forceinline__ void store(uint32_t s_hi, int p) const {
+  __device__ __forceinline__ static void convert(uint32_t s_hi, uint32_t s_lo, int p) {
     if (!MN) {
 #pragma unroll
-      for (int j = 0; j < kLoads; ++j) {
+      for (int j = 0; j < kChunks; ++j) {
         const int idx = j * kGProducers + p;
-        store_split4(s_hi, tile_off(idx >> 3, 4 * (idx & 7)), x[j]);
+        const uint32_t off = tile_off(idx >> 3, 4 * (idx & 7));
+        store_split4(s_hi, off, lds128f(s_lo + off));  // lo goes over the raw chunk
       }
     } else {
 #pragma unroll
-      for (int b = 0; b < kLoads / 4; ++b) {
+      for (int b = 0; b < kChunks / 4; ++b) {
         const int bi = b * kGProducers + p, l = bi & 31;
-        const int kc = 4 * (l & 7), r0 = 4 * (4 * (bi >> 5) + (l >> 3));
-        const float4* y = x + 4 * b;
-        store_split4(s_hi, tile_off(r0, kc), make_float4(y[0].x, y[1].x, y[2].x, y[3].x));
-        store_split4(s_hi, tile_off(r0 + 1, kc), make_float4(y[0].y, y[1].y, y[2].y, y[3].y));
-        store_split4(s_hi, tile_off(r0 + 2, kc), make_float4(y[0].z, y[1].z, y[2].z, y[3].z));
-        store_split4(s_hi, tile_off(r0 + 3, kc), make_float4(y[0].w, y[1].w, y[2].w, y[3].w));
+        const int kq = l & 7, rq = 4 * (bi >> 5) + (l >> 3);
+        float4 y[4];  // y[i]: rows 4 rq .. + 3 at k 4 kq + i
+#pragma unroll
+        for (int i = 0; i < 4; ++i) y[i] = lds128f(s_lo + tile_off(4 * rq + i, 4 * kq));
+        store_split4(s_hi, tile_off(4 * rq, 4 * kq), make_float4(y[0].x, y[1].x, y[2].x, y[3].x));
+        store_split4(s_hi, tile_off(4 * rq + 1, 4 * kq), make_float4(y[0].y, y[1].y, y[2].y, y[3].y));
+        store_split4(s_hi, tile_off(4 * rq + 2, 4 * kq), make_float4(y[0].z, y[1].z, y[2].z, y[3].z));
+        store_split4(s_hi, tile_off(4 * rq + 3, 4 * kq), make_float4(y[0].w, y[1].w, y[2].w, y[3].w));
       }
     }
   }
@@ -371,33 +414,45 @@ __global__ void __launch_bounds__(kGThreads, 1) tf32x3_gemm_kernel(const __grid_
     else
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGRegsProd));
     const int p = threadIdx.x;
-    uint32_t q = 0;  // k-block sequence number over this CTA's tiles
+    // k-block j - 1 is split as soon as its copies land (its stage was free when they were
+    // issued), which can be while the MMA still works on k-block j - 2; then the producers
+    // wait for the stage of k-block j (freed by k-block j - 2) and issue its copies, which fly
+    // while the MMA works on k-block j - 1
+    uint32_t j = 0;            // k-blocks issued so far (sequence over this CTA's tiles)
     TileCursor cur;
-    for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x) {
+    bool ok = true;
+    auto finish = [&](uint32_t jj) {  // convert k-block jj and hand its stage to the MMA
+      const uint32_t sa = sbase + (jj & 1u) * kGStageBytes;
+      Operand<kGM, TA == 1>::convert(sa, sa + kGLoOffset, p);
+      Operand<kGN, TB == 0>::convert(sa + kGATile, sa + kGATile + kGLoOffset, p);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMA
+      __syncwarp();
+      if (lane == 0) bar_arrive(bar(full0 + (int)(jj & 1u)));
+    };
+    for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
       GemmDesc d;
       int m0, n0;
       cur.at(P, t, d, m0, n0);
       const int nk = (d.k + kGK - 1) / kGK;
-      bool ok = true;
-      for (int kb = 0; kb < nk; ++kb, ++q) {
-        const int stage = (int)(q & 1u);
-        Operand<kGM, TA == 1> oa;
-        Operand<kGN, TB == 0> ob;
-        oa.load(d.a, d.lda, m0, d.m, kb * kGK, d.k, p);
-        ob.load(d.b, d.ldb, n0, d.n, kb * kGK, d.k, p);
-        if (*abort_flag || !bar_wait(bar(empty0 + stage), ((q >> 1) & 1u) ^ 1u, g)) {
+      for (int kb = 0; kb < nk; ++kb, ++j) {
+        const int stage = (int)(j & 1u);
+        if (j > 0) {
+          cp_async_wait<0>();  // this thread's copies of k-block j - 1 have landed
+          finish(j - 1);
+        }
+        if (*abort_flag || !bar_wait(bar(empty0 + stage), ((j >> 1) & 1u) ^ 1u, g)) {
           ok = false;
           break;
         }
         const uint32_t sa = sbase + (uint32_t)stage * kGStageBytes;
-        oa.store(sa, p);
-        ob.store(sa + kGATile, p);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMA
-        __syncwarp();
-        if (lane == 0) bar_arrive(bar(full0 + stage));
+        Operand<kGM, TA == 1>::issue(d.a, d.lda, m0, d.m, kb * kGK, d.k, sa + kGLoOffset, p);
+        Operand<kGN, TB == 0>::issue(d.b, d.ldb, n0, d.n, kb * kGK, d.k,
+                                     sa + kGATile + kGLoOffset, p);
+        cp_async_commit();
       }
-      if (!ok) break;
     }
+    cp_async_wait<0>();
+    if (ok && j > 0) finish(j - 1);
   } else if (warp < 8) {
     // ------------------------------------------------------------ MMA issuer (warpgroup 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGRegsMma));
