@@ -62,9 +62,9 @@ NS_TRAFFIC_SOURCES = ("matrix_optimizer_owner_gb300/csrc/ns_gemm.cu",
                       "matrix_optimizer_owner_gb300/csrc/mfsdp_internal.h")
 NS_TRAFFIC = {
     # config index: (sources sha256, bytes per launch, profile summary)
-    1: ("675dbfcdc57e3188bf1d042db694a7176e23005c54fd9b5e3c26ef2812d82eae", 209326353,
+    1: ("6c2c9ce5026f8bd42752ef4a23b32d3725692e7d723ca86b502322ef0a76c1fe", 209269452,
         "profiles/owner_step_gpt2_small_launch_list.md"),
-    4: ("675dbfcdc57e3188bf1d042db694a7176e23005c54fd9b5e3c26ef2812d82eae", 71367272721,
+    4: ("6c2c9ce5026f8bd42752ef4a23b32d3725692e7d723ca86b502322ef0a76c1fe", 110805183948,
         "profiles/owner_step_llama3_70b_launch_list.md"),
 }
 
