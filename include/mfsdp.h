@@ -450,6 +450,8 @@ int mfsdp_owner_reduce_momentum(const mfsdp_owner_set* set, const void* const* c
  * products such as X X^T that couple all rows).  Per matrix, with s = 1/(norm[i] + eps):
  *     X = s * U  (U = ns_input, + ns_input_lo for split matrices), transposed if rows > cols;
  *     repeat `steps` times:  A = X X^T;  B = b*A + c*A A;  X = a*X + B X
+ *     with bf16 operands computed as A = X X^T;  B' = a*I + b*A + c*A A;  X = B' X
+ *     (a X + B X = (a I + B) X); split matrices compute B and a X + B X as written.
  *     ortho_out = X (transposed back), ortho_lo = low half for split matrices.
  * Runs as three grouped, persistent tcgen05 GEMM launches per iteration over all matrices;
  * only the upper-triangle tiles of the symmetric A and A A are computed.  Operands are bf16

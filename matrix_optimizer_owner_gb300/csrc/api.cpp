@@ -417,7 +417,7 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
     };
     auto apply = [&](int src, int dst, int first) {
       NsProblem p{};
-      if (!m.tr) {  // X' = a X + B X: B rows (K-major) times X (MN-major)
+      if (!m.tr) {  // X' = B' X (or a X + B X): B' rows (K-major) times X (MN-major)
         p.M = (int32_t)m.m;
         p.N = (int32_t)m.n;
         p.a_mn = 0;
@@ -425,7 +425,7 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
         p.map_a = mb + 2 * kMapsPerHalf * kSlotB;
         p.map_b = mb + 2 * kMapsPerHalf * src;
         p.mn3d = view3d(m, src) ? 2 : 0;
-      } else {      // Y' = a Y + Y B with Y = X^T in the caller's layout: both K-major
+      } else {      // Y' = Y B' (or a Y + Y B), Y = X^T in the caller's layout: both K-major
         p.M = (int32_t)m.n;
         p.N = (int32_t)m.m;
         p.a_mn = 0;
@@ -437,9 +437,12 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
       p.kind = kApply;
       p.first = first;
       p.mat = i;
-      p.d_hi = slot_ptr(m, src, 0);
-      p.d_lo = m.split ? slot_ptr(m, src, 1) : nullptr;
-      p.ldd = slot_ld(m, src);
+      p.fold_a = m.split ? 0 : 1;  // bf16 operands: a X is folded into B' = a I + B
+      if (m.split) {               // split operands: X' = a X + B X, X as the addend
+        p.d_hi = slot_ptr(m, src, 0);
+        p.d_lo = slot_ptr(m, src, 1);
+        p.ldd = slot_ld(m, src);
+      }
       p.o_hi = slot_ptr(m, dst, 0);
       p.o_lo = m.split ? slot_ptr(m, dst, 1) : nullptr;
       p.ldo = slot_ld(m, dst);
@@ -450,6 +453,7 @@ int mfsdp_owner_set_bind(mfsdp_owner_set* set, void* workspace, size_t workspace
     poly.M = poly.N = poly.K = (int32_t)m.m;
     poly.sym = 1;
     poly.kind = kPoly;
+    poly.fold_a = m.split ? 0 : 1;
     poly.mat = i;
     poly.map_a = poly.map_b = mb + 2 * kMapsPerHalf * kSlotA;
     poly.d_hi = slot_ptr(m, kSlotA, 0);

@@ -147,7 +147,7 @@ struct NsProblem {         // one output matrix of one Newton–Schulz phase
   int32_t M, N, K;         // output M x N, contraction length K
   int32_t a_mn, b_mn;      // operand storage: 0 = K-major rows, 1 = MN-major rows
   int32_t sym;             // symmetric output: only tiles touching the upper triangle run
-  int32_t kind;            // NsKind: epilogue out = alpha*acc + beta*D
+  int32_t kind;            // NsKind: epilogue out = alpha*acc + beta*D (see fold_a)
   int32_t first;           // first iteration: fold s = 1/(norm + eps) into alpha / beta
   int32_t mat;             // matrix index (norm)
   int32_t map_a, map_b;    // tensor-map indices of the hi operands (2D 64x64 box); +1: 2D
@@ -155,8 +155,9 @@ struct NsProblem {         // one output matrix of one Newton–Schulz phase
                            // 64-byte swizzle (stores), +kMapsPerHalf: the lo half's maps
   int32_t mn3d;            // bit 0 / bit 1: the A / B operand is MN-major and has the 3D view
   int32_t map_o;           // tensor-map index of the output's 32x32 store box (hi, 64B swizzle)
-  int32_t pad2_;
-  const uint16_t* d_hi;    // epilogue addend D (kPoly: A, kApply: X), row pitch ldd
+  int32_t fold_a;          // 1: a X is folded into B' = a I + B (kPoly adds a on the diagonal,
+                           // kApply has no addend); 0: kApply adds a * alpha * D
+  const uint16_t* d_hi;    // epilogue addend D (kPoly: A, kApply without fold_a: X), pitch ldd
   const uint16_t* d_lo;
   int64_t ldd;
   uint16_t* o_hi;          // output, row pitch ldo

@@ -2,10 +2,16 @@
 //
 // "MatrixFSDP: communication-free matrix optimizers under ZeRO-3 parameter sharding", §2: Muon
 // orthogonalises each whole 2D matrix with Newton–Schulz steps whose products include X X^T.
-// One quintic iteration, X of shape m x n with m <= n, is three products:
-//     gram  A  = X X^T            (m x m, K = n, symmetric: upper-triangle tiles only)
-//     poly  B  = b*A + c*A A      (m x m, K = m, symmetric: upper-triangle tiles only)
-//     apply X' = a*X + B X        (m x n, K = m)
+// One quintic iteration, X of shape m x n with m <= n, is X' = a X + B X with A = X X^T and
+// B = b A + c A A.  It runs as three products; with bf16 operands the a X term is folded into
+// the second one (a X + B X = (a I + B) X):
+//     gram  A  = X X^T                  (m x m, K = n, symmetric: upper-triangle tiles only)
+//     poly  B' = a*I + b*A + c*A A      (m x m, K = m, symmetric: upper-triangle tiles only)
+//     apply X' = B' X                   (m x n, K = m, no addend)
+// so that only the polynomial phase reads an addend (A, m x m) and the apply phase, the
+// largest small-K product, streams nothing but its operands.  Split (hi + lo) operands keep
+// poly B = b*A + c*A A and apply X' = a*X + B X: there B is held to ~2^-17 of its own size,
+// which for directions with small singular values is much finer than 2^-17 of a I + B.
 // A launch runs one phase for every owned matrix: a static list of 128 x 256 output tiles,
 // taken round-robin by a persistent grid of one CTA per SM.
 //
@@ -14,9 +20,10 @@
 //                      bf16 boxes into a ring of stages guarded by full/empty mbarriers;
 //   warp 1 (one lane)  MMA issuer: tcgen05.mma kind::f16 (M=128, N=256, K=16) from shared-
 //                      memory descriptors into one of two TMEM accumulators (2 x 256 columns);
-//   warps 2-9          epilogue: tcgen05.ld rows of the accumulator, out = alpha*acc + beta*D,
-//                      round to bf16 (and the low half in split mode), store; symmetric tiles
-//                      store the upper triangle and its mirror.
+//   warps 2-9          epilogue: tcgen05.ld rows of the accumulator, out = alpha*acc + beta*D
+//                      (+ a on the diagonal in a folded polynomial phase), round to bf16 (and the
+//                      low half in split mode), store; symmetric tiles store the upper triangle
+//                      and its mirror.
 // Operands come from row-major bf16 buffers.  A "K-major" operand has the contraction index
 // contiguous (rows of X for X X^T); an "MN-major" operand has the output index contiguous
 // (X as the right factor of B X).  Both map to the canonical 128-byte-swizzled UMMA layouts.
@@ -445,7 +452,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
       const bool rvalid = r < M;
       const float s = 1.f / (P.norm[pr.mat] + P.eps);
       uint4 dpre[kEpiChunks][4];
-      if (!SPLIT && kind != kGram && rvalid) {
+      if (!SPLIT && (kind == kPoly || (kind == kApply && !pr.fold_a)) && rvalid) {
 #pragma unroll
         for (int q = 0; q < kEpiChunks; ++q) {
           const int c0 = n0 + (c_first + q) * 32;
@@ -466,7 +473,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
         beta = P.b;
       } else {
         alpha = pr.first ? s : 1.f;
-        beta = P.a * alpha;
+        if (!pr.fold_a) beta = P.a * alpha;
       }
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
 #pragma unroll
@@ -504,6 +511,11 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_kernel(const __grid_con
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= alpha;
+        }
+        if (kind == kPoly && pr.fold_a && c0 == rw) {  // a on the diagonal: column `lane`
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == lane) v[j] += P.a;
         }
         uint16_t h[32], l[32];
 #pragma unroll
@@ -953,7 +965,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
         beta = P.b;
       } else {
         alpha = pr.first ? s : 1.f;
-        beta = P.a * alpha;
+        if (!pr.fold_a) beta = P.a * alpha;
       }
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
 #pragma unroll 1
@@ -977,6 +989,11 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= alpha;
+        }
+        if (kind == kPoly && pr.fold_a && c0 == rw) {  // a on the diagonal: column `lane`
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == lane) v[j] += P.a;
         }
         uint16_t h[32], l[32];
 #pragma unroll
@@ -1057,7 +1074,8 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
       const NsProblem& pp = P.probs[tl.prob];
       const int rw_ = tl.tm * 256 + 128 * (int)rank + quarter * 32;
       const int cb = tl.tn * kBN + c_first * 32;
-      if (pp.kind == kGram || rw_ >= pp.M) return d;
+      const bool has_d = pp.kind == kPoly || (pp.kind == kApply && !pp.fold_a);
+      if (!has_d || rw_ >= pp.M) return d;
       d.p = pp.d_hi + (int64_t)rw_ * pp.ldd + cb;
       d.ld = (int)pp.ldd;
       uint32_t live = 0u;
@@ -1119,7 +1137,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
         beta = P.b;
       } else {
         alpha = pr.first ? s : 1.f;
-        beta = P.a * alpha;
+        if (!pr.fold_a) beta = P.a * alpha;
       }
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
 #pragma unroll
@@ -1160,6 +1178,8 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
         }
         refill(q);
         tc_ld_wait(a32);
+        // the polynomial phase adds a on the diagonal: column `lane` of a chunk on it
+        const float dg = (kind == kPoly && pr.fold_a && c0 == rw) ? P.a : 0.f;
         uint32_t hw[16];  // bf16 pairs (column 2k in the low half)
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -1170,6 +1190,10 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
           } else {
             v0 *= alpha;
             v1 *= alpha;
+          }
+          if (dg != 0.f) {
+            if (2 * k == lane) v0 += dg;
+            if (2 * k + 1 == lane) v1 += dg;
           }
           hw[k] = pack_bf16x2(v0, v1);
         }
