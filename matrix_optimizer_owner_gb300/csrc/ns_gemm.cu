@@ -247,6 +247,39 @@ __device__ __forceinline__ void store_row32(uint16_t* p, int64_t ld, int r, int 
 // lanes step through the k-block sequence in lockstep, each round issuing a fixed sequence of
 // predicated TMA instructions (operand major-ness only changes which predicates are on).
 
+// The table fields of one tile that the pair kernel's producer and MMA roles use, copied into
+// registers.  The roles read them a tile ahead (from a tile row read two tiles ahead) and
+// only use them a tile later, so no instruction waits for these loads inside the k-block loop.
+struct TileFields {
+  int K, a_mn, b_mn, sym, map_a, map_b, mn3d, tm, tn;
+  __device__ __forceinline__ int nk() const { return (K + kBK - 1) / kBK; }
+  // A tile (256-row blocks) on the diagonal of a symmetric product whose two operands are the
+  // same rows of the same buffer (Gram: X X^T; polynomial: A A): each CTA's B half then holds
+  // exactly its A half, so only A is loaded and the MMA reads it twice.
+  __device__ __forceinline__ bool self() const {
+    return sym && tm * 256 == tn * kBN && map_a == map_b && a_mn == b_mn;
+  }
+};
+__device__ __forceinline__ NsTile tile_row(const NsLaunchParams& P, int t) {
+  return t < P.ntiles ? P.tiles[t] : NsTile{0, 0, 0, 0};
+}
+__device__ __forceinline__ TileFields tile_fields(const NsLaunchParams& P, int t,
+                                                  const NsTile& row) {
+  TileFields f{0, 0, 0, 0, 0, 0, 0, 0, 0};
+  if (t >= P.ntiles) return f;
+  const NsProblem& pr = P.probs[row.prob];
+  f.K = pr.K;
+  f.a_mn = pr.a_mn;
+  f.b_mn = pr.b_mn;
+  f.sym = pr.sym;
+  f.map_a = pr.map_a;
+  f.map_b = pr.map_b;
+  f.mn3d = pr.mn3d;
+  f.tm = row.tm;
+  f.tn = row.tn;
+  return f;
+}
+
 // Position in the k-block sequence of the tiles t0, t0 + step, ...
 struct KCursor {
   int t, kb;
@@ -833,43 +866,54 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
     // leader's A lane arms the stage's full barrier for the bytes of both CTAs.
     if (lane < 4) {
       const int par = lane >> 1, opnd = lane & 1;
-      KCursor cur{pair, par};
-      cur.norm(P, npairs);
+      // This lane's tile and k-block; the tile's table fields come a tile ahead (TileFields).
+      int t = pair, kb = par;
+      TileFields cur = tile_fields(P, t, tile_row(P, t));
+      TileFields nxt = tile_fields(P, t + npairs, tile_row(P, t + npairs));
+      NsTile row2 = tile_row(P, t + 2 * npairs);
+      auto advance = [&]() {       // past the tiles whose k-blocks this lane has left
+        while (t < P.ntiles && kb >= cur.nk()) {
+          kb -= cur.nk();
+          t += npairs;
+          cur = nxt;
+          nxt = tile_fields(P, t + npairs, row2);
+          row2 = tile_row(P, t + 2 * npairs);
+        }
+      };
+      advance();
       uint32_t q = (uint32_t)par;  // position in the k-block sequence
       uint32_t armed = 0, last_par = 0;
       int last_q = -1;             // the last k-block this lane issued
       for (;;) {
-        bool act = cur.t < P.ntiles && !*abort_flag;
+        bool act = t < P.ntiles && !*abort_flag;
         if (!__any_sync(0xFu, act)) break;
         const int stage = (int)(q % S);
         const uint32_t ph = (q / S) & 1u;
         if (act && !mbar_wait(bar(empty0 + stage), ph ^ 1u, g)) act = false;
-        const CUtensorMap* mp = P.maps;
-        int mn = 0, view3 = 0, r0 = 0, k0 = 0;
-        if (act) {
-          const NsTile tile = P.tiles[cur.t];
-          const NsProblem& pr = P.probs[tile.prob];
-          mp = P.maps + (opnd ? pr.map_b : pr.map_a);
-          mn = opnd ? pr.b_mn : pr.a_mn;
-          view3 = SPLIT ? 0 : (pr.mn3d >> opnd) & 1;
-          r0 = opnd ? tile.tn * kBN + 128 * (int)rank : tile.tm * 256 + 128 * (int)rank;
-          k0 = cur.kb * kBK;
-          if (cur.kb == 0) prefetch_map(mp + (mn ? (view3 ? 2 : 0) : 1));
-        }
+        const CUtensorMap* mp = P.maps + (opnd ? cur.map_b : cur.map_a);
+        const int mn = opnd ? cur.b_mn : cur.a_mn;
+        const int view3 = SPLIT ? 0 : (cur.mn3d >> opnd) & 1;
+        const int r0 = opnd ? cur.tn * kBN + 128 * (int)rank : cur.tm * 256 + 128 * (int)rank;
+        const int k0 = kb * kBK;
+        const bool self = cur.self();
+        if (act && kb == 0) prefetch_map(mp + (mn ? (view3 ? 2 : 0) : 1));
         const uint32_t fb_local = bar(full0 + stage);
         const uint32_t fb = map_rank(fb_local, 0);
         const uint32_t dst = sbase + (uint32_t)stage * C::kStageBytes + (opnd ? C::kHalfA : 0u);
-        expect_tx_p(act && leader && opnd == 0, fb_local, 2 * C::kStageBytes);
-        tma_load3d_pair_p(act && mn && view3, dst, mp + 2, 0, k0, r0 / 64, fb);
-        tma_load_pair_p(act && mn && !view3, dst, mp, r0, k0, fb);
-        tma_load_pair_p(act && mn && !view3, dst + kBoxBytes, mp, r0 + 64, k0, fb);
-        tma_load_pair_p(act && !mn, dst, mp + 1, k0, r0, fb);
+        // a self-operand tile loads the A halves only (both CTAs' bytes on the leader's barrier)
+        expect_tx_p(act && leader && opnd == 0, fb_local,
+                    self ? 2u * C::kOps * C::kHalfA : 2u * C::kStageBytes);
+        const bool ld = act && !(self && opnd == 1);
+        tma_load3d_pair_p(ld && mn && view3, dst, mp + 2, 0, k0, r0 / 64, fb);
+        tma_load_pair_p(ld && mn && !view3, dst, mp, r0, k0, fb);
+        tma_load_pair_p(ld && mn && !view3, dst + kBoxBytes, mp, r0 + 64, k0, fb);
+        tma_load_pair_p(ld && !mn, dst, mp + 1, k0, r0, fb);
         if constexpr (SPLIT) {  // the lo copy of the same box, from the lo half's maps
           const CUtensorMap* ml = mp + kMapsPerHalf;
           const uint32_t dl = dst + C::kLoOffset;
-          tma_load_pair_p(act && mn, dl, ml, r0, k0, fb);
-          tma_load_pair_p(act && mn, dl + kBoxBytes, ml, r0 + 64, k0, fb);
-          tma_load_pair_p(act && !mn, dl, ml + 1, k0, r0, fb);
+          tma_load_pair_p(ld && mn, dl, ml, r0, k0, fb);
+          tma_load_pair_p(ld && mn, dl + kBoxBytes, ml, r0 + 64, k0, fb);
+          tma_load_pair_p(ld && !mn, dl, ml + 1, k0, r0, fb);
         }
         if (act && opnd == 0) {
           armed |= 1u << stage;
@@ -877,8 +921,8 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
           last_q = (int)q;
         }
         q += 2;
-        cur.kb += 2;
-        cur.norm(P, npairs);
+        kb += 2;
+        advance();
       }
       // teardown: the leader's full barriers count both CTAs' bytes
       if constexpr (S % 2 == 0) {
@@ -903,11 +947,15 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
     // ------------------------------------------------------------ MMA issuer (leader only)
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
+    // the tile's table fields come a tile ahead (TileFields)
+    TileFields nxt = tile_fields(P, pair, tile_row(P, pair));
+    NsTile row1 = tile_row(P, pair + npairs);
     for (int t = pair; t < P.ntiles; t += npairs) {
-      const NsTile tile = P.tiles[t];
-      const NsProblem& pr = P.probs[tile.prob];
-      const int nk = (pr.K + kBK - 1) / kBK;
-      const int a_mn = pr.a_mn, b_mn = pr.b_mn;
+      const TileFields cur = nxt;
+      nxt = tile_fields(P, t + npairs, row1);
+      row1 = tile_row(P, t + 2 * npairs);
+      const int nk = cur.nk(), a_mn = cur.a_mn, b_mn = cur.b_mn;
+      const uint32_t b_off = cur.self() ? 0u : C::kHalfA;  // B = A on the diagonal
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) |
                              ((uint32_t)b_mn << 16) | ((uint32_t)(kBN >> 3) << 17) |
                              ((uint32_t)(256 >> 4) << 24);
@@ -919,7 +967,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
         if (!mbar_wait(bar(full0 + stage), phase, g)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sa = sbase + (uint32_t)stage * C::kStageBytes;
-        const uint32_t sbb = sa + C::kHalfA;
+        const uint32_t sbb = sa + b_off;
 #pragma unroll
         for (int j = 0; j < kBK / 16; ++j) {
           const uint64_t ad = operand_desc(sa, a_mn, j), bd = operand_desc(sbb, b_mn, j);
@@ -1058,33 +1106,55 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
     const uint32_t stg_t = stg0 + 2048u;  // the transposed block of a symmetric output
     uint32_t nstore = 0;
     const int crow = lane >> 2, cchunk = lane & 3;
-    // Where this warp's D of tile t comes from: the addend at the warp's first row and first
+    // A tile's table fields, read two tiles ahead (from a tile row read three tiles ahead), and
+    // its norm, read one tile ahead: neither the tile setup nor the addend prefetch waits for a
+    // table read.
+    struct EpiFields {
+      int M, N, kind, sym, first, fold_a, map_o, mat, tm, tn, ldd;
+      const uint16_t* d_hi;
+    };
+    auto epi_fields = [&](int t, const NsTile& row) {
+      EpiFields f{0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, nullptr};
+      if (t >= P.ntiles) return f;
+      const NsProblem& pp = P.probs[row.prob];
+      f.M = pp.M;
+      f.N = pp.N;
+      f.kind = pp.kind;
+      f.sym = pp.sym;
+      f.first = pp.first;
+      f.fold_a = pp.fold_a;
+      f.map_o = pp.map_o;
+      f.mat = pp.mat;
+      f.tm = row.tm;
+      f.tn = row.tn;
+      f.ldd = (int)pp.ldd;
+      f.d_hi = pp.d_hi;
+      return f;
+    };
+    // Where this warp's D of a tile comes from: the addend at the warp's first row and first
     // column, its pitch, and packed in one word which of the four chunks have one (bits 0-3),
     // the rows left from there (bits 4-9, at most 32) and the columns left (bits 10-17, at
-    // most 128).
+    // most 128).  A tile past the end (M = 0) has none.
     struct DSrc {
       const uint16_t* p;
       int ld;
       uint32_t bits;
     };
-    auto dsrc_of = [&](int t) {
+    auto dsrc_of = [&](const EpiFields& f) {
       DSrc d{nullptr, 0, 0u};
-      if (t >= P.ntiles) return d;
-      const NsTile tl = P.tiles[t];
-      const NsProblem& pp = P.probs[tl.prob];
-      const int rw_ = tl.tm * 256 + 128 * (int)rank + quarter * 32;
-      const int cb = tl.tn * kBN + c_first * 32;
-      const bool has_d = pp.kind == kPoly || (pp.kind == kApply && !pp.fold_a);
-      if (!has_d || rw_ >= pp.M) return d;
-      d.p = pp.d_hi + (int64_t)rw_ * pp.ldd + cb;
-      d.ld = (int)pp.ldd;
+      const int rw_ = f.tm * 256 + 128 * (int)rank + quarter * 32;
+      const int cb = f.tn * kBN + c_first * 32;
+      const bool has_d = f.kind == kPoly || (f.kind == kApply && !f.fold_a);
+      if (!has_d || rw_ >= f.M) return d;
+      d.p = f.d_hi + (int64_t)rw_ * f.ldd + cb;
+      d.ld = f.ldd;
       uint32_t live = 0u;
 #pragma unroll
       for (int q = 0; q < kEpiChunks; ++q) {
         const int c0_ = cb + 32 * q;
-        if (c0_ < pp.N && !(pp.sym && c0_ + 31 < rw_)) live |= 1u << q;
+        if (c0_ < f.N && !(f.sym && c0_ + 31 < rw_)) live |= 1u << q;
       }
-      const uint32_t rows = (uint32_t)min(pp.M - rw_, 32), cols = (uint32_t)min(pp.N - cb, 128);
+      const uint32_t rows = (uint32_t)min(f.M - rw_, 32), cols = (uint32_t)min(f.N - cb, 128);
       d.bits = live | (rows << 4) | (cols << 10);
       return d;
     };
@@ -1105,21 +1175,27 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
     // D is prefetched two chunks ahead (chunk q + 2 of the tile, or chunk q - 2 of the next
     // one), in a ring of two register slots: slot q & 1 holds chunk q.
     uint4 dpre[2][4];
-    DSrc cur = dsrc_of(pair);
+    EpiFields f0 = epi_fields(pair, tile_row(P, pair));
+    EpiFields f1 = epi_fields(pair + npairs, tile_row(P, pair + npairs));
+    NsTile row2 = tile_row(P, pair + 2 * npairs);
+    float nrm0 = P.norm[f0.mat];
+    DSrc cur = dsrc_of(f0);
     load_d(cur, 0, dpre[0]);
     load_d(cur, 1, dpre[1]);
-    DSrc nxt = dsrc_of(pair + npairs);  // the tables are read a tile before they are needed
+    DSrc nxt = dsrc_of(f1);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = pair; t < P.ntiles; t += npairs) {
-      const NsTile tile = P.tiles[t];
-      const NsProblem& pr = P.probs[tile.prob];
-      const int M = pr.M, N = pr.N, kind = pr.kind, sym = pr.sym;
-      const int m0 = tile.tm * 256 + 128 * (int)rank, n0 = tile.tn * kBN;
+      const EpiFields f = f0;
+      const int M = f.M, N = f.N, kind = f.kind, sym = f.sym;
+      const int m0 = f.tm * 256 + 128 * (int)rank, n0 = f.tn * kBN;
       const int rw = m0 + quarter * 32;
       const int r = rw + lane;
-      const float s = 1.f / (P.norm[pr.mat] + P.eps);
-      const DSrc nxt2 = dsrc_of(t + 2 * npairs);
+      const float s = 1.f / (nrm0 + P.eps);
+      // read ahead: the fields of tile t + 2 npairs, the row of t + 3 npairs, the norm of t + npairs
+      const EpiFields f2 = epi_fields(t + 2 * npairs, row2);
+      row2 = tile_row(P, t + 3 * npairs);
+      const float nrm1 = P.norm[f1.mat];
       // refill slot q & 1 once chunk q has taken its D
       auto refill = [&](int q) {
         if (q + 2 < kEpiChunks)
@@ -1131,13 +1207,13 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
       tc_fence_after();
       float alpha = 1.f, beta = 0.f;
       if (kind == kGram) {
-        alpha = pr.first ? s * s : 1.f;
+        alpha = f.first ? s * s : 1.f;
       } else if (kind == kPoly) {
         alpha = P.c;
         beta = P.b;
       } else {
-        alpha = pr.first ? s : 1.f;
-        if (!pr.fold_a) beta = P.a * alpha;
+        alpha = f.first ? s : 1.f;
+        if (!f.fold_a) beta = P.a * alpha;
       }
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
 #pragma unroll
@@ -1179,7 +1255,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
         refill(q);
         tc_ld_wait(a32);
         // the polynomial phase adds a on the diagonal: column `lane` of a chunk on it
-        const float dg = (kind == kPoly && pr.fold_a && c0 == rw) ? P.a : 0.f;
+        const float dg = (kind == kPoly && f.fold_a && c0 == rw) ? P.a : 0.f;
         uint32_t hw[16];  // bf16 pairs (column 2k in the low half)
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -1243,7 +1319,7 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          const CUtensorMap* map_o = P.maps + pr.map_o;
+          const CUtensorMap* map_o = P.maps + f.map_o;
           tma_store_block(map_o, stg, c0, rw);
           if (sym && !diag) tma_store_block(map_o, stg_t, rw, c0);
           asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -1255,7 +1331,10 @@ __global__ void __launch_bounds__(kNsThreads, 1) ns_gemm_pair_kernel(const __gri
       if (lane == 0) mbar_arrive_cluster(map_rank(bar(tempty0 + acc), 0));
       if (++acc == C::kAccs) { acc = 0; acc_phase ^= 1u; }
       cur = nxt;
-      nxt = nxt2;
+      nxt = dsrc_of(f2);
+      f0 = f1;
+      f1 = f2;
+      nrm0 = nrm1;
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // stores done
     __syncwarp();
