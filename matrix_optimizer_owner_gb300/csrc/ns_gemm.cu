@@ -675,8 +675,14 @@ __device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, cons
   return mbar_try_wait_cl(bar, parity) || mbar_wait_cl_slow(bar, parity, g, honor_abort);
 }
 
+// Arrival on a barrier of either CTA of the pair (the accumulator-empty barrier, in the
+// leader).  What it publishes is that this warp's tensor-memory reads have completed
+// (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync); the MMA issuer reads no memory
+// this thread wrote, so the release is CTA-scoped.  A cluster-scoped release made every
+// epilogue warp wait at each tile's end for its outstanding memory operations (3 % of the
+// GPT-2-small Newton-Schulz time).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
 
