@@ -62,9 +62,9 @@ NS_TRAFFIC_SOURCES = ("matrix_optimizer_owner_gb300/csrc/ns_gemm.cu",
                       "matrix_optimizer_owner_gb300/csrc/mfsdp_internal.h")
 NS_TRAFFIC = {
     # config index: (sources sha256, bytes per launch, profile summary)
-    1: ("6c2c9ce5026f8bd42752ef4a23b32d3725692e7d723ca86b502322ef0a76c1fe", 209269452,
+    1: ("8ca8aec6e033299d0055b7b5873eb9190d0dbfb5b5e7b29973a93ed8fd853b9f", 207803341,
         "profiles/owner_step_gpt2_small_launch_list.md"),
-    4: ("6c2c9ce5026f8bd42752ef4a23b32d3725692e7d723ca86b502322ef0a76c1fe", 110805183948,
+    4: ("8ca8aec6e033299d0055b7b5873eb9190d0dbfb5b5e7b29973a93ed8fd853b9f", 80230672759,
         "profiles/owner_step_llama3_70b_launch_list.md"),
 }
 
