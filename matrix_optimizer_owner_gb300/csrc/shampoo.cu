@@ -14,10 +14,10 @@
 //     T_k = (5 I - M_k) / 4,  X_{k+1} = X_k T_k,  M_{k+1} = T_k^4 M_k,
 // so M_k -> I and X_k -> A^{-1/4}; an eigenvalue ratio of 1e-8 converges in 26 iterations.
 //
-// Two precisions.  fp32: every product is one launch of the batched fp32 GEMM (tcgen05
-// kind::tf32 with three split products per multiply, "3xTF32", fp32 accumulation; a launch
-// runs the same product for every owned matrix), the iteration's T = (5I - M) / 4 written by
-// the epilogue of the product that forms M.  Split-bf16: the statistics as above, the root
+// Two precisions.  fp32: the products run on the batched fp32 GEMM (tcgen05 kind::tf32 with
+// three split products per multiply, "3xTF32", fp32 accumulation; a launch runs a product for
+// every owned matrix, X' and T^2 together), the iteration's T = (5I - M) / 4 written by the
+// epilogue of the product that forms M.  Split-bf16: the statistics as above, the root
 // iteration and P on the tensor cores through the Newton-Schulz path's CTA-pair kernel in its
 // split mode (values held as bf16 pairs hi + lo, three MMAs per product, fp32 accumulation,
 // 256 x 256 tiles), symmetric side products as upper-triangle tiles.
@@ -765,10 +765,14 @@ extern "C" int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* gra
   frob_kernel<<<2 * n, 1024, 0, st>>>(d_norm);
   root_prep_kernel<<<dim3(256, (unsigned)(2 * n)), 256, 0, st>>>(d_prep);
   if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
+  // Three launches per iteration: X' = X T with T2 = T T (both read only the current T, so
+  // they share one launch of 4n problems), then T4 = T2 T2, then M' = T4 M (whose epilogue
+  // writes the next T).
   for (int it = 0; it < root_iters; ++it) {
     const GemmDesc* tbl = (it & 1) ? d_odd : d_even;
     const GemmDesc* htbl = (it & 1) ? iter_odd.data() : iter.data();
-    for (int prod = 0; prod < 4; ++prod)
+    if ((e = launch_gemm(tbl, htbl, 4 * n, 0, 0, st)) != MFSDP_OK) return e;
+    for (int prod = 2; prod < 4; ++prod)
       if ((e = launch_gemm(tbl + prod * 2 * n, htbl + prod * 2 * n, 2 * n, 0, 0, st)) !=
           MFSDP_OK)
         return e;

@@ -26,9 +26,13 @@
 // of a block are 64-term fp32 sums, whose rounding leaves couplings of a few u ||L|| between
 // nearly equal eigenvalues, and eigenvectors are accurate to about tol ||L|| / gap.
 //
-// Every product (statistics, A = Q^T L Q, the rotations into and out of the eigenbasis) is
-// the batched fp32 SGEMM on the CUDA cores; the Jacobi rotations are fp32 FFMA as well: the
-// accumulated basis must stay orthogonal to fp32 precision over hundreds of rounds.
+// Every product (statistics, A = Q^T L Q, the rotations into and out of the eigenbasis, the
+// basis' final polar step Z^T <- (3I - Z^T Z) Z^T / 2) is the batched fp32 GEMM on the tensor
+// cores (3xTF32 with k-block accumulation in fp32 registers, an fp32 GEMM's accuracy).  The
+// Jacobi rotations stay fp32 FFMA: applied to A, their rounding is a backward error of the
+// eigenproblem that the eigenvectors amplify by 1 / gap (a 3xTF32 form, measured, missed the
+// eigenvector tolerance on tight spectra), and applied to Z, as a third launch per round, they
+// cost more in launches than they saved.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -207,6 +211,7 @@ __global__ void __launch_bounds__(kSolveThreads) jacobi_solve_kernel(const SideD
     if (tid == 0) sweep_rot = 0;
     __syncthreads();
     for (int r = 0; r < kJP - 1; ++r) {
+      int rotate = 0;
       if (tid < kJP / 2) {
         const int pq = ptab[r * (kJP / 2) + tid], p = pq & 0xff, q = pq >> 8;
         const float app = S[p][p], aqq = S[q][q], apq = S[p][q];
@@ -221,8 +226,11 @@ __global__ void __launch_bounds__(kSolveThreads) jacobi_solve_kernel(const SideD
         }
         cs[tid] = c;
         sn[tid] = sv;
+        rotate = sv != 0.f;
       }
-      __syncthreads();
+      // an inner round that rotates no pair leaves S and V as they are: skip its update (and
+      // its second barrier); common once the subproblem is nearly diagonal
+      if (!__syncthreads_or(rotate)) continue;
       // S <- J^T S J over the 2 x 2 blocks (pair a rows, pair b columns), a <= b, mirrored
       // (S stays symmetric), and V <- V J: all disjoint.  A thread's blocks and V row-pairs
       // are loaded first, then rotated, then stored, so that their latencies overlap.
@@ -614,6 +622,28 @@ __global__ void soap_update_kernel(const MatDev* mats, float* w, const float* nb
     atomicOr(status, kStatusNonFinite);
 }
 
+// Final polar step of the solve, Z^T <- (3I - Z^T Z) Z^T / 2 on the leading d x d block (the
+// padding rows and columns stay the identity): T = 1.5 I here, T = -Z^T Z / 2 + T and
+// A = T Z^T by the batched GEMM, then Z^T = A.  Hundreds of rounds of fp32 rotations leave
+// Z^T a few 1e-6 from orthogonal; the next step starts from this basis (A = Q^T L Q), where
+// that is a perturbation of the eigenproblem.  One step leaves about the square of it.
+__global__ void polar_prep_kernel(const SideDev* sides) {
+  const SideDev s = sides[blockIdx.y];
+  const int64_t n = (int64_t)s.d * s.d;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x)
+    s.t[e] = (e / s.d) == (e % s.d) ? 1.5f : 0.f;
+}
+__global__ void polar_copy_kernel(const SideDev* sides) {
+  const SideDev s = sides[blockIdx.y];
+  const int64_t n = (int64_t)s.d * s.d;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t at = (e / s.d) * s.dp + e % s.d;
+    s.zt[at] = s.a[at];
+  }
+}
+
 // L = R = 0, Q = I, eigenvalues 0 for every side; M = V = 0 over every matrix.
 __global__ void soap_init_side_kernel(const SideDev* sides) {
   const SideDev s = sides[blockIdx.y];
@@ -678,14 +708,15 @@ namespace {
 
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
-constexpr int kGemmsPerMat = 14;  // stats 2, T 2, A 2, Rayleigh 2, into the basis 4, back 2
+constexpr int kGemmsPerMat = 18;  // stats 2, T 2, A 2, polar 4, Rayleigh 2, into the basis 4,
+                                  // back 2
 
 // Device tables of one step, in upload order.
 struct SoapTables {
   std::vector<SideDev> sides;
   std::vector<int32_t> solve_begin[2], apply_begin[2];  // compact grids of the two groups
   std::vector<MatDev> mats;
-  std::vector<GemmDesc> stats_l, stats_r, t, a, ray, rot1, rot2, back1, back2;
+  std::vector<GemmDesc> stats_l, stats_r, t, a, polar1, polar2, ray, rot1, rot2, back1, back2;
 };
 
 size_t soap_table_bytes(size_t n) {
@@ -933,6 +964,11 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
     // after the solve: T = Z^T L (rows z_i^T L) for the Rayleigh quotients
     float* ztl = reinterpret_cast<float*>(ws + set->sides[(size_t)i].z);
     float* ztr = reinterpret_cast<float*>(ws + set->sides[(size_t)(n + i)].z);
+    // the polar step: T = -Z^T Z / 2 + T (T = 1.5 I), then A = T Z^T
+    tb.polar1.push_back({ztl, ztl, tl, nullptr, rows, rows, rows, dpl, dpl, rows, -0.5f, 1.f});
+    tb.polar1.push_back({ztr, ztr, tr, nullptr, cols, cols, cols, dpr, dpr, cols, -0.5f, 1.f});
+    tb.polar2.push_back({tl, ztl, al, nullptr, rows, rows, rows, rows, dpl, dpl, 1.f, 0.f});
+    tb.polar2.push_back({tr, ztr, ar, nullptr, cols, cols, cols, cols, dpr, dpr, 1.f, 0.f});
     tb.ray.push_back({ztl, l, tl, nullptr, rows, rows, rows, dpl, rows, rows, 1.f, 0.f});
     tb.ray.push_back({ztr, r, tr, nullptr, cols, cols, cols, dpr, cols, cols, 1.f, 0.f});
     // into the new basis: Q_L^T G, Q_L^T M, then times Q_R
@@ -963,6 +999,8 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
   const GemmDesc* d_stats_r = put(host, at, dev, tb.stats_r);
   const GemmDesc* d_t = put(host, at, dev, tb.t);
   const GemmDesc* d_a = put(host, at, dev, tb.a);
+  const GemmDesc* d_polar1 = put(host, at, dev, tb.polar1);
+  const GemmDesc* d_polar2 = put(host, at, dev, tb.polar2);
   const GemmDesc* d_ray = put(host, at, dev, tb.ray);
   const GemmDesc* d_rot1 = put(host, at, dev, tb.rot1);
   const GemmDesc* d_rot2 = put(host, at, dev, tb.rot2);
@@ -1022,6 +1060,12 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
         cudaStreamWaitEvent(st, set->ev_join, 0) != cudaSuccess)
       return MFSDP_ECUDA;
     if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
+    // the final polar step on Z^T (every side, converged at once or not)
+    polar_prep_kernel<<<dim3(64, ns), 256, 0, st>>>(d_sides);
+    if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
+    if ((e = run_gemms(tb.polar1, d_polar1, 0, 1, st)) != MFSDP_OK) return e;
+    if ((e = run_gemms(tb.polar2, d_polar2, 0, 0, st)) != MFSDP_OK) return e;
+    polar_copy_kernel<<<dim3(64, ns), 256, 0, st>>>(d_sides);
     // eigenvalues (Rayleigh quotients) in descending order, the basis columns with them
     if ((e = run_gemms(tb.ray, d_ray, 0, 0, st)) != MFSDP_OK) return e;
     rayleigh_kernel<<<dim3(64, ns), 256, 0, st>>>(d_sides);
