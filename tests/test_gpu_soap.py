@@ -20,6 +20,11 @@ The eigenvectors themselves are not unique there (rank-deficient L or R, cluster
 eps = 1e-4 there: in the null space of a rank-deficient L, G' is rounding noise (~1e-8 against
 entries of 1e-3), and eps keeps N' = M' / (sqrt(V) + eps) of that noise below 1e-4 on both
 sides, so the comparison measures the kernels rather than two different noises.
+On the small sets eps = 1e-4 has a second reason.  As eps -> 0 the first step's
+N' = M' / sqrt(V) is sign(G') times a constant, which is discontinuous where an entry of G'
+is near zero, so any rounding flips some of them.  Measured with eps = 1e-8 on the first case
+below: step-1 N 1.8-2.5e-2 from the oracle while the bases agree to 3e-4, then 2-3e-3 at
+step 2 and 3-7e-4 at step 3, as V accumulates.
 """
 
 import numpy as np
