@@ -675,8 +675,8 @@ def run_ours(args, rank, world, local_rank):
     launches = m.pop("gpu_launches")
     roofline = m.pop("roofline")
 
-    e2e_ms, h2d, d2h = time_e2e(wb, max(3, min(args.steps, 10)), stream) if not args.no_e2e \
-        else (None, 0, 0)
+    e2e_steps = max(3, args.steps)  # the same K as the device timing
+    e2e_ms, h2d, d2h = time_e2e(wb, e2e_steps, stream) if not args.no_e2e else (None, 0, 0)
     if world > 1 and e2e_ms is not None:
         t = torch.tensor([e2e_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -692,7 +692,8 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline,
         "e2e": {"value": round(e2e_ms, 4) if e2e_ms is not None else None, "unit": "ms",
                 "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps if e2e_ms is not None else 0},
         "gpu_launches": launches,
         "clocks": clocks, "device_status": status,
     }

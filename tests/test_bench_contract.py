@@ -89,6 +89,7 @@ def test_our_arm_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert e["steps"] == 3  # the same K steps as the device timing
     assert d["gpu_launches"] == 19 * 3
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     assert d["device_status"] == 0
