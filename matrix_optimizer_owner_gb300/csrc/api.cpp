@@ -105,6 +105,23 @@ bool encode_map3d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D fp32 tensor map over a row-major rows x cols buffer of pitch ld elements: boxes of 32
+// columns (128 bytes) x box_rows rows with a 128-byte swizzle, zero fill outside the tensor
+// (the 3xTF32 GEMM's K-major operand tiles).
+bool encode_map_f32(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int64_t ld,
+                    uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 4)};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2D bf16 tensor map over a row-major rows x cols buffer of pitch ld; boxes of box_rows x
 // box_cols with a 128-byte swizzle (operand loads) or a 64-byte swizzle (the epilogue's
 // 32 x 32 staging blocks).

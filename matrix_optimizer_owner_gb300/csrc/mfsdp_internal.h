@@ -198,6 +198,10 @@ cudaError_t launch_ns_pair_split(const NsLaunchParams& p, int pairs, cudaStream_
 bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
                 uint32_t box_rows, uint32_t box_cols = 64, bool swizzle128 = true);
 bool encode_map3d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld);
+// 2D fp32 tensor map (boxes of 32 columns x box_rows rows, 128-byte swizzle); false when the
+// driver refuses it (the base must be 16-byte aligned and ld a multiple of 4).
+bool encode_map_f32(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int64_t ld,
+                    uint32_t box_rows);
 // Output tiles (bm x kBN) of one problem in the rasterised order; `sym` keeps the tiles that
 // reach the upper triangle.
 void add_tiles(std::vector<NsTile>& out, int32_t prob, int64_t M, int64_t N, bool sym,

@@ -767,19 +767,21 @@ extern "C" int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* gra
   if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
   // Three launches per iteration: X' = X T with T2 = T T (both read only the current T, so
   // they share one launch of 4n problems), then T4 = T2 T2, then M' = T4 M (whose epilogue
-  // writes the next T).
+  // writes the next T).  Every right factor (T, T2, M) is a polynomial in the statistics
+  // matrix, so symmetric: it is read as its own transpose (trans_b = 1), which puts both
+  // operands K-major and lets the GEMM load them by TMA.
   for (int it = 0; it < root_iters; ++it) {
     const GemmDesc* tbl = (it & 1) ? d_odd : d_even;
     const GemmDesc* htbl = (it & 1) ? iter_odd.data() : iter.data();
-    if ((e = launch_gemm(tbl, htbl, 4 * n, 0, 0, st)) != MFSDP_OK) return e;
+    if ((e = launch_gemm(tbl, htbl, 4 * n, 0, 1, st)) != MFSDP_OK) return e;
     for (int prod = 2; prod < 4; ++prod)
-      if ((e = launch_gemm(tbl + prod * 2 * n, htbl + prod * 2 * n, 2 * n, 0, 0, st)) !=
+      if ((e = launch_gemm(tbl + prod * 2 * n, htbl + prod * 2 * n, 2 * n, 0, 1, st)) !=
           MFSDP_OK)
         return e;
   }
-  // P = L^{-1/4} G R^{-1/4}
+  // P = L^{-1/4} G R^{-1/4} (R^{-1/4} symmetric: read as its own transpose)
   if ((e = launch_gemm(d_pre, pre.data(), n, 0, 0, st)) != MFSDP_OK) return e;
-  if ((e = launch_gemm(d_pre + n, pre.data() + n, n, 0, 0, st)) != MFSDP_OK) return e;
+  if ((e = launch_gemm(d_pre + n, pre.data() + n, n, 0, 1, st)) != MFSDP_OK) return e;
   // W = W (1 - lr wd) - lr P, matrix by matrix
   int* status = status_word_address();
   if (status == nullptr) return MFSDP_ECUDA;

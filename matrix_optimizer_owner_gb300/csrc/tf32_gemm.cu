@@ -24,7 +24,8 @@
 //                stage is free, so they fly while the MMA works on the other stage;
 //   warp 4       lane 0 issues the MMAs (M = 128, N = 256, K = 8; 12 per k-block) into one of
 //                two TMEM accumulators (2 x 256 columns), one k-block each, alternating;
-//                warps 5-7 idle (24 registers);
+//                warps 5-7 idle (32 registers; in the TMA variant warp 5 lane 0 issues the
+//                operand loads);
 //   warps 8-15   epilogue (176 registers): warp w reads TMEM lanes 32 (w % 4) .. + 31 and
 //                columns 128 ((w - 8) / 4) .. + 127 of each k-block partial (tcgen05.ld),
 //                adds them into a 128-value running sum per thread, releases the
@@ -39,6 +40,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <climits>
 #include <cstdint>
 #include <vector>
@@ -64,7 +66,7 @@ constexpr uint32_t kGSmem = 1024 + kGBarOffset + 256;
 constexpr uint32_t kGTmemCols = 2 * kGN;
 // Registers per thread after setmaxnreg: the four warpgroups together must stay within the
 // 512 x 128 the block is launched with (launch_gemm checks the kernel's register count).
-constexpr int kGRegsProd = 104, kGRegsMma = 24, kGRegsEpi = 176;
+constexpr int kGRegsProd = 104, kGRegsMma = 32, kGRegsEpi = 176;
 static_assert(128 * kGRegsProd + 128 * kGRegsMma + 256 * kGRegsEpi <= kGThreads * 128,
               "register split");
 static_assert(kGRegsMma <= 128 && kGRegsEpi >= 128, "the MMA warpgroup frees, the epilogue takes");
@@ -229,6 +231,22 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+// ---------------------------------------------------------------- TMA (the TMA variant)
+__device__ __forceinline__ void tma_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+// Box at (x, y) of a 2D tensor map (x = the innermost coordinate, a multiple of 32 fp32 here)
+// into shared memory; completion is counted on the mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128u(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -350,6 +368,16 @@ struct GemmLaunch {
 };
 static_assert(sizeof(GemmLaunch) <= 4096, "kernel parameter space");
 
+// The TMA variant (both operands K-major, pitches TMA can address): the launch also carries
+// each problem's tensor maps, in launch order, for at most kGTmaProbs problems (the kernel
+// parameter space holds 32 KB).
+constexpr int kGTmaProbs = 64;
+struct GemmLaunchTma : GemmLaunch {
+  alignas(64) CUtensorMap amap[kGTmaProbs];  // A, m x k: boxes of 32 k x 128 rows
+  alignas(64) CUtensorMap bmap[kGTmaProbs];  // B stored n x k: boxes of 32 k x 256 rows
+};
+static_assert(sizeof(GemmLaunchTma) <= 32000, "kernel parameter space");
+
 // Walks the tiles of one CTA in the launch order: next() moves to tile t (increasing) and
 // yields its problem and origin.
 struct TileCursor {
@@ -367,18 +395,26 @@ struct TileCursor {
 
 // op(A) is m x k: A stored m x k (TA = 0, K-major) or k x m (TA = 1, MN-major).  op(B) is
 // k x n: B stored k x n (TB = 0, MN-major for the MMA's N x K operand) or n x k (TB = 1).
-template <int TA, int TB>
-__global__ void __launch_bounds__(kGThreads, 1) tf32x3_gemm_kernel(const __grid_constant__ GemmLaunch P) {
+//
+// TMA = true (TA = 0, TB = 1 only): one thread of the MMA warpgroup (warp 5) loads each
+// k-block's raw fp32 tiles by TMA straight into the lo halves (the same 128-byte-swizzled
+// K-major layout) and the producer warps only split them: they wait for the tiles to land,
+// split in place and hand the stage to the MMA.  The cp.async producers spend most of their
+// issue slots on copy addresses; here that work is the TMA unit's.
+template <int TA, int TB, bool TMA>
+__global__ void __launch_bounds__(kGThreads, 1)
+    tf32x3_gemm_kernel(const __grid_constant__ std::conditional_t<TMA, GemmLaunchTma, GemmLaunch> P) {
+  static_assert(!TMA || (TA == 0 && TB == 1), "the TMA variant reads both operands K-major");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kGBarOffset);
-  // bars: full[2] | empty[2] | tfull[2] | tempty[2] | drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
+  // bars: full[2] | empty[2] | tfull[2] | tempty[2] | drain | landed[2] (TMA tiles arrived)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   auto bar = [&](int i) { return smem_addr(bars + i); };
-  constexpr int full0 = 0, empty0 = 2, tfull0 = 4, tempty0 = 6, drain = 8;
+  constexpr int full0 = 0, empty0 = 2, tfull0 = 4, tempty0 = 6, drain = 8, landed0 = 9;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGStages; ++s) {
@@ -390,6 +426,8 @@ __global__ void __launch_bounds__(kGThreads, 1) tf32x3_gemm_kernel(const __grid_
       bar_init(bar(tempty0 + a), kGEpiWarps);
     }
     bar_init(bar(drain), 1);
+    bar_init(bar(landed0), 1);
+    bar_init(bar(landed0 + 1), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -421,6 +459,28 @@ __global__ void __launch_bounds__(kGThreads, 1) tf32x3_gemm_kernel(const __grid_
     uint32_t j = 0;            // k-blocks issued so far (sequence over this CTA's tiles)
     TileCursor cur;
     bool ok = true;
+    if constexpr (TMA) {
+      // the tiles of k-block j arrive by TMA (landed[j % 2]); split them and hand them on
+      for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+        GemmDesc d;
+        int m0, n0;
+        cur.at(P, t, d, m0, n0);
+        const int nk = (d.k + kGK - 1) / kGK;
+        for (int kb = 0; kb < nk; ++kb, ++j) {
+          const int stage = (int)(j & 1u);
+          if (!bar_wait(bar(landed0 + stage), (j >> 1) & 1u, g)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = sbase + (uint32_t)stage * kGStageBytes;
+          Operand<kGM, false>::convert(sa, sa + kGLoOffset, p);
+          Operand<kGN, false>::convert(sa + kGATile, sa + kGATile + kGLoOffset, p);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMA
+          __syncwarp();
+          if (lane == 0) bar_arrive(bar(full0 + stage));
+        }
+      }
+    } else {
     auto finish = [&](uint32_t jj) {  // convert k-block jj and hand its stage to the MMA
       const uint32_t sa = sbase + (jj & 1u) * kGStageBytes;
       Operand<kGM, TA == 1>::convert(sa, sa + kGLoOffset, p);
@@ -453,6 +513,7 @@ __global__ void __launch_bounds__(kGThreads, 1) tf32x3_gemm_kernel(const __grid_
     }
     cp_async_wait<0>();
     if (ok && j > 0) finish(j - 1);
+    }
   } else if (warp < 8) {
     // ------------------------------------------------------------ MMA issuer (warpgroup 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGRegsMma));
@@ -490,6 +551,40 @@ __global__ void __launch_bounds__(kGThreads, 1) tf32x3_gemm_kernel(const __grid_
       }
       mma_commit(bar(drain));
       bar_wait(bar(drain), 0u, g, false);  // every MMA of this CTA has completed
+    }
+    if constexpr (TMA) {
+      if (warp == kGMmaWarp + 1 && lane == 0) {
+        // ---------------------------------------------------------- TMA loads (warp 5)
+        uint32_t j = 0, armed = 0, last_par = 0;
+        bool ok = true;
+        TileCursor cur;
+        for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+          GemmDesc d;
+          int m0, n0;
+          cur.at(P, t, d, m0, n0);
+          const CUtensorMap* am = &P.amap[cur.pos];
+          const CUtensorMap* bm = &P.bmap[cur.pos];
+          const int nk = (d.k + kGK - 1) / kGK;
+          for (int kb = 0; kb < nk; ++kb, ++j) {
+            const int stage = (int)(j & 1u);
+            if (!bar_wait(bar(empty0 + stage), ((j >> 1) & 1u) ^ 1u, g)) {
+              ok = false;
+              break;
+            }
+            const uint32_t sa = sbase + (uint32_t)stage * kGStageBytes;
+            const uint32_t lb = bar(landed0 + stage);
+            tma_expect_tx(lb, kGATile + kGBTile);
+            tma_load_2d(sa + kGLoOffset, am, kb * kGK, m0, lb);
+            tma_load_2d(sa + kGATile + kGLoOffset, bm, kb * kGK, n0, lb);
+            armed |= 1u << stage;
+            last_par = (last_par & ~(1u << stage)) | (((j >> 1) & 1u) << stage);
+          }
+        }
+        // loads in flight when the kernel gives up must land before the CTA leaves
+        if (!ok)
+          for (int st = 0; st < 2; ++st)
+            if (armed & (1u << st)) bar_wait(bar(landed0 + st), (last_par >> st) & 1u, g, false);
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue (warpgroups 2, 3)
@@ -581,8 +676,9 @@ __global__ void __launch_bounds__(kGThreads, 1) tf32x3_gemm_kernel(const __grid_
   }
 }
 
-template <int TA, int TB>
-cudaError_t launch_one(const GemmLaunch& p, int grid, cudaStream_t st) {
+template <int TA, int TB, bool TMA>
+cudaError_t launch_one(const std::conditional_t<TMA, GemmLaunchTma, GemmLaunch>& p, int grid,
+                       cudaStream_t st) {
   static int attr_set[64] = {};  // per device: the dynamic shared-memory limit was raised
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -592,17 +688,25 @@ cudaError_t launch_one(const GemmLaunch& p, int grid, cudaStream_t st) {
     // setmaxnreg.inc draws on the registers the block was launched with: a kernel built with
     // fewer than the split needs would wait forever in it, so it is refused here instead
     cudaFuncAttributes fa{};
-    e = cudaFuncGetAttributes(&fa, tf32x3_gemm_kernel<TA, TB>);
+    e = cudaFuncGetAttributes(&fa, tf32x3_gemm_kernel<TA, TB, TMA>);
     if (e != cudaSuccess) return e;
     if ((int64_t)fa.numRegs * kGThreads < 128 * kGRegsProd + 128 * kGRegsMma + 256 * kGRegsEpi)
       return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(tf32x3_gemm_kernel<TA, TB>,
+    e = cudaFuncSetAttribute(tf32x3_gemm_kernel<TA, TB, TMA>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
-  tf32x3_gemm_kernel<TA, TB><<<(unsigned)grid, kGThreads, kGSmem, st>>>(p);
+  tf32x3_gemm_kernel<TA, TB, TMA><<<(unsigned)grid, kGThreads, kGSmem, st>>>(p);
   return cudaGetLastError();
+}
+
+// Whether the TMA variant can read this problem: both operands K-major (A m x k, B n x k),
+// 16-byte aligned bases and pitches that are multiples of 4 floats.
+bool tma_ok(const GemmDesc& d) {
+  auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  return d.k > 0 && al(d.a) && al(d.b) && d.lda % 4 == 0 && d.ldb % 4 == 0 && d.lda >= d.k &&
+         d.ldb >= d.k;
 }
 
 }  // namespace
@@ -623,9 +727,12 @@ int launch_gemm(const GemmDesc* dev_descs, const GemmDesc* host_descs, int nprob
     if (host_descs[z].m > 0 && host_descs[z].n > 0) order.push_back(z);
   std::stable_sort(order.begin(), order.end(),
                    [&](int a, int b) { return host_descs[a].k > host_descs[b].k; });
-  for (size_t first = 0; first < order.size(); first += kGMaxProbs) {
-    const size_t cnt = std::min(order.size() - first, (size_t)kGMaxProbs);
-    GemmLaunch p{};
+  bool tma = ta == 0 && tb == 1;
+  for (int z : order) tma = tma && tma_ok(host_descs[z]);
+  const size_t per_launch = tma ? (size_t)kGTmaProbs : (size_t)kGMaxProbs;
+  for (size_t first = 0; first < order.size(); first += per_launch) {
+    const size_t cnt = std::min(order.size() - first, per_launch);
+    GemmLaunchTma p{};
     p.descs = dev_descs;
     p.nprob = (int32_t)cnt;
     p.wait_limit_ns = wait_limit_ns();
@@ -643,10 +750,21 @@ int launch_gemm(const GemmDesc* dev_descs, const GemmDesc* host_descs, int nprob
     p.total_tiles = (int32_t)tiles;
     const int grid = (int)std::min<int64_t>(tiles, sms);
     cudaError_t e;
-    if (ta == 0 && tb == 0) e = launch_one<0, 0>(p, grid, st);
-    else if (ta == 0 && tb == 1) e = launch_one<0, 1>(p, grid, st);
-    else if (ta == 1 && tb == 0) e = launch_one<1, 0>(p, grid, st);
-    else e = launch_one<1, 1>(p, grid, st);
+    if (tma) {
+      for (size_t j = 0; j < cnt; ++j) {
+        const GemmDesc& d = host_descs[order[first + j]];
+        if (!encode_map_f32(&p.amap[j], d.a, d.m, d.k, d.lda, kGM) ||
+            !encode_map_f32(&p.bmap[j], d.b, d.n, d.k, d.ldb, kGN))
+          return MFSDP_ECUDA;
+      }
+      e = launch_one<0, 1, true>(p, grid, st);
+    } else {
+      const GemmLaunch& q = p;
+      if (ta == 0 && tb == 0) e = launch_one<0, 0, false>(q, grid, st);
+      else if (ta == 0 && tb == 1) e = launch_one<0, 1, false>(q, grid, st);
+      else if (ta == 1 && tb == 0) e = launch_one<1, 0, false>(q, grid, st);
+      else e = launch_one<1, 1, false>(q, grid, st);
+    }
     if (e != cudaSuccess) return MFSDP_ECUDA;
   }
   return MFSDP_OK;

@@ -4,7 +4,8 @@ against the fp64 product of the same fp32 inputs.
 Cases: every transpose combination; one launch holding problems of different shapes; ragged
 sizes (m, n, k not multiples of the 128 x 256 x 32 tiles, k = 1, a 1 x 1 problem); pitches
 larger than the row (and not multiples of 4, so the loads fall back from 16-byte vectors);
-alpha / beta with C read back; an empty problem in the table.  Bound: the 3xTF32 error is
+alpha / beta with C read back; an empty problem in the table; both operands K-major with
+TMA-addressable pitches (the launch's TMA variant).  Bound: the 3xTF32 error is
 below 2^-21 of each product |a||b|, so |C - C_ref| <= k 2^-20 max|a| max|b| elementwise and
 the relative Frobenius error stays under 2e-6 (an fp32 FFMA GEMM of these sizes is ~1e-6).
 A plain TF32 product (2^-11) fails both.
@@ -61,6 +62,13 @@ def _run(shapes, ta, tb, alpha=1.0, beta=0.0, pitch_extra=0, seed=0):
 def test_transposes_and_mixed_batch(ta, tb):
     _run([(300, 520, 700), (128, 256, 32), (1, 1, 1), (257, 129, 65), (768, 768, 768)], ta, tb,
          seed=ta * 2 + tb)
+
+
+def test_k_major_operands_by_tma():
+    # both operands K-major with pitches a multiple of 4 floats: the launch takes the TMA
+    # variant (every problem qualifies); ragged m, n and k, alpha and beta
+    _run([(300, 520, 700), (128, 256, 32), (257, 129, 68), (768, 768, 768), (130, 70, 4),
+          (1, 300, 36)], 0, 1, alpha=0.7, beta=0.3, seed=11)
 
 
 def test_alpha_beta_and_ragged_pitches():
