@@ -288,7 +288,9 @@ int mfsdp_shampoo_step(const mfsdp_shampoo_set* set, const float* grad, float* l
  * op(A) = A (stored m x k, pitch lda >= k) or A^T when trans_a (A stored k x m, lda >= m);
  * op(B) = B (stored k x n, ldb >= n) or B^T when trans_b (B stored n x k, ldb >= k); C is
  * m x n with pitch ldc >= n.  All row-major fp32 in DEVICE memory; C may not overlap A or B
- * (beta = 0: C is not read).  Every problem runs in one persistent tcgen05 launch:
+ * (beta = 0: C is not read).  The problems run in persistent tcgen05 launches (up to 480
+ * problems each; with trans_a = 0, trans_b = 1, 16-byte-aligned A and B and lda, ldb
+ * multiples of 4, up to 64 each, the operand tiles then loaded by TMA):
  * values are cut into a TF32 high part and an fp32 remainder and each multiply is three
  * TF32 products (hi hi + hi lo + lo hi) accumulated in fp32, about 21 significant bits per
  * product.  `workspace` (DEVICE, >= mfsdp_gemm_f32_workspace_bytes(n_probs) bytes, 256-byte
