@@ -1067,7 +1067,8 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
     if ((e = run_gemms(tb.polar2, d_polar2, 0, 0, st)) != MFSDP_OK) return e;
     polar_copy_kernel<<<dim3(64, ns), 256, 0, st>>>(d_sides);
     // eigenvalues (Rayleigh quotients) in descending order, the basis columns with them
-    if ((e = run_gemms(tb.ray, d_ray, 0, 0, st)) != MFSDP_OK) return e;
+    // (T = Z^T L with the symmetric L read as its own transpose: both operands K-major)
+    if ((e = run_gemms(tb.ray, d_ray, 0, 1, st)) != MFSDP_OK) return e;
     rayleigh_kernel<<<dim3(64, ns), 256, 0, st>>>(d_sides);
     eig_rank_kernel<<<dim3((unsigned)((set->d_max + 255) / 256), ns), 256, 0, st>>>(d_sides);
     {
