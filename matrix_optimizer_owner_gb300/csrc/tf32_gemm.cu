@@ -21,7 +21,8 @@
 //                problem), then split each value in place into hi and lo; two stages of
 //                96 KB (A hi, B hi, A lo, B lo), full / empty mbarriers.  A k-block is split
 //                as soon as its copies land and the next one's copies go out as soon as its
-//                stage is free, so they fly while the MMA works on the other stage;
+//                stage is free, so they fly while the MMA works on the other stage.  (In the
+//                TMA variant below the tiles arrive by TMA and these warps only split them.)
 //   warp 4       lane 0 issues the MMAs (M = 128, N = 256, K = 8; 12 per k-block) into one of
 //                two TMEM accumulators (2 x 256 columns), one k-block each, alternating;
 //                warps 5-7 idle (32 registers; in the TMA variant warp 5 lane 0 issues the
@@ -40,9 +41,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <type_traits>
 #include <climits>
 #include <cstdint>
+#include <type_traits>
 #include <vector>
 
 #include "mfsdp.h"
@@ -481,38 +482,38 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
       }
     } else {
-    auto finish = [&](uint32_t jj) {  // convert k-block jj and hand its stage to the MMA
-      const uint32_t sa = sbase + (jj & 1u) * kGStageBytes;
-      Operand<kGM, TA == 1>::convert(sa, sa + kGLoOffset, p);
-      Operand<kGN, TB == 0>::convert(sa + kGATile, sa + kGATile + kGLoOffset, p);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMA
-      __syncwarp();
-      if (lane == 0) bar_arrive(bar(full0 + (int)(jj & 1u)));
-    };
-    for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
-      GemmDesc d;
-      int m0, n0;
-      cur.at(P, t, d, m0, n0);
-      const int nk = (d.k + kGK - 1) / kGK;
-      for (int kb = 0; kb < nk; ++kb, ++j) {
-        const int stage = (int)(j & 1u);
-        if (j > 0) {
-          cp_async_wait<0>();  // this thread's copies of k-block j - 1 have landed
-          finish(j - 1);
+      auto finish = [&](uint32_t jj) {  // convert k-block jj and hand its stage to the MMA
+        const uint32_t sa = sbase + (jj & 1u) * kGStageBytes;
+        Operand<kGM, TA == 1>::convert(sa, sa + kGLoOffset, p);
+        Operand<kGN, TB == 0>::convert(sa + kGATile, sa + kGATile + kGLoOffset, p);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMA
+        __syncwarp();
+        if (lane == 0) bar_arrive(bar(full0 + (int)(jj & 1u)));
+      };
+      for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+        GemmDesc d;
+        int m0, n0;
+        cur.at(P, t, d, m0, n0);
+        const int nk = (d.k + kGK - 1) / kGK;
+        for (int kb = 0; kb < nk; ++kb, ++j) {
+          const int stage = (int)(j & 1u);
+          if (j > 0) {
+            cp_async_wait<0>();  // this thread's copies of k-block j - 1 have landed
+            finish(j - 1);
+          }
+          if (*abort_flag || !bar_wait(bar(empty0 + stage), ((j >> 1) & 1u) ^ 1u, g)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = sbase + (uint32_t)stage * kGStageBytes;
+          Operand<kGM, TA == 1>::issue(d.a, d.lda, m0, d.m, kb * kGK, d.k, sa + kGLoOffset, p);
+          Operand<kGN, TB == 0>::issue(d.b, d.ldb, n0, d.n, kb * kGK, d.k,
+                                       sa + kGATile + kGLoOffset, p);
+          cp_async_commit();
         }
-        if (*abort_flag || !bar_wait(bar(empty0 + stage), ((j >> 1) & 1u) ^ 1u, g)) {
-          ok = false;
-          break;
-        }
-        const uint32_t sa = sbase + (uint32_t)stage * kGStageBytes;
-        Operand<kGM, TA == 1>::issue(d.a, d.lda, m0, d.m, kb * kGK, d.k, sa + kGLoOffset, p);
-        Operand<kGN, TB == 0>::issue(d.b, d.ldb, n0, d.n, kb * kGK, d.k,
-                                     sa + kGATile + kGLoOffset, p);
-        cp_async_commit();
       }
-    }
-    cp_async_wait<0>();
-    if (ok && j > 0) finish(j - 1);
+      cp_async_wait<0>();
+      if (ok && j > 0) finish(j - 1);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ MMA issuer (warpgroup 1)
