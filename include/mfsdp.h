@@ -328,7 +328,8 @@ int mfsdp_gemm_f32_batched(const mfsdp_gemm_problem* probs, int32_t n_probs, int
  *     W = W (1 - lr weight_decay) - lr N
  * The eigenbases come from cyclic block Jacobi on Q^T L Q, started from the basis the state
  * holds (the previous step's), until a sweep rotates nothing or `max_sweeps` sweeps ran;
- * the statistics, Q^T L Q, the Rayleigh quotients and the rotations into and out of the
+ * each solve ends with one polar step on its basis (Z <- Z (3I - Z^T Z) / 2); the statistics,
+ * Q^T L Q, that polar step, the Rayleigh quotients and the rotations into and out of the
  * eigenbasis are fp32 GEMMs on the tensor cores (3xTF32, as mfsdp_gemm_f32_batched), the
  * Jacobi rotations fp32 on the CUDA cores.  Eigenvectors are fixed up to sign, and N does not
  * depend on the signs.  The solves run on `stream` and on one internal stream of the set,
