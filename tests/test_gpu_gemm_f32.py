@@ -71,6 +71,13 @@ def test_k_major_operands_by_tma():
           (1, 300, 36)], 0, 1, alpha=0.7, beta=0.3, seed=11)
 
 
+def test_tma_launches_split_at_64_problems():
+    # 70 TMA-eligible problems: the launch carries the tensor maps of at most 64, so the
+    # table runs as two launches (64 + 6), longest contraction first
+    shapes = [(32 + 8 * (i % 5), 40 + 16 * (i % 3), 36 + 4 * (i % 7)) for i in range(70)]
+    _run(shapes, 0, 1, alpha=1.0, beta=0.5, seed=12)
+
+
 def test_alpha_beta_and_ragged_pitches():
     _run([(200, 300, 97), (64, 1000, 3), (130, 70, 1)], 0, 1, alpha=0.05, beta=0.95,
          pitch_extra=3, seed=7)
