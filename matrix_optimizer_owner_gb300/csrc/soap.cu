@@ -50,7 +50,7 @@ namespace {
 constexpr int kJB = 32;           // Jacobi block (indices)
 constexpr int kJP = 2 * kJB;      // a pair of blocks: one 64 x 64 subproblem
 constexpr int kJLd = kJP + 1;     // shared-memory pitch (conflict-free column access)
-constexpr int kJThreads = 256;      // apply kernel (4 x 4 outputs per thread)
+constexpr int kJThreads = 128;      // apply kernel (4 x 8 outputs per thread)
 constexpr int kSolveThreads = 512;  // solve kernel
 // Sweeps of one 64 x 64 subproblem per round.  One suffices: the subproblem need not be
 // diagonalised exactly for the outer iteration to converge (an emulation of the solve on
@@ -351,23 +351,29 @@ __global__ void __launch_bounds__(kSolveThreads) jacobi_solve_kernel(const SideD
 constexpr int kALd = kJP + 4;  // apply kernel's shared-memory pitch: rows 16-byte aligned
 constexpr size_t kApplySmem = 3 * sizeof(float) * kJP * kALd;  // 4 CTAs per SM
 
-// acc (rows 4ty + i, columns 4tx + j of a 64 x 64 tile) = P^T Q, i.e. sum_k P[k][.] Q[k][.]:
-// both operands read along rows with 128-bit loads.
+// acc = P^T Q over a 64 x 64 tile, acc[i][j] = sum_k P[k][4ty + i] Q[k][col_j] with one fmaf
+// per k in increasing k; thread (ty, tx), ty in [0, 16), tx in [0, 8), owns rows 4ty .. + 3
+// and columns col_j = 4tx + j (j < 4) and 32 + 4tx + j - 4 (j >= 4).  Each k reads three
+// 128-bit words per thread for 32 FMAs: per warp one 64-byte P row segment (four ty) and two
+// 128-byte Q row segments.
+__device__ __forceinline__ int col8(int tx, int j) { return (j < 4 ? 4 * tx : 28 + 4 * tx) + j; }
 __device__ __forceinline__ void mm64_tn(const float (*P)[kALd], const float (*Q)[kALd], int ty,
-                                        int tx, float (&acc)[4][4]) {
+                                        int tx, float (&acc)[4][8]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 8
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
   for (int kk = 0; kk < kJP; ++kk) {
     const float4 pv = *reinterpret_cast<const float4*>(&P[kk][4 * ty]);
-    const float4 qv = *reinterpret_cast<const float4*>(&Q[kk][4 * tx]);
-    const float pa[4] = {pv.x, pv.y, pv.z, pv.w}, qa[4] = {qv.x, qv.y, qv.z, qv.w};
+    const float4 q0 = *reinterpret_cast<const float4*>(&Q[kk][4 * tx]);
+    const float4 q1 = *reinterpret_cast<const float4*>(&Q[kk][32 + 4 * tx]);
+    const float pa[4] = {pv.x, pv.y, pv.z, pv.w};
+    const float qa[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(pa[i], qa[j], acc[i][j]);
+      for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(pa[i], qa[j], acc[i][j]);
   }
 }
 
@@ -421,8 +427,8 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
   float (*B1)[kALd] = B0 + kJP;
   float (*B2)[kALd] = B1 + kJP;
   __shared__ int ip[kJP], iq[kJP];  // global indices of the two pair-blocks
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  float acc[4][4];
+  const int tid = threadIdx.x, ty = tid >> 3, tx = tid & 7;
+  float acc[4][8];
   if (bid < na) {
     int p = 0, rem = bid;
     while (rem >= P - p) { rem -= P - p; ++p; }
@@ -444,21 +450,26 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
     mm64_tn(B0, B2, ty, tx, acc);  // W = A_pq Jq
     __syncthreads();               // B0 is free: W goes there
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 4; ++i) {
       *reinterpret_cast<float4*>(&B0[4 * ty + i][4 * tx]) =
           make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      *reinterpret_cast<float4*>(&B0[4 * ty + i][32 + 4 * tx]) =
+          make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    }
     __syncthreads();
     mm64_tn(B1, B0, ty, tx, acc);  // Y = Jp^T W
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int gr = idx(p, 4 * ty + i), gc = idx(q, 4 * tx);
-      *reinterpret_cast<float4*>(s.a + (int64_t)gr * s.dp + gc) =
+      float* row = s.a + (int64_t)idx(p, 4 * ty + i) * s.dp;
+      *reinterpret_cast<float4*>(row + idx(q, 4 * tx)) =
           make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      *reinterpret_cast<float4*>(row + idx(q, 32 + 4 * tx)) =
+          make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
     }
     if (p != q) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int gr = idx(q, 4 * tx + j), gc = idx(p, 4 * ty);
+      for (int j = 0; j < 8; ++j) {
+        const int gr = idx(q, col8(tx, j)), gc = idx(p, 4 * ty);
         *reinterpret_cast<float4*>(s.a + (int64_t)gr * s.dp + gc) =
             make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
       }
@@ -485,9 +496,11 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
       mm64_tn(B1, cur, ty, tx, acc);  // Jp^T Z^T_p over tile t
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int gr = ip[4 * ty + i];
-        *reinterpret_cast<float4*>(s.zt + (int64_t)gr * s.dp + t * kJP + 4 * tx) =
+        float* row = s.zt + (int64_t)ip[4 * ty + i] * s.dp + t * kJP;
+        *reinterpret_cast<float4*>(row + 4 * tx) =
             make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        *reinterpret_cast<float4*>(row + 32 + 4 * tx) =
+            make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
       }
       __syncthreads();  // cur is free: the next iteration loads into it
     }
