@@ -377,7 +377,7 @@ __device__ __forceinline__ void mm64_tn(const float (*P)[kALd], const float (*Q)
   }
 }
 
-constexpr int kZTiles = 4;  // 64-column tiles of Z^T one apply CTA updates with the same J_p
+constexpr int kZTiles = 8;  // 64-column tiles of Z^T one apply CTA updates with the same J_p
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
@@ -410,7 +410,9 @@ __device__ __forceinline__ void load_block(float (*dst)[kALd], const float* src,
 // A_pq Jq formed from the mirrored block (A is symmetric), Y written to (p, q) and Y^T to
 // (q, p).  The next P ceil(P / kZTiles) blocks update the rows I_p of Z^T, Z^T <- Jp^T Z^T,
 // over kZTiles 64-column tiles each: J_p stays in shared memory and the tiles stream through
-// two buffers, the next one loading while the current one is multiplied.
+// two buffers, the next one loading while the current one is multiplied.  A block-pair CTA
+// loads A_pq and Jq as one copy group and Jp as a second, which lands while W = A_pq Jq is
+// formed.
 __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* sides,
                                                                  const int32_t* begin,
                                                                  int nsides,
@@ -442,10 +444,11 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
     const float* jq = s.j + (int64_t)q * kJP * kJP;
     // B0[k][i] = A[I_q(k)][I_p(i)] = A_pq[i][k]
     load_block(B0, s.a, s.dp, [&](int r) { return idx(q, r); }, [&](int c) { return idx(p, c); });
-    load_block(B1, jp, kJP, [](int r) { return r; }, [](int c) { return c; });
     load_block(B2, jq, kJP, [](int r) { return r; }, [](int c) { return c; });
     cp_async_commit();
-    cp_async_wait<0>();
+    load_block(B1, jp, kJP, [](int r) { return r; }, [](int c) { return c; });
+    cp_async_commit();
+    cp_async_wait<1>();
     __syncthreads();
     mm64_tn(B0, B2, ty, tx, acc);  // W = A_pq Jq
     __syncthreads();               // B0 is free: W goes there
@@ -456,6 +459,7 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
       *reinterpret_cast<float4*>(&B0[4 * ty + i][32 + 4 * tx]) =
           make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
     }
+    cp_async_wait<0>();
     __syncthreads();
     mm64_tn(B1, B0, ty, tx, acc);  // Y = Jp^T W
 #pragma unroll
