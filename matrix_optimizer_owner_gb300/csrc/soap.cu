@@ -51,7 +51,7 @@ constexpr int kJB = 32;           // Jacobi block (indices)
 constexpr int kJP = 2 * kJB;      // a pair of blocks: one 64 x 64 subproblem
 constexpr int kJLd = kJP + 1;     // shared-memory pitch (conflict-free column access)
 constexpr int kJThreads = 128;      // apply kernel (4 x 8 outputs per thread)
-constexpr int kSolveThreads = 512;  // solve kernel
+constexpr int kSolveThreads = 544;  // solve kernel: one S block per thread (528), 17 warps
 // Sweeps of one 64 x 64 subproblem per round.  One suffices: the subproblem need not be
 // diagonalised exactly for the outer iteration to converge (an emulation of the solve on
 // rank-deficient statistics takes the same number of outer sweeps with 1, 2, 3 or 12), and
@@ -169,19 +169,26 @@ __device__ __forceinline__ void mm64(const float (*X)[kJLd], const float (*Y)[kJ
   }
 }
 
+constexpr int kTri = (kJP / 2) * (kJP / 2 + 1) / 2;                // 528 blocks (a, b), a <= b
+constexpr int kTriPer = (kTri + kSolveThreads - 1) / kSolveThreads;  // per thread
+constexpr int kVPer = (kJP * (kJP / 2) + kSolveThreads - 33) / (kSolveThreads - 32);  // V units
+
 // One round's subproblems: CTA (pair, side) diagonalises the 64 x 64 block of its pair.
-// Compact grid: blocks [begin[k], begin[k + 1]) are the dp_k / 64 pairs of side k.
-__global__ void __launch_bounds__(kSolveThreads) jacobi_solve_kernel(const SideDev* sides,
-                                                                     const int32_t* begin,
-                                                                     int nsides, JacobiCtl* ctl,
-                                                                     int round) {
+// Compact grid: blocks [begin[k], begin[k + 1]) are the dp_k / 64 pairs of side k.  Each
+// inner round has two phases between block barriers: warp 0 forms the round's 32 rotations
+// while warps 1-16 apply the previous round's rotations to V; then every thread rotates one
+// 2 x 2 block of S (528 blocks on 17 warps).  V takes each round's rotations in round order,
+// so its result does not depend on the overlap.
+__global__ void __launch_bounds__(kSolveThreads, 1)
+    jacobi_solve_kernel(const SideDev* sides, const int32_t* begin, int nsides, JacobiCtl* ctl,
+                        int round) {
   const int k = side_of(begin, nsides, blockIdx.x);
   const SideDev s = sides[k];
   const int nb = s.dp / kJB;
   if (ctl[k].converged || round >= nb - 1) return;
   __shared__ float S[kJP][kJLd];
   __shared__ float V[kJP][kJLd];
-  __shared__ float cs[kJP / 2], sn[kJP / 2];
+  __shared__ float cs[2][kJP / 2], sn[2][kJP / 2];  // rotations of two rounds
   __shared__ int sweep_rot, any_rot;
   __shared__ int gi[kJP];
   __shared__ uint16_t ptab[(kJP - 1) * (kJP / 2)];  // round r, pair a: p | q << 8, p < q
@@ -210,6 +217,39 @@ __global__ void __launch_bounds__(kSolveThreads) jacobi_solve_kernel(const SideD
     __syncthreads();  // every thread has read the previous sweep's flag
     if (tid == 0) sweep_rot = 0;
     __syncthreads();
+    // V <- V J of the round `vr` (its rotations in buffer vr & 1) by warps 1-15, 2048 units
+    // (row i, pair a) over 480 threads: the update of V runs beside the next round's
+    // rotations (warp 0) instead of on the path between the two barriers of a round
+    auto rotate_v = [&](int vr) {
+      const uint16_t* pr = ptab + vr * (kJP / 2);
+      const float* c_ = cs[vr & 1];
+      const float* s_ = sn[vr & 1];
+      const int kx = tid - 32;
+      float vv[kVPer][2], vc[kVPer][2];
+      int vidx[kVPer][2];
+      bool va[kVPer];
+#pragma unroll
+      for (int u = 0; u < kVPer; ++u) {
+        const int e = kx + u * (kSolveThreads - 32);
+        va[u] = e < kJP * (kJP / 2);
+        if (!va[u]) continue;
+        const int i = e % kJP, a = e / kJP;
+        const int pa = pr[a], p = pa & 0xff, p2 = pa >> 8;
+        vc[u][0] = c_[a]; vc[u][1] = s_[a];
+        vidx[u][0] = i * kJLd + p; vidx[u][1] = i * kJLd + p2;
+        vv[u][0] = (&V[0][0])[vidx[u][0]];
+        vv[u][1] = (&V[0][0])[vidx[u][1]];
+      }
+#pragma unroll
+      for (int u = 0; u < kVPer; ++u) {
+        if (!va[u]) continue;
+        const float ca = vc[u][0], sa = vc[u][1];
+        if (sa == 0.f) continue;
+        (&V[0][0])[vidx[u][0]] = ca * vv[u][0] - sa * vv[u][1];
+        (&V[0][0])[vidx[u][1]] = sa * vv[u][0] + ca * vv[u][1];
+      }
+    };
+    int vpend = -1;  // the round whose rotations V has still to take
     for (int r = 0; r < kJP - 1; ++r) {
       int rotate = 0;
       if (tid < kJP / 2) {
@@ -224,19 +264,22 @@ __global__ void __launch_bounds__(kSolveThreads) jacobi_solve_kernel(const SideD
           sv = t * c;
           sweep_rot = 1;
         }
-        cs[tid] = c;
-        sn[tid] = sv;
+        cs[r & 1][tid] = c;
+        sn[r & 1][tid] = sv;
         rotate = sv != 0.f;
+      } else if (vpend >= 0) {
+        rotate_v(vpend);
       }
+      vpend = -1;
       // an inner round that rotates no pair leaves S and V as they are: skip its update (and
       // its second barrier); common once the subproblem is nearly diagonal
       if (!__syncthreads_or(rotate)) continue;
       // S <- J^T S J over the 2 x 2 blocks (pair a rows, pair b columns), a <= b, mirrored
-      // (S stays symmetric), and V <- V J: all disjoint.  A thread's blocks and V row-pairs
-      // are loaded first, then rotated, then stored, so that their latencies overlap.
+      // (S stays symmetric): all disjoint.  A thread's blocks are loaded first, then
+      // rotated, then stored, so that their latencies overlap.
       const uint16_t* pr = ptab + r * (kJP / 2);
-      constexpr int kTri = (kJP / 2) * (kJP / 2 + 1) / 2;  // 528 blocks
-      constexpr int kTriPer = (kTri + kSolveThreads - 1) / kSolveThreads;
+      const float* c_ = cs[r & 1];
+      const float* s_ = sn[r & 1];
       float sval[kTriPer][4], csv[kTriPer][4];
       int sidx[kTriPer][4];
       bool sact[kTriPer], sdiag[kTriPer];
@@ -248,23 +291,12 @@ __global__ void __launch_bounds__(kSolveThreads) jacobi_solve_kernel(const SideD
         const int a = ttab[e] & 0xff, b = ttab[e] >> 8;
         const int pa = pr[a], pb = pr[b];
         const int p = pa & 0xff, p2 = pa >> 8, q = pb & 0xff, q2 = pb >> 8;
-        csv[u][0] = cs[a]; csv[u][1] = sn[a]; csv[u][2] = cs[b]; csv[u][3] = sn[b];
+        csv[u][0] = c_[a]; csv[u][1] = s_[a]; csv[u][2] = c_[b]; csv[u][3] = s_[b];
         sdiag[u] = a == b;
         sidx[u][0] = p * kJLd + q; sidx[u][1] = p * kJLd + q2;
         sidx[u][2] = p2 * kJLd + q; sidx[u][3] = p2 * kJLd + q2;
 #pragma unroll
         for (int w = 0; w < 4; ++w) sval[u][w] = (&S[0][0])[sidx[u][w]];
-      }
-      float vv[4][2], vcs[4][2];
-      int vidx[4][2];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = tid + u * kSolveThreads, i = e % kJP, a = e / kJP;
-        const int pa = pr[a], p = pa & 0xff, p2 = pa >> 8;
-        vcs[u][0] = cs[a]; vcs[u][1] = sn[a];
-        vidx[u][0] = i * kJLd + p; vidx[u][1] = i * kJLd + p2;
-        vv[u][0] = (&V[0][0])[vidx[u][0]];
-        vv[u][1] = (&V[0][0])[vidx[u][1]];
       }
 #pragma unroll
       for (int u = 0; u < kTriPer; ++u) {
@@ -297,13 +329,11 @@ __global__ void __launch_bounds__(kSolveThreads) jacobi_solve_kernel(const SideD
           S0[q2 * kJLd + p2] = z22;
         }
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float ca = vcs[u][0], sa = vcs[u][1];
-        if (sa == 0.f) continue;
-        (&V[0][0])[vidx[u][0]] = ca * vv[u][0] - sa * vv[u][1];
-        (&V[0][0])[vidx[u][1]] = sa * vv[u][0] + ca * vv[u][1];
-      }
+      vpend = r;
+      __syncthreads();
+    }
+    if (vpend >= 0) {
+      if (tid >= 32) rotate_v(vpend);
       __syncthreads();
     }
     const bool more = sweep_rot != 0;
