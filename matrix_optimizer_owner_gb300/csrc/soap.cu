@@ -170,7 +170,7 @@ __device__ __forceinline__ void mm64(const float (*X)[kJLd], const float (*Y)[kJ
 }
 
 constexpr int kTri = (kJP / 2) * (kJP / 2 + 1) / 2;                // 528 blocks (a, b), a <= b
-constexpr int kTriPer = (kTri + kSolveThreads - 1) / kSolveThreads;  // per thread
+static_assert(kTri <= kSolveThreads, "one S block per solve thread");
 constexpr int kVPer = (kJP * (kJP / 2) + kSolveThreads - 33) / (kSolveThreads - 32);  // V units
 
 // One round's subproblems: CTA (pair, side) diagonalises the 64 x 64 block of its pair.
@@ -212,12 +212,14 @@ __global__ void __launch_bounds__(kSolveThreads, 1)
     V[r][c] = r == c ? 1.f : 0.f;
   }
   const float tol = s.tol * *s.diag_max;
+  // this thread's block of S: pair ta rows, pair tb columns (ta <= tb)
+  const int tt = tid < kTri ? ttab[tid] : 0, ta = tt & 0xff, tb = tt >> 8;
   if (tid == 0) any_rot = 0;
   for (int sw = 0; sw < kSubSweeps; ++sw) {
     __syncthreads();  // every thread has read the previous sweep's flag
     if (tid == 0) sweep_rot = 0;
     __syncthreads();
-    // V <- V J of the round `vr` (its rotations in buffer vr & 1) by warps 1-15, 2048 units
+    // V <- V J of the round `vr` (its rotations in buffer vr & 1) by warps 1-16, 2048 units
     // (row i, pair a) over 480 threads: the update of V runs beside the next round's
     // rotations (warp 0) instead of on the path between the two barriers of a round
     auto rotate_v = [&](int vr) {
@@ -275,58 +277,29 @@ __global__ void __launch_bounds__(kSolveThreads, 1)
       // its second barrier); common once the subproblem is nearly diagonal
       if (!__syncthreads_or(rotate)) continue;
       // S <- J^T S J over the 2 x 2 blocks (pair a rows, pair b columns), a <= b, mirrored
-      // (S stays symmetric): all disjoint.  A thread's blocks are loaded first, then
-      // rotated, then stored, so that their latencies overlap.
-      const uint16_t* pr = ptab + r * (kJP / 2);
-      const float* c_ = cs[r & 1];
-      const float* s_ = sn[r & 1];
-      float sval[kTriPer][4], csv[kTriPer][4];
-      int sidx[kTriPer][4];
-      bool sact[kTriPer], sdiag[kTriPer];
-#pragma unroll
-      for (int u = 0; u < kTriPer; ++u) {
-        const int e = tid + u * kSolveThreads;
-        sact[u] = e < kTri;
-        if (!sact[u]) continue;
-        const int a = ttab[e] & 0xff, b = ttab[e] >> 8;
-        const int pa = pr[a], pb = pr[b];
+      // (S stays symmetric): all disjoint, one per thread.
+      if (tid < kTri) {
+        const uint16_t* pr = ptab + r * (kJP / 2);
+        const int pa = pr[ta], pb = pr[tb];
         const int p = pa & 0xff, p2 = pa >> 8, q = pb & 0xff, q2 = pb >> 8;
-        csv[u][0] = c_[a]; csv[u][1] = s_[a]; csv[u][2] = c_[b]; csv[u][3] = s_[b];
-        sdiag[u] = a == b;
-        sidx[u][0] = p * kJLd + q; sidx[u][1] = p * kJLd + q2;
-        sidx[u][2] = p2 * kJLd + q; sidx[u][3] = p2 * kJLd + q2;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) sval[u][w] = (&S[0][0])[sidx[u][w]];
-      }
-#pragma unroll
-      for (int u = 0; u < kTriPer; ++u) {
-        if (!sact[u]) continue;
-        const float ca = csv[u][0], sa = csv[u][1], cb = csv[u][2], sb = csv[u][3];
-        if (sa == 0.f && sb == 0.f) continue;
-        const float x11 = sval[u][0], x12 = sval[u][1], x21 = sval[u][2], x22 = sval[u][3];
-        const float y11 = ca * x11 - sa * x21, y12 = ca * x12 - sa * x22;
-        const float y21 = sa * x11 + ca * x21, y22 = sa * x12 + ca * x22;
-        float z11 = cb * y11 - sb * y12, z12 = sb * y11 + cb * y12;
-        float z21 = cb * y21 - sb * y22, z22 = sb * y21 + cb * y22;
-        float* S0 = &S[0][0];
-        if (sdiag[u]) {
-          z12 = z21 = 0.f;  // the coupling this rotation removes
-          S0[sidx[u][0]] = z11;
-          S0[sidx[u][1]] = 0.f;
-          S0[sidx[u][2]] = 0.f;
-          S0[sidx[u][3]] = z22;
-        } else {
-          // block (a, b) and its mirror (b, a): S[q][p] = z11, S[q2][p] = z12, ...
-          const int p = sidx[u][0] / kJLd, p2 = sidx[u][2] / kJLd;
-          const int q = sidx[u][0] % kJLd, q2 = sidx[u][1] % kJLd;
-          S0[sidx[u][0]] = z11;
-          S0[sidx[u][1]] = z12;
-          S0[sidx[u][2]] = z21;
-          S0[sidx[u][3]] = z22;
-          S0[q * kJLd + p] = z11;
-          S0[q2 * kJLd + p] = z12;
-          S0[q * kJLd + p2] = z21;
-          S0[q2 * kJLd + p2] = z22;
+        const float ca = cs[r & 1][ta], sa = sn[r & 1][ta];
+        const float cb = cs[r & 1][tb], sb = sn[r & 1][tb];
+        const float x11 = S[p][q], x12 = S[p][q2], x21 = S[p2][q], x22 = S[p2][q2];
+        if (sa != 0.f || sb != 0.f) {
+          const float y11 = ca * x11 - sa * x21, y12 = ca * x12 - sa * x22;
+          const float y21 = sa * x11 + ca * x21, y22 = sa * x12 + ca * x22;
+          const float z11 = cb * y11 - sb * y12, z12 = sb * y11 + cb * y12;
+          const float z21 = cb * y21 - sb * y22, z22 = sb * y21 + cb * y22;
+          if (ta == tb) {
+            S[p][q] = z11;
+            S[p][q2] = 0.f;  // the coupling this rotation removes
+            S[p2][q] = 0.f;
+            S[p2][q2] = z22;
+          } else {
+            // block (a, b) and its mirror (b, a)
+            S[p][q] = z11; S[p][q2] = z12; S[p2][q] = z21; S[p2][q2] = z22;
+            S[q][p] = z11; S[q2][p] = z12; S[q][p2] = z21; S[q2][p2] = z22;
+          }
         }
       }
       vpend = r;
