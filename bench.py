@@ -62,9 +62,9 @@ NS_TRAFFIC_SOURCES = ("matrix_optimizer_owner_gb300/csrc/ns_gemm.cu",
                       "matrix_optimizer_owner_gb300/csrc/mfsdp_internal.h")
 NS_TRAFFIC = {
     # config index: (sources sha256, bytes per launch, profile summary)
-    1: ("8ca8aec6e033299d0055b7b5873eb9190d0dbfb5b5e7b29973a93ed8fd853b9f", 207803341,
+    1: ("37d8b0068cdbb9c6d0c975d47beecdac27dc53780c59d966e0f94750898c9ef9", 207298184,
         "profiles/owner_step_gpt2_small_launch_list.md"),
-    4: ("8ca8aec6e033299d0055b7b5873eb9190d0dbfb5b5e7b29973a93ed8fd853b9f", 80230672759,
+    4: ("37d8b0068cdbb9c6d0c975d47beecdac27dc53780c59d966e0f94750898c9ef9", 71944308701,
         "profiles/owner_step_llama3_70b_launch_list.md"),
 }
 
