@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kSolveThreads, 1)
     if (tid == 0) sweep_rot = 0;
     __syncthreads();
     // V <- V J of the round `vr` (its rotations in buffer vr & 1) by warps 1-16, 2048 units
-    // (row i, pair a) over 480 threads: the update of V runs beside the next round's
+    // (row i, pair a) over the other 512 threads: the update of V runs beside the next round's
     // rotations (warp 0) instead of on the path between the two barriers of a round
     auto rotate_v = [&](int vr) {
       const uint16_t* pr = ptab + vr * (kJP / 2);
