@@ -540,6 +540,7 @@ def time_soap(device, warm=3, reps=2, max_sweeps=20):
         gemm += 2 * r * r * c + 2 * r * c * c            # statistics
         gemm += 2 * (2 * r ** 3 + 2 * c ** 3)            # Q^T L Q
         gemm += 2 * r ** 3 + 2 * c ** 3                  # Rayleigh quotients
+        gemm += 2 * (2 * r ** 3 + 2 * c ** 3)            # polar step: Z^T Z, then T Z^T
         gemm += 2 * (2 * r * r * c + 2 * r * c * c)      # G', M' into the eigenbasis
         gemm += 2 * r * r * c + 2 * r * c * c            # N back out
     jac = 0
