@@ -66,8 +66,10 @@ struct SideDev {           // one statistics matrix of the Jacobi solve ("side")
   float* a;                // dp x dp working matrix (pitch dp)
   float* zt;               // dp x dp accumulated eigenvectors, one per ROW (pitch dp)
   float* t;                // d x d scratch (pitch d)
-  float* j;                // dp / 64 rotations of the current round, 64 x 64 row-major each
-  int32_t* rot;            // per pair of the round: 1 unless its rotation is the identity
+  float* j;                // two buffers (by round parity) of the dp / 64 rotations of a
+                           // round, 64 x 64 row-major each
+  int32_t* rot;            // two buffers of, per pair of a round: 1 unless its rotation is
+                           // the identity
   int32_t* rank;           // d: position of eigenvalue i in descending order
   float* diag_max;         // max_i |a_ii| of the working matrix (refreshed every sweep)
   float tol;               // relative rotation threshold
@@ -181,7 +183,7 @@ constexpr int kVPer = (kJP * (kJP / 2) + kSolveThreads - 33) / (kSolveThreads - 
 // so its result does not depend on the overlap.
 __global__ void __launch_bounds__(kSolveThreads, 1)
     jacobi_solve_kernel(const SideDev* sides, const int32_t* begin, int nsides, JacobiCtl* ctl,
-                        int round) {
+                        int round, int buf) {
   const int k = side_of(begin, nsides, blockIdx.x);
   const SideDev s = sides[k];
   const int nb = s.dp / kJB;
@@ -343,10 +345,11 @@ __global__ void __launch_bounds__(kSolveThreads, 1)
     }
     __syncthreads();
   }
-  float* jout = s.j + (int64_t)pb * kJP * kJP;
+  const int nbp = s.dp / kJP;  // pairs of a round
+  float* jout = s.j + ((int64_t)buf * nbp + pb) * kJP * kJP;
   for (int e = tid; e < kJP * kJP; e += kSolveThreads) jout[e] = V[e / kJP][e % kJP];
   if (tid == 0) {
-    s.rot[pb] = any_rot;
+    s.rot[buf * nbp + pb] = any_rot;
     if (any_rot) ctl[k].rotated = 1;
   }
 }
@@ -420,13 +423,16 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
                                                                  const int32_t* begin,
                                                                  int nsides,
                                                                  const JacobiCtl* ctl,
-                                                                 int round) {
+                                                                 int round, int buf, int part) {
   const int k = side_of(begin, nsides, blockIdx.x);
   const SideDev s = sides[k];
   const int nb = s.dp / kJB, P = nb / 2;
   if (ctl[k].converged || round >= nb - 1) return;
   const int na = P * (P + 1) / 2;
-  const int bid = blockIdx.x - begin[k];
+  // part 0: the A block pairs, blocks [0, na); part 1: the Z^T rows, blocks from na on
+  const int bid = blockIdx.x - begin[k] + (part ? na : 0);
+  const float* jb = s.j + (int64_t)buf * P * kJP * kJP;
+  const int32_t* rb = s.rot + buf * P;
   extern __shared__ __align__(16) float smem[];
   float (*B0)[kALd] = reinterpret_cast<float (*)[kALd]>(smem);
   float (*B1)[kALd] = B0 + kJP;
@@ -438,13 +444,13 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
     int p = 0, rem = bid;
     while (rem >= P - p) { rem -= P - p; ++p; }
     const int q = p + rem;
-    if (!s.rot[p] && !s.rot[q]) return;
+    if (!rb[p] && !rb[q]) return;
     if (tid < kJP) ip[tid] = pair_index(nb, round, p, tid);
     else if (tid < 2 * kJP) iq[tid - kJP] = pair_index(nb, round, q, tid - kJP);
     __syncthreads();
     auto idx = [&](int pb, int c) { return pb == p ? ip[c] : iq[c]; };
-    const float* jp = s.j + (int64_t)p * kJP * kJP;
-    const float* jq = s.j + (int64_t)q * kJP * kJP;
+    const float* jp = jb + (int64_t)p * kJP * kJP;
+    const float* jq = jb + (int64_t)q * kJP * kJP;
     // B0[k][i] = A[I_q(k)][I_p(i)] = A_pq[i][k]
     load_block(B0, s.a, s.dp, [&](int r) { return idx(q, r); }, [&](int c) { return idx(p, c); });
     load_block(B2, jq, kJP, [](int r) { return r; }, [](int c) { return c; });
@@ -483,12 +489,12 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
     }
   } else {
     const int e0 = bid - na, c = e0 / P, p = e0 % P;
-    if (!s.rot[p]) return;
+    if (!rb[p]) return;
     if (tid < kJP) ip[tid] = pair_index(nb, round, p, tid);
     __syncthreads();
     const int t0 = c * kZTiles, t1 = min(P, t0 + kZTiles);
     auto rows = [&](int r) { return ip[r]; };
-    const float* jp = s.j + (int64_t)p * kJP * kJP;
+    const float* jp = jb + (int64_t)p * kJP * kJP;
     // B1 = J_p; B0 and B2 take turns holding a tile, B[k][j] = Z^T[I_p(k)][64 t + j]
     load_block(B1, jp, kJP, [](int r) { return r; }, [](int c) { return c; });
     load_block(B0, s.zt, s.dp, rows, [&](int c) { return t0 * kJP + c; });
@@ -717,10 +723,23 @@ struct mfsdp_soap_set {
   int32_t nb_max_group[2] = {0, 0};
   mutable cudaStream_t aux = nullptr;
   mutable cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  // Each group's Z^T rotations run on a stream of their own, a round or two behind its A
+  // rotations: ev_j[g][b] marks round rotations written to buffer b, ev_z[g][b] the Z^T
+  // rotations that read buffer b done, ev_zjoin[g] the group's last Z^T rotation.
+  mutable cudaStream_t zst[2] = {nullptr, nullptr};
+  mutable cudaEvent_t ev_j[2][2] = {}, ev_z[2][2] = {}, ev_zjoin[2] = {};
   ~mfsdp_soap_set() {
     if (aux) cudaStreamDestroy(aux);
     if (ev_fork) cudaEventDestroy(ev_fork);
     if (ev_join) cudaEventDestroy(ev_join);
+    for (int g = 0; g < 2; ++g) {
+      if (zst[g]) cudaStreamDestroy(zst[g]);
+      if (ev_zjoin[g]) cudaEventDestroy(ev_zjoin[g]);
+      for (int b = 0; b < 2; ++b) {
+        if (ev_j[g][b]) cudaEventDestroy(ev_j[g][b]);
+        if (ev_z[g][b]) cudaEventDestroy(ev_z[g][b]);
+      }
+    }
   }
 };
 
@@ -734,14 +753,15 @@ constexpr int kGemmsPerMat = 18;  // stats 2, T 2, A 2, polar 4, Rayleigh 2, int
 // Device tables of one step, in upload order.
 struct SoapTables {
   std::vector<SideDev> sides;
-  std::vector<int32_t> solve_begin[2], apply_begin[2];  // compact grids of the two groups
+  // compact grids of the two groups: subproblems, A block pairs, Z^T row groups
+  std::vector<int32_t> solve_begin[2], apply_begin[2], zrot_begin[2];
   std::vector<MatDev> mats;
   std::vector<GemmDesc> stats_l, stats_r, t, a, polar1, polar2, ray, rot1, rot2, back1, back2;
 };
 
 size_t soap_table_bytes(size_t n) {
   return al256(sizeof(SideDev) * 2 * n) + al256(sizeof(MatDev) * n) +
-         4 * al256(sizeof(int32_t) * (2 * n + 1)) + al256(sizeof(GemmDesc) * kGemmsPerMat * n) +
+         6 * al256(sizeof(int32_t) * (2 * n + 1)) + al256(sizeof(GemmDesc) * kGemmsPerMat * n) +
          20 * 256;
 }
 
@@ -779,8 +799,8 @@ extern "C" int mfsdp_soap_set_create(const mfsdp_matrix* mats, int32_t n_mats,
       sd.a = off; off = al256(off + dp2);
       sd.z = off; off = al256(off + dp2);
       sd.t = off; off = al256(off + (size_t)sd.d * sd.d * sizeof(float));
-      sd.j = off; off = al256(off + (size_t)(sd.dp / 64) * 64 * 64 * sizeof(float));
-      sd.rot = off; off = al256(off + (size_t)(sd.dp / 64) * sizeof(int32_t));
+      sd.j = off; off = al256(off + 2 * (size_t)(sd.dp / 64) * 64 * 64 * sizeof(float));
+      sd.rot = off; off = al256(off + 2 * (size_t)(sd.dp / 64) * sizeof(int32_t));
       sd.rank = off; off = al256(off + (size_t)sd.d * sizeof(int32_t));
       s->dp_max = std::max(s->dp_max, sd.dp);
       s->d_max = std::max(s->d_max, sd.d);
@@ -879,16 +899,19 @@ void soap_fill(const mfsdp_soap_set* set, const mfsdp_soap_state* st, uint8_t* w
   for (const auto& m : set->mats) tb.mats.push_back(MatDev{m.offset, m.rows * m.cols});
   for (int g = 0; g < 2; ++g) {
     const int lo = g ? set->split : 0, hi = g ? 2 * n : set->split;
-    int32_t sb = 0, ab = 0;
+    int32_t sb = 0, ab = 0, zb = 0;
     for (int pos = lo; pos < hi; ++pos) {
       const int32_t P = set->sides[(size_t)set->order[(size_t)pos]].dp / 64;
       tb.solve_begin[g].push_back(sb);
       tb.apply_begin[g].push_back(ab);
+      tb.zrot_begin[g].push_back(zb);
       sb += P;
-      ab += P * (P + 1) / 2 + P * ((P + kZTiles - 1) / kZTiles);
+      ab += P * (P + 1) / 2;
+      zb += P * ((P + kZTiles - 1) / kZTiles);
     }
     tb.solve_begin[g].push_back(sb);
     tb.apply_begin[g].push_back(ab);
+    tb.zrot_begin[g].push_back(zb);
   }
 }
 
@@ -1015,6 +1038,8 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
                                       put(host, at, dev, tb.solve_begin[1])};
   const int32_t* d_apply_begin[2] = {put(host, at, dev, tb.apply_begin[0]),
                                       put(host, at, dev, tb.apply_begin[1])};
+  const int32_t* d_zrot_begin[2] = {put(host, at, dev, tb.zrot_begin[0]),
+                                     put(host, at, dev, tb.zrot_begin[1])};
   const GemmDesc* d_stats_l = put(host, at, dev, tb.stats_l);
   const GemmDesc* d_stats_r = put(host, at, dev, tb.stats_r);
   const GemmDesc* d_t = put(host, at, dev, tb.t);
@@ -1049,26 +1074,52 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
     // block Jacobi sweeps, the two groups of sides on two streams (forked from and joined back
     // into `st`); converged sides return at once
     if (!set->aux) {
-      if (cudaStreamCreateWithFlags(&set->aux, cudaStreamNonBlocking) != cudaSuccess ||
-          cudaEventCreateWithFlags(&set->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&set->ev_join, cudaEventDisableTiming) != cudaSuccess)
-        return MFSDP_ECUDA;
+      bool ok = cudaStreamCreateWithFlags(&set->aux, cudaStreamNonBlocking) == cudaSuccess &&
+                cudaEventCreateWithFlags(&set->ev_fork, cudaEventDisableTiming) == cudaSuccess &&
+                cudaEventCreateWithFlags(&set->ev_join, cudaEventDisableTiming) == cudaSuccess;
+      for (int g = 0; g < 2 && ok; ++g) {
+        ok = cudaStreamCreateWithFlags(&set->zst[g], cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&set->ev_zjoin[g], cudaEventDisableTiming) == cudaSuccess;
+        for (int b = 0; b < 2 && ok; ++b)
+          ok = cudaEventCreateWithFlags(&set->ev_j[g][b], cudaEventDisableTiming) ==
+                   cudaSuccess &&
+               cudaEventCreateWithFlags(&set->ev_z[g][b], cudaEventDisableTiming) == cudaSuccess;
+      }
+      if (!ok) return MFSDP_ECUDA;
     }
     if (cudaEventRecord(set->ev_fork, st) != cudaSuccess ||
-        cudaStreamWaitEvent(set->aux, set->ev_fork, 0) != cudaSuccess)
+        cudaStreamWaitEvent(set->aux, set->ev_fork, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(set->zst[0], set->ev_fork, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(set->zst[1], set->ev_fork, 0) != cudaSuccess)
       return MFSDP_ECUDA;
     const cudaStream_t gst[2] = {st, set->aux};
     const int goff[2] = {0, set->split}, gn[2] = {set->split, (int)ns - set->split};
     const int nb_max = std::max(set->nb_max_group[0], set->nb_max_group[1]);
+    // Per round of group g: the subproblems, then A's block pairs, on the group's stream;
+    // Z^T's rows on the group's Z^T stream once the round's rotations are written.  The
+    // rotations alternate between two buffers, so a round waits only for the Z^T rotations
+    // of the round two before it (the last reader of its buffer).
+    long rounds[2] = {0, 0};
+    cudaError_t ce = cudaSuccess;
+    auto ok = [&](cudaError_t x) { if (ce == cudaSuccess) ce = x; };
     for (int sw = 0; sw < h->max_sweeps; ++sw) {
       for (int r = 0; r < nb_max - 1; ++r)
         for (int g = 0; g < 2; ++g) {
           if (gn[g] == 0 || r >= set->nb_max_group[g] - 1) continue;
+          const int b = (int)(rounds[g] & 1);
+          if (rounds[g] >= 2) ok(cudaStreamWaitEvent(gst[g], set->ev_z[g][b], 0));
           jacobi_solve_kernel<<<(unsigned)tb.solve_begin[g].back(), kSolveThreads, 0, gst[g]>>>(
-              d_sides + goff[g], d_solve_begin[g], gn[g], ctl + goff[g], r);
+              d_sides + goff[g], d_solve_begin[g], gn[g], ctl + goff[g], r, b);
+          ok(cudaEventRecord(set->ev_j[g][b], gst[g]));
           jacobi_apply_kernel<<<(unsigned)tb.apply_begin[g].back(), kJThreads, kApplySmem,
                                 gst[g]>>>(d_sides + goff[g], d_apply_begin[g], gn[g],
-                                          ctl + goff[g], r);
+                                          ctl + goff[g], r, b, 0);
+          ok(cudaStreamWaitEvent(set->zst[g], set->ev_j[g][b], 0));
+          jacobi_apply_kernel<<<(unsigned)tb.zrot_begin[g].back(), kJThreads, kApplySmem,
+                                set->zst[g]>>>(d_sides + goff[g], d_zrot_begin[g], gn[g],
+                                               ctl + goff[g], r, b, 1);
+          ok(cudaEventRecord(set->ev_z[g][b], set->zst[g]));
+          ++rounds[g];
         }
       for (int g = 0; g < 2; ++g) {
         if (gn[g] == 0) continue;
@@ -1076,9 +1127,13 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
         diag_max_kernel<<<(unsigned)gn[g], 1024, 0, gst[g]>>>(d_sides + goff[g], ctl + goff[g]);
       }
     }
-    if (cudaEventRecord(set->ev_join, set->aux) != cudaSuccess ||
-        cudaStreamWaitEvent(st, set->ev_join, 0) != cudaSuccess)
-      return MFSDP_ECUDA;
+    ok(cudaEventRecord(set->ev_join, set->aux));
+    ok(cudaStreamWaitEvent(st, set->ev_join, 0));
+    for (int g = 0; g < 2; ++g) {
+      ok(cudaEventRecord(set->ev_zjoin[g], set->zst[g]));
+      ok(cudaStreamWaitEvent(st, set->ev_zjoin[g], 0));
+    }
+    if (ce != cudaSuccess) return MFSDP_ECUDA;
     if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
     // the final polar step on Z^T (every side, converged at once or not)
     polar_prep_kernel<<<dim3(64, ns), 256, 0, st>>>(d_sides);
