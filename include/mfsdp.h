@@ -332,10 +332,14 @@ int mfsdp_gemm_f32_batched(const mfsdp_gemm_problem* probs, int32_t n_probs, int
  * Q^T L Q, that polar step, the Rayleigh quotients and the rotations into and out of the
  * eigenbasis are fp32 GEMMs on the tensor cores (3xTF32, as mfsdp_gemm_f32_batched), the
  * Jacobi rotations fp32 on the CUDA cores.  Eigenvectors are fixed up to sign, and N does not
- * depend on the signs.  The solves run on `stream` and on one internal stream of the set,
- * forked from and joined back into `stream` with events (created at the first step, on the
- * device current then), so a capture of `stream` takes both; a set serves one host thread at
- * a time.
+ * depend on the signs.  The Jacobi sweeps run as a CUDA graph that the set builds at its
+ * first refresh step for a given workspace and max_sweeps and launches on `stream`: per group
+ * of sides a while loop whose body is one sweep, ending on the device once every side of the
+ * group has converged.  While `stream` is being captured (or if the graph cannot be built)
+ * the same sweeps are issued one by one on `stream` and three internal streams of the set,
+ * forked from and joined back into `stream` with events, so a capture of `stream` takes them
+ * all.  Streams, events and the graph are created on the device current at the first step; a
+ * set serves one host thread at a time.
  *
  * State (DEVICE, fp32, caller-owned, updated in place): `l`, `q_l` hold every matrix's L and
  * Q_L (rows^2 each) back to back in table order, `r`, `q_r` its R and Q_R (cols^2); `eig_l`

@@ -533,6 +533,17 @@ __global__ void jacobi_sweep_end_kernel(JacobiCtl* ctl, int nsides) {
   ctl[k] = c;
 }
 
+// The condition of a group's sweep loop when the sweeps run as a CUDA graph: go on while a
+// side is unconverged and under the sweep limit.
+__global__ void jacobi_loop_kernel(const JacobiCtl* ctl, int nsides, int max_sweeps,
+                                   cudaGraphConditionalHandle handle) {
+  int more = 0;
+  for (int k = threadIdx.x; k < nsides; k += blockDim.x)
+    more |= (!ctl[k].converged && ctl[k].sweeps < max_sweeps) ? 1 : 0;
+  more = __syncthreads_or(more);
+  if (threadIdx.x == 0) cudaGraphSetConditional(handle, more ? 1u : 0u);
+}
+
 // Rayleigh quotients of the final basis: lambda_i = z_i^T L z_i / z_i^T z_i, with T = Z^T L
 // (rows z_i^T L) formed by the SGEMM; one warp per eigenvector.  They replace diag(A), whose
 // entries carry the rounding of every rotation applied to A.
@@ -728,7 +739,16 @@ struct mfsdp_soap_set {
   // rotations that read buffer b done, ev_zjoin[g] the group's last Z^T rotation.
   mutable cudaStream_t zst[2] = {nullptr, nullptr};
   mutable cudaEvent_t ev_j[2][2] = {}, ev_z[2][2] = {}, ev_zjoin[2] = {};
+  // The sweeps as a CUDA graph: per group a while node whose body is one sweep, so that the
+  // sweeps stop on the device once every side of the group has converged (no launches of
+  // sweeps that would find every side converged).  Built for one workspace and sweep limit
+  // (the kernels' arguments point into the workspace).
+  mutable cudaGraphExec_t jgraph = nullptr;
+  mutable const void* jgraph_ws = nullptr;
+  mutable int jgraph_sweeps = 0;
+  mutable bool jgraph_off = false;  // the graph could not be built: issue the sweeps one by one
   ~mfsdp_soap_set() {
+    if (jgraph) cudaGraphExecDestroy(jgraph);
     if (aux) cudaStreamDestroy(aux);
     if (ev_fork) cudaEventDestroy(ev_fork);
     if (ev_join) cudaEventDestroy(ev_join);
@@ -1071,8 +1091,8 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
     if ((e = run_gemms(tb.t, d_t, 0, 0, st)) != MFSDP_OK) return e;
     if ((e = run_gemms(tb.a, d_a, 1, 0, st)) != MFSDP_OK) return e;
     diag_max_kernel<<<ns, 1024, 0, st>>>(d_sides, nullptr);
-    // block Jacobi sweeps, the two groups of sides on two streams (forked from and joined back
-    // into `st`); converged sides return at once
+    // block Jacobi sweeps: the two groups of sides, each on two streams of its own (the
+    // subproblems and A, and Z^T), as the graph's while loops, or issued sweep by sweep
     if (!set->aux) {
       bool ok = cudaStreamCreateWithFlags(&set->aux, cudaStreamNonBlocking) == cudaSuccess &&
                 cudaEventCreateWithFlags(&set->ev_fork, cudaEventDisableTiming) == cudaSuccess &&
@@ -1087,51 +1107,120 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
       }
       if (!ok) return MFSDP_ECUDA;
     }
-    if (cudaEventRecord(set->ev_fork, st) != cudaSuccess ||
-        cudaStreamWaitEvent(set->aux, set->ev_fork, 0) != cudaSuccess ||
-        cudaStreamWaitEvent(set->zst[0], set->ev_fork, 0) != cudaSuccess ||
-        cudaStreamWaitEvent(set->zst[1], set->ev_fork, 0) != cudaSuccess)
-      return MFSDP_ECUDA;
     const cudaStream_t gst[2] = {st, set->aux};
     const int goff[2] = {0, set->split}, gn[2] = {set->split, (int)ns - set->split};
     const int nb_max = std::max(set->nb_max_group[0], set->nb_max_group[1]);
-    // Per round of group g: the subproblems, then A's block pairs, on the group's stream;
-    // Z^T's rows on the group's Z^T stream once the round's rotations are written.  The
-    // rotations alternate between two buffers, so a round waits only for the Z^T rotations
-    // of the round two before it (the last reader of its buffer).
-    long rounds[2] = {0, 0};
     cudaError_t ce = cudaSuccess;
     auto ok = [&](cudaError_t x) { if (ce == cudaSuccess) ce = x; };
-    for (int sw = 0; sw < h->max_sweeps; ++sw) {
-      for (int r = 0; r < nb_max - 1; ++r)
-        for (int g = 0; g < 2; ++g) {
-          if (gn[g] == 0 || r >= set->nb_max_group[g] - 1) continue;
-          const int b = (int)(rounds[g] & 1);
-          if (rounds[g] >= 2) ok(cudaStreamWaitEvent(gst[g], set->ev_z[g][b], 0));
-          jacobi_solve_kernel<<<(unsigned)tb.solve_begin[g].back(), kSolveThreads, 0, gst[g]>>>(
-              d_sides + goff[g], d_solve_begin[g], gn[g], ctl + goff[g], r, b);
-          ok(cudaEventRecord(set->ev_j[g][b], gst[g]));
-          jacobi_apply_kernel<<<(unsigned)tb.apply_begin[g].back(), kJThreads, kApplySmem,
-                                gst[g]>>>(d_sides + goff[g], d_apply_begin[g], gn[g],
-                                          ctl + goff[g], r, b, 0);
-          ok(cudaStreamWaitEvent(set->zst[g], set->ev_j[g][b], 0));
-          jacobi_apply_kernel<<<(unsigned)tb.zrot_begin[g].back(), kJThreads, kApplySmem,
-                                set->zst[g]>>>(d_sides + goff[g], d_zrot_begin[g], gn[g],
-                                               ctl + goff[g], r, b, 1);
-          ok(cudaEventRecord(set->ev_z[g][b], set->zst[g]));
-          ++rounds[g];
-        }
-      for (int g = 0; g < 2; ++g) {
+    // Round r of group g, its `rounds`-th overall: the subproblems, then A's block pairs, on
+    // the group's stream `ms`; Z^T's rows on the group's Z^T stream `zs` once the round's
+    // rotations are written.  The rotations alternate between two buffers, so a round waits
+    // only for the Z^T rotations of the round two before it (the last reader of its buffer).
+    auto round_launches = [&](int g, int r, long& rounds, cudaStream_t ms, cudaStream_t zs) {
+      const int b = (int)(rounds & 1);
+      if (rounds >= 2) ok(cudaStreamWaitEvent(ms, set->ev_z[g][b], 0));
+      jacobi_solve_kernel<<<(unsigned)tb.solve_begin[g].back(), kSolveThreads, 0, ms>>>(
+          d_sides + goff[g], d_solve_begin[g], gn[g], ctl + goff[g], r, b);
+      ok(cudaEventRecord(set->ev_j[g][b], ms));
+      jacobi_apply_kernel<<<(unsigned)tb.apply_begin[g].back(), kJThreads, kApplySmem, ms>>>(
+          d_sides + goff[g], d_apply_begin[g], gn[g], ctl + goff[g], r, b, 0);
+      ok(cudaStreamWaitEvent(zs, set->ev_j[g][b], 0));
+      jacobi_apply_kernel<<<(unsigned)tb.zrot_begin[g].back(), kJThreads, kApplySmem, zs>>>(
+          d_sides + goff[g], d_zrot_begin[g], gn[g], ctl + goff[g], r, b, 1);
+      ok(cudaEventRecord(set->ev_z[g][b], zs));
+      ++rounds;
+    };
+    auto sweep_end = [&](int g, cudaStream_t ms) {
+      jacobi_sweep_end_kernel<<<(gn[g] + 255) / 256, 256, 0, ms>>>(ctl + goff[g], gn[g]);
+      diag_max_kernel<<<(unsigned)gn[g], 1024, 0, ms>>>(d_sides + goff[g], ctl + goff[g]);
+    };
+    // Build the graph: per group a while node; its body, captured from the group's two
+    // streams, is one sweep followed by the loop condition.
+    auto build_graph = [&]() -> bool {
+      if (set->jgraph) cudaGraphExecDestroy(set->jgraph);
+      set->jgraph = nullptr;
+      cudaGraph_t top = nullptr;
+      if (cudaGraphCreate(&top, 0) != cudaSuccess) return false;
+      bool good = true;
+      for (int g = 0; g < 2 && good; ++g) {
         if (gn[g] == 0) continue;
-        jacobi_sweep_end_kernel<<<(gn[g] + 255) / 256, 256, 0, gst[g]>>>(ctl + goff[g], gn[g]);
-        diag_max_kernel<<<(unsigned)gn[g], 1024, 0, gst[g]>>>(d_sides + goff[g], ctl + goff[g]);
+        cudaGraphConditionalHandle hnd;
+        good = cudaGraphConditionalHandleCreate(&hnd, top, 1u, cudaGraphCondAssignDefault) ==
+               cudaSuccess;
+        cudaGraphNodeParams np{};
+        np.type = cudaGraphNodeTypeConditional;
+        np.conditional.handle = hnd;
+        np.conditional.type = cudaGraphCondTypeWhile;
+        np.conditional.size = 1;
+        cudaGraphNode_t node;
+        good = good && cudaGraphAddNode(&node, top, nullptr, nullptr, 0, &np) == cudaSuccess;
+        if (!good) break;
+        const cudaStream_t cs = set->aux, czs = set->zst[g];
+        if (cudaStreamBeginCaptureToGraph(cs, np.conditional.phGraph_out[0], nullptr, nullptr, 0,
+                                          cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+          good = false;
+          break;
+        }
+        ce = cudaSuccess;
+        ok(cudaEventRecord(set->ev_fork, cs));
+        ok(cudaStreamWaitEvent(czs, set->ev_fork, 0));
+        long rounds = 0;
+        for (int r = 0; r < set->nb_max_group[g] - 1; ++r) round_launches(g, r, rounds, cs, czs);
+        ok(cudaEventRecord(set->ev_zjoin[g], czs));
+        ok(cudaStreamWaitEvent(cs, set->ev_zjoin[g], 0));
+        sweep_end(g, cs);
+        jacobi_loop_kernel<<<1, 256, 0, cs>>>(ctl + goff[g], gn[g], h->max_sweeps, hnd);
+        ok(cudaGetLastError());
+        cudaGraph_t captured = nullptr;
+        const cudaError_t ec = cudaStreamEndCapture(cs, &captured);
+        good = ce == cudaSuccess && ec == cudaSuccess;
       }
+      good = good && cudaGraphInstantiate(&set->jgraph, top, 0) == cudaSuccess;
+      cudaGraphDestroy(top);
+      ce = cudaSuccess;
+      if (!good) {
+        cudaGetLastError();
+        if (set->jgraph) cudaGraphExecDestroy(set->jgraph);
+        set->jgraph = nullptr;
+        return false;
+      }
+      set->jgraph_ws = workspace;
+      set->jgraph_sweeps = h->max_sweeps;
+      return true;
+    };
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MFSDP_ECUDA;
+    bool use_graph = !set->jgraph_off && cap == cudaStreamCaptureStatusNone;
+    if (use_graph && (!set->jgraph || set->jgraph_ws != workspace ||
+                      set->jgraph_sweeps != h->max_sweeps)) {
+      use_graph = build_graph();
+      if (!use_graph) set->jgraph_off = true;
     }
-    ok(cudaEventRecord(set->ev_join, set->aux));
-    ok(cudaStreamWaitEvent(st, set->ev_join, 0));
-    for (int g = 0; g < 2; ++g) {
-      ok(cudaEventRecord(set->ev_zjoin[g], set->zst[g]));
-      ok(cudaStreamWaitEvent(st, set->ev_zjoin[g], 0));
+    if (use_graph) {
+      if (cudaGraphLaunch(set->jgraph, st) != cudaSuccess) return MFSDP_ECUDA;
+    } else {
+      // the same launches issued sweep by sweep on the streams, forked from and joined back
+      // into `st`; sweeps after a side has converged find it converged and return at once
+      ok(cudaEventRecord(set->ev_fork, st));
+      ok(cudaStreamWaitEvent(set->aux, set->ev_fork, 0));
+      ok(cudaStreamWaitEvent(set->zst[0], set->ev_fork, 0));
+      ok(cudaStreamWaitEvent(set->zst[1], set->ev_fork, 0));
+      long rounds[2] = {0, 0};
+      for (int sw = 0; sw < h->max_sweeps; ++sw) {
+        for (int r = 0; r < nb_max - 1; ++r)
+          for (int g = 0; g < 2; ++g) {
+            if (gn[g] == 0 || r >= set->nb_max_group[g] - 1) continue;
+            round_launches(g, r, rounds[g], gst[g], set->zst[g]);
+          }
+        for (int g = 0; g < 2; ++g)
+          if (gn[g] > 0) sweep_end(g, gst[g]);
+      }
+      ok(cudaEventRecord(set->ev_join, set->aux));
+      ok(cudaStreamWaitEvent(st, set->ev_join, 0));
+      for (int g = 0; g < 2; ++g) {
+        ok(cudaEventRecord(set->ev_zjoin[g], set->zst[g]));
+        ok(cudaStreamWaitEvent(st, set->ev_zjoin[g], 0));
+      }
     }
     if (ce != cudaSuccess) return MFSDP_ECUDA;
     if (cudaGetLastError() != cudaSuccess) return MFSDP_ECUDA;
