@@ -18,7 +18,8 @@
 // forms a 64 x 64 subproblem [A_PP A_PQ; A_QP A_QQ], reduced by a CTA in shared memory (one
 // cyclic sweep of plane rotations, Golub & Van Loan §8.5, then one polar step), giving a
 // 64 x 64 orthogonal J; a second launch applies all of the round's J to A (A <- J^T A J, block
-// by block) and to Z, kept transposed (Z^T <- J^T Z^T: eigenvectors as rows).  A sweep in
+// by block) and a third, beside the next round, to Z, kept transposed (Z^T <- J^T Z^T:
+// eigenvectors as rows).  A sweep in
 // which no subproblem rotated ends the solve for that matrix.  The eigenvalues are the
 // Rayleigh quotients of the final basis, sorted (descending, ties by index), and Z's columns
 // are scattered into Q in that order.  Plane rotations are skipped where the coupling is at
@@ -28,11 +29,11 @@
 //
 // Every product (statistics, A = Q^T L Q, the rotations into and out of the eigenbasis, the
 // basis' final polar step Z^T <- (3I - Z^T Z) Z^T / 2) is the batched fp32 GEMM on the tensor
-// cores (3xTF32 with k-block accumulation in fp32 registers, an fp32 GEMM's accuracy).  The
-// Jacobi rotations stay fp32 FFMA: applied to A, their rounding is a backward error of the
+// cores (3xTF32 with k-block accumulation in fp32 registers, an fp32 GEMM's accuracy), and so
+// are the Jacobi rotations of Z^T (jacobi_zrot_tc_kernel, the same split, on a stream of their
+// own).  The rotations of A stay fp32 FFMA: there their rounding is a backward error of the
 // eigenproblem that the eigenvectors amplify by 1 / gap (a 3xTF32 form, measured, missed the
-// eigenvector tolerance on tight spectra), and applied to Z, as a third launch per round, they
-// cost more in launches than they saved.
+// eigenvector tolerance on tight spectra).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -383,7 +384,7 @@ __device__ __forceinline__ void mm64_tn(const float (*P)[kALd], const float (*Q)
   }
 }
 
-constexpr int kZTiles = 8;  // 64-column tiles of Z^T one apply CTA updates with the same J_p
+constexpr int kZCols = 512;  // columns of Z^T one rotation CTA updates with the same J_p
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
@@ -411,26 +412,21 @@ __device__ __forceinline__ void load_block(float (*dst)[kALd], const float* src,
   }
 }
 
-// The round's rotations applied; compact grid, blocks [begin[k], begin[k + 1]) for side k.
-// Its blocks [0, P(P+1)/2) update A's block pair (p, q), p <= q: Y = Jp^T (A_pq Jq), with
-// A_pq Jq formed from the mirrored block (A is symmetric), Y written to (p, q) and Y^T to
-// (q, p).  The next P ceil(P / kZTiles) blocks update the rows I_p of Z^T, Z^T <- Jp^T Z^T,
-// over kZTiles 64-column tiles each: J_p stays in shared memory and the tiles stream through
-// two buffers, the next one loading while the current one is multiplied.  A block-pair CTA
-// loads A_pq and Jq as one copy group and Jp as a second, which lands while W = A_pq Jq is
-// formed.
+// The round's rotations applied to A; compact grid, blocks [begin[k], begin[k + 1]) for side
+// k, one per block pair (p, q), p <= q: Y = Jp^T (A_pq Jq), with A_pq Jq formed from the
+// mirrored block (A is symmetric), Y written to (p, q) and Y^T to (q, p).  A CTA loads A_pq
+// and Jq as one copy group and Jp as a second, which lands while W = A_pq Jq is formed.
+// (Z^T's rows take the same rotations in jacobi_zrot_tc_kernel.)
 __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* sides,
                                                                  const int32_t* begin,
                                                                  int nsides,
                                                                  const JacobiCtl* ctl,
-                                                                 int round, int buf, int part) {
+                                                                 int round, int buf) {
   const int k = side_of(begin, nsides, blockIdx.x);
   const SideDev s = sides[k];
   const int nb = s.dp / kJB, P = nb / 2;
   if (ctl[k].converged || round >= nb - 1) return;
-  const int na = P * (P + 1) / 2;
-  // part 0: the A block pairs, blocks [0, na); part 1: the Z^T rows, blocks from na on
-  const int bid = blockIdx.x - begin[k] + (part ? na : 0);
+  const int bid = blockIdx.x - begin[k];
   const float* jb = s.j + (int64_t)buf * P * kJP * kJP;
   const int32_t* rb = s.rot + buf * P;
   extern __shared__ __align__(16) float smem[];
@@ -440,85 +436,354 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
   __shared__ int ip[kJP], iq[kJP];  // global indices of the two pair-blocks
   const int tid = threadIdx.x, ty = tid >> 3, tx = tid & 7;
   float acc[4][8];
-  if (bid < na) {
-    int p = 0, rem = bid;
-    while (rem >= P - p) { rem -= P - p; ++p; }
-    const int q = p + rem;
-    if (!rb[p] && !rb[q]) return;
-    if (tid < kJP) ip[tid] = pair_index(nb, round, p, tid);
-    else if (tid < 2 * kJP) iq[tid - kJP] = pair_index(nb, round, q, tid - kJP);
-    __syncthreads();
-    auto idx = [&](int pb, int c) { return pb == p ? ip[c] : iq[c]; };
-    const float* jp = jb + (int64_t)p * kJP * kJP;
-    const float* jq = jb + (int64_t)q * kJP * kJP;
-    // B0[k][i] = A[I_q(k)][I_p(i)] = A_pq[i][k]
-    load_block(B0, s.a, s.dp, [&](int r) { return idx(q, r); }, [&](int c) { return idx(p, c); });
-    load_block(B2, jq, kJP, [](int r) { return r; }, [](int c) { return c; });
-    cp_async_commit();
-    load_block(B1, jp, kJP, [](int r) { return r; }, [](int c) { return c; });
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    mm64_tn(B0, B2, ty, tx, acc);  // W = A_pq Jq
-    __syncthreads();               // B0 is free: W goes there
+  int p = 0, rem = bid;
+  while (rem >= P - p) { rem -= P - p; ++p; }
+  const int q = p + rem;
+  if (!rb[p] && !rb[q]) return;
+  if (tid < kJP) ip[tid] = pair_index(nb, round, p, tid);
+  else if (tid < 2 * kJP) iq[tid - kJP] = pair_index(nb, round, q, tid - kJP);
+  __syncthreads();
+  auto idx = [&](int pb, int c) { return pb == p ? ip[c] : iq[c]; };
+  const float* jp = jb + (int64_t)p * kJP * kJP;
+  const float* jq = jb + (int64_t)q * kJP * kJP;
+  // B0[k][i] = A[I_q(k)][I_p(i)] = A_pq[i][k]
+  load_block(B0, s.a, s.dp, [&](int r) { return idx(q, r); }, [&](int c) { return idx(p, c); });
+  load_block(B2, jq, kJP, [](int r) { return r; }, [](int c) { return c; });
+  cp_async_commit();
+  load_block(B1, jp, kJP, [](int r) { return r; }, [](int c) { return c; });
+  cp_async_commit();
+  cp_async_wait<1>();
+  __syncthreads();
+  mm64_tn(B0, B2, ty, tx, acc);  // W = A_pq Jq
+  __syncthreads();               // B0 is free: W goes there
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      *reinterpret_cast<float4*>(&B0[4 * ty + i][4 * tx]) =
-          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-      *reinterpret_cast<float4*>(&B0[4 * ty + i][32 + 4 * tx]) =
-          make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-    }
-    cp_async_wait<0>();
-    __syncthreads();
-    mm64_tn(B1, B0, ty, tx, acc);  // Y = Jp^T W
+  for (int i = 0; i < 4; ++i) {
+    *reinterpret_cast<float4*>(&B0[4 * ty + i][4 * tx]) =
+        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    *reinterpret_cast<float4*>(&B0[4 * ty + i][32 + 4 * tx]) =
+        make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  mm64_tn(B1, B0, ty, tx, acc);  // Y = Jp^T W
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float* row = s.a + (int64_t)idx(p, 4 * ty + i) * s.dp;
-      *reinterpret_cast<float4*>(row + idx(q, 4 * tx)) =
-          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-      *reinterpret_cast<float4*>(row + idx(q, 32 + 4 * tx)) =
-          make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-    }
-    if (p != q) {
+  for (int i = 0; i < 4; ++i) {
+    float* row = s.a + (int64_t)idx(p, 4 * ty + i) * s.dp;
+    *reinterpret_cast<float4*>(row + idx(q, 4 * tx)) =
+        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    *reinterpret_cast<float4*>(row + idx(q, 32 + 4 * tx)) =
+        make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+  }
+  if (p != q) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int gr = idx(q, col8(tx, j)), gc = idx(p, 4 * ty);
-        *reinterpret_cast<float4*>(s.a + (int64_t)gr * s.dp + gc) =
-            make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
-      }
-    }
-  } else {
-    const int e0 = bid - na, c = e0 / P, p = e0 % P;
-    if (!rb[p]) return;
-    if (tid < kJP) ip[tid] = pair_index(nb, round, p, tid);
-    __syncthreads();
-    const int t0 = c * kZTiles, t1 = min(P, t0 + kZTiles);
-    auto rows = [&](int r) { return ip[r]; };
-    const float* jp = jb + (int64_t)p * kJP * kJP;
-    // B1 = J_p; B0 and B2 take turns holding a tile, B[k][j] = Z^T[I_p(k)][64 t + j]
-    load_block(B1, jp, kJP, [](int r) { return r; }, [](int c) { return c; });
-    load_block(B0, s.zt, s.dp, rows, [&](int c) { return t0 * kJP + c; });
-    cp_async_commit();
-    for (int t = t0; t < t1; ++t) {
-      float (*cur)[kALd] = ((t - t0) & 1) ? B2 : B0;
-      float (*nxt)[kALd] = ((t - t0) & 1) ? B0 : B2;
-      if (t + 1 < t1) load_block(nxt, s.zt, s.dp, rows, [&](int c) { return (t + 1) * kJP + c; });
-      cp_async_commit();
-      cp_async_wait<1>();  // everything but the next tile has landed
-      __syncthreads();
-      mm64_tn(B1, cur, ty, tx, acc);  // Jp^T Z^T_p over tile t
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float* row = s.zt + (int64_t)ip[4 * ty + i] * s.dp + t * kJP;
-        *reinterpret_cast<float4*>(row + 4 * tx) =
-            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        *reinterpret_cast<float4*>(row + 32 + 4 * tx) =
-            make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-      }
-      __syncthreads();  // cur is free: the next iteration loads into it
+    for (int j = 0; j < 8; ++j) {
+      const int gr = idx(q, col8(tx, j)), gc = idx(p, 4 * ty);
+      *reinterpret_cast<float4*>(s.a + (int64_t)gr * s.dp + gc) =
+          make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
     }
   }
 }
+
+// ---------------------------------------------------------------- Z^T rotations, tensor cores
+// Z^T <- J_p^T Z^T over the rows I_p of a pair, as D = A B^T on tcgen05 (kind::tf32) with
+// A[c][k] = Z^T[I_p(k)][c0 + c] (128 columns of Z^T: the MMA's M) and B[i][k] = J_p[k][i]
+// (N = 64), K = 64 in two 32-wide k-blocks (the two 32-row halves of I_p).  fp32 accuracy
+// as in the batched GEMM: every operand value x is split into hi = x with its 13 low mantissa
+// bits cleared and lo = x - hi, each k-block forms hi*hi + hi*lo + lo*hi (12 MMAs) in a TMEM
+// accumulator of its own, and the two k-block partials are added in fp32 registers.  The
+// operands are MN-major in memory; 128 threads copy 4 x 4 blocks into the 128-byte-swizzled
+// K-major layout the MMA reads and transpose them in registers while splitting.
+namespace ztc {
+
+constexpr int kM = 128, kN = 64, kK = 32;           // MMA tile, k-block
+constexpr int kGroups = kZCols / 128;               // 128-column groups per CTA
+constexpr uint32_t kATile = kM * kK * 4;            // 16 KB per k-block
+constexpr uint32_t kBTile = kN * kK * 4;            // 8 KB per k-block
+constexpr uint32_t kAHi = 0, kALo = 2 * kATile;     // A: [hi kb0 | hi kb1 | lo kb0 | lo kb1]
+constexpr uint32_t kBHi = 4 * kATile, kBLo = kBHi + 2 * kBTile;
+constexpr uint32_t kBarOff = kBLo + 2 * kBTile;     // 96 KB
+constexpr size_t kSmem = 1024 + kBarOff + 64;
+constexpr uint32_t kTmemCols = 2 * kN;              // one accumulator per k-block
+// kind::tf32: fp32 accumulator (bit 4), TF32 A and B (2 at bits 7 and 10), both K-major,
+// N >> 3 at bit 17, M >> 4 at bit 24
+constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(kN >> 3) << 17) |
+                            ((uint32_t)(kM >> 4) << 24);
+static_assert(kSmem <= 227 * 1024, "shared memory");
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of `parity`; false when the limit ran out.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (try_wait(bar, parity)) return true;
+  const uint64_t t0 = now_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (try_wait(bar, parity)) return true;
+    if ((i & 31) == 0 && now_ns() - t0 > limit_ns) return false;
+  }
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                    uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// K-major operand in the 128-byte-swizzled layout: rows of 32 fp32 (128 B), 8-row atoms
+// 1024 B apart (stride offset), leading offset unused (16 B), version 1, swizzle mode 2.
+__device__ __forceinline__ uint64_t kdesc(uint32_t s) {
+  return (uint64_t)((s >> 4) & 0x3FFFu) | ((uint64_t)(16u >> 4) << 16) |
+         ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Byte offset of (row r, k) in a K-major 32-wide tile: 16-byte chunk k / 4 of row r at chunk
+// (k / 4) ^ (r % 8).
+__device__ __forceinline__ uint32_t toff(int r, int k) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((k >> 2) ^ (r & 7)) & 7) << 4) +
+                    (k & 3) * 4);
+}
+__device__ __forceinline__ void cp16(uint32_t dst, const float* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ float4 lds4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts4(uint32_t a, float4 v) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void split(float x, float& hi, float& lo) {
+  hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+  lo = x - hi;
+}
+// The 4 x 4 block of rows 4 rq .. + 3 and k 4 kq .. + 3 of an MN-major source (element
+// (r, k) at src[k * ld + r]), `avail` rows of it inside (the rest zero), copied one k-row at a
+// time into the places the block's four rows take in the K-major tile at s_lo.
+__device__ __forceinline__ void issue_block(const float* src, int64_t ld, int rq, int kq,
+                                            int avail, uint32_t s_lo) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float* g = src + (int64_t)(4 * kq + i) * ld + 4 * rq;
+    cp16(s_lo + toff(4 * rq + i, 4 * kq), avail > 0 ? g : src, avail >= 4 ? 16 : 0);
+  }
+}
+// Transpose the block in registers and split it: hi to s_hi, lo over the raw values.
+__device__ __forceinline__ void convert_block(int rq, int kq, uint32_t s_hi, uint32_t s_lo) {
+  float4 y[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) y[i] = lds4(s_lo + toff(4 * rq + i, 4 * kq));
+  const float v[4][4] = {{y[0].x, y[1].x, y[2].x, y[3].x}, {y[0].y, y[1].y, y[2].y, y[3].y},
+                         {y[0].z, y[1].z, y[2].z, y[3].z}, {y[0].w, y[1].w, y[2].w, y[3].w}};
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    float4 h, l;
+    split(v[r][0], h.x, l.x);
+    split(v[r][1], h.y, l.y);
+    split(v[r][2], h.z, l.z);
+    split(v[r][3], h.w, l.w);
+    const uint32_t off = toff(4 * rq + r, 4 * kq);
+    sts4(s_hi + off, h);
+    sts4(s_lo + off, l);
+  }
+}
+
+}  // namespace ztc
+
+// One CTA of 128 threads per (pair p of a side, 512 columns of Z^T): J_p is split once, then
+// four 128-column groups go through copy, split, 24 MMAs and the epilogue, the next group's
+// copies flying while the current one's results are stored.  Compact grid as the FFMA Z^T
+// blocks of jacobi_apply_kernel (blocks [begin[k], begin[k + 1]) of side k, P per 512
+// columns).  Every wait is bounded: on a timeout the CTA records it in the status word, waits
+// (bounded) for its MMAs, frees its tensor memory and returns.
+__global__ void __launch_bounds__(128) jacobi_zrot_tc_kernel(const SideDev* sides,
+                                                             const int32_t* begin, int nsides,
+                                                             const JacobiCtl* ctl, int round,
+                                                             int buf, uint64_t limit_ns,
+                                                             int* status) {
+  using namespace ztc;
+  const int k = side_of(begin, nsides, blockIdx.x);
+  const SideDev s = sides[k];
+  const int nb = s.dp / kJB, P = nb / 2;
+  if (ctl[k].converged || round >= nb - 1) return;
+  const int bid = blockIdx.x - begin[k], cgrp = bid / P, p = bid % P;
+  if (!s.rot[buf * P + p]) return;
+  int b0, b1;
+  circle_pair(nb, round, p, b0, b1);
+  const float* jp = s.j + ((int64_t)buf * P + p) * kJP * kJP;
+  const int ngroups = (s.dp + kM - 1) / kM;
+  const int g0 = cgrp * kGroups, g1 = min(ngroups, g0 + kGroups);
+  if (g0 >= g1) return;
+
+  extern __shared__ uint8_t zsm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(zsm_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const uint32_t sb = saddr(sm);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kBarOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  const uint32_t mbar = saddr(bar);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(1) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     saddr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // this thread's 4 x 4 blocks: B (64 rows i): one per k-block; A (128 rows c): two
+  const int l = tid & 31, kq = l & 7;
+  const int rq_b = 4 * (tid >> 5) + (l >> 3);                     // 0 .. 15
+  auto rq_a = [&](int u) { return 4 * (4 * u + (tid >> 5)) + (l >> 3); };  // 0 .. 31
+  // B[i][k] = J_p[k][i]: k-block kb holds J_p rows 32 kb .. + 31
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb)
+    issue_block(jp + (int64_t)(kK * kb) * kJP, kJP, rq_b, kq, 4, sb + kBLo + kb * kBTile);
+  // A[c][k] = Z^T[I_p(k)][c0 + c]: k-block kb holds the rows of block b_kb
+  auto issue_a = [&](int grp) {
+    const int c0 = grp * kM;
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+      const float* src = s.zt + (int64_t)(kJB * (kb ? b1 : b0)) * s.dp + c0;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int rq = rq_a(u);
+        issue_block(src, s.dp, rq, kq, s.dp - (c0 + 4 * rq), sb + kALo + kb * kATile);
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  issue_a(g0);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+  uint32_t phase = 0;
+  for (int grp = g0; grp < g1; ++grp) {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (grp == g0) {
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb)
+        convert_block(rq_b, kq, sb + kBHi + kb * kBTile, sb + kBLo + kb * kBTile);
+    }
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        convert_block(rq_a(u), kq, sb + kAHi + kb * kATile, sb + kALo + kb * kATile);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMA
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (tid == 0) {
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb) {
+        const uint32_t d = tmem + (uint32_t)(kb * kN);
+        const uint32_t ah = sb + kAHi + kb * kATile, al = sb + kALo + kb * kATile;
+        const uint32_t bh = sb + kBHi + kb * kBTile, bl = sb + kBLo + kb * kBTile;
+#pragma unroll
+        for (int j = 0; j < kK / 8; ++j) {
+          mma(d, kdesc(ah + 32u * j), kdesc(bh + 32u * j), j != 0);
+          mma(d, kdesc(ah + 32u * j), kdesc(bl + 32u * j), 1u);
+          mma(d, kdesc(al + 32u * j), kdesc(bh + 32u * j), 1u);
+        }
+      }
+      commit(mbar);
+    }
+    if (!wait_bar(mbar, phase, limit_ns)) {
+      atomicOr(status, kStatusTimeout);
+      ok = false;
+    }
+    phase ^= 1u;
+    fence_after();
+    // A's buffers are free once the MMAs completed: the next group's copies fly while this
+    // group's results are stored
+    if (ok && grp + 1 < g1) issue_a(grp + 1);
+    if (ok) {
+      const int c = grp * kM + 32 * warp + lane;  // this thread's TMEM lane = column of Z^T
+      const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16);
+#pragma unroll
+      for (int q = 0; q < kN / 16; ++q) {
+        float v0[16], v1[16];
+        tmem_ld16(ta + (uint32_t)(16 * q), v0);
+        tmem_ld16(ta + (uint32_t)(kN + 16 * q), v1);
+        if (c < s.dp) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int i = 16 * q + e;  // output row I_p(i)
+            const int row = (i < kJB ? b0 : b1) * kJB + (i & (kJB - 1));
+            s.zt[(int64_t)row * s.dp + c] = v0[e] + v1[e];
+          }
+        }
+      }
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (!__syncthreads_and(ok)) break;
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  if (!ok && tid == 0) wait_bar(mbar, phase ^ 1u, limit_ns);  // MMAs still in flight
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
 
 // End of a sweep: a side whose sweep rotated nothing is converged.
 __global__ void jacobi_sweep_end_kernel(JacobiCtl* ctl, int nsides) {
@@ -927,7 +1192,7 @@ void soap_fill(const mfsdp_soap_set* set, const mfsdp_soap_state* st, uint8_t* w
       tb.zrot_begin[g].push_back(zb);
       sb += P;
       ab += P * (P + 1) / 2;
-      zb += P * ((P + kZTiles - 1) / kZTiles);
+      zb += P * ((64 * P + kZCols - 1) / kZCols);
     }
     tb.solve_begin[g].push_back(sb);
     tb.apply_begin[g].push_back(ab);
@@ -1077,6 +1342,12 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
   if (cudaFuncSetAttribute(jacobi_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kApplySmem) != cudaSuccess)
     return MFSDP_ECUDA;
+  if (cudaFuncSetAttribute(jacobi_zrot_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)ztc::kSmem) != cudaSuccess)
+    return MFSDP_ECUDA;
+  const uint64_t limit_ns = wait_limit_ns();
+  int* status = status_word_address();
+  if (status == nullptr) return MFSDP_ECUDA;
 
   const unsigned ns = 2u * (unsigned)n;
   const int sweep_blocks = (int)((ns + 255) / 256);
@@ -1123,10 +1394,10 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
           d_sides + goff[g], d_solve_begin[g], gn[g], ctl + goff[g], r, b);
       ok(cudaEventRecord(set->ev_j[g][b], ms));
       jacobi_apply_kernel<<<(unsigned)tb.apply_begin[g].back(), kJThreads, kApplySmem, ms>>>(
-          d_sides + goff[g], d_apply_begin[g], gn[g], ctl + goff[g], r, b, 0);
+          d_sides + goff[g], d_apply_begin[g], gn[g], ctl + goff[g], r, b);
       ok(cudaStreamWaitEvent(zs, set->ev_j[g][b], 0));
-      jacobi_apply_kernel<<<(unsigned)tb.zrot_begin[g].back(), kJThreads, kApplySmem, zs>>>(
-          d_sides + goff[g], d_zrot_begin[g], gn[g], ctl + goff[g], r, b, 1);
+      jacobi_zrot_tc_kernel<<<(unsigned)tb.zrot_begin[g].back(), 128, ztc::kSmem, zs>>>(
+          d_sides + goff[g], d_zrot_begin[g], gn[g], ctl + goff[g], r, b, limit_ns, status);
       ok(cudaEventRecord(set->ev_z[g][b], zs));
       ++rounds;
     };
@@ -1258,8 +1529,6 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
   if ((e = run_gemms(tb.back1, d_back1, 0, 0, st)) != MFSDP_OK) return e;
   if ((e = run_gemms(tb.back2, d_back2, 0, 1, st)) != MFSDP_OK) return e;
   const float decay = (float)(1.0 - (double)h->lr * (double)h->weight_decay);
-  int* status = status_word_address();
-  if (status == nullptr) return MFSDP_ECUDA;
   soap_update_kernel<<<dim3(128, (unsigned)n), 256, 0, st>>>(d_mats, weights, g_rot, decay,
                                                              h->lr, status);
   return cudaGetLastError() == cudaSuccess ? MFSDP_OK : MFSDP_ECUDA;
