@@ -762,9 +762,11 @@ def run_ours(args, rank, world, local_rank):
         ffma_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
         ach = (gemm + jac) / (sms_ * 1e-3) / 1e12
         line["soap"] = {
-            "kernel": "jacobi_apply_kernel + jacobi_solve_kernel (block Jacobi eigenbases, fp32 "
-                      "CUDA cores) + tf32x3_gemm_kernel (statistics, Q^T L Q, Rayleigh "
-                      "quotients, rotations: tcgen05 3xTF32)",
+            "kernel": "jacobi_solve_kernel + jacobi_apply_kernel (block Jacobi subproblems and "
+                      "A's rotations, fp32 CUDA cores) + jacobi_zrot_tc_kernel (Z^T's "
+                      "rotations) + tf32x3_gemm_kernel (statistics, Q^T L Q, polar step, "
+                      "Rayleigh quotients, rotations into and out of the eigenbasis) (tcgen05 "
+                      "3xTF32)",
             "what": "one owner SOAP step of one GPT-2-small layer (2304x768, 768x768, 3072x768, "
                     "768x3072), exact eigenbases every step, warm-started",
             "ms": round(sms_, 3), "sweeps_per_side": sweeps, "bound": "alu",
@@ -775,7 +777,9 @@ def run_ours(args, rank, world, local_rank):
             "frac": round(ach / ffma_peak, 4),
             "flops_counted": "SGEMMs + 8 dp^3 per side per rotating sweep (every 64x64 block "
                              "product of the rotations): an upper bound, since pairs whose "
-                             "rotation is the identity skip their blocks"}
+                             "rotation is the identity skip their blocks; half of the "
+                             "rotation FLOPs (Z^T's) run on the tensor cores, so the fraction "
+                             "of the FFMA peak is a mixed figure"}
     return line
 
 
