@@ -338,8 +338,10 @@ int mfsdp_gemm_f32_batched(const mfsdp_gemm_problem* probs, int32_t n_probs, int
  * group has converged.  While `stream` is being captured (or if the graph cannot be built)
  * the same sweeps are issued one by one on `stream` and three internal streams of the set,
  * forked from and joined back into `stream` with events, so a capture of `stream` takes them
- * all.  Streams, events and the graph are created on the device current at the first step; a
- * set serves one host thread at a time.
+ * all; so does MFSDP_SOAP_SWEEP_GRAPH=0 in the environment (read once per process), for
+ * profilers that do not list kernels inside conditional graph nodes.  Streams, events and the
+ * graph are created on the device current at the first step; a set serves one host thread at
+ * a time.
  *
  * State (DEVICE, fp32, caller-owned, updated in place): `l`, `q_l` hold every matrix's L and
  * Q_L (rows^2 each) back to back in table order, `r`, `q_r` its R and Q_R (cols^2); `eig_l`

@@ -39,6 +39,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -1461,7 +1462,13 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
     };
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MFSDP_ECUDA;
-    bool use_graph = !set->jgraph_off && cap == cudaStreamCaptureStatusNone;
+    // MFSDP_SOAP_SWEEP_GRAPH=0 in the environment issues the sweeps one by one (profilers
+    // that do not see kernels inside conditional graph nodes list them then)
+    static const bool graph_env_off = [] {
+      const char* v = std::getenv("MFSDP_SOAP_SWEEP_GRAPH");
+      return v != nullptr && v[0] == '0';
+    }();
+    bool use_graph = !set->jgraph_off && !graph_env_off && cap == cudaStreamCaptureStatusNone;
     if (use_graph && (!set->jgraph || set->jgraph_ws != workspace ||
                       set->jgraph_sweeps != h->max_sweeps)) {
       use_graph = build_graph();
