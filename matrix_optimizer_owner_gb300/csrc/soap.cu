@@ -106,6 +106,20 @@ __device__ __forceinline__ int pair_index(int nb, int r, int p, int c) {
   return (c < kJB ? b0 : b1) * kJB + (c & (kJB - 1));
 }
 
+// The pair of round r that holds block x, and x's partner in it (inverse of circle_pair).
+__device__ __forceinline__ int pair_of(int nb, int r, int x) {
+  const int m = nb - 1, half = nb / 2;
+  if (x == nb - 1 || x == r) return 0;
+  int d = x - r;
+  if (d < 0) d += m;
+  return d <= half - 1 ? d : m - d;
+}
+__device__ __forceinline__ int partner_of(int nb, int r, int x) {
+  int a, b;
+  circle_pair(nb, r, pair_of(nb, r, x), a, b);
+  return a == x ? b : a;
+}
+
 // The side whose range [begin[k], begin[k + 1]) of a compact grid holds block `bid`.
 __device__ __forceinline__ int side_of(const int32_t* begin, int nsides, int bid) {
   int lo = 0, hi = nsides - 1;
@@ -413,16 +427,27 @@ __device__ __forceinline__ void load_block(float (*dst)[kALd], const float* src,
   }
 }
 
-// The round's rotations applied to A; compact grid, blocks [begin[k], begin[k + 1]) for side
-// k, one per block pair (p, q), p <= q: Y = Jp^T (A_pq Jq), with A_pq Jq formed from the
-// mirrored block (A is symmetric), Y written to (p, q) and Y^T to (q, p).  A CTA loads A_pq
-// and Jq as one copy group and Jp as a second, which lands while W = A_pq Jq is formed.
-// (Z^T's rows take the same rotations in jacobi_zrot_tc_kernel.)
+// The round's rotations applied to A, one CTA per block pair (p, q), p <= q: Y = Jp^T (A_pq
+// Jq), with A_pq Jq formed from the mirrored block (A is symmetric), Y written to (p, q) and
+// Y^T to (q, p).  A CTA loads A_pq and Jq as one copy group and Jp as a second, which lands
+// while W = A_pq Jq is formed.  (Z^T's rows take the same rotations in jacobi_zrot_tc_kernel.)
+// The next round's subproblems read only the block pairs of `critical` CTAs: (p, p) for
+// every p, and for every pair of the next round (blocks x, y) the CTA of this round's pairs
+// of x and y.  Part 1 (compact grid of 2P blocks per side) runs those; part 2 (the triangle of
+// P(P + 1) / 2 per side) runs the others, beside the next round's subproblems.
+__device__ __forceinline__ bool critical_pair(int nb, int round, int p, int q) {
+  if (p == q) return true;
+  const int rn = round + 1 == nb - 1 ? 0 : round + 1;
+  int b0, b1;
+  circle_pair(nb, round, p, b0, b1);
+  return pair_of(nb, round, partner_of(nb, rn, b0)) == q ||
+         pair_of(nb, round, partner_of(nb, rn, b1)) == q;
+}
 __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* sides,
                                                                  const int32_t* begin,
                                                                  int nsides,
                                                                  const JacobiCtl* ctl,
-                                                                 int round, int buf) {
+                                                                 int round, int buf, int part) {
   const int k = side_of(begin, nsides, blockIdx.x);
   const SideDev s = sides[k];
   const int nb = s.dp / kJB, P = nb / 2;
@@ -437,9 +462,29 @@ __global__ void __launch_bounds__(kJThreads) jacobi_apply_kernel(const SideDev* 
   __shared__ int ip[kJP], iq[kJP];  // global indices of the two pair-blocks
   const int tid = threadIdx.x, ty = tid >> 3, tx = tid & 7;
   float acc[4][8];
-  int p = 0, rem = bid;
-  while (rem >= P - p) { rem -= P - p; ++p; }
-  const int q = p + rem;
+  int p = 0, q = 0;
+  if (part == 1) {
+    if (bid < P) {
+      p = q = bid;
+    } else {
+      // the CTA of next-round pair pp (blocks x, y); of two next-round pairs that meet the
+      // same two pairs of this round, the lower one runs it
+      const int pp = bid - P, rn = round + 1 == nb - 1 ? 0 : round + 1;
+      int x, y;
+      circle_pair(nb, rn, pp, x, y);
+      const int px = pair_of(nb, round, x), py = pair_of(nb, round, y);
+      if (px == py) return;
+      const int x2 = partner_of(nb, round, x), p2 = pair_of(nb, rn, x2);
+      if (p2 < pp && pair_of(nb, round, partner_of(nb, rn, x2)) == py) return;
+      p = min(px, py);
+      q = max(px, py);
+    }
+  } else {
+    int rem = bid;
+    while (rem >= P - p) { rem -= P - p; ++p; }
+    q = p + rem;
+    if (part == 2 && critical_pair(nb, round, p, q)) return;
+  }
   if (!rb[p] && !rb[q]) return;
   if (tid < kJP) ip[tid] = pair_index(nb, round, p, tid);
   else if (tid < 2 * kJP) iq[tid - kJP] = pair_index(nb, round, q, tid - kJP);
@@ -1005,6 +1050,10 @@ struct mfsdp_soap_set {
   // rotations that read buffer b done, ev_zjoin[g] the group's last Z^T rotation.
   mutable cudaStream_t zst[2] = {nullptr, nullptr};
   mutable cudaEvent_t ev_j[2][2] = {}, ev_z[2][2] = {}, ev_zjoin[2] = {};
+  // A's non-critical block pairs run on a third stream per group, beside the next round's
+  // subproblems; ev_rest[g] marks the last of them.
+  mutable cudaStream_t rst[2] = {nullptr, nullptr};
+  mutable cudaEvent_t ev_rest[2] = {};
   // The sweeps as a CUDA graph: per group a while node whose body is one sweep, so that the
   // sweeps stop on the device once every side of the group has converged (no launches of
   // sweeps that would find every side converged).  Built for one workspace and sweep limit
@@ -1019,6 +1068,8 @@ struct mfsdp_soap_set {
     if (ev_fork) cudaEventDestroy(ev_fork);
     if (ev_join) cudaEventDestroy(ev_join);
     for (int g = 0; g < 2; ++g) {
+      if (rst[g]) cudaStreamDestroy(rst[g]);
+      if (ev_rest[g]) cudaEventDestroy(ev_rest[g]);
       if (zst[g]) cudaStreamDestroy(zst[g]);
       if (ev_zjoin[g]) cudaEventDestroy(ev_zjoin[g]);
       for (int b = 0; b < 2; ++b) {
@@ -1039,15 +1090,16 @@ constexpr int kGemmsPerMat = 18;  // stats 2, T 2, A 2, polar 4, Rayleigh 2, int
 // Device tables of one step, in upload order.
 struct SoapTables {
   std::vector<SideDev> sides;
-  // compact grids of the two groups: subproblems, A block pairs, Z^T row groups
-  std::vector<int32_t> solve_begin[2], apply_begin[2], zrot_begin[2];
+  // compact grids of the two groups: subproblems, A block pairs (all; the critical ones),
+  // Z^T row groups
+  std::vector<int32_t> solve_begin[2], apply_begin[2], crit_begin[2], zrot_begin[2];
   std::vector<MatDev> mats;
   std::vector<GemmDesc> stats_l, stats_r, t, a, polar1, polar2, ray, rot1, rot2, back1, back2;
 };
 
 size_t soap_table_bytes(size_t n) {
   return al256(sizeof(SideDev) * 2 * n) + al256(sizeof(MatDev) * n) +
-         6 * al256(sizeof(int32_t) * (2 * n + 1)) + al256(sizeof(GemmDesc) * kGemmsPerMat * n) +
+         8 * al256(sizeof(int32_t) * (2 * n + 1)) + al256(sizeof(GemmDesc) * kGemmsPerMat * n) +
          20 * 256;
 }
 
@@ -1185,18 +1237,21 @@ void soap_fill(const mfsdp_soap_set* set, const mfsdp_soap_state* st, uint8_t* w
   for (const auto& m : set->mats) tb.mats.push_back(MatDev{m.offset, m.rows * m.cols});
   for (int g = 0; g < 2; ++g) {
     const int lo = g ? set->split : 0, hi = g ? 2 * n : set->split;
-    int32_t sb = 0, ab = 0, zb = 0;
+    int32_t sb = 0, ab = 0, cb = 0, zb = 0;
     for (int pos = lo; pos < hi; ++pos) {
       const int32_t P = set->sides[(size_t)set->order[(size_t)pos]].dp / 64;
       tb.solve_begin[g].push_back(sb);
       tb.apply_begin[g].push_back(ab);
+      tb.crit_begin[g].push_back(cb);
       tb.zrot_begin[g].push_back(zb);
       sb += P;
       ab += P * (P + 1) / 2;
+      cb += 2 * P;
       zb += P * ((64 * P + kZCols - 1) / kZCols);
     }
     tb.solve_begin[g].push_back(sb);
     tb.apply_begin[g].push_back(ab);
+    tb.crit_begin[g].push_back(cb);
     tb.zrot_begin[g].push_back(zb);
   }
 }
@@ -1326,6 +1381,8 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
                                       put(host, at, dev, tb.apply_begin[1])};
   const int32_t* d_zrot_begin[2] = {put(host, at, dev, tb.zrot_begin[0]),
                                      put(host, at, dev, tb.zrot_begin[1])};
+  const int32_t* d_crit_begin[2] = {put(host, at, dev, tb.crit_begin[0]),
+                                     put(host, at, dev, tb.crit_begin[1])};
   const GemmDesc* d_stats_l = put(host, at, dev, tb.stats_l);
   const GemmDesc* d_stats_r = put(host, at, dev, tb.stats_r);
   const GemmDesc* d_t = put(host, at, dev, tb.t);
@@ -1371,7 +1428,9 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
                 cudaEventCreateWithFlags(&set->ev_join, cudaEventDisableTiming) == cudaSuccess;
       for (int g = 0; g < 2 && ok; ++g) {
         ok = cudaStreamCreateWithFlags(&set->zst[g], cudaStreamNonBlocking) == cudaSuccess &&
-             cudaEventCreateWithFlags(&set->ev_zjoin[g], cudaEventDisableTiming) == cudaSuccess;
+             cudaEventCreateWithFlags(&set->ev_zjoin[g], cudaEventDisableTiming) == cudaSuccess &&
+             cudaStreamCreateWithFlags(&set->rst[g], cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&set->ev_rest[g], cudaEventDisableTiming) == cudaSuccess;
         for (int b = 0; b < 2 && ok; ++b)
           ok = cudaEventCreateWithFlags(&set->ev_j[g][b], cudaEventDisableTiming) ==
                    cudaSuccess &&
@@ -1388,14 +1447,22 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
     // the group's stream `ms`; Z^T's rows on the group's Z^T stream `zs` once the round's
     // rotations are written.  The rotations alternate between two buffers, so a round waits
     // only for the Z^T rotations of the round two before it (the last reader of its buffer).
-    auto round_launches = [&](int g, int r, long& rounds, cudaStream_t ms, cudaStream_t zs) {
+    auto round_launches = [&](int g, int r, long& rounds, cudaStream_t ms, cudaStream_t rs,
+                              cudaStream_t zs) {
       const int b = (int)(rounds & 1);
       if (rounds >= 2) ok(cudaStreamWaitEvent(ms, set->ev_z[g][b], 0));
       jacobi_solve_kernel<<<(unsigned)tb.solve_begin[g].back(), kSolveThreads, 0, ms>>>(
           d_sides + goff[g], d_solve_begin[g], gn[g], ctl + goff[g], r, b);
       ok(cudaEventRecord(set->ev_j[g][b], ms));
-      jacobi_apply_kernel<<<(unsigned)tb.apply_begin[g].back(), kJThreads, kApplySmem, ms>>>(
-          d_sides + goff[g], d_apply_begin[g], gn[g], ctl + goff[g], r, b);
+      // A's critical block pairs once the previous round's others are done; the others beside
+      // the next round's subproblems
+      if (rounds >= 1) ok(cudaStreamWaitEvent(ms, set->ev_rest[g], 0));
+      jacobi_apply_kernel<<<(unsigned)tb.crit_begin[g].back(), kJThreads, kApplySmem, ms>>>(
+          d_sides + goff[g], d_crit_begin[g], gn[g], ctl + goff[g], r, b, 1);
+      ok(cudaStreamWaitEvent(rs, set->ev_j[g][b], 0));
+      jacobi_apply_kernel<<<(unsigned)tb.apply_begin[g].back(), kJThreads, kApplySmem, rs>>>(
+          d_sides + goff[g], d_apply_begin[g], gn[g], ctl + goff[g], r, b, 2);
+      ok(cudaEventRecord(set->ev_rest[g], rs));
       ok(cudaStreamWaitEvent(zs, set->ev_j[g][b], 0));
       jacobi_zrot_tc_kernel<<<(unsigned)tb.zrot_begin[g].back(), 128, ztc::kSmem, zs>>>(
           d_sides + goff[g], d_zrot_begin[g], gn[g], ctl + goff[g], r, b, limit_ns, status);
@@ -1427,7 +1494,7 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
         cudaGraphNode_t node;
         good = good && cudaGraphAddNode(&node, top, nullptr, nullptr, 0, &np) == cudaSuccess;
         if (!good) break;
-        const cudaStream_t cs = set->aux, czs = set->zst[g];
+        const cudaStream_t cs = set->aux, czs = set->zst[g], crs = set->rst[g];
         if (cudaStreamBeginCaptureToGraph(cs, np.conditional.phGraph_out[0], nullptr, nullptr, 0,
                                           cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
           good = false;
@@ -1436,10 +1503,13 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
         ce = cudaSuccess;
         ok(cudaEventRecord(set->ev_fork, cs));
         ok(cudaStreamWaitEvent(czs, set->ev_fork, 0));
+        ok(cudaStreamWaitEvent(crs, set->ev_fork, 0));
         long rounds = 0;
-        for (int r = 0; r < set->nb_max_group[g] - 1; ++r) round_launches(g, r, rounds, cs, czs);
+        for (int r = 0; r < set->nb_max_group[g] - 1; ++r)
+          round_launches(g, r, rounds, cs, crs, czs);
         ok(cudaEventRecord(set->ev_zjoin[g], czs));
         ok(cudaStreamWaitEvent(cs, set->ev_zjoin[g], 0));
+        ok(cudaStreamWaitEvent(cs, set->ev_rest[g], 0));
         sweep_end(g, cs);
         jacobi_loop_kernel<<<1, 256, 0, cs>>>(ctl + goff[g], gn[g], h->max_sweeps, hnd);
         ok(cudaGetLastError());
@@ -1481,14 +1551,16 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
       // into `st`; sweeps after a side has converged find it converged and return at once
       ok(cudaEventRecord(set->ev_fork, st));
       ok(cudaStreamWaitEvent(set->aux, set->ev_fork, 0));
-      ok(cudaStreamWaitEvent(set->zst[0], set->ev_fork, 0));
-      ok(cudaStreamWaitEvent(set->zst[1], set->ev_fork, 0));
+      for (int g = 0; g < 2; ++g) {
+        ok(cudaStreamWaitEvent(set->zst[g], set->ev_fork, 0));
+        ok(cudaStreamWaitEvent(set->rst[g], set->ev_fork, 0));
+      }
       long rounds[2] = {0, 0};
       for (int sw = 0; sw < h->max_sweeps; ++sw) {
         for (int r = 0; r < nb_max - 1; ++r)
           for (int g = 0; g < 2; ++g) {
             if (gn[g] == 0 || r >= set->nb_max_group[g] - 1) continue;
-            round_launches(g, r, rounds[g], gst[g], set->zst[g]);
+            round_launches(g, r, rounds[g], gst[g], set->rst[g], set->zst[g]);
           }
         for (int g = 0; g < 2; ++g)
           if (gn[g] > 0) sweep_end(g, gst[g]);
@@ -1497,6 +1569,8 @@ extern "C" int mfsdp_soap_step(const mfsdp_soap_set* set, const float* grad, flo
       ok(cudaStreamWaitEvent(st, set->ev_join, 0));
       for (int g = 0; g < 2; ++g) {
         ok(cudaEventRecord(set->ev_zjoin[g], set->zst[g]));
+        ok(cudaStreamWaitEvent(st, set->ev_zjoin[g], 0));
+        ok(cudaEventRecord(set->ev_zjoin[g], set->rst[g]));
         ok(cudaStreamWaitEvent(st, set->ev_zjoin[g], 0));
       }
     }
