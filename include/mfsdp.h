@@ -330,8 +330,9 @@ int mfsdp_gemm_f32_batched(const mfsdp_gemm_problem* probs, int32_t n_probs, int
  * holds (the previous step's), until a sweep rotates nothing or `max_sweeps` sweeps ran;
  * each solve ends with one polar step on its basis (Z <- Z (3I - Z^T Z) / 2); the statistics,
  * Q^T L Q, that polar step, the Rayleigh quotients and the rotations into and out of the
- * eigenbasis are fp32 GEMMs on the tensor cores (3xTF32, as mfsdp_gemm_f32_batched), the
- * Jacobi rotations fp32 on the CUDA cores.  Eigenvectors are fixed up to sign, and N does not
+ * eigenbasis are fp32 GEMMs on the tensor cores (3xTF32, as mfsdp_gemm_f32_batched); the
+ * Jacobi rotations of Q^T L Q run in fp32 on the CUDA cores, those of the basis on the tensor
+ * cores (3xTF32).  Eigenvectors are fixed up to sign, and N does not
  * depend on the signs.  The Jacobi sweeps run as a CUDA graph that the set builds at its
  * first refresh step for a given workspace and max_sweeps and launches on `stream`: per group
  * of sides a while loop whose body is one sweep, ending on the device once every side of the
