@@ -684,10 +684,10 @@ __device__ __forceinline__ void convert_block(int rq, int kq, uint32_t s_hi, uin
 
 // One CTA of 128 threads per (pair p of a side, 512 columns of Z^T): J_p is split once, then
 // four 128-column groups go through copy, split, 24 MMAs and the epilogue, the next group's
-// copies flying while the current one's results are stored.  Compact grid as the FFMA Z^T
-// blocks of jacobi_apply_kernel (blocks [begin[k], begin[k + 1]) of side k, P per 512
-// columns).  Every wait is bounded: on a timeout the CTA records it in the status word, waits
-// (bounded) for its MMAs, frees its tensor memory and returns.
+// copies flying while the current one's results are stored.  Compact grid: blocks
+// [begin[k], begin[k + 1]) of side k, block c P + p for pair p and columns 512 c .. + 511.
+// Every wait is bounded: on a timeout the CTA records it in the status word, waits (bounded)
+// for its MMAs, frees its tensor memory and returns.
 __global__ void __launch_bounds__(128) jacobi_zrot_tc_kernel(const SideDev* sides,
                                                              const int32_t* begin, int nsides,
                                                              const JacobiCtl* ctl, int round,
