@@ -262,3 +262,46 @@ def test_non_finite_gradient_sets_the_status():
     assert mfsdp.mfsdp_query_status() == -8   # MFSDP_ENONFINITE, then cleared
     assert mfsdp.mfsdp_query_status() == 0
     sset.close()
+
+
+def _sweep_path_run(out_path):
+    """Three refreshing SOAP steps on a small ragged set from seeded CPU draws; saves the
+    weights and the state (run in this process and in a child without the sweep graph)."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    shapes = [(100, 37), (129, 130), (64, 256), (300, 70)]
+    sset, ws, state, offs, numel = _setup(shapes, dev)
+    gen = torch.Generator().manual_seed(17)
+    w = (torch.randn(numel, generator=gen) * 0.02).to(dev)
+    info = torch.zeros(2 * len(shapes), dtype=torch.int32, device=dev)
+    for t in range(1, 4):
+        g = (torch.randn(numel, generator=gen) * 1e-3).to(dev)
+        sset.step(g, w, state, t, max_sweeps=SWEEPS, workspace=ws, info=info, **H)
+    torch.cuda.synchronize()
+    out = {"w": w.cpu(), "info": info.cpu()}
+    out.update({k: v.cpu() for k, v in state.items()})
+    torch.save(out, out_path)
+    sset.close()
+
+
+def test_sweep_graph_and_stream_launches_give_the_same_bits(tmp_path):
+    """The Jacobi sweeps run as a CUDA graph (a device-side while loop per group of sides)
+    unless MFSDP_SOAP_SWEEP_GRAPH=0, when the host issues them one by one on the streams.  The
+    two issue the same kernels on the same data in the same dependency order, so every output
+    is bit-identical; the variable is read once per process, so the second run is a child."""
+    import os
+    import subprocess
+    import sys
+    a, b = tmp_path / "graph.pt", tmp_path / "streams.pt"
+    _sweep_path_run(str(a))
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, MFSDP_SOAP_SWEEP_GRAPH="0")
+    code = ("import sys; sys.path.insert(0, 'tests'); import test_gpu_soap as t; "
+            "t._sweep_path_run(sys.argv[1])")
+    r = subprocess.run([sys.executable, "-c", code, str(b)], cwd=root, env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    x, y = torch.load(str(a)), torch.load(str(b))
+    assert (x["info"] > 0).all(), x["info"]
+    for k in x:
+        assert torch.equal(x[k], y[k]), k
